@@ -1,0 +1,512 @@
+"""Pins that tie the CPU oracle to what the pages and the mathematics fix.
+
+Every check takes the oracle module ``O`` and raises AssertionError when the
+oracle disagrees with a closed form, a special case, an independently written
+model or brute force. ``tests/test_oracle_pins.py`` runs them against the
+oracle as it stands; ``tests/test_oracle_mutants.py`` plants plausible
+mistakes in the oracle and checks that at least one pin fails for each.
+
+Nothing here reuses oracle arithmetic: the vanilla Transformer, the MLP-only
+stack, the complex-number RoPE and the RMSNorm closed forms are written out
+afresh below.
+"""
+
+from __future__ import annotations
+
+import math
+from types import SimpleNamespace
+
+import numpy as np
+import scipy.special
+
+RTOL = 1e-10
+
+
+def _cfg(**kw):
+    base = dict(L=4, D=16, k=2, p=2, p_offset=0, Hq=4, Hkv=2, d=8, F=24, V=32,
+                eps=1e-6, rope_base=1e4)
+    base.update(kw)
+    c = SimpleNamespace(**base)
+    c.nR = len([l for l in range(c.L) if l % c.p == c.p_offset])
+    return c
+
+
+def _weights(c, seed=0, std=0.3, jitter=0.2):
+    """Seeded fp64 weights for the pins (numpy; larger std than the workloads
+    so that every term visibly moves the result)."""
+    rng = np.random.default_rng(seed)
+    L, D, k, d = c.L, c.D, c.k, c.d
+    shapes = {
+        "embed": (c.V, D), "lm_head": (c.V, D), "final_norm": (D,),
+        "in_norm": (L, D), "post_norm": (L, D), "q_norm": (L, d),
+        "Wq": (L, c.Hq * d, D), "Wo": (L, D, c.Hq * d),
+        "Wgate": (L, c.F, D), "Wup": (L, c.F, D), "Wdown": (L, D, c.F),
+        "src_norm": (2, L, D), "Wr": (2, k * L, c.nR * D),
+        "chan_norm": (2, k, D), "Wk": (k, c.Hkv * d, D), "Wv": (k, c.Hkv * d, D),
+        "k_norm": (k, d),
+    }
+    gains = {"final_norm", "in_norm", "post_norm", "q_norm", "src_norm", "chan_norm", "k_norm"}
+    W = {}
+    for n, s in shapes.items():
+        if n in gains:
+            W[n] = 1.0 + jitter * rng.standard_normal(s)
+        else:
+            W[n] = std * rng.standard_normal(s)
+    return W
+
+
+def _close(a, b, rtol=RTOL, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    scale = max(np.max(np.abs(b)), 1e-300)
+    err = np.max(np.abs(a - b)) / scale if a.size else 0.0
+    assert err <= rtol, f"{what}: max rel err {err:.3e} > {rtol:.1e}"
+
+
+def _tokens(c, B, T, seed):
+    return np.random.default_rng(1000 + seed).integers(0, c.V, size=(B, T))
+
+
+# ---------------------------------------------------------------------------
+# Independent restatements used as references
+# ---------------------------------------------------------------------------
+
+def _rms(x, w, eps):
+    # RMSNorm written as x * (mean square + eps)^(-1/2) * w.
+    return x * np.power(np.mean(np.square(x), axis=-1, keepdims=True) + eps, -0.5) * w
+
+
+def _rope_complex(x, pos, base):
+    """RoPE as multiplication of z_t = x_t + i*x_{t+d/2} by exp(i*pos*theta_t)."""
+    d = x.shape[-1]
+    h = d // 2
+    theta = np.exp(-np.log(base) * (2.0 * np.arange(h)) / d)
+    z = x[..., :h] + 1j * x[..., h:]
+    z = z * np.exp(1j * np.asarray(pos, dtype=np.float64)[..., None] * theta)
+    return np.concatenate([z.real, z.imag], axis=-1)
+
+
+def _swish(x):
+    return x * scipy.special.expit(x)
+
+
+def _mlp_only_stack(c, W, tokens):
+    """Logits of the stack when every attention output is zero."""
+    h = W["embed"][tokens]
+    for l in range(c.L):
+        f = _rms(h, W["post_norm"][l], c.eps)
+        h = h + (_swish(f @ W["Wgate"][l].T) * (f @ W["Wup"][l].T)) @ W["Wdown"][l].T
+    return _rms(h, W["final_norm"], c.eps) @ W["lm_head"].T
+
+
+def _vanilla_strict_causal(c, W, tokens):
+    """A vanilla Qwen3-style Transformer whose layer l computes its own K/V
+    from its input h^l through the double norm (sigma^b_l then tau^b_l), the
+    channel-l projections, the K-norm and RoPE; token i attends to s < i only.
+    Whole sequence at once with masked score matrices. tokens [T]."""
+    T = len(tokens)
+    Hq, Hkv, d = c.Hq, c.Hkv, c.d
+    pos = np.arange(T)
+    vis = np.arange(T)[None, :] < np.arange(T)[:, None]          # [i, s]: s < i
+    h = W["embed"][tokens]
+    for l in range(c.L):
+        ck = _rms(_rms(h, W["src_norm"][0][l], c.eps), W["chan_norm"][0][l], c.eps)
+        cv = _rms(_rms(h, W["src_norm"][1][l], c.eps), W["chan_norm"][1][l], c.eps)
+        K = _rms((ck @ W["Wk"][l].T).reshape(T, Hkv, d), W["k_norm"][l], c.eps)
+        K = _rope_complex(K, pos[:, None], c.rope_base)
+        V = (cv @ W["Wv"][l].T).reshape(T, Hkv, d)
+        a = _rms(h, W["in_norm"][l], c.eps)
+        Q = _rms((a @ W["Wq"][l].T).reshape(T, Hq, d), W["q_norm"][l], c.eps)
+        Q = _rope_complex(Q, pos[:, None], c.rope_base)
+        O = np.zeros((T, Hq, d))
+        rep = Hq // Hkv
+        for hq in range(Hq):
+            hk = hq // rep
+            S = (Q[:, hq, :] @ K[:, hk, :].T) / math.sqrt(d)
+            S = np.where(vis, S, -np.inf)
+            has = vis.any(axis=1)
+            P = np.zeros((T, T))
+            P[has] = scipy.special.softmax(S[has], axis=1)
+            O[:, hq, :] = P @ V[:, hk, :]
+        h = h + O.reshape(T, Hq * d) @ W["Wo"][l].T
+        f = _rms(h, W["post_norm"][l], c.eps)
+        h = h + (_swish(f @ W["Wgate"][l].T) * (f @ W["Wup"][l].T)) @ W["Wdown"][l].T
+    return _rms(h, W["final_norm"], c.eps) @ W["lm_head"].T
+
+
+def _ar(O, c, W, tokens, Tmax=None, static=None):
+    B, T = tokens.shape
+    ck, cv = O.new_cache(c, B, Tmax or T)
+    lg = O.autoregressive(c, W, tokens, ck, cv, static_coeff=static)
+    return lg, ck, cv
+
+
+def _cyclic(O, c, W, tokens, g, passes, static=None, logits="all"):
+    B, T = tokens.shape
+    ck, cv = O.new_cache(c, B, T)
+    lg = None
+    for _ in range(passes):
+        lg = O.cyclic_pass(c, W, tokens, g, ck, cv, logits=logits, static_coeff=static)
+    return lg, ck, cv
+
+
+# ---------------------------------------------------------------------------
+# Elementwise pieces
+# ---------------------------------------------------------------------------
+
+def check_rmsnorm_closed_forms(O):
+    eps = 1e-6
+    # constant vector c*1: every element becomes w * c / sqrt(c^2 + eps)
+    for cval in (3.0, -0.5, 1e-3):
+        x = np.full(8, cval)
+        y = O.rmsnorm(x, np.ones(8), eps)
+        _close(y, np.full(8, cval / math.sqrt(cval * cval + eps)), 1e-13, "rmsnorm const")
+    # gain picks an element; scale invariance; mean square of the result
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(12)
+    w = np.zeros(12)
+    w[5] = 2.0
+    y = O.rmsnorm(x, w, 0.0)
+    assert y[5] == 2.0 * x[5] / math.sqrt(np.dot(x, x) / 12) or abs(
+        y[5] - 2.0 * x[5] / math.sqrt(np.dot(x, x) / 12)) < 1e-13
+    assert np.count_nonzero(y) == 1
+    _close(O.rmsnorm(7.5 * x, np.ones(12), 0.0), O.rmsnorm(x, np.ones(12), 0.0), 1e-13, "scale inv")
+    y = O.rmsnorm(x, np.ones(12), 0.0)
+    assert abs(np.dot(y, y) / 12 - 1.0) < 1e-13
+    # batched over leading axes, per-row statistic
+    X = rng.standard_normal((3, 5, 12))
+    Y = O.rmsnorm(X, np.ones(12), 0.0)
+    _close(Y[1, 2], O.rmsnorm(X[1, 2], np.ones(12), 0.0), 1e-14, "row-wise")
+
+
+def check_rope_closed_forms(O):
+    # d = 2: theta_0 = 1, the pair (1, 0) turns into (cos p, sin p)
+    for p in (0, 1, 5, 37):
+        _close(O.rope(np.array([1.0, 0.0]), p, 1e4), [math.cos(p), math.sin(p)], 1e-14, "rope d2")
+    # d = 4: second pair turns by p * base^(-1/2)
+    base = 1e4
+    e1 = np.array([0.0, 1.0, 0.0, 0.0])
+    for p in (3, 11):
+        a = p * base ** -0.5
+        _close(O.rope(e1, p, base), [0.0, math.cos(a), 0.0, math.sin(a)], 1e-14, "rope d4")
+    # position 0 is the identity; complex-number formulation agrees
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((5, 16))
+    _close(O.rope(x, 0, 1e6), x, 1e-15, "rope p0")
+    pos = np.array([0, 1, 2, 100, 2047])
+    _close(O.rope(x, pos[:, None][:, 0], 1e6), _rope_complex(x, pos, 1e6), 1e-12, "rope complex")
+    # relative invariance of the score
+    q, k = rng.standard_normal(16), rng.standard_normal(16)
+    s1 = O.rope(q, 9, 1e6) @ O.rope(k, 4, 1e6)
+    s2 = O.rope(q, 105, 1e6) @ O.rope(k, 100, 1e6)
+    assert abs(s1 - s2) < 1e-12
+
+
+def check_silu(O):
+    x = np.array([-30.0, -1.0, 0.0, 1.0, 2.0, 30.0])
+    ref = np.array([-30.0 / (1 + math.exp(30)), -1 / (1 + math.e), 0.0, 1 / (1 + math.exp(-1)),
+                    2 / (1 + math.exp(-2)), 30.0 / (1 + math.exp(-30))])
+    _close(O.silu(x), ref, 1e-14, "silu")
+
+
+# ---------------------------------------------------------------------------
+# Indexing rules
+# ---------------------------------------------------------------------------
+
+def check_indexing_rules(O):
+    c = _cfg(L=28, k=14, p=2)
+    assert O.router_sources(c) == list(range(0, 28, 2))
+    c1 = _cfg(L=28, k=14, p=2, p_offset=1)
+    assert O.router_sources(c1) == list(range(1, 28, 2))
+    assert [O.channel_of_layer(c, l) for l in range(28)] == [l % 14 for l in range(28)]
+    c_one = _cfg(L=5, k=1)
+    assert all(O.channel_of_layer(c_one, l) == 0 for l in range(5))
+    c_full = _cfg(L=5, k=5)
+    assert [O.channel_of_layer(c_full, l) for l in range(5)] == [0, 1, 2, 3, 4]
+    T, g = 11, 4
+    groups = [list(O.group_positions(T, g, q)) for q in range(g)]
+    assert groups == [[0, 4, 8], [1, 5, 9], [2, 6, 10], [3, 7]]
+    assert sorted(sum(groups, [])) == list(range(T))
+
+
+# ---------------------------------------------------------------------------
+# Channel attention
+# ---------------------------------------------------------------------------
+
+def check_attention_uniform_closed_form(O):
+    """Zero keys give uniform weights over s < i: the output is the mean of
+    the visible values. Values encode (channel, sequence, position)."""
+    Hq, Hkv, d, S = 4, 2, 8, 12
+    rng = np.random.default_rng(5)
+    for chan, seqid in ((3, 7), (0, 1)):
+        K = np.zeros((Hkv, S, d))
+        V = np.zeros((Hkv, S, d))
+        V[:, :, 0] = chan
+        V[:, :, 1] = seqid
+        V[:, :, 2] = np.arange(S)[None, :]
+        V[:, :, 3] = np.arange(Hkv)[:, None]
+        q = rng.standard_normal((Hq, d))
+        for i in range(S):
+            out = O.channel_attention(q, K, V, i, Hq, Hkv)
+            if i == 0:
+                assert np.all(out == 0.0)
+                continue
+            _close(out[:, 0], np.full(Hq, chan), 1e-14, "chan")
+            _close(out[:, 1], np.full(Hq, seqid), 1e-14, "seq")
+            _close(out[:, 2], np.full(Hq, (i - 1) / 2.0), 1e-13, "mean pos")
+            _close(out[:, 3], [h * Hkv // Hq for h in range(Hq)], 1e-14, "gqa")
+
+
+def check_attention_against_softmax(O):
+    rng = np.random.default_rng(6)
+    Hq, Hkv, d, S = 6, 3, 8, 9
+    q = rng.standard_normal((Hq, d))
+    K = rng.standard_normal((Hkv, S, d)) * 2
+    V = rng.standard_normal((Hkv, S, d))
+    for i in (1, 4, 9):
+        out = O.channel_attention(q, K, V, i, Hq, Hkv)
+        for h in range(Hq):
+            hk = h // (Hq // Hkv)
+            w = scipy.special.softmax(K[hk, :i] @ q[h] / math.sqrt(d))
+            _close(out[h], w @ V[hk, :i], 1e-12, "softmax attn")
+
+
+# ---------------------------------------------------------------------------
+# Pool
+# ---------------------------------------------------------------------------
+
+def check_pool_selection_router(O):
+    """A router row with one 1 copies one normed source element into one
+    coefficient: pins R, the concat order and the j*L + l output order."""
+    c = _cfg(L=6, D=8, k=3, p=2, p_offset=1, Hq=2, Hkv=1, d=8)
+    W = _weights(c, seed=7)
+    rng = np.random.default_rng(8)
+    N = 3
+    states = rng.standard_normal((N, c.L, c.D))
+    R = [l for l in range(c.L) if l % c.p == c.p_offset]
+    for beta, j, l, r, t in ((0, 2, 5, 1, 3), (1, 0, 1, 2, 7), (1, 1, 0, 0, 0)):
+        Wsel = dict(W)
+        Wr = np.zeros_like(W["Wr"])
+        Wr[beta, j * c.L + l, r * c.D + t] = 1.0
+        Wsel["Wr"] = Wr
+        res = O.pool(c, Wsel, states, np.zeros(N, dtype=np.int64))
+        src = states[:, R[r], :]
+        expect = W["src_norm"][beta][R[r]][t] * src[:, t] / np.sqrt(np.mean(src * src, axis=1) + c.eps)
+        _close(res["coeff"][:, beta, j, l], expect, 1e-13, "selected coefficient")
+        mask = np.ones((2, c.k, c.L), dtype=bool)
+        mask[beta, j, l] = False
+        assert np.all(res["coeff"][:, mask] == 0.0)
+
+
+def check_pool_one_hot_static(O):
+    """One-hot coefficients pick one source: the channel is the double norm
+    of that state; V is its projection, K its normed, rotated projection."""
+    c = _cfg(L=5, D=8, k=2, Hq=2, Hkv=1, d=8)
+    W = _weights(c, seed=9)
+    rng = np.random.default_rng(10)
+    N = 4
+    states = rng.standard_normal((N, c.L, c.D))
+    pos = np.array([0, 3, 17, 250])
+    pick = [[3, 0], [1, 4]]                   # pick[beta][j] = source layer
+    static = np.zeros((2, c.k, c.L))
+    for beta in range(2):
+        for j in range(c.k):
+            static[beta, j, pick[beta][j]] = 1.0
+    res = O.pool(c, W, states, pos, static_coeff=static)
+    for beta in range(2):
+        for j in range(c.k):
+            l = pick[beta][j]
+            ch = _rms(_rms(states[:, l], W["src_norm"][beta][l], c.eps), W["chan_norm"][beta][j], c.eps)
+            _close(res["mixed"][:, beta, j], ch, 1e-12, "double norm")
+            if beta == 0:
+                kt = _rms((ch @ W["Wk"][j].T).reshape(N, 1, c.d), W["k_norm"][j], c.eps)
+                _close(res["K"][:, j], _rope_complex(kt, pos[:, None], c.rope_base), 1e-12, "K")
+            else:
+                _close(res["V"][:, j], (ch @ W["Wv"][j].T).reshape(N, 1, c.d), 1e-12, "V")
+
+
+def check_pool_sign_and_mix(O):
+    """Signed weights: negating a channel's coefficients negates it; a
+    positive scale leaves it unchanged; a two-source mix is the normed sum."""
+    c = _cfg(L=4, D=8, k=2, Hq=2, Hkv=1, d=8, eps=0.0)
+    W = _weights(c, seed=11)
+    rng = np.random.default_rng(12)
+    states = rng.standard_normal((3, c.L, c.D))
+    pos = np.zeros(3, dtype=np.int64)
+    A = rng.standard_normal((2, c.k, c.L))
+    r1 = O.pool(c, W, states, pos, static_coeff=A)
+    r2 = O.pool(c, W, states, pos, static_coeff=-A)
+    r3 = O.pool(c, W, states, pos, static_coeff=3.0 * A)
+    _close(r2["mixed"], -r1["mixed"], 1e-13, "sign")
+    _close(r3["mixed"], r1["mixed"], 1e-12, "scale")
+    # explicit two-term mix
+    S2 = np.zeros((2, c.k, c.L))
+    S2[0, 1, 0], S2[0, 1, 2] = 0.7, -1.3
+    with np.errstate(invalid="ignore"):      # the all-zero channels normalise 0/0 at eps = 0
+        r4 = O.pool(c, W, states, pos, static_coeff=S2)
+    n0 = _rms(states[:, 0], W["src_norm"][0][0], c.eps)
+    n2 = _rms(states[:, 2], W["src_norm"][0][2], c.eps)
+    _close(r4["mixed"][:, 0, 1], _rms(0.7 * n0 - 1.3 * n2, W["chan_norm"][0][1], c.eps), 1e-12, "mix")
+
+
+def check_router_is_linear_in_normed_sources(O):
+    """Coefficients equal W_R^b applied to the concatenated normed R-states,
+    here checked against an explicit double loop over (source, element)."""
+    c = _cfg(L=4, D=6, k=2, p=2, Hq=2, Hkv=1, d=6)
+    W = _weights(c, seed=13)
+    rng = np.random.default_rng(14)
+    states = rng.standard_normal((2, c.L, c.D))
+    res = O.pool(c, W, states, np.zeros(2, dtype=np.int64))
+    R = [0, 2]
+    for n in range(2):
+        for beta in range(2):
+            for j in range(c.k):
+                for l in range(c.L):
+                    acc = 0.0
+                    for ri, src in enumerate(R):
+                        x = states[n, src]
+                        inv = 1.0 / math.sqrt(sum(v * v for v in x) / c.D + c.eps)
+                        for t in range(c.D):
+                            acc += W["Wr"][beta, j * c.L + l, ri * c.D + t] * W["src_norm"][beta][src][t] * x[t] * inv
+                    assert abs(res["coeff"][n, beta, j, l] - acc) <= 1e-12 * max(1.0, abs(acc))
+
+
+# ---------------------------------------------------------------------------
+# Whole model and schedules
+# ---------------------------------------------------------------------------
+
+def check_identity_router_equals_vanilla(O):
+    """k = L with the identity mixture: the fixed point is a vanilla
+    strict-causal Transformer whose layer l reads K/V made from its own input."""
+    c = _cfg(L=3, D=16, k=3, Hq=4, Hkv=2, d=8)
+    W = _weights(c, seed=15)
+    static = np.zeros((2, c.k, c.L))
+    for beta in range(2):
+        static[beta] = np.eye(c.L)
+    tokens = _tokens(c, 2, 6, 0)
+    lg, _, _ = _ar(O, c, W, tokens, static=static)
+    for b in range(2):
+        _close(lg[b], _vanilla_strict_causal(c, W, tokens[b]), 1e-10, "vanilla")
+    lg2, _, _ = _cyclic(O, c, W, tokens, 2, 3, static=static)
+    _close(lg2, lg, 1e-10, "cyclic fixed point")
+
+
+def check_zero_router_is_mlp(O):
+    c = _cfg()
+    W = _weights(c, seed=16)
+    W["Wr"] = np.zeros_like(W["Wr"])
+    tokens = _tokens(c, 2, 5, 1)
+    ref = _mlp_only_stack(c, W, tokens)
+    for g, passes in ((1, 1), (1, 2), (2, 2), (5, 1)):
+        lg, ck, cv = _cyclic(O, c, W, tokens, g, passes)
+        _close(lg, ref, 1e-10, f"zero router g={g}")
+        assert np.all(ck == 0.0) and np.all(cv == 0.0)
+
+
+def check_token0_and_first_jacobi_pass(O):
+    """Token 0 never sees a key; one Jacobi pass from the zero cache gives
+    every token zero attention, since all rows read the same snapshot."""
+    c = _cfg()
+    W = _weights(c, seed=17)
+    tokens = _tokens(c, 2, 6, 2)
+    ref = _mlp_only_stack(c, W, tokens)
+    lg1, _, _ = _cyclic(O, c, W, tokens, 1, 1)
+    _close(lg1, ref, 1e-10, "jacobi pass 1")
+    for g, passes in ((2, 3), (6, 1), (3, 2)):
+        lg, _, _ = _cyclic(O, c, W, tokens, g, passes)
+        _close(lg[:, 0], ref[:, 0], 1e-10, "token 0")
+    lgar, _, _ = _ar(O, c, W, tokens)
+    _close(lgar[:, 0], ref[:, 0], 1e-10, "token 0 AR")
+    # and attention does matter after the first position
+    assert np.max(np.abs(lgar[:, 1:] - ref[:, 1:])) > 1e-3
+
+
+def check_prefix_exactness(O):
+    """After n cyclic passes with g groups from a zero cache, positions
+    i < min(T, n*g) hold the autoregressive values; beyond the prefix they
+    still differ (the snapshot is taken per group)."""
+    c = _cfg()
+    W = _weights(c, seed=18)
+    B, T = 2, 8
+    tokens = _tokens(c, B, T, 3)
+    lgar, kar, var = _ar(O, c, W, tokens)
+    for g in (1, 3, 8):
+        ck, cv = O.new_cache(c, B, T)
+        for n in range(1, -(-T // g) + 1):
+            lg = O.cyclic_pass(c, W, tokens, g, ck, cv, logits="all")
+            P = min(T, n * g)
+            _close(ck[..., :P, :], kar[..., :P, :], 1e-10, f"K prefix g={g} n={n}")
+            _close(cv[..., :P, :], var[..., :P, :], 1e-10, f"V prefix g={g} n={n}")
+            _close(lg[:, :P], lgar[:, :P], 1e-10, f"logits prefix g={g} n={n}")
+            if P < T:
+                assert np.max(np.abs(ck[..., P:, :] - kar[..., P:, :])) > 1e-6, "beyond prefix"
+        _close(lg, lgar, 1e-10, f"converged g={g}")
+
+
+def check_bruteforce_T4(O):
+    """Brute force on 4-token inputs: every g in 1..4 and pass count 1..4."""
+    c = _cfg(L=3, D=8, k=2, Hq=2, Hkv=1, d=8, F=12, V=16)
+    for seed in range(4):
+        W = _weights(c, seed=100 + seed)
+        tokens = _tokens(c, 1, 4, 10 + seed)
+        lgar, kar, _ = _ar(O, c, W, tokens)
+        for g in (1, 2, 3, 4):
+            ck, cv = O.new_cache(c, 1, 4)
+            for n in range(1, 5):
+                lg = O.cyclic_pass(c, W, tokens, g, ck, cv, logits="all")
+                P = min(4, n * g)
+                _close(lg[:, :P], lgar[:, :P], 1e-10, f"bf g={g} n={n}")
+                _close(ck[..., :P, :], kar[..., :P, :], 1e-10, f"bf K g={g} n={n}")
+
+
+def check_partial_pass_positions(O):
+    """Groups q_begin..q_end-1 write exactly the positions i with
+    q_begin <= i mod g < q_end, in every sequence and channel."""
+    c = _cfg()
+    W = _weights(c, seed=19)
+    B, T, g = 2, 11, 4
+    tokens = _tokens(c, B, T, 4)
+    for qb, qe in ((0, 2), (1, 4), (3, 4)):
+        ck = np.full((B, c.k, c.Hkv, T, c.d), 123.25)
+        cv = np.full((B, c.k, c.Hkv, T, c.d), 123.25)
+        O.cyclic_pass(c, W, tokens, g, ck, cv, q_begin=qb, q_end=qe)
+        changed = np.any(ck != 123.25, axis=(1, 2, 4)) | np.any(cv != 123.25, axis=(1, 2, 4))
+        expect = np.array([[qb <= (i % g) < qe for i in range(T)]] * B)
+        assert np.array_equal(changed, expect), (qb, qe, changed)
+
+
+def check_last_logits_and_decode(O):
+    """'last' logits equal the final position of 'all'; a decode step after a
+    converged prefill equals the autoregressive logits of the next token."""
+    c = _cfg()
+    W = _weights(c, seed=20)
+    B, T = 2, 7
+    tokens = _tokens(c, B, T, 5)
+    lgar, _, _ = _ar(O, c, W, tokens)
+    ck, cv = O.new_cache(c, B, T)
+    for _ in range(3):
+        last = O.cyclic_pass(c, W, tokens[:, :6], 2, ck, cv, logits="last")
+    _close(last, lgar[:, 5], 1e-10, "last")
+    lg = O.decode_step(c, W, tokens[:, 6], 6, ck, cv)
+    _close(lg, lgar[:, 6], 1e-10, "decode")
+
+
+ALL_CHECKS = [
+    check_rmsnorm_closed_forms,
+    check_rope_closed_forms,
+    check_silu,
+    check_indexing_rules,
+    check_attention_uniform_closed_form,
+    check_attention_against_softmax,
+    check_pool_selection_router,
+    check_pool_one_hot_static,
+    check_pool_sign_and_mix,
+    check_router_is_linear_in_normed_sources,
+    check_identity_router_equals_vanilla,
+    check_zero_router_is_mlp,
+    check_token0_and_first_jacobi_pass,
+    check_prefix_exactness,
+    check_bruteforce_T4,
+    check_partial_pass_positions,
+    check_last_logits_and_decode,
+]

@@ -1,0 +1,102 @@
+"""Plant plausible mistakes in the CPU oracle and check that the pins catch
+each one. A mutant replaces one oracle function by a copy of its source with
+one edit (a dropped term, a wrong sign, index or order); the pin suite must
+then fail somewhere. This is how the pins are shown to be strong enough."""
+
+import inspect
+
+import numpy as np
+import pytest
+
+import oracle.whitematter as O
+from tests import oracle_pins
+
+MUTANTS = [
+    # (id, function, old text, new text)
+    ("rope_sign", "rope", "x1 * c - x2 * s", "x1 * c + x2 * s"),
+    ("rope_theta", "rope", "-2.0 * np.arange", "-1.0 * np.arange"),
+    ("rope_pairing", "rope", "half = d // 2", "half = d // 2 - 1 if d > 2 else 1"),
+    ("rmsnorm_eps", "rmsnorm", "np.sqrt(ms + eps)", "(np.sqrt(ms) + eps)"),
+    ("rmsnorm_sum", "rmsnorm", "np.mean(x * x, axis=-1", "np.sum(x * x, axis=-1"),
+    ("silu_sigmoid", "silu", "return x / (1.0 + np.exp(-x))", "return 1.0 / (1.0 + np.exp(-x))"),
+    ("router_offset", "router_sources", "l % cfg.p == cfg.p_offset", "l % cfg.p == (cfg.p_offset + 1) % cfg.p"),
+    ("channel_shift", "channel_of_layer", "return l % cfg.k", "return (l + 1) % cfg.k"),
+    ("groups_contiguous", "group_positions", "np.arange(q, T, g, dtype=np.int64)",
+     "np.arange(q * -(-T // g), min(T, (q + 1) * -(-T // g)), dtype=np.int64)"),
+    ("attn_self_visible", "channel_attention", "    if n_keys <= 0:\n        return out",
+     "    n_keys = n_keys + 1\n    if n_keys <= 0:\n        return out"),
+    ("attn_gqa_modulo", "channel_attention", "hk = (h * Hkv) // Hq", "hk = h % Hkv"),
+    ("attn_no_scale", "channel_attention", "z = keys @ q[h] / math.sqrt(d)", "z = keys @ q[h]"),
+    ("layer_no_attn_residual", "consumer_layer", "h2 = h + o.reshape", "h2 = 0.0 * h + o.reshape"),
+    ("layer_swap_gate_up", "consumer_layer", "silu(gate) * up", "silu(up) * gate"),
+    ("layer_no_qnorm", "consumer_layer", 'q = rmsnorm(q, W["q_norm"][l], cfg.eps)', 'q = q * _f64(W["q_norm"][l])'),
+    ("layer_no_q_rope", "consumer_layer", "q = rope(q, _f64(pos)[:, None], cfg.rope_base)", "q = q"),
+    ("pool_coeff_transposed", "pool", "reshape(N, k, L)", "reshape(N, L, k).transpose(0, 2, 1)"),
+    ("pool_router_raw_states", "pool", "x = n[:, R, :]", "x = states[:, R, :]"),
+    ("pool_mix_raw_states", "pool", 'np.einsum("njl,nld->njd", a, n)', 'np.einsum("njl,nld->njd", a, states)'),
+    ("pool_no_channel_norm", "pool", 'mixed[:, beta] = rmsnorm(m, W["chan_norm"][beta], cfg.eps)',
+     'mixed[:, beta] = m * _f64(W["chan_norm"][beta])'),
+    ("pool_knorm_after_rope", "pool",
+     'kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)\n        K[:, j] = rope(kt, _f64(pos)[:, None], cfg.rope_base)',
+     'kt = rope(kt, _f64(pos)[:, None], cfg.rope_base)\n        K[:, j] = rmsnorm(kt, W["k_norm"][j], cfg.eps)'),
+    ("pool_v_uses_wk", "pool", 'W["Wv"][j]', 'W["Wk"][j]'),
+    ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
+     'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
+    ("states_are_outputs", "run_rows", "        states[:, l] = h\n        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)",
+     "        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)\n        states[:, l] = h"),
+    ("write_shifted", "_write", "cache_k[int(seq[r]), :, :, int(pos[r]), :] = K[r]",
+     "cache_k[int(seq[r]), :, :, (int(pos[r]) + 1) % cache_k.shape[3], :] = K[r]"),
+    ("groups_reversed", "cyclic_pass", "for q in range(q_begin, q_end):", "for q in reversed(range(q_begin, q_end)):"),
+    ("decode_sees_self", "decode_step", "pos = np.full(B, t, dtype=np.int64)", "pos = np.full(B, t + 1, dtype=np.int64)"),
+]
+
+
+def _no_snapshot_cyclic_pass(cfg, W, tokens, g, cache_k, cache_v, q_begin=0, q_end=None,
+                             logits=None, static_coeff=None):
+    """Mutant: rows of a group are run one at a time and written immediately,
+    so later rows of the same group see earlier rows' updates."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    B, T = tokens.shape
+    q_end = g if q_end is None else q_end
+    out = np.zeros((B, T, cfg.V)) if logits == "all" else (np.zeros((B, cfg.V)) if logits == "last" else None)
+    for q in range(q_begin, q_end):
+        for i in O.group_positions(T, g, q):
+            for b in range(B):
+                res, lg, _ = O.run_rows(cfg, W, tokens[b:b + 1, i], [b], [i], cache_k, cache_v,
+                                        logits is not None, static_coeff)
+                O._write(cache_k, cache_v, [b], [i], res["K"], res["V"])
+                if logits == "all":
+                    out[b, i] = lg[0]
+                elif logits == "last" and i == T - 1:
+                    out[b] = lg[0]
+    return out
+
+
+def _mutant(fname, old, new):
+    src = inspect.getsource(getattr(O, fname))
+    assert old in src, f"mutation text not found in {fname}"
+    ns = {}
+    exec(compile(src.replace(old, new, 1), f"<mutant of {fname}>", "exec"), O.__dict__, ns)
+    return ns[fname]
+
+
+def _caught():
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            with np.errstate(all="ignore"):
+                check(O)
+        except Exception:          # AssertionError, or the mutant crashing
+            return check.__name__
+    return None
+
+
+@pytest.mark.parametrize("mut", MUTANTS, ids=lambda m: m[0])
+def test_mutant_is_caught(mut, monkeypatch):
+    _, fname, old, new = mut
+    monkeypatch.setattr(O, fname, _mutant(fname, old, new))
+    assert _caught() is not None, f"no pin caught mutant {mut[0]}"
+
+
+def test_snapshot_violation_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "cyclic_pass", _no_snapshot_cyclic_pass)
+    assert _caught() is not None
