@@ -1,0 +1,436 @@
+// libwm C ABI: argument validation, workspace layout and the host-side
+// drivers of the pool, the cyclic Gauss-Seidel pass and the decode step.
+// Every arithmetic step runs in the kernels launched from here.
+#include <cstring>
+
+#include "kernels.h"
+
+using namespace wm;
+
+namespace {
+
+enum Buf {
+  B_FLAGS, B_ROPE, B_TOK, B_SEQ, B_POS, B_ROWMAP, B_STASH, B_HMID, B_HL, B_XN, B_Q, B_O,
+  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_LASTX, NBUF
+};
+
+struct Layout {
+  size_t off[NBUF];
+  size_t total;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int count_nR(const wm_config& c) {
+  int n = 0;
+  for (int l = 0; l < c.L; ++l) n += (l % c.p) == c.p_offset;
+  return n;
+}
+
+Layout make_layout(const wm_config& c, long long N, long long Tmax) {
+  const size_t es = elem_size(c.dtype);
+  const long long nR = count_nR(c);
+  size_t sz[NBUF];
+  sz[B_FLAGS] = 256;
+  sz[B_ROPE] = (size_t)Tmax * (c.d / 2) * sizeof(float2);
+  sz[B_TOK] = sz[B_SEQ] = sz[B_POS] = sz[B_ROWMAP] = (size_t)N * 4;
+  sz[B_STASH] = (size_t)N * c.L * c.D * es;
+  sz[B_HMID] = sz[B_HL] = sz[B_XN] = sz[B_LASTX] = (size_t)N * c.D * es;
+  sz[B_Q] = sz[B_O] = (size_t)N * c.Hq * c.d * es;
+  sz[B_ACT] = (size_t)N * c.F * es;
+  sz[B_RIN] = (size_t)2 * N * nR * c.D * es;
+  sz[B_INV] = (size_t)N * c.L * 4;
+  sz[B_COEFF] = (size_t)N * 2 * c.k * c.L * 4;
+  sz[B_MIXED] = (size_t)N * 2 * c.k * c.D * es;
+  Layout lay;
+  size_t o = 0;
+  for (int i = 0; i < NBUF; ++i) {
+    lay.off[i] = o;
+    o += align256(sz[i]);
+  }
+  lay.total = o;
+  return lay;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+wm_status check_config(const wm_config* c) {
+  if (!c) return WM_ERR_INVALID_ARG;
+  if (c->L < 1 || c->L > 256 || c->D < 64 || c->D % 64 || c->D > 8192) return WM_ERR_INVALID_ARG;
+  if (c->k < 1 || c->k > c->L || c->p < 1 || c->p_offset < 0 || c->p_offset >= c->p)
+    return WM_ERR_INVALID_ARG;
+  if (c->Hq < 1 || c->Hkv < 1 || c->Hq % c->Hkv) return WM_ERR_INVALID_ARG;
+  if (c->F < 64 || c->F % 64 || c->V < 1 || !(c->eps >= 0.f) || !(c->rope_base > 0.f))
+    return WM_ERR_INVALID_ARG;
+  if (c->dtype != WM_F32 && c->dtype != WM_BF16) return WM_ERR_INVALID_ARG;
+  if (c->d != 64 && c->d != 128) return WM_ERR_UNSUPPORTED;
+  if (count_nR(*c) < 1) return WM_ERR_INVALID_ARG;
+  if (c->flags & ~(uint32_t)WM_FLAG_SIMT_GEMM) return WM_ERR_INVALID_ARG;
+  return WM_OK;
+}
+
+wm_status check_weights(const wm_weights* w) {
+  if (!w) return WM_ERR_INVALID_ARG;
+  const void* ps[] = {w->embed, w->lm_head, w->final_norm, w->in_norm, w->post_norm,
+                      w->q_norm, w->Wq, w->Wo, w->Wgate, w->Wup, w->Wdown, w->src_norm,
+                      w->Wr, w->chan_norm, w->Wk, w->Wv, w->k_norm};
+  for (const void* p : ps)
+    if (!p || !aligned16(p)) return WM_ERR_INVALID_ARG;
+  if (w->static_coeff && !aligned16(w->static_coeff)) return WM_ERR_INVALID_ARG;
+  return WM_OK;
+}
+
+wm_status check_ws(const wm_config& c, void* ws, size_t ws_bytes, long long N, long long Tmax) {
+  if (!ws || ((uintptr_t)ws & 255u)) return WM_ERR_WORKSPACE;
+  if (ws_bytes < make_layout(c, N, Tmax).total) return WM_ERR_WORKSPACE;
+  return WM_OK;
+}
+
+struct Ctx {
+  const wm_config* c;
+  const wm_weights* w;
+  char* ws;
+  Layout lay;
+  cudaStream_t st;
+  int nR;
+  bool tc;
+  size_t es;
+  template <typename T> T* buf(Buf b) const { return reinterpret_cast<T*>(ws + lay.off[b]); }
+  const char* wp(const void* p, long long elems) const {
+    return static_cast<const char*>(p) + elems * (long long)es;
+  }
+  uint32_t* flags() const { return buf<uint32_t>(B_FLAGS); }
+};
+
+Ctx make_ctx(const wm_config* c, const wm_weights* w, void* ws, long long N, long long Tmax,
+             void* stream) {
+  Ctx x;
+  x.c = c;
+  x.w = w;
+  x.ws = static_cast<char*>(ws);
+  x.lay = make_layout(*c, N, Tmax);
+  x.st = static_cast<cudaStream_t>(stream);
+  x.nR = count_nR(*c);
+  x.tc = c->dtype == WM_BF16 && !(c->flags & WM_FLAG_SIMT_GEMM);
+  x.es = elem_size(c->dtype);
+  return x;
+}
+
+void gemm(const Ctx& x, const GemmDesc& g) {
+  if (x.tc && gemm_tc_supported(g)) {
+    if (launch_gemm_tc(g, x.st) == cudaSuccess) return;
+  }
+  launch_gemm_simt(x.c->dtype, g, x.st);
+}
+
+Epi base_epi(const Ctx& x) {
+  Epi e;
+  e.flags = x.flags();
+  e.eps = x.c->eps;
+  e.d = x.c->d;
+  e.rope = x.buf<float2>(B_ROPE);
+  return e;
+}
+
+// Layer stack of N rows whose h^0 is already in stash[:, 0]. Layer l reads
+// stash[:, l], writes stash[:, l+1] (or h^L), and emits inv_rms / router
+// inputs of its input state. The last layer's body runs only if requested.
+void run_stack(const Ctx& x, int N, bool last_layer, void* cache_k, void* cache_v, int B,
+               int Tmax, bool emit_rin) {
+  const wm_config& c = *x.c;
+  const wm_weights& w = *x.w;
+  const long long LD = (long long)c.L * c.D;
+  const int Hd = c.Hq * c.d;
+  char* stash = x.buf<char>(B_STASH);
+  for (int l = 0; l < c.L; ++l) {
+    const bool body = l < c.L - 1 || last_layer;
+    char* h_in = stash + (long long)l * c.D * x.es;
+    launch_norm_emit(c.dtype, stash, LD, c.D, N, l, 1, c.D, c.L, w.in_norm,
+                     body ? x.buf<void>(B_XN) : nullptr, x.buf<float>(B_INV), w.src_norm,
+                     emit_rin ? x.buf<void>(B_RIN) : nullptr, x.nR, c.p, c.p_offset, c.eps, x.st);
+    if (!body) break;
+    {  // Q projection + per-head q-norm + RoPE
+      GemmDesc g;
+      g.M = N; g.N = Hd; g.K = c.D;
+      g.A = x.buf<void>(B_XN); g.lda = c.D;
+      g.B = x.wp(w.Wq, (long long)l * Hd * c.D); g.ldb = c.D;
+      g.epi = base_epi(x);
+      g.epi.mode = EPI_QNORM_ROPE;
+      g.epi.C = x.buf<void>(B_Q); g.epi.ldc = Hd;
+      g.epi.gain = x.wp(w.q_norm, (long long)l * c.d);
+      g.epi.pos = x.buf<int>(B_POS);
+      g.epi.Tmax = Tmax;
+      gemm(x, g);
+    }
+    {  // attention to channel l mod k over s < pos
+      AttnArgs a;
+      a.q = x.buf<void>(B_Q); a.N = N; a.seq = x.buf<int32_t>(B_SEQ); a.pos = x.buf<int32_t>(B_POS);
+      a.channel = l % c.k; a.cache_k = cache_k; a.cache_v = cache_v;
+      a.B = B; a.k = c.k; a.Hq = c.Hq; a.Hkv = c.Hkv; a.d = c.d; a.Tmax = Tmax;
+      a.out = x.buf<void>(B_O); a.flags = x.flags();
+      launch_attention(c.dtype, a, !x.tc, x.st);
+    }
+    {  // O projection + residual
+      GemmDesc g;
+      g.M = N; g.N = c.D; g.K = Hd;
+      g.A = x.buf<void>(B_O); g.lda = Hd;
+      g.B = x.wp(w.Wo, (long long)l * c.D * Hd); g.ldb = Hd;
+      g.epi = base_epi(x);
+      g.epi.mode = EPI_RESID;
+      g.epi.R = h_in; g.epi.ldr = LD;
+      g.epi.C = x.buf<void>(B_HMID); g.epi.ldc = c.D;
+      gemm(x, g);
+    }
+    launch_rmsnorm(c.dtype, x.buf<void>(B_HMID), c.D, 0, 1, N, c.D,
+                   x.wp(w.post_norm, (long long)l * c.D), x.buf<void>(B_XN), c.eps, x.st);
+    {  // gate/up + SwiGLU
+      GemmDesc g;
+      g.M = N; g.N = c.F; g.K = c.D;
+      g.A = x.buf<void>(B_XN); g.lda = c.D;
+      g.B = x.wp(w.Wgate, (long long)l * c.F * c.D); g.ldb = c.D;
+      g.B2 = x.wp(w.Wup, (long long)l * c.F * c.D);
+      g.epi = base_epi(x);
+      g.epi.mode = EPI_SWIGLU;
+      g.epi.C = x.buf<void>(B_ACT); g.epi.ldc = c.F;
+      gemm(x, g);
+    }
+    {  // down + residual -> next state
+      GemmDesc g;
+      g.M = N; g.N = c.D; g.K = c.F;
+      g.A = x.buf<void>(B_ACT); g.lda = c.F;
+      g.B = x.wp(w.Wdown, (long long)l * c.D * c.F); g.ldb = c.F;
+      g.epi = base_epi(x);
+      g.epi.mode = EPI_RESID;
+      g.epi.R = x.buf<void>(B_HMID); g.epi.ldr = c.D;
+      if (l + 1 < c.L) {
+        g.epi.C = stash + (long long)(l + 1) * c.D * x.es; g.epi.ldc = LD;
+      } else {
+        g.epi.C = x.buf<void>(B_HL); g.epi.ldc = c.D;
+      }
+      gemm(x, g);
+    }
+  }
+}
+
+// Router (or static weights) -> coefficients; mix + channel norm; channel
+// projections with K-norm + RoPE; scatter into the cache at (seq, pos).
+void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* coeff,
+              void* mixed, void* cache_k, void* cache_v, int B, int Tmax) {
+  const wm_config& c = *x.c;
+  const wm_weights& w = *x.w;
+  const int kL = c.k * c.L;
+  if (w.static_coeff) {
+    launch_broadcast_coeff(w.static_coeff, N, 2 * kL, coeff, x.st);
+  } else {
+    GemmDesc g;
+    g.M = N; g.N = kL; g.K = x.nR * c.D; g.batch = 2;
+    g.A = x.buf<void>(B_RIN); g.lda = (long long)x.nR * c.D; g.a_bstride = (long long)N * x.nR * c.D;
+    g.B = w.Wr; g.ldb = (long long)x.nR * c.D; g.b_bstride = (long long)kL * x.nR * c.D;
+    g.epi = base_epi(x);
+    g.epi.mode = EPI_STORE;
+    g.epi.out_f32 = 1;
+    g.epi.C = coeff; g.epi.ldc = 2LL * kL; g.epi.c_bstride = kL;
+    gemm(x, g);
+  }
+  MixArgs m;
+  m.stash = states; m.ld_row = ld_row; m.inv = x.buf<float>(B_INV); m.coeff = coeff;
+  m.src_norm = w.src_norm; m.chan_norm = w.chan_norm; m.mixed = mixed;
+  m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
+  launch_mix(c.dtype, m, !x.tc, x.st);
+  for (int branch = 0; branch < 2; ++branch) {
+    GemmDesc g;
+    g.M = N; g.N = c.Hkv * c.d; g.K = c.D; g.batch = c.k;
+    g.A = static_cast<const char*>(mixed) + (long long)branch * c.k * c.D * x.es;
+    g.lda = 2LL * c.k * c.D; g.a_bstride = c.D;
+    g.B = branch == 0 ? w.Wk : w.Wv; g.ldb = c.D; g.b_bstride = (long long)c.Hkv * c.d * c.D;
+    g.epi = base_epi(x);
+    g.epi.mode = EPI_KV;
+    g.epi.kv_branch = branch;
+    g.epi.gain = w.k_norm; g.epi.gain_bstride = c.d;
+    g.epi.pos = x.buf<int>(B_POS); g.epi.seq = x.buf<int>(B_SEQ);
+    g.epi.cache_k = cache_k; g.epi.cache_v = cache_v;
+    g.epi.k = c.k; g.epi.Hkv = c.Hkv; g.epi.Tmax = Tmax; g.epi.B = B;
+    gemm(x, g);
+  }
+}
+
+wm_status finish() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? WM_OK : WM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t wm_abi_version(void) { return WM_ABI_VERSION; }
+
+const char* wm_status_string(wm_status s) {
+  switch (s) {
+    case WM_OK: return "ok";
+    case WM_ERR_INVALID_ARG: return "invalid argument";
+    case WM_ERR_UNSUPPORTED: return "unsupported configuration";
+    case WM_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case WM_ERR_CUDA: return "CUDA error";
+    case WM_ERR_TIMEOUT: return "device-side wait timed out";
+    case WM_ERR_DEVICE_BOUNDS: return "device-side index check failed";
+  }
+  return "unknown status";
+}
+
+size_t wm_workspace_size(const wm_config* cfg, int32_t max_rows, int32_t Tmax) {
+  if (check_config(cfg) != WM_OK || max_rows < 1 || Tmax < 1) return 0;
+  return make_layout(*cfg, max_rows, Tmax).total;
+}
+
+wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* states, int32_t N,
+                      const int32_t* seq, const int32_t* pos, void* cache_k, void* cache_v,
+                      int32_t B, int32_t Tmax, float* coeff_out, void* mixed_out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (N < 1 || B < 1 || Tmax < 1 || !states || !seq || !pos || !cache_k || !cache_v)
+    return WM_ERR_INVALID_ARG;
+  if (!aligned16(states) || !aligned16(cache_k) || !aligned16(cache_v) ||
+      (coeff_out && !aligned16(coeff_out)) || (mixed_out && !aligned16(mixed_out)))
+    return WM_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes, N, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, w, ws, N, Tmax, stream);
+  const wm_config& c = *cfg;
+  cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
+  launch_norm_emit(c.dtype, states, (long long)c.L * c.D, c.D, N, 0, c.L, c.D, c.L, nullptr,
+                   nullptr, x.buf<float>(B_INV), w->src_norm,
+                   w->static_coeff ? nullptr : x.buf<void>(B_RIN), x.nR, c.p, c.p_offset, c.eps,
+                   x.st);
+  run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
+           mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  return finish();
+}
+
+wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const int32_t* seq,
+                          const int32_t* pos, int32_t channel, const void* cache_k,
+                          const void* cache_v, int32_t B, int32_t Tmax, void* out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if (N < 1 || B < 1 || Tmax < 1 || !q || !seq || !pos || !cache_k || !cache_v || !out)
+    return WM_ERR_INVALID_ARG;
+  if (channel < 0 || channel >= cfg->k) return WM_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(cache_k) || !aligned16(cache_v))
+    return WM_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes, N, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, nullptr, ws, N, Tmax, stream);
+  AttnArgs a;
+  a.q = q; a.N = N; a.seq = seq; a.pos = pos; a.channel = channel;
+  a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
+  a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
+  launch_attention(cfg->dtype, a, !x.tc, x.st);
+  return finish();
+}
+
+wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
+                         int32_t B, int32_t T, int32_t g, int32_t q_begin, int32_t q_end,
+                         void* cache_k, void* cache_v, int32_t Tmax, float* logits,
+                         int32_t logits_mode, void* ws, size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (!tokens || !cache_k || !cache_v || B < 1 || T < 1 || T > Tmax || g < 1 || g > T)
+    return WM_ERR_INVALID_ARG;
+  if (q_begin < 0 || q_end < q_begin || q_end > g) return WM_ERR_INVALID_ARG;
+  if (logits_mode < WM_LOGITS_NONE || logits_mode > WM_LOGITS_ALL) return WM_ERR_INVALID_ARG;
+  if (logits_mode != WM_LOGITS_NONE && (!logits || !aligned16(logits))) return WM_ERR_INVALID_ARG;
+  if (!aligned16(cache_k) || !aligned16(cache_v)) return WM_ERR_INVALID_ARG;
+  const long long nq_max = (T + g - 1) / g;
+  if ((long long)B * nq_max > (1LL << 26)) return WM_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes, B * nq_max, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, w, ws, B * nq_max, Tmax, stream);
+  const wm_config& c = *cfg;
+  launch_rope_table(x.buf<float2>(B_ROPE), 0, T, c.d, c.rope_base, x.st);
+  for (int q = q_begin; q < q_end; ++q) {
+    const int nq = (T - q + g - 1) / g;
+    const int N = B * nq;
+    launch_group_rows(tokens, B, T, g, q, nq, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
+                      x.buf<int32_t>(B_POS), x.buf<int32_t>(B_ROWMAP), x.st);
+    launch_embed(c.dtype, x.buf<int32_t>(B_TOK), N, w->embed, c.V, c.D, x.buf<void>(B_STASH),
+                 (long long)c.L * c.D, x.flags(), x.st);
+    const bool has_last = (T - 1) % g == q;
+    const bool want = logits_mode == WM_LOGITS_ALL || (logits_mode == WM_LOGITS_LAST && has_last);
+    run_stack(x, N, want, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+    if (want) {
+      GemmDesc lg;
+      lg.N = c.V; lg.K = c.D; lg.B = w->lm_head; lg.ldb = c.D;
+      lg.epi = base_epi(x);
+      lg.epi.mode = EPI_STORE;
+      lg.epi.out_f32 = 1;
+      lg.epi.C = logits; lg.epi.ldc = c.V;
+      if (logits_mode == WM_LOGITS_ALL) {
+        launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, N, c.D, w->final_norm,
+                       x.buf<void>(B_LASTX), c.eps, x.st);
+        lg.M = N; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+        lg.epi.rowmap = x.buf<int>(B_ROWMAP);
+      } else {
+        launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, (T - 1 - q) / g, nq, B, c.D,
+                       w->final_norm, x.buf<void>(B_LASTX), c.eps, x.st);
+        lg.M = B; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+      }
+      gemm(x, lg);
+    }
+    run_pool(x, N, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
+             x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  }
+  return finish();
+}
+
+wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
+                         int32_t B, int32_t pos, void* cache_k, void* cache_v, int32_t Tmax,
+                         float* logits, void* ws, size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (!tokens || !cache_k || !cache_v || !logits || B < 1 || pos < 0 || pos >= Tmax)
+    return WM_ERR_INVALID_ARG;
+  if (!aligned16(cache_k) || !aligned16(cache_v) || !aligned16(logits)) return WM_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes, B, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, w, ws, B, Tmax, stream);
+  const wm_config& c = *cfg;
+  launch_rope_table(x.buf<float2>(B_ROPE), pos, pos + 1, c.d, c.rope_base, x.st);
+  launch_decode_rows(tokens, B, pos, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
+                     x.buf<int32_t>(B_POS), x.st);
+  launch_embed(c.dtype, x.buf<int32_t>(B_TOK), B, w->embed, c.V, c.D, x.buf<void>(B_STASH),
+               (long long)c.L * c.D, x.flags(), x.st);
+  run_stack(x, B, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+  launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, B, c.D, w->final_norm,
+                 x.buf<void>(B_LASTX), c.eps, x.st);
+  GemmDesc lg;
+  lg.M = B; lg.N = c.V; lg.K = c.D;
+  lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+  lg.B = w->lm_head; lg.ldb = c.D;
+  lg.epi = base_epi(x);
+  lg.epi.mode = EPI_STORE;
+  lg.epi.out_f32 = 1;
+  lg.epi.C = logits; lg.epi.ldc = c.V;
+  gemm(x, lg);
+  run_pool(x, B, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
+           x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  return finish();
+}
+
+wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream) {
+  if (!ws || ws_bytes < 256 || ((uintptr_t)ws & 255u) || !flags_out) return WM_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t f = 0;
+  if (cudaMemcpyAsync(&f, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return WM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return WM_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, 4, st) != cudaSuccess) return WM_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return WM_ERR_CUDA;
+  *flags_out = f;
+  if (f & FLAG_TIMEOUT) return WM_ERR_TIMEOUT;
+  if (f & (FLAG_BAD_TOKEN | FLAG_BAD_SEQ | FLAG_BAD_POS)) return WM_ERR_DEVICE_BOUNDS;
+  return WM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,227 @@
+// Element-wise and row-wise kernels: RoPE table, row metadata of a group,
+// embedding gather, RMSNorm with the pool's per-source emissions.
+#include "kernels.h"
+
+namespace wm {
+
+// 16-byte vector load/store of the storage type as floats.
+template <typename S> struct VecT { static constexpr int N = 16 / sizeof(S); };
+
+__device__ __forceinline__ void ld_vec(const float* p, float* v) {
+  const float4 x = *reinterpret_cast<const float4*>(p);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+}
+__device__ __forceinline__ void ld_vec(const __nv_bfloat16* p, float* v) {
+  const uint4 x = *reinterpret_cast<const uint4*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x; v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void st_vec(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void st_vec(__nv_bfloat16* p, const float* v) {
+  uint4 x;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = x;
+}
+
+// ---------------------------------------------------------------------------
+// RoPE table: tab[pos][t] = (cos, sin)(pos * base^(-2t/d)), angles in fp64.
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* tab, int p0, int p1, int d, double base) {
+  const int half = d >> 1;
+  const long long n = (long long)(p1 - p0) * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int pos = p0 + (int)(idx / half), t = (int)(idx % half);
+    const double theta = pow(base, -2.0 * (double)t / (double)d);
+    double s, c;
+    sincos((double)pos * theta, &s, &c);
+    tab[(long long)pos * half + t] = make_float2((float)c, (float)s);
+  }
+}
+
+void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStream_t st) {
+  const long long n = (long long)(p1 - p0) * (d / 2);
+  if (n <= 0) return;
+  const int blocks = (int)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184);
+  rope_table_kernel<<<blocks, 256, 0, st>>>(tab, p0, p1, d, (double)base);
+}
+
+// ---------------------------------------------------------------------------
+// Rows of cyclic group q: row r = b * nq + u holds position i = q + u * g.
+// ---------------------------------------------------------------------------
+__global__ void group_rows_kernel(const int32_t* __restrict__ tokens, int B, int T, int g, int q,
+                                  int nq, int32_t* tok, int32_t* seq, int32_t* pos,
+                                  int32_t* rowmap) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= B * nq) return;
+  const int b = r / nq, u = r % nq, i = q + u * g;
+  tok[r] = tokens[(long long)b * T + i];
+  seq[r] = b;
+  pos[r] = i;
+  if (rowmap) rowmap[r] = b * T + i;
+}
+
+void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq, int32_t* tok,
+                       int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st) {
+  const int n = B * nq;
+  group_rows_kernel<<<(n + 255) / 256, 256, 0, st>>>(tokens, B, T, g, q, nq, tok, seq, pos, rowmap);
+}
+
+__global__ void decode_rows_kernel(const int32_t* __restrict__ tokens, int B, int t, int32_t* tok,
+                                   int32_t* seq, int32_t* pos) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= B) return;
+  tok[r] = tokens[r];
+  seq[r] = r;
+  pos[r] = t;
+}
+
+void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32_t* seq,
+                        int32_t* pos, cudaStream_t st) {
+  decode_rows_kernel<<<(B + 255) / 256, 256, 0, st>>>(tokens, B, t, tok, seq, pos);
+}
+
+// ---------------------------------------------------------------------------
+// h^0 = embed[token]; an out-of-range id writes zeros and sets a flag.
+// ---------------------------------------------------------------------------
+template <typename S>
+__global__ void embed_kernel(const int32_t* __restrict__ tok, const S* __restrict__ embed, int V,
+                             int D, S* __restrict__ out, long long ld_out, uint32_t* flags) {
+  constexpr int VN = VecT<S>::N;
+  const int r = blockIdx.x;
+  const int id = tok[r];
+  const bool ok = id >= 0 && id < V;
+  if (!ok && threadIdx.x == 0) atomicOr(flags, FLAG_BAD_TOKEN);
+  S* o = out + (long long)r * ld_out;
+  const S* e = embed + (long long)(ok ? id : 0) * D;
+  for (int c = threadIdx.x * VN; c < D; c += blockDim.x * VN) {
+    if (ok) {
+      *reinterpret_cast<uint4*>(o + c) = *reinterpret_cast<const uint4*>(e + c);
+    } else {
+      *reinterpret_cast<uint4*>(o + c) = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V, int D, void* out,
+                  long long ld_out, uint32_t* flags, cudaStream_t st) {
+  if (N <= 0) return;
+  WM_DISPATCH_S(dtype, embed_kernel<S><<<N, 128, 0, st>>>(tok, (const S*)embed, V, D, (S*)out,
+                                                         ld_out, flags));
+}
+
+// ---------------------------------------------------------------------------
+// Layer-input RMSNorm with the pool's emissions (one block per (row, layer)).
+// ---------------------------------------------------------------------------
+template <typename S>
+__global__ void norm_emit_kernel(const S* __restrict__ X, long long ldx_row, long long ldx_l,
+                                 int l0, int D, int L, const S* __restrict__ gain_in,
+                                 S* __restrict__ xn, float* __restrict__ inv_out,
+                                 const S* __restrict__ src_norm, S* __restrict__ rin, int N,
+                                 int nR, int p, int p_off, float eps) {
+  constexpr int VN = VecT<S>::N;
+  __shared__ float red[32];
+  const int r = blockIdx.x, l = l0 + blockIdx.y;
+  const S* x = X + (long long)r * ldx_row + (long long)l * ldx_l;
+  float ss = 0.f;
+  for (int c = threadIdx.x * VN; c < D; c += blockDim.x * VN) {
+    float v[VN];
+    ld_vec(x + c, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) ss += v[i] * v[i];
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)D + eps);
+  if (threadIdx.x == 0) inv_out[(long long)r * L + l] = inv;
+  const bool in_R = rin != nullptr && (l % p) == p_off;
+  const int ridx = (l - p_off) / p;
+  if (xn == nullptr && !in_R) return;
+  const long long rin_b = (long long)N * nR * D;
+  for (int c = threadIdx.x * VN; c < D; c += blockDim.x * VN) {
+    float v[VN], o[VN], gv[VN];
+    ld_vec(x + c, v);
+    if (xn) {
+      ld_vec(gain_in + (long long)l * D + c, gv);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) o[i] = v[i] * inv * gv[i];
+      st_vec(xn + (long long)r * D + c, o);
+    }
+    if (in_R) {
+#pragma unroll
+      for (int beta = 0; beta < 2; ++beta) {
+        ld_vec(src_norm + ((long long)beta * L + l) * D + c, gv);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) o[i] = v[i] * inv * gv[i];
+        st_vec(rin + beta * rin_b + (long long)r * nR * D + (long long)ridx * D + c, o);
+      }
+    }
+  }
+}
+
+void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx_l, int N, int l0,
+                      int nl, int D, int L, const void* gain_in, void* xn, float* inv,
+                      const void* src_norm, void* rin, int nR, int p, int p_off, float eps,
+                      cudaStream_t st) {
+  if (N <= 0 || nl <= 0) return;
+  dim3 grid(N, nl);
+  WM_DISPATCH_S(dtype, norm_emit_kernel<S><<<grid, 256, 0, st>>>(
+                           (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in, (S*)xn, inv,
+                           (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
+}
+
+template <typename S>
+__global__ void rmsnorm_kernel(const S* __restrict__ X, long long ldx, int row0, int rstride,
+                               int D, const S* __restrict__ gain, S* __restrict__ y, float eps) {
+  constexpr int VN = VecT<S>::N;
+  __shared__ float red[32];
+  const int r = blockIdx.x;
+  const S* x = X + (long long)(row0 + (long long)r * rstride) * ldx;
+  float ss = 0.f;
+  for (int c = threadIdx.x * VN; c < D; c += blockDim.x * VN) {
+    float v[VN];
+    ld_vec(x + c, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) ss += v[i] * v[i];
+  }
+  ss = block_sum(ss, red);
+  const float inv = rsqrtf(ss / (float)D + eps);
+  for (int c = threadIdx.x * VN; c < D; c += blockDim.x * VN) {
+    float v[VN], gv[VN];
+    ld_vec(x + c, v);
+    ld_vec(gain + c, gv);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) v[i] = v[i] * inv * gv[i];
+    st_vec(y + (long long)r * D + c, v);
+  }
+}
+
+void launch_rmsnorm(int dtype, const void* X, long long ldx, int row0, int rstride, int N, int D,
+                    const void* gain, void* y, float eps, cudaStream_t st) {
+  if (N <= 0) return;
+  WM_DISPATCH_S(dtype, rmsnorm_kernel<S><<<N, 256, 0, st>>>((const S*)X, ldx, row0, rstride, D,
+                                                           (const S*)gain, (S*)y, eps));
+}
+
+__global__ void broadcast_coeff_kernel(const float* __restrict__ stat, long long total, int n_per_row,
+                                       float* __restrict__ coeff) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x)
+    coeff[i] = stat[i % n_per_row];
+}
+
+void launch_broadcast_coeff(const float* stat, int N, int n_per_row, float* coeff, cudaStream_t st) {
+  const long long total = (long long)N * n_per_row;
+  if (total <= 0) return;
+  const long long b = (total + 255) / 256;
+  broadcast_coeff_kernel<<<(int)(b < 4096 ? b : 4096), 256, 0, st>>>(stat, total, n_per_row, coeff);
+}
+
+}  // namespace wm

@@ -1,0 +1,77 @@
+// Host-side launch functions of libwm's kernels (internal interface).
+#pragma once
+
+#include "common.cuh"
+
+namespace wm {
+
+// Storage-type dispatch helper: dtype is WM_F32 or WM_BF16.
+#define WM_DISPATCH_S(dtype, ...)                          \
+  do {                                                     \
+    if ((dtype) == WM_F32) {                               \
+      using S = float;                                     \
+      __VA_ARGS__;                                         \
+    } else {                                               \
+      using S = __nv_bfloat16;                             \
+      __VA_ARGS__;                                         \
+    }                                                      \
+  } while (0)
+
+inline size_t elem_size(int dtype) { return dtype == WM_F32 ? 4 : 2; }
+
+// ---- elem.cu ---------------------------------------------------------------
+void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStream_t st);
+void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq,
+                       int32_t* tok, int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st);
+void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32_t* seq,
+                        int32_t* pos, cudaStream_t st);
+void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V, int D,
+                  void* out, long long ld_out, uint32_t* flags, cudaStream_t st);
+// Per (row, layer l = l0 + y): inv_rms of X[row][l] -> inv[row*L + l];
+// optional xn = X*inv*gain_in[l]; for l in the router set, rin[beta][row][ridx*D..]
+// = X*inv*src_norm[beta][l].
+void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx_l, int N,
+                      int l0, int nl, int D, int L, const void* gain_in, void* xn,
+                      float* inv, const void* src_norm, void* rin, int nR, int p, int p_off,
+                      float eps, cudaStream_t st);
+// y[r] = RMSNorm(X[row0 + r*rstride]; gain) for r < N.
+void launch_rmsnorm(int dtype, const void* X, long long ldx, int row0, int rstride, int N, int D,
+                    const void* gain, void* y, float eps, cudaStream_t st);
+void launch_broadcast_coeff(const float* stat, int N, int n_per_row, float* coeff,
+                            cudaStream_t st);
+
+// ---- gemm_simt.cu / gemm_tc.cu --------------------------------------------
+void launch_gemm_simt(int dtype, const GemmDesc& g, cudaStream_t st);
+bool gemm_tc_supported(const GemmDesc& g);
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st);
+
+// ---- attn.cu ---------------------------------------------------------------
+struct AttnArgs {
+  const void* q;          // [N][Hq][d]
+  int N;
+  const int32_t* seq;
+  const int32_t* pos;
+  int channel;
+  const void* cache_k;    // [B][k][Hkv][Tmax][d]
+  const void* cache_v;
+  int B, k, Hq, Hkv, d, Tmax;
+  void* out;              // [N][Hq*d]
+  uint32_t* flags;
+};
+void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st);
+
+// ---- pool.cu ---------------------------------------------------------------
+struct MixArgs {
+  const void* stash;      // [N][L][D] source states
+  long long ld_row;       // elements between rows (L*D for a stash)
+  const float* inv;       // [N][L] inverse RMS of each source state
+  const float* coeff;     // [N][2][k][L]
+  const void* src_norm;   // [2][L][D]
+  const void* chan_norm;  // [2][k][D]
+  void* mixed;            // [N][2][k][D]
+  int N, L, D, k;
+  float eps;
+};
+void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st);
+
+}  // namespace wm

@@ -1,0 +1,200 @@
+"""ctypes binding of libwm (include/wm.h). Argument marshalling only.
+
+Tensors are torch tensors in device memory (PyTorch supplies allocation and
+streams); every computation happens in the library's CUDA kernels. The
+library must have been built (``python -m cross_layer_kv_pool_b300.build``):
+there is no other implementation to fall back to, and ``lib()`` raises if it
+is missing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .synth import WEIGHT_ORDER, ModelShape
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwm.so")
+
+WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, \
+    WM_ERR_TIMEOUT, WM_ERR_DEVICE_BOUNDS = range(7)
+WM_F32, WM_BF16 = 0, 1
+LOGITS = {"none": 0, None: 0, "last": 1, "all": 2}
+WM_FLAG_SIMT_GEMM = 1
+
+EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
+            "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version")
+
+
+class WMError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class WMConfig(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int32), ("D", ctypes.c_int32), ("k", ctypes.c_int32),
+                ("p", ctypes.c_int32), ("p_offset", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("V", ctypes.c_int32), ("eps", ctypes.c_float), ("rope_base", ctypes.c_float),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class WMWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_ORDER] + [("static_coeff", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libwm.so (once). Raises FileNotFoundError if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise FileNotFoundError(f"{LIB_PATH} is missing: build it with "
+                                    "`python -m cross_layer_kv_pool_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        cfgp, wp = ctypes.POINTER(WMConfig), ctypes.POINTER(WMWeights)
+        L.wm_workspace_size.restype = sz
+        L.wm_workspace_size.argtypes = [cfgp, i32, i32]
+        L.wm_pool_mix.restype = ctypes.c_int
+        L.wm_pool_mix.argtypes = [cfgp, wp, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp, vp, sz, vp]
+        L.wm_channel_attn.restype = ctypes.c_int
+        L.wm_channel_attn.argtypes = [cfgp, vp, i32, vp, vp, i32, vp, vp, i32, i32, vp, vp, sz, vp]
+        L.wm_cyclic_pass.restype = ctypes.c_int
+        L.wm_cyclic_pass.argtypes = [cfgp, wp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32,
+                                     vp, sz, vp]
+        L.wm_decode_step.restype = ctypes.c_int
+        L.wm_decode_step.argtypes = [cfgp, wp, vp, i32, i32, vp, vp, i32, vp, vp, sz, vp]
+        L.wm_check_flags.restype = ctypes.c_int
+        L.wm_check_flags.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_uint32), vp]
+        L.wm_status_string.restype = ctypes.c_char_p
+        L.wm_status_string.argtypes = [ctypes.c_int]
+        L.wm_abi_version.restype = i32
+        L.wm_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().wm_status_string(int(s)).decode()
+
+
+def _check(status, where):
+    if status != WM_OK:
+        raise WMError(status, where)
+
+
+def make_config(shape: ModelShape, flags: int = 0) -> WMConfig:
+    return WMConfig(shape.L, shape.D, shape.k, shape.p, shape.p_offset, shape.Hq, shape.Hkv,
+                    shape.d, shape.F, shape.V, shape.eps, shape.rope_base,
+                    WM_F32 if shape.dtype == "f32" else WM_BF16, flags)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_weights_struct(W: dict, static_coeff: torch.Tensor | None = None) -> WMWeights:
+    """Pointer struct for device weight tensors (kept alive by the caller)."""
+    s = WMWeights()
+    for n in WEIGHT_ORDER:
+        setattr(s, n, W[n].data_ptr())
+    s.static_coeff = None if static_coeff is None else static_coeff.data_ptr()
+    return s
+
+
+class Model:
+    """Device weights of one model plus the C structs that describe them."""
+
+    def __init__(self, shape: ModelShape, weights: dict, static_coeff=None, flags: int = 0):
+        self.shape = shape
+        self.W = weights
+        self.static_coeff = None if static_coeff is None else \
+            static_coeff.to(device=weights["embed"].device, dtype=torch.float32).contiguous()
+        self.cfg = make_config(shape, flags)
+        self.wstruct = make_weights_struct(weights, self.static_coeff)
+
+    def new_cache(self, B: int, Tmax: int, fill: float = 0.0):
+        s = self.shape
+        shp = (B, s.k, s.Hkv, Tmax, s.d)
+        dev = self.W["embed"].device
+        ck = torch.full(shp, fill, dtype=s.torch_dtype, device=dev)
+        cv = torch.full(shp, fill, dtype=s.torch_dtype, device=dev)
+        return ck, cv
+
+    def workspace(self, max_rows: int, Tmax: int):
+        n = workspace_size(self.cfg, max_rows, Tmax)
+        return torch.zeros(n, dtype=torch.uint8, device=self.W["embed"].device)
+
+
+def workspace_size(cfg: WMConfig, max_rows: int, Tmax: int) -> int:
+    n = lib().wm_workspace_size(ctypes.byref(cfg), int(max_rows), int(Tmax))
+    if n == 0:
+        raise WMError(WM_ERR_INVALID_ARG, "wm_workspace_size")
+    return n
+
+
+def wm_pool_mix(m: Model, states, seq, pos, cache_k, cache_v, ws, coeff_out=None,
+                mixed_out=None, stream=None):
+    B, Tmax = cache_k.shape[0], cache_k.shape[3]
+    st = lib().wm_pool_mix(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(states),
+                           states.shape[0], _ptr(seq), _ptr(pos), _ptr(cache_k), _ptr(cache_v),
+                           B, Tmax, _ptr(coeff_out), _ptr(mixed_out), _ptr(ws), ws.numel(),
+                           _stream(stream))
+    _check(st, "wm_pool_mix")
+
+
+def wm_channel_attn(cfg: WMConfig, q, seq, pos, channel: int, cache_k, cache_v, out, ws,
+                    stream=None):
+    B, Tmax = cache_k.shape[0], cache_k.shape[3]
+    st = lib().wm_channel_attn(ctypes.byref(cfg), _ptr(q), q.shape[0], _ptr(seq), _ptr(pos),
+                               int(channel), _ptr(cache_k), _ptr(cache_v), B, Tmax, _ptr(out),
+                               _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "wm_channel_attn")
+
+
+def wm_cyclic_pass(m: Model, tokens, g: int, cache_k, cache_v, ws, q_begin: int = 0,
+                   q_end: int | None = None, logits=None, logits_mode="none", stream=None):
+    B, T = tokens.shape
+    Tmax = cache_k.shape[3]
+    q_end = g if q_end is None else q_end
+    st = lib().wm_cyclic_pass(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(tokens), B, T,
+                              int(g), int(q_begin), int(q_end), _ptr(cache_k), _ptr(cache_v),
+                              Tmax, _ptr(logits), LOGITS[logits_mode], _ptr(ws), ws.numel(),
+                              _stream(stream))
+    _check(st, "wm_cyclic_pass")
+
+
+def wm_decode_step(m: Model, tokens, pos: int, cache_k, cache_v, logits, ws, stream=None):
+    B = tokens.shape[0]
+    Tmax = cache_k.shape[3]
+    st = lib().wm_decode_step(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(tokens), B,
+                              int(pos), _ptr(cache_k), _ptr(cache_v), Tmax, _ptr(logits),
+                              _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "wm_decode_step")
+
+
+def wm_check_flags(ws, stream=None) -> int:
+    """Reads and clears the device-side flag word; raises on a set check bit."""
+    f = ctypes.c_uint32(0)
+    st = lib().wm_check_flags(_ptr(ws), ws.numel(), ctypes.byref(f), _stream(stream))
+    if st not in (WM_OK,):
+        raise WMError(st, f"wm_check_flags (flags=0x{f.value:x})")
+    return f.value
+
+
+def rows_for_pass(B: int, T: int, g: int) -> int:
+    """Rows of the largest group of a cyclic pass: B * ceil(T / g)."""
+    return B * (-(-T // g))

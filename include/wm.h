@@ -1,0 +1,185 @@
+/*
+ * wm.h - C ABI of libwm, the B300 (sm_103a) implementation of the WhiteMatter
+ * cross-layer KV pool and its cyclic Gauss-Seidel prefill / decode schedule.
+ *
+ * Sources (public pages about arXiv 2608.18486, "WhiteMatter: All-to-All
+ * Cross-Layer Connections via KV Mixing"), cited by tag and section:
+ *   [PL] paperlayer.ai summary, sections "3 METHOD" and "5 ANALYSIS";
+ *   [OD] onedev.kr review "WhiteMatter가 모든 층의 KV 재사용으로 캐시를 절반으로
+ *        줄인다", sections "How it works" (어떻게 동작하나), "How it differs"
+ *        (무엇과 다른가) and "How it is used" (어떻게 쓰나).
+ *
+ * Conventions for every entry point
+ *  - Pointers named in a weights struct or as tensors are DEVICE pointers,
+ *    caller-owned, row-major, 16-byte aligned, in the storage type chosen by
+ *    wm_config.dtype (fp32 or bf16) unless stated otherwise. Integer arrays are
+ *    int32 device arrays. ``stream`` is a cudaStream_t (NULL = legacy stream).
+ *  - The library allocates no memory and keeps no state between calls. All
+ *    scratch lives in the caller's workspace ``ws`` of ``ws_bytes`` bytes
+ *    (device memory, 256-byte aligned, size from wm_workspace_size). Calls
+ *    that share one workspace must not overlap on the GPU.
+ *  - Calls are asynchronous on ``stream``. The returned status covers argument
+ *    validation and kernel launch only; on any error nothing is launched.
+ *    Device-side checks (token ids, sequence indices, positions out of range)
+ *    skip the offending access and set bits in the workspace's flag word, read
+ *    (and cleared) by wm_check_flags after the work.
+ *  - Cache layout: cache_k and cache_v are [B][k][Hkv][Tmax][d] each. Keys are
+ *    stored after K-norm and RoPE, values raw ([PL 3 METHOD, "Cross-layer KV
+ *    pool"]: stored keys are rotated and K-normalised, values stay raw; the
+ *    cache holds k*T*Hkv*d elements). The caller initialises the cache (zeros
+ *    for a fresh prefill); entry points write only the positions they process.
+ */
+#ifndef WM_H
+#define WM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WM_ABI_VERSION 1
+
+typedef enum {
+    WM_OK = 0,
+    WM_ERR_INVALID_ARG = 1,   /* null pointer, bad size or range, misalignment */
+    WM_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. d not 64/128)  */
+    WM_ERR_WORKSPACE = 3,     /* ws too small or misaligned                     */
+    WM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed              */
+    WM_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up             */
+    WM_ERR_DEVICE_BOUNDS = 6  /* device-side index check failed (wm_check_flags) */
+} wm_status;
+
+typedef enum { WM_F32 = 0, WM_BF16 = 1 } wm_dtype;
+
+typedef enum {
+    WM_LOGITS_NONE = 0,       /* no logits                                       */
+    WM_LOGITS_LAST = 1,       /* logits of position T-1 of each sequence, [B][V] */
+    WM_LOGITS_ALL = 2         /* logits of every position, [B][T][V]             */
+} wm_logits_mode;
+
+/* Engine flags (wm_config.flags). */
+#define WM_FLAG_SIMT_GEMM 1u  /* run every contraction on CUDA cores (debug aid) */
+
+/* Model shape. The router reads the source states l < L with
+ * l % p == p_offset ([OD How it works]: the router reads every p-th layer's
+ * state, stride p = 2, yet emits weights for all L layers). */
+typedef struct {
+    int32_t L;          /* layers = source states per token                    */
+    int32_t D;          /* model width, multiple of 64                         */
+    int32_t k;          /* pool channels, 1 <= k <= L                          */
+    int32_t p;          /* router stride, >= 1                                 */
+    int32_t p_offset;   /* first router source, 0 <= p_offset < p             */
+    int32_t Hq;         /* query heads                                         */
+    int32_t Hkv;        /* KV heads, divides Hq                                */
+    int32_t d;          /* head size, 64 or 128                                */
+    int32_t F;          /* SwiGLU width, multiple of 64                        */
+    int32_t V;          /* vocabulary                                          */
+    float eps;          /* RMSNorm epsilon                                     */
+    float rope_base;    /* RoPE base                                           */
+    int32_t dtype;      /* wm_dtype: storage and GEMM operand type             */
+    uint32_t flags;     /* WM_FLAG_* engine flags                              */
+} wm_config;
+
+/* Weights (device pointers, storage type). nR = number of router sources.
+ * Matrices are [out][in]: y = W x. Gains are RMSNorm weights. */
+typedef struct {
+    const void* embed;       /* [V][D]                                          */
+    const void* lm_head;     /* [V][D]                                          */
+    const void* final_norm;  /* [D]                                             */
+    const void* in_norm;     /* [L][D]   layer input norm                       */
+    const void* post_norm;   /* [L][D]   norm before the FFN                    */
+    const void* q_norm;      /* [L][d]   per-head query norm                    */
+    const void* Wq;          /* [L][Hq*d][D]                                    */
+    const void* Wo;          /* [L][D][Hq*d]                                    */
+    const void* Wgate;       /* [L][F][D]                                       */
+    const void* Wup;         /* [L][F][D]                                       */
+    const void* Wdown;       /* [L][D][F]                                       */
+    const void* src_norm;    /* [2][L][D]  per-source gains, branch 0 = K, 1 = V */
+    const void* Wr;          /* [2][k*L][nR*D]  router, output index j*L + l    */
+    const void* chan_norm;   /* [2][k][D]  per-channel gains                    */
+    const void* Wk;          /* [k][Hkv*d][D]  channel key projections           */
+    const void* Wv;          /* [k][Hkv*d][D]  channel value projections         */
+    const void* k_norm;      /* [k][d]   per-channel key norm gains             */
+    const float* static_coeff; /* nullable fp32 [2][k][L]: when set, these
+                              * constant mixing weights replace the router for
+                              * every token (static-mixing variant, [PL 5
+                              * ANALYSIS, "Dynamic routing"])                   */
+} wm_weights;
+
+/* Bytes of workspace needed by calls that process up to ``max_rows`` token
+ * rows at once against a cache of ``Tmax`` positions. For wm_cyclic_pass the
+ * rows of one group are B * ceil(T/g); for wm_decode_step they are B. */
+size_t wm_workspace_size(const wm_config* cfg, int32_t max_rows, int32_t Tmax);
+
+/* The cross-layer KV pool for N token rows ([OD How it works]; [PL 3 METHOD,
+ * "Cross-layer KV pool"]). For each row n, with states[n] = its L layer
+ * states [L][D] (the inputs of layers 0..L-1), per branch b in {K, V}:
+ *   n_l   = RMSNorm(h_l; src_norm[b][l])
+ *   a     = Wr[b] . concat_{l in R} n_l   viewed [k][L]  (signed, no softmax)
+ *   m_j   = sum_l a[j][l] n_l ;  c_j = RMSNorm(m_j; chan_norm[b][j])
+ * then K_j = RoPE_pos(RMSNorm_d(Wk[j] c^K_j per head; k_norm[j])) and
+ * V_j = Wv[j] c^V_j are written to cache_{k,v}[seq[n]][j][:][pos[n]][:].
+ * states: [N][L][D]; seq, pos: [N] with seq < B, pos < Tmax.
+ * coeff_out (nullable): fp32 [N][2][k][L] router output (or static weights).
+ * mixed_out (nullable): [N][2][k][D] channel-normed mixtures c.
+ * Rows must have distinct (seq, pos) pairs. */
+wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w,
+                      const void* states, int32_t N,
+                      const int32_t* seq, const int32_t* pos,
+                      void* cache_k, void* cache_v, int32_t B, int32_t Tmax,
+                      float* coeff_out, void* mixed_out,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* Strictly causal attention of N query rows to one cache channel ([OD How it
+ * differs]: token i attends only to s < i; [PL 3 METHOD, "Per-layer channel
+ * selection"]: layer l reads channel l mod k, which the caller passes here).
+ * q: [N][Hq][d], already q-normed and rotated; row n sees keys s < pos[n] of
+ * sequence seq[n]; query head h reads KV head h*Hkv/Hq; scale 1/sqrt(d); a row
+ * with pos = 0 gets 0. out: [N][Hq*d]. */
+wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N,
+                          const int32_t* seq, const int32_t* pos, int32_t channel,
+                          const void* cache_k, const void* cache_v,
+                          int32_t B, int32_t Tmax, void* out,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Groups q_begin..q_end-1 of one cyclic Gauss-Seidel pass over tokens [B][T]
+ * ([OD How it differs]: positions split into G_q = {i : i mod g = q}, groups in
+ * order q = 0..g-1, parallel inside a group, the cache updated after every
+ * group). Each group runs the whole layer stack of its B*|G_q| rows against
+ * the cache as it stood before the group, then writes their pooled channels
+ * at their positions. g = 1 is a Jacobi pass, g = T exact autoregressive
+ * evaluation. 1 <= g <= T <= Tmax; 0 <= q_begin <= q_end <= g.
+ * logits (fp32, nullable unless logits_mode != NONE): LAST -> [B][V] for
+ * position T-1, computed by the group that holds it; ALL -> [B][T][V].
+ * When logits_mode is NONE the last layer, whose output feeds only the LM
+ * head, is not evaluated. */
+wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w,
+                         const int32_t* tokens, int32_t B, int32_t T, int32_t g,
+                         int32_t q_begin, int32_t q_end,
+                         void* cache_k, void* cache_v, int32_t Tmax,
+                         float* logits, int32_t logits_mode,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* One autoregressive decode step at position ``pos`` for tokens [B]
+ * ([PL 3 METHOD, "Execution schedules"]: a token's pooled channels are
+ * appended only after its layer stack). The stack attends to s < pos, then
+ * the token's channels are written at pos. logits: fp32 [B][V]. */
+wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w,
+                         const int32_t* tokens, int32_t B, int32_t pos,
+                         void* cache_k, void* cache_v, int32_t Tmax,
+                         float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Waits for ``stream``, copies the workspace flag word to *flags_out (host)
+ * and clears it. Returns WM_ERR_DEVICE_BOUNDS if an index check failed and
+ * WM_ERR_TIMEOUT if a bounded wait gave up since the last call. */
+wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream);
+
+const char* wm_status_string(wm_status s);
+int32_t wm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WM_H */

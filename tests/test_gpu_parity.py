@@ -1,0 +1,260 @@
+"""GPU path (through the C ABI) against the CPU oracle on seeded inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.whitematter as O
+from cross_layer_kv_pool_b300 import synth, wm
+from tests.gpu_util import TOL, ensure_lib, host, model, relerr, small_shape
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+# ---------------------------------------------------------------------------
+# Channel attention
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,Hq,Hkv", [(64, 4, 2), (128, 14, 2), (64, 8, 8)])
+def test_attention_uniform_closed_form(dtype, d, Hq, Hkv):
+    """Zero keys: the output is the mean of the visible values, which encode
+    channel, sequence, position and KV head; checked exactly."""
+    s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=3)
+    cfg = wm.make_config(s)
+    B, Tmax = 2, 200
+    ck = torch.zeros((B, s.k, Hkv, Tmax, d), dtype=s.torch_dtype, device="cuda")
+    cv = torch.zeros_like(ck)
+    for c in range(s.k):
+        cv[:, c, :, :, 0] = c
+    cv[:, :, :, :, 1] = torch.arange(B, device="cuda").view(B, 1, 1, 1).to(s.torch_dtype)
+    cv[:, :, :, :, 2] = torch.arange(Tmax, device="cuda").view(1, 1, 1, Tmax).to(s.torch_dtype)
+    cv[:, :, :, :, 3] = torch.arange(Hkv, device="cuda").view(1, 1, Hkv, 1).to(s.torch_dtype)
+    seq = torch.arange(B, device="cuda", dtype=torch.int32).repeat_interleave(Tmax)
+    pos = torch.arange(Tmax, device="cuda", dtype=torch.int32).repeat(B)
+    N = B * Tmax
+    q = synth.make_normal((N, Hq, d), seed=3, device="cuda", dtype=s.torch_dtype)
+    out = torch.empty((N, Hq * d), dtype=s.torch_dtype, device="cuda")
+    ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
+    for c in range(s.k):
+        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws)
+        torch.cuda.synchronize()
+        o = host(out).reshape(N, Hq, d)
+        P = host(pos)
+        Sq = host(seq)
+        z = P == 0
+        assert np.all(o[z] == 0.0)
+        nz = ~z
+        assert np.all(o[nz, :, 0] == c)
+        assert np.all(o[nz, :, 1] == Sq[nz, None])
+        assert np.all(o[nz, :, 3] == (np.arange(Hq) * Hkv // Hq)[None, :])
+        mean_pos = (P[nz] - 1) / 2.0
+        if dtype == "bf16":
+            assert np.all(o[nz, :, 2] == mean_pos[:, None])
+        else:
+            assert np.max(np.abs(o[nz, :, 2] - mean_pos[:, None])) <= 1e-5 * Tmax
+    assert wm.wm_check_flags(ws) == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,Hq,Hkv,Tmax", [(64, 4, 2, 300), (128, 14, 2, 257), (64, 8, 8, 130)])
+def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax):
+    s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=2)
+    cfg = wm.make_config(s)
+    B = 2
+    ck = synth.make_normal((B, s.k, Hkv, Tmax, d), 11, "cuda", 2.0, s.torch_dtype)
+    cv = synth.make_normal((B, s.k, Hkv, Tmax, d), 12, "cuda", 1.0, s.torch_dtype)
+    rng = np.random.default_rng(0)
+    N = 97
+    pos_h = rng.integers(0, Tmax, size=N)
+    pos_h[:3] = [0, 1, Tmax - 1]
+    seq_h = rng.integers(0, B, size=N)
+    seq = torch.tensor(seq_h, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(pos_h, dtype=torch.int32, device="cuda")
+    q = synth.make_normal((N, Hq, d), 13, "cuda", 1.0, s.torch_dtype)
+    out = torch.empty((N, Hq * d), dtype=s.torch_dtype, device="cuda")
+    ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
+    for c in range(s.k):
+        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws)
+        torch.cuda.synchronize()
+        K, Vv, Q = host(ck), host(cv), host(q)
+        ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
+                        for r in range(N)])
+        err = relerr(host(out).reshape(N, Hq, d), ref)
+        assert err <= TOL[dtype]["attn"], err
+
+
+# ---------------------------------------------------------------------------
+# Pool
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape_kw", [dict(), dict(L=6, k=3, p=2, p_offset=1, d=128, Hq=2, Hkv=1, D=256),
+                                      dict(L=5, k=5, p=3, Hkv=4, Hq=4)])
+def test_pool_mix_vs_oracle(dtype, shape_kw):
+    s = small_shape(dtype, **shape_kw)
+    m, Wn = model(s, seed=5, jitter=0.2)
+    B, Tmax, N = 3, 40, 37
+    rng = np.random.default_rng(1)
+    flat = rng.choice(B * Tmax, size=N, replace=False)
+    seq_h, pos_h = flat // Tmax, flat % Tmax
+    states = synth.make_normal((N, s.L, s.D), 21, "cuda", 1.0, s.torch_dtype)
+    seq = torch.tensor(seq_h, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(pos_h, dtype=torch.int32, device="cuda")
+    ck, cv = m.new_cache(B, Tmax, fill=float("nan"))
+    coeff = torch.empty((N, 2, s.k, s.L), dtype=torch.float32, device="cuda")
+    mixed = torch.empty((N, 2, s.k, s.D), dtype=s.torch_dtype, device="cuda")
+    ws = m.workspace(N, Tmax)
+    wm.wm_pool_mix(m, states, seq, pos, ck, cv, ws, coeff_out=coeff, mixed_out=mixed)
+    torch.cuda.synchronize()
+    assert wm.wm_check_flags(ws) == 0
+    ref = O.pool(s, Wn, host(states), pos_h)
+    tol = TOL[dtype]
+    assert relerr(host(coeff), ref["coeff"]) <= tol["coeff"]
+    assert relerr(host(mixed), ref["mixed"]) <= tol["mixed"]
+    K, Vv = host(ck), host(cv)
+    written = np.zeros((B, Tmax), dtype=bool)
+    written[seq_h, pos_h] = True
+    assert np.array_equal(~np.isnan(K).any(axis=(1, 2, 4)), written)
+    assert np.array_equal(~np.isnan(Vv).any(axis=(1, 2, 4)), written)
+    gk = K[seq_h, :, :, pos_h, :]
+    gv = Vv[seq_h, :, :, pos_h, :]
+    assert relerr(gk, ref["K"]) <= tol["cache"]
+    assert relerr(gv, ref["V"]) <= tol["cache"]
+
+
+# ---------------------------------------------------------------------------
+# Whole passes and decode
+# ---------------------------------------------------------------------------
+
+def _gpu_passes(m, tokens_h, g, passes, Tmax=None, logits_mode="all", static=None):
+    s = m.shape
+    B, T = tokens_h.shape
+    Tmax = Tmax or T
+    tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
+    ck, cv = m.new_cache(B, Tmax)
+    ws = m.workspace(wm.rows_for_pass(B, T, g), Tmax)
+    shp = (B, T, s.V) if logits_mode == "all" else (B, s.V)
+    lg = torch.zeros(shp, dtype=torch.float32, device="cuda")
+    for n in range(passes):
+        last = n == passes - 1
+        wm.wm_cyclic_pass(m, tok, g, ck, cv, ws, logits=lg if last else None,
+                          logits_mode=logits_mode if last else "none")
+    torch.cuda.synchronize()
+    assert wm.wm_check_flags(ws) == 0
+    return host(lg), host(ck), host(cv)
+
+
+def _oracle_passes(s, Wn, tokens_h, g, passes, Tmax=None, logits="all", static=None):
+    B, T = tokens_h.shape
+    ck, cv = O.new_cache(s, B, Tmax or T)
+    lg = None
+    for n in range(passes):
+        lg = O.cyclic_pass(s, Wn, tokens_h, g, ck, cv, logits=logits if n == passes - 1 else None,
+                           static_coeff=static)
+    return lg, ck, cv
+
+
+def test_tiny_fp32_cyclic_and_jacobi():
+    """The tiny fp32 workload: cyclic g=4 for 3 passes and Jacobi for 64."""
+    wl = synth.WORKLOADS["tiny_fp32"]
+    s = wl["shape"]
+    m, Wn = model(s, seed=0, jitter=0.1)
+    tokens = host(synth.make_tokens(s, wl["B"], wl["T"], seed=1)).astype(np.int64)
+    for g, passes in ((4, 3), (1, 64)):
+        lg, ck, cv = _gpu_passes(m, tokens, g, passes)
+        rlg, rck, rcv = _oracle_passes(s, Wn, tokens, g, passes)
+        assert relerr(lg, rlg) <= 1e-4, (g, relerr(lg, rlg))
+        assert relerr(ck, rck) <= 1e-4
+        assert relerr(cv, rcv) <= 1e-4
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_steps_equal_oracle_and_g_equals_T(dtype):
+    s = small_shape(dtype)
+    m, Wn = model(s, seed=2)
+    B, T = 2, 12
+    tokens = np.random.default_rng(3).integers(0, s.V, size=(B, T))
+    ck, cv = m.new_cache(B, T)
+    ws = m.workspace(B, T)
+    lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
+    tok = torch.tensor(tokens, dtype=torch.int32, device="cuda")
+    out = []
+    for t in range(T):
+        wm.wm_decode_step(m, tok[:, t].contiguous(), t, ck, cv, lg, ws)
+        out.append(host(lg))
+    torch.cuda.synchronize()
+    dec = np.stack(out, axis=1)
+    rck, rcv = O.new_cache(s, B, T)
+    ref = O.autoregressive(s, Wn, tokens, rck, rcv)
+    tol = TOL[dtype]
+    assert relerr(dec, ref) <= tol["logits"]
+    assert relerr(host(ck), rck) <= tol["cache"]
+    # one cyclic pass with g = T is the same schedule on the GPU
+    lg2, ck2, _ = _gpu_passes(m, tokens, T, 1)
+    assert relerr(lg2, dec) <= tol["logits"]
+    assert relerr(ck2, host(ck)) <= tol["cache"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_partial_pass_writes_exact_positions(dtype):
+    s = small_shape(dtype)
+    m, _ = model(s, seed=4)
+    B, T, g = 2, 23, 5
+    tok = synth.make_tokens(s, B, T, seed=9, device="cuda")
+    ws = m.workspace(wm.rows_for_pass(B, T, g), T)
+    for qb, qe in ((0, 2), (1, 5), (4, 5), (2, 2)):
+        ck, cv = m.new_cache(B, T, fill=1000.0)
+        wm.wm_cyclic_pass(m, tok, g, ck, cv, ws, q_begin=qb, q_end=qe)
+        torch.cuda.synchronize()
+        K, Vv = host(ck), host(cv)
+        changed = (K != 1000.0).any(axis=(1, 2, 4)) | (Vv != 1000.0).any(axis=(1, 2, 4))
+        expect = np.array([[qb <= i % g < qe for i in range(T)]] * B)
+        assert np.array_equal(changed, expect), (qb, qe)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_uneven_groups_and_last_logits(dtype):
+    s = small_shape(dtype, Hkv=4, Hq=4)
+    m, Wn = model(s, seed=6, jitter=0.2)
+    B, T, g = 2, 29, 6
+    tokens = np.random.default_rng(7).integers(0, s.V, size=(B, T))
+    lg, ck, cv = _gpu_passes(m, tokens, g, 3, Tmax=T + 3, logits_mode="last")
+    rlg, rck, rcv = _oracle_passes(s, Wn, tokens, g, 3, Tmax=T + 3, logits="last")
+    tol = TOL[dtype]
+    assert relerr(lg, rlg) <= tol["logits"]
+    assert relerr(ck, rck) <= tol["cache"] and relerr(cv, rcv) <= tol["cache"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_identity_router_full_cache(dtype):
+    """k = L with the forced identity mixture (static weights)."""
+    s = small_shape(dtype, L=4, k=4)
+    static = np.zeros((2, s.k, s.L))
+    static[0] = static[1] = np.eye(s.L)
+    m, Wn = model(s, seed=8, static=torch.tensor(static))
+    B, T = 1, 16
+    tokens = np.random.default_rng(8).integers(0, s.V, size=(B, T))
+    lg, ck, _ = _gpu_passes(m, tokens, 4, 4, static=static)
+    rlg, rck, _ = _oracle_passes(s, Wn, tokens, 4, 4, static=static)
+    tol = TOL[dtype]
+    assert relerr(lg, rlg) <= tol["logits"]
+    assert relerr(ck, rck) <= tol["cache"]
+
+
+def test_half_small_bf16_short_sequence():
+    """The half-cache small model (L16 D512 k8, vocab 151936) in bf16 on a
+    short sequence: 3 cyclic passes with g = 16, last-position logits."""
+    s = synth.HALF_SMALL
+    m, Wn = model(s, seed=0, jitter=0.1)
+    B, T, g = 2, 96, 16
+    tokens = host(synth.make_tokens(s, B, T, seed=1)).astype(np.int64)
+    lg, ck, cv = _gpu_passes(m, tokens, g, 3, logits_mode="last")
+    rlg, rck, rcv = _oracle_passes(s, Wn, tokens, g, 3, logits="last")
+    assert relerr(lg, rlg) <= 2e-2
+    assert relerr(ck, rck) <= 2e-2 and relerr(cv, rcv) <= 2e-2
