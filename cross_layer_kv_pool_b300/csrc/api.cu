@@ -240,8 +240,8 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   for (int branch = 0; branch < 2; ++branch) {
     GemmDesc g;
     g.M = N; g.N = c.Hkv * c.d; g.K = c.D; g.batch = c.k;
-    g.A = static_cast<const char*>(mixed) + (long long)branch * c.k * c.D * x.es;
-    g.lda = 2LL * c.k * c.D; g.a_bstride = c.D;
+    g.A = static_cast<const char*>(mixed) + (long long)branch * c.k * N * c.D * x.es;
+    g.lda = c.D; g.a_bstride = (long long)N * c.D;
     g.B = branch == 0 ? w.Wk : w.Wv; g.ldb = c.D; g.b_bstride = (long long)c.Hkv * c.d * c.D;
     g.epi = base_epi(x);
     g.epi.mode = EPI_KV;

@@ -68,7 +68,7 @@ struct MixArgs {
   const float* coeff;     // [N][2][k][L]
   const void* src_norm;   // [2][L][D]
   const void* chan_norm;  // [2][k][D]
-  void* mixed;            // [N][2][k][D]
+  void* mixed;            // [2][k][N][D]
   int N, L, D, k;
   float eps;
 };

@@ -1,6 +1,8 @@
 // The pool's mix and channel norm for N token rows:
 //   m^b_j = sum_l a^b_{j,l} * inv_l * src_norm[b][l] (.) h_l,
-//   c^b_j = RMSNorm(m^b_j; chan_norm[b][j]).
+//   c^b_j = RMSNorm(m^b_j; chan_norm[b][j]),
+// written channel-major: mixed[b][j][row][:], the operand layout of the
+// per-channel projections.
 #include "kernels.h"
 
 namespace wm {
@@ -15,7 +17,7 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
   const float* inv = a.inv + (long long)r * a.L;
   const S* sn = (const S*)a.src_norm;
   const S* cn = (const S*)a.chan_norm;
-  S* out = (S*)a.mixed + (long long)r * 2 * a.k * a.D;
+  S* out = (S*)a.mixed;
   for (int beta = 0; beta < 2; ++beta) {
     for (int j = 0; j < a.k; ++j) {
       const float* cf = a.coeff + (((long long)r * 2 + beta) * a.k + j) * a.L;
@@ -31,7 +33,7 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
       ss = block_sum(ss, red);
       const float im = rsqrtf(ss / (float)a.D + a.eps);
       for (int t = threadIdx.x; t < a.D; t += blockDim.x)
-        out[((long long)beta * a.k + j) * a.D + t] =
+        out[(((long long)beta * a.k + j) * a.N + r) * a.D + t] =
             from_f<S>(mbuf[t] * im * to_f(cn[((long long)beta * a.k + j) * a.D + t]));
     }
   }

@@ -67,7 +67,7 @@ typedef enum {
  * state, stride p = 2, yet emits weights for all L layers). */
 typedef struct {
     int32_t L;          /* layers = source states per token                    */
-    int32_t D;          /* model width, multiple of 64                         */
+    int32_t D;          /* model width, multiple of 64, at most 8192           */
     int32_t k;          /* pool channels, 1 <= k <= L                          */
     int32_t p;          /* router stride, >= 1                                 */
     int32_t p_offset;   /* first router source, 0 <= p_offset < p             */
@@ -123,7 +123,8 @@ size_t wm_workspace_size(const wm_config* cfg, int32_t max_rows, int32_t Tmax);
  * V_j = Wv[j] c^V_j are written to cache_{k,v}[seq[n]][j][:][pos[n]][:].
  * states: [N][L][D]; seq, pos: [N] with seq < B, pos < Tmax.
  * coeff_out (nullable): fp32 [N][2][k][L] router output (or static weights).
- * mixed_out (nullable): [N][2][k][D] channel-normed mixtures c.
+ * mixed_out (nullable): [2][k][N][D] channel-normed mixtures c, channel-major
+ * (branch, channel, row), the operand layout of the channel projections.
  * Rows must have distinct (seq, pos) pairs. */
 wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w,
                       const void* states, int32_t N,

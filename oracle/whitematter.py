@@ -50,6 +50,14 @@ Readings where the pages are silent (each listed again in the design notes):
   R10 The cache starts at zero; unwritten positions are read as zeros.
   R11 Groups run q = 0..g-1 every pass; any 1 <= g <= T is allowed.
   R13 RMSNorm eps = 1e-6; RoPE rotate-half, theta_t = base^(-2t/d).
+  R14 bf16 storage. The pages run the 1.3B model in BF16 ([OD "Assumptions
+      and limits" (전제와 한계): RTX A6000, BF16]). With ``cfg.storage ==
+      "bf16"`` the oracle rounds (to nearest even) every tensor that a bf16
+      pipeline stores between operations: normalised GEMM inputs, queries,
+      attention outputs, residual-stream states, the SwiGLU activation, the
+      router input, the mixed channels and the cached K/V. Arithmetic between
+      those points stays fp64; router coefficients and logits stay unrounded.
+      Without ``storage`` (the default) nothing is rounded.
 
 Parity pins for every function below live in tests/test_oracle_pins.py and
 tests/test_oracle_mutants.py (closed forms, special cases, brute force and an
@@ -63,7 +71,7 @@ import math
 import numpy as np
 
 __all__ = [
-    "rmsnorm", "rope", "silu", "router_sources", "channel_of_layer",
+    "round_bf16", "rmsnorm", "rope", "silu", "router_sources", "channel_of_layer",
     "group_positions", "channel_attention", "consumer_layer", "pool",
     "run_rows", "new_cache", "cyclic_pass", "decode_step",
     "autoregressive", "kv_residual",
@@ -72,6 +80,22 @@ __all__ = [
 
 def _f64(x):
     return np.asarray(x, dtype=np.float64)
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as fp64: first
+    to fp32 (nearest), then the low 16 bits of the fp32 pattern are rounded."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _st(cfg, x):
+    """A stored activation: rounded to bf16 in bf16-storage mode (R14)."""
+    if getattr(cfg, "storage", None) == "bf16":
+        return round_bf16(x)
+    return _f64(x)
 
 
 # ----------------------------------------------------------------------------
@@ -181,20 +205,22 @@ def consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v):
     N = h.shape[0]
     Hq, Hkv, d = cfg.Hq, cfg.Hkv, cfg.d
     h = _f64(h)
-    a = rmsnorm(h, W["in_norm"][l], cfg.eps)
+    a = _st(cfg, rmsnorm(h, W["in_norm"][l], cfg.eps))
     q = (a @ _f64(W["Wq"][l]).T).reshape(N, Hq, d)
     q = rmsnorm(q, W["q_norm"][l], cfg.eps)
-    q = rope(q, _f64(pos)[:, None], cfg.rope_base)
+    q = _st(cfg, rope(q, _f64(pos)[:, None], cfg.rope_base))
     c = channel_of_layer(cfg, l)
     o = np.zeros((N, Hq, d), dtype=np.float64)
     for r in range(N):
         b = int(seq[r])
         o[r] = channel_attention(q[r], cache_k[b, c], cache_v[b, c], int(pos[r]), Hq, Hkv)
-    h2 = h + o.reshape(N, Hq * d) @ _f64(W["Wo"][l]).T
-    f = rmsnorm(h2, W["post_norm"][l], cfg.eps)
+    o = _st(cfg, o)
+    h2 = _st(cfg, h + o.reshape(N, Hq * d) @ _f64(W["Wo"][l]).T)
+    f = _st(cfg, rmsnorm(h2, W["post_norm"][l], cfg.eps))
     gate = f @ _f64(W["Wgate"][l]).T
     up = f @ _f64(W["Wup"][l]).T
-    return h2 + (silu(gate) * up) @ _f64(W["Wdown"][l]).T
+    act = _st(cfg, silu(gate) * up)
+    return _st(cfg, h2 + act @ _f64(W["Wdown"][l]).T)
 
 
 # ----------------------------------------------------------------------------
@@ -228,20 +254,20 @@ def pool(cfg, W, states, pos, static_coeff=None):
     for beta in range(2):
         n = rmsnorm(states, W["src_norm"][beta], cfg.eps)          # [N, L, D]
         if static_coeff is None:
-            x = n[:, R, :].reshape(N, len(R) * D)
+            x = _st(cfg, n[:, R, :].reshape(N, len(R) * D))
             a = (x @ _f64(W["Wr"][beta]).T).reshape(N, k, L)
         else:
             a = np.broadcast_to(_f64(static_coeff)[beta], (N, k, L))
         m = np.einsum("njl,nld->njd", a, n)
         coeff[:, beta] = a
-        mixed[:, beta] = rmsnorm(m, W["chan_norm"][beta], cfg.eps)
+        mixed[:, beta] = _st(cfg, rmsnorm(m, W["chan_norm"][beta], cfg.eps))
     K = np.zeros((N, k, Hkv, d), dtype=np.float64)
     V = np.zeros((N, k, Hkv, d), dtype=np.float64)
     for j in range(k):
         kt = (mixed[:, 0, j] @ _f64(W["Wk"][j]).T).reshape(N, Hkv, d)
         kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)
-        K[:, j] = rope(kt, _f64(pos)[:, None], cfg.rope_base)
-        V[:, j] = (mixed[:, 1, j] @ _f64(W["Wv"][j]).T).reshape(N, Hkv, d)
+        K[:, j] = _st(cfg, rope(kt, _f64(pos)[:, None], cfg.rope_base))
+        V[:, j] = _st(cfg, (mixed[:, 1, j] @ _f64(W["Wv"][j]).T).reshape(N, Hkv, d))
     return {"K": K, "V": V, "coeff": coeff, "mixed": mixed}
 
 
@@ -266,7 +292,7 @@ def run_rows(cfg, W, tokens, seq, pos, cache_k, cache_v, want_logits=False,
         h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)
     logits = None
     if want_logits:
-        logits = rmsnorm(h, W["final_norm"], cfg.eps) @ _f64(W["lm_head"]).T
+        logits = _st(cfg, rmsnorm(h, W["final_norm"], cfg.eps)) @ _f64(W["lm_head"]).T
     return pool(cfg, W, states, pos, static_coeff), logits, states
 
 

@@ -2,6 +2,9 @@
 
 from __future__ import annotations
 
+import dataclasses
+from types import SimpleNamespace
+
 import numpy as np
 import torch
 
@@ -34,6 +37,17 @@ def host(t) -> np.ndarray:
 def model(shape, seed=0, jitter=0.1, static=None, flags=0):
     W = synth.make_weights(shape, seed=seed, device="cuda", gain_jitter=jitter)
     return wm.Model(shape, W, static_coeff=static, flags=flags), synth.to_numpy_weights(W)
+
+
+def ocfg(shape):
+    """The oracle's view of a model: bf16 workloads use its bf16-storage mode
+    (activations rounded where a bf16 pipeline stores them), fp32 workloads
+    the plain fp64 arithmetic."""
+    ns = SimpleNamespace(**dataclasses.asdict(shape))
+    ns.nR = shape.nR
+    if shape.dtype == "bf16":
+        ns.storage = "bf16"
+    return ns
 
 
 def small_shape(dtype="f32", **kw):

@@ -491,7 +491,40 @@ def check_last_logits_and_decode(O):
     _close(lg, lgar[:, 6], 1e-10, "decode")
 
 
+def check_round_bf16(O):
+    """Ties to even at the 2^-8 midpoints near 1; agreement with torch's own
+    fp32 -> bf16 conversion on random values of many magnitudes."""
+    import torch
+    vals = np.array([1.0, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8), 3.0, 0.0, 2.0 ** -130])
+    exp = np.array([1.0, 1.0, 1 + 2.0 ** -6, -1.0, 3.0, 0.0, 2.0 ** -130])
+    assert np.array_equal(O.round_bf16(vals), exp)
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal(4096) * np.exp(rng.uniform(-20, 20, 4096))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_bf16(x), ref)
+
+
+def check_bf16_storage_mode(O):
+    """In bf16-storage mode every cached value is a bf16 number and the
+    result stays near the unrounded one on a well-conditioned case (the
+    identity mixture); without the mode nothing is rounded."""
+    c = _cfg(L=3, D=16, k=3, Hq=4, Hkv=2, d=8)
+    W = {n: O.round_bf16(v) for n, v in _weights(c, seed=22, std=0.1).items()}
+    static = np.zeros((2, c.k, c.L))
+    static[0] = static[1] = np.eye(c.L)
+    tokens = _tokens(c, 1, 6, 7)
+    lg, ck, cv = _cyclic(O, c, W, tokens, 6, 1, static=static)
+    cb = SimpleNamespace(**vars(c), storage="bf16")
+    lgb, ckb, cvb = _cyclic(O, cb, W, tokens, 6, 1, static=static)
+    assert np.array_equal(O.round_bf16(ckb), ckb) and np.array_equal(O.round_bf16(cvb), cvb)
+    assert not np.array_equal(O.round_bf16(ck), ck)
+    _close(lgb, lg, 3e-2, "bf16 storage near fp64")
+    assert np.max(np.abs(lgb - lg)) > 0
+
+
 ALL_CHECKS = [
+    check_round_bf16,
+    check_bf16_storage_mode,
     check_rmsnorm_closed_forms,
     check_rope_closed_forms,
     check_silu,

@@ -6,7 +6,7 @@ import torch
 
 import oracle.whitematter as O
 from cross_layer_kv_pool_b300 import synth, wm
-from tests.gpu_util import TOL, ensure_lib, host, model, relerr, small_shape
+from tests.gpu_util import TOL, ensure_lib, host, model, ocfg, relerr, small_shape
 
 pytestmark = pytest.mark.gpu
 
@@ -108,15 +108,15 @@ def test_pool_mix_vs_oracle(dtype, shape_kw):
     pos = torch.tensor(pos_h, dtype=torch.int32, device="cuda")
     ck, cv = m.new_cache(B, Tmax, fill=float("nan"))
     coeff = torch.empty((N, 2, s.k, s.L), dtype=torch.float32, device="cuda")
-    mixed = torch.empty((N, 2, s.k, s.D), dtype=s.torch_dtype, device="cuda")
+    mixed = torch.empty((2, s.k, N, s.D), dtype=s.torch_dtype, device="cuda")
     ws = m.workspace(N, Tmax)
     wm.wm_pool_mix(m, states, seq, pos, ck, cv, ws, coeff_out=coeff, mixed_out=mixed)
     torch.cuda.synchronize()
     assert wm.wm_check_flags(ws) == 0
-    ref = O.pool(s, Wn, host(states), pos_h)
+    ref = O.pool(ocfg(s), Wn, host(states), pos_h)
     tol = TOL[dtype]
     assert relerr(host(coeff), ref["coeff"]) <= tol["coeff"]
-    assert relerr(host(mixed), ref["mixed"]) <= tol["mixed"]
+    assert relerr(host(mixed).transpose(2, 0, 1, 3), ref["mixed"]) <= tol["mixed"]
     K, Vv = host(ck), host(cv)
     written = np.zeros((B, Tmax), dtype=bool)
     written[seq_h, pos_h] = True
@@ -152,6 +152,7 @@ def _gpu_passes(m, tokens_h, g, passes, Tmax=None, logits_mode="all", static=Non
 
 def _oracle_passes(s, Wn, tokens_h, g, passes, Tmax=None, logits="all", static=None):
     B, T = tokens_h.shape
+    s = ocfg(s)
     ck, cv = O.new_cache(s, B, Tmax or T)
     lg = None
     for n in range(passes):
@@ -191,7 +192,7 @@ def test_decode_steps_equal_oracle_and_g_equals_T(dtype):
     torch.cuda.synchronize()
     dec = np.stack(out, axis=1)
     rck, rcv = O.new_cache(s, B, T)
-    ref = O.autoregressive(s, Wn, tokens, rck, rcv)
+    ref = O.autoregressive(ocfg(s), Wn, tokens, rck, rcv)
     tol = TOL[dtype]
     assert relerr(dec, ref) <= tol["logits"]
     assert relerr(host(ck), rck) <= tol["cache"]

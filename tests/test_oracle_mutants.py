@@ -27,18 +27,18 @@ MUTANTS = [
      "    n_keys = n_keys + 1\n    if n_keys <= 0:\n        return out"),
     ("attn_gqa_modulo", "channel_attention", "hk = (h * Hkv) // Hq", "hk = h % Hkv"),
     ("attn_no_scale", "channel_attention", "z = keys @ q[h] / math.sqrt(d)", "z = keys @ q[h]"),
-    ("layer_no_attn_residual", "consumer_layer", "h2 = h + o.reshape", "h2 = 0.0 * h + o.reshape"),
+    ("layer_no_attn_residual", "consumer_layer", "_st(cfg, h + o.reshape", "_st(cfg, 0.0 * h + o.reshape"),
     ("layer_swap_gate_up", "consumer_layer", "silu(gate) * up", "silu(up) * gate"),
     ("layer_no_qnorm", "consumer_layer", 'q = rmsnorm(q, W["q_norm"][l], cfg.eps)', 'q = q * _f64(W["q_norm"][l])'),
-    ("layer_no_q_rope", "consumer_layer", "q = rope(q, _f64(pos)[:, None], cfg.rope_base)", "q = q"),
+    ("layer_no_q_rope", "consumer_layer", "q = _st(cfg, rope(q, _f64(pos)[:, None], cfg.rope_base))", "q = _st(cfg, q)"),
     ("pool_coeff_transposed", "pool", "reshape(N, k, L)", "reshape(N, L, k).transpose(0, 2, 1)"),
-    ("pool_router_raw_states", "pool", "x = n[:, R, :]", "x = states[:, R, :]"),
+    ("pool_router_raw_states", "pool", "x = _st(cfg, n[:, R, :]", "x = _st(cfg, states[:, R, :]"),
     ("pool_mix_raw_states", "pool", 'np.einsum("njl,nld->njd", a, n)', 'np.einsum("njl,nld->njd", a, states)'),
-    ("pool_no_channel_norm", "pool", 'mixed[:, beta] = rmsnorm(m, W["chan_norm"][beta], cfg.eps)',
-     'mixed[:, beta] = m * _f64(W["chan_norm"][beta])'),
+    ("pool_no_channel_norm", "pool", 'mixed[:, beta] = _st(cfg, rmsnorm(m, W["chan_norm"][beta], cfg.eps))',
+     'mixed[:, beta] = _st(cfg, m * _f64(W["chan_norm"][beta]))'),
     ("pool_knorm_after_rope", "pool",
-     'kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)\n        K[:, j] = rope(kt, _f64(pos)[:, None], cfg.rope_base)',
-     'kt = rope(kt, _f64(pos)[:, None], cfg.rope_base)\n        K[:, j] = rmsnorm(kt, W["k_norm"][j], cfg.eps)'),
+     'kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)\n        K[:, j] = _st(cfg, rope(kt, _f64(pos)[:, None], cfg.rope_base))',
+     'kt = rope(kt, _f64(pos)[:, None], cfg.rope_base)\n        K[:, j] = _st(cfg, rmsnorm(kt, W["k_norm"][j], cfg.eps))'),
     ("pool_v_uses_wk", "pool", 'W["Wv"][j]', 'W["Wk"][j]'),
     ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
      'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
@@ -47,6 +47,9 @@ MUTANTS = [
     ("write_shifted", "_write", "cache_k[int(seq[r]), :, :, int(pos[r]), :] = K[r]",
      "cache_k[int(seq[r]), :, :, (int(pos[r]) + 1) % cache_k.shape[3], :] = K[r]"),
     ("groups_reversed", "cyclic_pass", "for q in range(q_begin, q_end):", "for q in reversed(range(q_begin, q_end)):"),
+    ("bf16_truncates", "round_bf16", "u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000", "u = u & 0xFFFF0000"),
+    ("bf16_ties_away", "round_bf16", "u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000", "u = (u + 0x8000) & 0xFFFF0000"),
+    ("storage_ignored", "_st", 'if getattr(cfg, "storage", None) == "bf16":', "if False:"),
     ("decode_sees_self", "decode_step", "pos = np.full(B, t, dtype=np.int64)", "pos = np.full(B, t + 1, dtype=np.int64)"),
 ]
 
