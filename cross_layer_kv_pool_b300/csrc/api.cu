@@ -87,6 +87,7 @@ wm_status check_ws(const wm_config& c, void* ws, size_t ws_bytes, long long N, l
 }
 
 struct Ctx {
+  mutable cudaError_t err = cudaSuccess;   // first failed launch of this call
   const wm_config* c;
   const wm_weights* w;
   char* ws;
@@ -116,9 +117,13 @@ Ctx make_ctx(const wm_config* c, const wm_weights* w, void* ws, long long N, lon
   return x;
 }
 
+// bf16 contractions run on the tensor-core engine; shapes it cannot express
+// (operand strides not 16-byte multiples) and the fp32 mode run on CUDA cores.
 void gemm(const Ctx& x, const GemmDesc& g) {
   if (x.tc && gemm_tc_supported(g)) {
-    if (launch_gemm_tc(g, x.st) == cudaSuccess) return;
+    const cudaError_t e = launch_gemm_tc(g, x.st);
+    if (e != cudaSuccess && x.err == cudaSuccess) x.err = e;
+    return;
   }
   launch_gemm_simt(x.c->dtype, g, x.st);
 }
@@ -254,9 +259,9 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   }
 }
 
-wm_status finish() {
+wm_status finish(const Ctx& x) {
   const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? WM_OK : WM_ERR_CUDA;
+  return (e == cudaSuccess && x.err == cudaSuccess) ? WM_OK : WM_ERR_CUDA;
 }
 
 }  // namespace
@@ -307,7 +312,7 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
                    x.st);
   run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
            mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
-  return finish();
+  return finish(x);
 }
 
 wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const int32_t* seq,
@@ -328,7 +333,7 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
   launch_attention(cfg->dtype, a, !x.tc, x.st);
-  return finish();
+  return finish(x);
 }
 
 wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
@@ -382,7 +387,7 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
     run_pool(x, N, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
              x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
   }
-  return finish();
+  return finish(x);
 }
 
 wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
@@ -416,7 +421,7 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
   gemm(x, lg);
   run_pool(x, B, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
            x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
-  return finish();
+  return finish(x);
 }
 
 wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream) {

@@ -1,9 +1,584 @@
-// Tensor-core (tcgen05) GEMM engine for bf16 operands.
+// Tensor-core GEMM engine for bf16 operands on sm_103a (tcgen05 + TMA + TMEM).
+//
+//   C[b][m][n] = epilogue( sum_k A[b][m][k] * B[b][n][k] ),  fp32 accumulation
+//
+// Persistent kernel, one CTA per SM, 192 threads in three roles:
+//   warp 0      one lane issues TMA loads of 128x64 A and BNx64 B tiles (128-byte
+//               swizzle) into a ring of shared-memory stages;
+//   warp 1      one lane issues tcgen05.mma (M=128, N=BN, K=16) into one of two
+//               TMEM accumulators, committing stage releases and tile completion
+//               to mbarriers; the warp also owns the TMEM allocation;
+//   warps 2-5   read the accumulator rows back with tcgen05.ld (each warp owns
+//               the 32 TMEM lanes of its quarter), apply the fused epilogue and
+//               store to global memory, then hand the accumulator back.
+// Every mbarrier wait is bounded: on timeout the kernel raises FLAG_TIMEOUT,
+// stops issuing work, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "kernels.h"
 
 namespace wm {
+namespace tc {
 
-bool gemm_tc_supported(const GemmDesc&) { return false; }
-cudaError_t launch_gemm_tc(const GemmDesc&, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr int BM = 128, BK = 64, NTHREADS = 192;
+constexpr unsigned long long WAIT_NS = 4000000000ull;  // 4 s bound on any wait
+
+struct Params {
+  int M, N, K, batch;
+  int m_tiles, n_tiles, num_kb;
+  long long total_tiles;
+  int vec_out, vec_res;
+  Epi epi;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout or when another role already gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try(b, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  while (true) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > WAIT_NS) return false;
+  }
+}
+__device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint64_t* bar, void* dst, int c0,
+                                          int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
+      "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+// K-major operand tile, 128-byte swizzle: rows of 128 B, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;              // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;    // stride byte offset
+  d |= (uint64_t)1 << 46;              // descriptor version
+  d |= (uint64_t)2 << 61;              // 128-byte swizzle
+  return d;
+}
+// kind::f16 instruction descriptor: bf16 A/B, fp32 D, both K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+    reinterpret_cast<uint4*>(p)[q] = u;
+  }
+}
+__device__ __forceinline__ void ld_bf16x32(const __nv_bfloat16* p, float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = reinterpret_cast<const uint4*>(p)[q];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      v[8 * q + 2 * i] = f.x;
+      v[8 * q + 2 * i + 1] = f.y;
+    }
+  }
+}
+
+// RMSNorm over one head held in registers, gain, then rotate-half RoPE.
+template <int HD>
+__device__ __forceinline__ void norm_rope(float (&v)[HD], const __nv_bfloat16* gain, float eps,
+                                          const float2* rt) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < HD; ++i) ss += v[i] * v[i];
+  const float inv = rsqrtf(ss / (float)HD + eps);
+#pragma unroll
+  for (int i = 0; i < HD; ++i) v[i] *= inv * __bfloat162float(gain[i]);
+#pragma unroll
+  for (int t = 0; t < HD / 2; ++t) {
+    const float2 cs = rt[t];
+    const float x1 = v[t], x2 = v[t + HD / 2];
+    v[t] = x1 * cs.x - x2 * cs.y;
+    v[t + HD / 2] = x2 * cs.x + x1 * cs.y;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue of one 128 x BN tile: this thread owns accumulator row ``lane_row``.
+// ---------------------------------------------------------------------------
+template <int BN, bool DUAL, int MODE, int HD>
+__device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, int row, int bidx,
+                                              int n0) {
+  const Epi& e = p.epi;
+  const bool row_ok = row < p.M;
+  if constexpr (MODE == EPI_QNORM_ROPE || MODE == EPI_KV) {
+#pragma unroll 1
+    for (int h0 = 0; h0 < BN; h0 += HD) {
+      float v[HD];
+      __syncwarp();
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          tmem_ld32(taddr + h0 + 32 * c, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]);
+        }
+      }
+      const int col0 = n0 + h0;
+      if (!row_ok || col0 >= p.N) continue;
+      const int ps = e.pos[row];
+      if (ps < 0 || ps >= e.Tmax) {
+        atomicOr(e.flags, FLAG_BAD_POS);
+        continue;
+      }
+      const float2* rt = e.rope + (long long)ps * (HD / 2);
+      __nv_bfloat16* dst;
+      if constexpr (MODE == EPI_QNORM_ROPE) {
+        norm_rope<HD>(v, (const __nv_bfloat16*)e.gain, e.eps, rt);
+        dst = (__nv_bfloat16*)e.C + (long long)row * e.ldc + col0;
+      } else {
+        const int sq = e.seq[row];
+        if (sq < 0 || sq >= e.B) {
+          atomicOr(e.flags, FLAG_BAD_SEQ);
+          continue;
+        }
+        if (e.kv_branch == 0)
+          norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps,
+                        rt);
+        dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
+              ((((long long)sq * e.k + bidx) * e.Hkv + col0 / HD) * e.Tmax + ps) * HD;
+      }
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);
+    }
+  } else {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += 32) {
+      uint32_t r[32];
+      float v[32];
+      __syncwarp();
+      tmem_ld32(taddr + c0, r);
+      if constexpr (DUAL) {
+        uint32_t r2[32];
+        tmem_ld32(taddr + BN + c0, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float gt = __uint_as_float(r[i]);
+          v[i] = gt / (1.f + __expf(-gt)) * __uint_as_float(r2[i]);
+        }
+      } else {
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      }
+      const int col = n0 + c0;
+      if (!row_ok || col >= p.N) continue;
+      const bool full = col + 32 <= p.N;
+      if constexpr (MODE == EPI_RESID) {
+        const __nv_bfloat16* rp = (const __nv_bfloat16*)e.R + (long long)row * e.ldr + col;
+        if (full && p.vec_res) {
+          float rv[32];
+          ld_bf16x32(rp, rv);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] += rv[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col + i < p.N) v[i] += __bfloat162float(rp[i]);
+        }
+      }
+      const long long orow = (MODE == EPI_STORE && e.rowmap) ? e.rowmap[row] : row;
+      const long long off = (long long)bidx * e.c_bstride + orow * e.ldc + col;
+      if (e.out_f32) {
+        float* cp = (float*)e.C + off;
+        if (full && p.vec_out) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(cp + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col + i < p.N) cp[i] = v[i];
+        }
+      } else {
+        __nv_bfloat16* cp = (__nv_bfloat16*)e.C + off;
+        if (full && p.vec_out) {
+          st_bf16x32(cp, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col + i < p.N) cp[i] = __float2bfloat16_rn(v[i]);
+        }
+      }
+    }
+  }
+}
+
+template <int BN, bool DUAL>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (DUAL ? 2 : 1);
+  static constexpr int STAGES = (DUAL || BN == 256) ? 4 : 6;
+  static constexpr int ACC_COLS = BN * (DUAL ? 2 : 1);
+  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+template <int BN, bool DUAL, int MODE, int HD>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmB2, const Params p) {
+  using C = Cfg<BN, DUAL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* mma_done = tempty + 2;
+  uint32_t* tmem_holder = (uint32_t*)(mma_done + 1);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+    if (DUAL) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB2) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_holder)),
+                 "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0, used = 0, last_phase = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const int bidx = (int)(t / tiles_per_batch);
+        const int rem = (int)(t % tiles_per_batch);
+        const int mt = rem % p.m_tiles, nt = rem / p.m_tiles;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+          tma_load3(&tmA, &full[stage], sa, kb * BK, mt * BM, bidx);
+          tma_load3(&tmB, &full[stage], sa + C::A_BYTES, kb * BK, nt * BN, bidx);
+          if (DUAL) tma_load3(&tmB2, &full[stage], sa + C::A_BYTES + C::B_BYTES, kb * BK, nt * BN, bidx);
+          used |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.epi.flags, FLAG_TIMEOUT);
+      }
+      // Drain: every issued copy has landed before the CTA may exit.
+      volatile int no_abort = 0;
+      for (int s = 0; s < C::STAGES; ++s)
+        if (used & (1u << s)) mbar_wait(&full[s], (last_phase >> s) & 1, &no_abort);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = idesc_bf16(BN);
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        fence_after();
+        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t sa = su32(smem + stage * C::STAGE_BYTES);
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16) {
+            const uint32_t accum = (kb | k16) != 0;
+            umma(d_tmem, sdesc(sa + 32 * k16), sdesc(sb + 32 * k16), idesc, accum);
+            if (DUAL) umma(d_tmem + BN, sdesc(sa + 32 * k16), sdesc(sb + C::B_BYTES + 32 * k16), idesc, accum);
+          }
+          umma_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.epi.flags, FLAG_TIMEOUT);
+      }
+      // Every issued MMA has completed before TMEM is released.
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, &no_abort);
+    }
+  } else {
+    // ---------------- epilogue warps ----------------
+    const int quarter = warp & 3;
+    int it = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          *abort_flag = 1;
+          atomicOr(p.epi.flags, FLAG_TIMEOUT);
+        }
+        break;
+      }
+      fence_after();
+      const int bidx = (int)(t / tiles_per_batch);
+      const int rem = (int)(t % tiles_per_batch);
+      const int mt = rem % p.m_tiles, nt = rem / p.m_tiles;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS;
+      epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"((uint32_t)C::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, long long K, long long rows, long long batch,
+              long long ld, long long bstride, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)batch};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2,
+                           (cuuint64_t)(batch > 1 ? bstride : rows * ld) * 2};
+  cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 148;
+}
+
+template <int BN, bool DUAL, int MODE, int HD>
+cudaError_t run(const GemmDesc& g, cudaStream_t st) {
+  using C = Cfg<BN, DUAL>;
+  CUtensorMap ta, tb, tb2;
+  if (!make_map(&ta, g.A, g.K, g.M, g.batch, g.lda, g.a_bstride, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tb, g.B, g.K, g.N, g.batch, g.ldb, g.b_bstride, BN)) return cudaErrorInvalidValue;
+  if (DUAL) {
+    if (!make_map(&tb2, g.B2, g.K, g.N, g.batch, g.ldb, g.b_bstride, BN))
+      return cudaErrorInvalidValue;
+  } else {
+    tb2 = tb;
+  }
+  Params p;
+  p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
+  p.m_tiles = (g.M + BM - 1) / BM;
+  p.n_tiles = (g.N + BN - 1) / BN;
+  p.num_kb = (g.K + BK - 1) / BK;
+  p.total_tiles = (long long)p.m_tiles * p.n_tiles * g.batch;
+  p.epi = g.epi;
+  const size_t osz = g.epi.out_f32 ? 4 : 2;
+  p.vec_out = ((uintptr_t)g.epi.C % 16 == 0) && ((g.epi.ldc * osz) % 16 == 0) &&
+              ((g.epi.c_bstride * osz) % 16 == 0);
+  p.vec_res = ((uintptr_t)g.epi.R % 16 == 0) && ((g.epi.ldr * 2) % 16 == 0);
+  auto kern = gemm_tc_kernel<BN, DUAL, MODE, HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  kern<<<(int)grid, NTHREADS, C::SMEM, st>>>(ta, tb, tb2, p);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+bool gemm_tc_supported(const GemmDesc& g) {
+  auto a16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
+  if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batch <= 0) return false;
+  if (!a16(g.A) || !a16(g.B) || (g.B2 && !a16(g.B2))) return false;
+  if (g.lda % 8 || g.ldb % 8) return false;
+  if (g.batch > 1 && (g.a_bstride % 8 || g.b_bstride % 8)) return false;
+  if (g.epi.mode == EPI_QNORM_ROPE || g.epi.mode == EPI_KV) {
+    if ((g.epi.d != 64 && g.epi.d != 128) || g.N % g.epi.d) return false;
+  }
+  if ((g.epi.mode == EPI_SWIGLU) != (g.B2 != nullptr)) return false;
+  return tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
+  switch (g.epi.mode) {
+    case EPI_SWIGLU:
+      return tc::run<128, true, EPI_SWIGLU, 0>(g, st);
+    case EPI_STORE:
+      return g.N >= 256 ? tc::run<256, false, EPI_STORE, 0>(g, st)
+                        : tc::run<128, false, EPI_STORE, 0>(g, st);
+    case EPI_RESID:
+      return g.N >= 256 ? tc::run<256, false, EPI_RESID, 0>(g, st)
+                        : tc::run<128, false, EPI_RESID, 0>(g, st);
+    case EPI_QNORM_ROPE:
+    case EPI_KV: {
+      const bool wide = g.N % 256 == 0;
+      if (g.epi.mode == EPI_QNORM_ROPE) {
+        if (g.epi.d == 128)
+          return wide ? tc::run<256, false, EPI_QNORM_ROPE, 128>(g, st)
+                      : tc::run<128, false, EPI_QNORM_ROPE, 128>(g, st);
+        return wide ? tc::run<256, false, EPI_QNORM_ROPE, 64>(g, st)
+                    : tc::run<128, false, EPI_QNORM_ROPE, 64>(g, st);
+      }
+      if (g.epi.d == 128)
+        return wide ? tc::run<256, false, EPI_KV, 128>(g, st)
+                    : tc::run<128, false, EPI_KV, 128>(g, st);
+      return wide ? tc::run<256, false, EPI_KV, 64>(g, st) : tc::run<128, false, EPI_KV, 64>(g, st);
+    }
+  }
+  return cudaErrorNotSupported;
+}
 
 }  // namespace wm

@@ -54,3 +54,75 @@ def small_shape(dtype="f32", **kw):
     base = dict(L=4, D=128, k=2, p=2, Hq=4, Hkv=2, d=64, F=256, V=512, dtype=dtype)
     base.update(kw)
     return synth.ModelShape(**base)
+
+
+def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", check=None):
+    """Run ``passes`` cyclic passes on the GPU one group at a time. Before each
+    checked group (``check(n, q)``), copy the GPU cache to the host, run the
+    oracle's same group from that snapshot, and compare what the group wrote
+    (its cache positions and logits). Returns the worst relative errors.
+
+    Comparing step by step gives both sides identical inputs at every group,
+    which whole-sequence comparison cannot: the random-weight models amplify
+    any bf16-level difference along the sequence (see the design notes)."""
+    import oracle.whitematter as O
+    s = m.shape
+    oc = ocfg(s)
+    B, T = tokens_h.shape
+    Tmax = Tmax or T
+    tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
+    ck, cv = m.new_cache(B, Tmax)
+    ws = m.workspace(wm.rows_for_pass(B, T, g), Tmax)
+    lg = torch.zeros((B, T, s.V) if logits_mode == "all" else (B, s.V), dtype=torch.float32,
+                     device="cuda")
+    worst = {"cache": 0.0, "logits": 0.0, "checked": 0}
+    for n in range(passes):
+        mode = logits_mode if n == passes - 1 else "none"
+        for q in range(g):
+            do = check is None or check(n, q)
+            if do:
+                torch.cuda.synchronize()
+                sk, sv = host(ck), host(cv)
+            wm.wm_cyclic_pass(m, tok, g, ck, cv, ws, q_begin=q, q_end=q + 1,
+                              logits=None if mode == "none" else lg, logits_mode=mode)
+            if not do:
+                continue
+            torch.cuda.synchronize()
+            rl = O.cyclic_pass(oc, Wn, tokens_h, g, sk, sv, q_begin=q, q_end=q + 1,
+                               logits=None if mode == "none" else mode)
+            P = np.arange(q, T, g)
+            gk, gv = host(ck), host(cv)
+            worst["cache"] = max(worst["cache"], relerr(gk[:, :, :, P], sk[:, :, :, P]),
+                                 relerr(gv[:, :, :, P], sv[:, :, :, P]))
+            if mode == "all":
+                worst["logits"] = max(worst["logits"], relerr(host(lg)[:, P], rl[:, P]))
+            elif mode == "last" and (T - 1) % g == q:
+                worst["logits"] = max(worst["logits"], relerr(host(lg), rl))
+            worst["checked"] += 1
+    assert wm.wm_check_flags(ws) == 0
+    return worst
+
+
+def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None):
+    """Decode steps t = 0..T-1 on the GPU; each step is compared with the
+    oracle's step from the GPU's cache snapshot. Returns worst errors."""
+    import oracle.whitematter as O
+    s = m.shape
+    oc = ocfg(s)
+    B, T = tokens_h.shape
+    ck, cv = m.new_cache(B, Tmax) if start_cache is None else start_cache
+    ws = m.workspace(B, Tmax)
+    lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
+    tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
+    worst = {"cache": 0.0, "logits": 0.0}
+    for t in range(T):
+        torch.cuda.synchronize()
+        sk, sv = host(ck), host(cv)
+        wm.wm_decode_step(m, tok[:, t].contiguous(), t, ck, cv, lg, ws)
+        torch.cuda.synchronize()
+        rl = O.decode_step(oc, Wn, tokens_h[:, t], t, sk, sv)
+        worst["logits"] = max(worst["logits"], relerr(host(lg), rl))
+        worst["cache"] = max(worst["cache"], relerr(host(ck)[:, :, :, t], sk[:, :, :, t]),
+                             relerr(host(cv)[:, :, :, t], sv[:, :, :, t]))
+    assert wm.wm_check_flags(ws) == 0
+    return worst
