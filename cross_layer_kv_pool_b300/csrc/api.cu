@@ -140,7 +140,7 @@ Epi base_epi(const Ctx& x) {
 // Layer stack of N rows whose h^0 is already in stash[:, 0]. Layer l reads
 // stash[:, l], writes stash[:, l+1] (or h^L), and emits inv_rms / router
 // inputs of its input state. The last layer's body runs only if requested.
-void run_stack(const Ctx& x, int N, bool last_layer, void* cache_k, void* cache_v, int B,
+void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void* cache_v, int B,
                int Tmax, bool emit_rin) {
   const wm_config& c = *x.c;
   const wm_weights& w = *x.w;
@@ -173,7 +173,7 @@ void run_stack(const Ctx& x, int N, bool last_layer, void* cache_k, void* cache_
       a.channel = l % c.k; a.cache_k = cache_k; a.cache_v = cache_v;
       a.B = B; a.k = c.k; a.Hq = c.Hq; a.Hkv = c.Hkv; a.d = c.d; a.Tmax = Tmax;
       a.out = x.buf<void>(B_O); a.flags = x.flags();
-      launch_attention(c.dtype, a, !x.tc, x.st);
+      launch_attention(c.dtype, a, !x.tc, x.st, nq);
     }
     {  // O projection + residual
       GemmDesc g;
@@ -332,7 +332,7 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.q = q; a.N = N; a.seq = seq; a.pos = pos; a.channel = channel;
   a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
-  launch_attention(cfg->dtype, a, !x.tc, x.st);
+  launch_attention(cfg->dtype, a, !x.tc, x.st, 0);
   return finish(x);
 }
 
@@ -364,7 +364,7 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
                  (long long)c.L * c.D, x.flags(), x.st);
     const bool has_last = (T - 1) % g == q;
     const bool want = logits_mode == WM_LOGITS_ALL || (logits_mode == WM_LOGITS_LAST && has_last);
-    run_stack(x, N, want, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+    run_stack(x, N, nq, want, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
     if (want) {
       GemmDesc lg;
       lg.N = c.V; lg.K = c.D; lg.B = w->lm_head; lg.ldb = c.D;
@@ -407,7 +407,7 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
                      x.buf<int32_t>(B_POS), x.st);
   launch_embed(c.dtype, x.buf<int32_t>(B_TOK), B, w->embed, c.V, c.D, x.buf<void>(B_STASH),
                (long long)c.L * c.D, x.flags(), x.st);
-  run_stack(x, B, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+  run_stack(x, B, 1, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
   launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, B, c.D, w->final_norm,
                  x.buf<void>(B_LASTX), c.eps, x.st);
   GemmDesc lg;

@@ -48,9 +48,285 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const AttnArgs a) {
   for (int e = 0; e < per; ++e) out[lane * per + e] = from_f<S>(i > 0 ? o[e] / l : 0.f);
 }
 
-void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st) {
+// ---------------------------------------------------------------------------
+// Tensor-core engine (bf16): flash attention on mma.sync m16n8k16.
+// A CTA owns one KV head and a tile of consecutive rows; the G = Hq/Hkv query
+// heads of each row are packed into the 64-row M dimension (row-major: M-row
+// m = row (m / G), head hk*G + m % G). The tile is processed as maximal runs of
+// rows sharing a sequence, so any row list is handled; rows of one sequence
+// that are contiguous (every prefill group) form a single run. Keys stream
+// through shared memory in blocks of 64 with cp.async double buffering; the
+// softmax is online in fp32 (exp2 with the 1/sqrt(d) scale folded in).
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int AQ = 64, AKV = 64, ATHREADS = 128;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src), "r"(n)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+}  // namespace
+
+template <int HD>
+__global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, int rpt, int nq) {
+  constexpr int LDS = HD + 8;  // padded smem row (elements): conflict-free ldmatrix
+  extern __shared__ __align__(16) uint8_t sm[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm);
+  __nv_bfloat16* sK = sQ + AQ * LDS;           // [2][AKV][LDS]
+  __nv_bfloat16* sV = sK + 2 * AKV * LDS;      // [2][AKV][LDS]
+  __shared__ int s_pos[AQ];
+  __shared__ int s_maxp;
+
+  const int G = a.Hq / a.Hkv;
+  const int hk = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int t0, t1;  // rows of this tile
+  if (nq > 0) {
+    const int tps = (nq + rpt - 1) / rpt;
+    const int b = blockIdx.x / tps, t = tps - 1 - blockIdx.x % tps;  // late positions first
+    t0 = b * nq + t * rpt;
+    t1 = min(t0 + rpt, (b + 1) * nq);
+  } else {
+    t0 = blockIdx.x * rpt;
+    t1 = min(t0 + rpt, a.N);
+  }
+  const float sl2 = 1.4426950408889634f / sqrtf((float)HD);
+  const __nv_bfloat16* qg = (const __nv_bfloat16*)a.q;
+  __nv_bfloat16* og = (__nv_bfloat16*)a.out;
+
+  for (int ra = t0; ra < t1;) {
+    // ---- the run [ra, rb) of rows sharing sequence seq[ra] ----
+    const int sq = a.seq[ra];
+    int rb = ra + 1;
+    while (rb < t1 && a.seq[rb] == sq) ++rb;
+    const int mrows = (rb - ra) * G;
+    const bool seq_ok = sq >= 0 && sq < a.B;
+    __syncthreads();  // previous run finished with shared memory
+    if (threadIdx.x == 0) s_maxp = 0;
+    __syncthreads();
+    if (threadIdx.x < AQ) {
+      int p = -1;
+      if (threadIdx.x < mrows) {
+        p = a.pos[ra + threadIdx.x / G];
+        if (!seq_ok || p < 0 || p >= a.Tmax) {
+          if (threadIdx.x % G == 0) atomicOr(a.flags, seq_ok ? FLAG_BAD_POS : FLAG_BAD_SEQ);
+          p = -2;  // invalid row: output zeros
+        }
+      }
+      s_pos[threadIdx.x] = p;
+      if (p > 0) atomicMax(&s_maxp, p);
+    }
+    // Q tile: M-row m -> q[row][head]
+    for (int c = threadIdx.x; c < AQ * (HD / 8); c += ATHREADS) {
+      const int m = c / (HD / 8), part = c % (HD / 8);
+      const bool v = m < mrows;
+      const int r = ra + (v ? m / G : 0), h = hk * G + (v ? m % G : 0);
+      cp_async16(sQ + m * LDS + part * 8, qg + ((long long)r * a.Hq + h) * HD + part * 8, v);
+    }
+    cp_async_commit();
+    __syncthreads();
+    const int maxp = s_maxp;
+    const int nkb = (maxp + AKV - 1) / AKV;
+    const long long kvbase = seq_ok ? (((long long)sq * a.k + a.channel) * a.Hkv + hk) * a.Tmax * HD : 0;
+    const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.cache_k + kvbase;
+    const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.cache_v + kvbase;
+
+    auto load_kv = [&](int kb, int buf) {
+      for (int c = threadIdx.x; c < AKV * (HD / 8); c += ATHREADS) {
+        const int rr = c / (HD / 8), part = c % (HD / 8);
+        const int s = kb * AKV + rr;
+        const bool v = s < maxp;
+        const long long off = (long long)(v ? s : 0) * HD + part * 8;
+        cp_async16(sK + (buf * AKV + rr) * LDS + part * 8, Kg + off, v);
+        cp_async16(sV + (buf * AKV + rr) * LDS + part * 8, Vg + off, v);
+      }
+      cp_async_commit();
+    };
+    if (nkb > 0) load_kv(0, 0);
+
+    // per-thread rows: g and g + 8 of this warp's 16
+    const int mr0 = warp * 16 + (lane >> 2), mr1 = mr0 + 8;
+    const int p0 = s_pos[mr0], p1 = s_pos[mr1];
+    float o[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t qf[HD / 16][4];
+    cp_async_wait<0>();  // Q (and the first K/V block) landed
+    __syncthreads();
+    {
+      const int row = warp * 16 + (lane & 15), col = (lane >> 4) * 8;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks)
+        ldsm_x4(smem_addr(sQ + row * LDS + ks * 16 + col), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    }
+
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int buf = kb & 1;
+      if (kb + 1 < nkb) {
+        load_kv(kb + 1, buf ^ 1);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      __syncthreads();
+      const __nv_bfloat16* Kb = sK + buf * AKV * LDS;
+      const __nv_bfloat16* Vb = sV + buf * AKV * LDS;
+      // S = Q K^T for 16 rows x 64 keys
+      float sc[AKV / 8][4];
+#pragma unroll
+      for (int nt = 0; nt < AKV / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < AKV / 8; ++nt) {
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ks += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(smem_addr(Kb + (nt * 8 + (lane & 7)) * LDS + ks * 16 + (lane >> 3) * 8), b0, b1,
+                  b2, b3);
+          mma_bf16(sc[nt], qf[ks], b0, b1);
+          mma_bf16(sc[nt], qf[ks + 1], b2, b3);
+        }
+      }
+      // mask keys s >= pos of the row, online softmax
+      float mx0 = m0, mx1 = m1;
+#pragma unroll
+      for (int nt = 0; nt < AKV / 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int s = kb * AKV + nt * 8 + 2 * (lane & 3) + e;
+          sc[nt][e] = s < p0 ? sc[nt][e] * sl2 : -INFINITY;
+          sc[nt][2 + e] = s < p1 ? sc[nt][2 + e] * sl2 : -INFINITY;
+          mx0 = fmaxf(mx0, sc[nt][e]);
+          mx1 = fmaxf(mx1, sc[nt][2 + e]);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float base0 = mx0 == -INFINITY ? 0.f : mx0;
+      const float base1 = mx1 == -INFINITY ? 0.f : mx1;
+      const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+      m0 = mx0;
+      m1 = mx1;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pf[AKV / 16][4];
+#pragma unroll
+      for (int nt = 0; nt < AKV / 8; ++nt) {
+        const float e0 = exp2f(sc[nt][0] - base0), e1 = exp2f(sc[nt][1] - base0);
+        const float e2 = exp2f(sc[nt][2] - base1), e3 = exp2f(sc[nt][3] - base1);
+        rs0 += e0 + e1;
+        rs1 += e2 + e3;
+        pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(e0, e1);
+        pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(e2, e3);
+      }
+      l0 = l0 * corr0 + rs0;
+      l1 = l1 * corr1 + rs1;
+#pragma unroll
+      for (int i = 0; i < HD / 8; ++i) {
+        o[i][0] *= corr0; o[i][1] *= corr0;
+        o[i][2] *= corr1; o[i][3] *= corr1;
+      }
+      // O += P V
+#pragma unroll
+      for (int j = 0; j < AKV / 16; ++j) {
+        const uint32_t pa[4] = {pf[j][0], pf[j][1], pf[j][2], pf[j][3]};
+#pragma unroll
+        for (int dn = 0; dn < HD / 8; dn += 2) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(smem_addr(Vb + (j * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + dn * 8 +
+                              (lane >> 4) * 8),
+                    b0, b1, b2, b3);
+          mma_bf16(o[dn], pa, b0, b1);
+          mma_bf16(o[dn + 1], pa, b2, b3);
+        }
+      }
+      __syncthreads();  // this buffer may be overwritten by the next prefetch
+    }
+    // quad-reduce the row sums, normalise, store
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const float i0 = p0 > 0 ? 1.f / l0 : 0.f, i1 = p1 > 0 ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int m = half ? mr1 : mr0;
+      const float inv = half ? i1 : i0;
+      if (m >= mrows) continue;
+      const int r = ra + m / G, h = hk * G + m % G;
+      __nv_bfloat16* dst = og + ((long long)r * a.Hq + h) * HD + 2 * (lane & 3);
+#pragma unroll
+      for (int dn = 0; dn < HD / 8; ++dn) {
+        const float x = o[dn][half * 2] * inv, y = o[dn][half * 2 + 1] * inv;
+        *reinterpret_cast<__nv_bfloat162*>(dst + dn * 8) = __floats2bfloat162_rn(x, y);
+      }
+    }
+    ra = rb;
+  }
+}
+
+template <int HD>
+void launch_attn_mma(const AttnArgs& a, int nq, cudaStream_t st) {
+  const int G = a.Hq / a.Hkv;
+  const int rpt = AQ / G;
+  int tiles;
+  if (nq > 0) {
+    const int B = a.N / nq;
+    tiles = B * ((nq + rpt - 1) / rpt);
+  } else {
+    tiles = (a.N + rpt - 1) / rpt;
+  }
+  const size_t smem = (size_t)(AQ + 4 * AKV) * (HD + 8) * 2;
+  cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid(tiles, a.Hkv);
+  attn_mma_kernel<HD><<<grid, ATHREADS, smem, st>>>(a, rpt, nq);
+}
+
+// nq > 0 declares the rows as B = N / nq sequences of nq consecutive rows
+// (cyclic groups and decode steps); 0 = no structure assumed.
+void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq) {
   if (a.N <= 0) return;
-  (void)simt;
+  const int G = a.Hq / a.Hkv;
+  if (dtype == WM_BF16 && !simt && G <= AQ) {
+    if (nq > 0 && a.N % nq) nq = 0;
+    if (a.d == 128) launch_attn_mma<128>(a, nq, st);
+    else launch_attn_mma<64>(a, nq, st);
+    return;
+  }
   const long long warps = (long long)a.N * a.Hq;
   const int blocks = (int)((warps + 3) / 4);
   WM_DISPATCH_S(dtype, attn_simt_kernel<S><<<blocks, 128, 0, st>>>(a));

@@ -58,7 +58,7 @@ struct AttnArgs {
   void* out;              // [N][Hq*d]
   uint32_t* flags;
 };
-void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st);
+void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq);
 
 // ---- pool.cu ---------------------------------------------------------------
 struct MixArgs {

@@ -11,10 +11,24 @@ import torch
 from cross_layer_kv_pool_b300 import build, synth, wm
 
 # Tolerances, max|gpu - ref| / max|ref| per tensor: 1e-4 in fp32 mode; in bf16
-# mode 2e-2 on logits and caches after whole passes, 1e-2 on the mixed
-# channels and on a single attention call given identical inputs.
-TOL = {"f32": dict(logits=1e-4, cache=1e-4, mixed=1e-4, coeff=1e-4, attn=1e-4),
-       "bf16": dict(logits=2e-2, cache=2e-2, mixed=1e-2, coeff=2e-2, attn=1e-2)}
+# mode 2e-2 on logits, 1e-2 on the mixed channels and on a single attention
+# call, 2e-2 on K/V written from identical states. Cache entries written by a
+# whole bf16 group step of a deep stack (8+ layers) use ``cache_step``: the
+# oracle in bf16-storage mode, run against itself with weights perturbed by
+# 1e-7..1e-5 (the scale of fp32-vs-fp64 arithmetic), already differs by
+# 2.5-3.8% max-element and 1.0-1.6% in norm on those entries, because single
+# bf16 rounding flips are amplified by the signed mixing; the bounds are about
+# 2.5x that spread. Logits keep 2e-2 in every case.
+TOL = {"f32": dict(logits=1e-4, cache=1e-4, mixed=1e-4, coeff=1e-4, attn=1e-4,
+                   cache_step=1e-4, cache_step_norm=1e-4),
+       "bf16": dict(logits=2e-2, cache=2e-2, mixed=1e-2, coeff=2e-2, attn=1e-2,
+                    cache_step=1e-1, cache_step_norm=3e-2)}
+
+
+def normerr(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
 
 def ensure_lib():
@@ -75,7 +89,7 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
     ws = m.workspace(wm.rows_for_pass(B, T, g), Tmax)
     lg = torch.zeros((B, T, s.V) if logits_mode == "all" else (B, s.V), dtype=torch.float32,
                      device="cuda")
-    worst = {"cache": 0.0, "logits": 0.0, "checked": 0}
+    worst = {"cache": 0.0, "cache_norm": 0.0, "logits": 0.0, "checked": 0}
     for n in range(passes):
         mode = logits_mode if n == passes - 1 else "none"
         for q in range(g):
@@ -94,6 +108,8 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
             gk, gv = host(ck), host(cv)
             worst["cache"] = max(worst["cache"], relerr(gk[:, :, :, P], sk[:, :, :, P]),
                                  relerr(gv[:, :, :, P], sv[:, :, :, P]))
+            worst["cache_norm"] = max(worst["cache_norm"], normerr(gk[:, :, :, P], sk[:, :, :, P]),
+                                      normerr(gv[:, :, :, P], sv[:, :, :, P]))
             if mode == "all":
                 worst["logits"] = max(worst["logits"], relerr(host(lg)[:, P], rl[:, P]))
             elif mode == "last" and (T - 1) % g == q:
