@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the WhiteMatter cross-layer KV pool path on one B300.
+
+One step is one whole prefill of a batch: a zeroed k-channel cache, three
+cyclic Gauss-Seidel passes with g = 16 over B x T tokens (the cache updated
+after every group), and the last-position logits in the final pass, all
+through the C ABI (``wm_cyclic_pass``). The default workload is the 1.3B-scale
+half-cache model (L=28, D=1792, k=14, p=2, Hq=14, Hkv=2, d=128, F=4608,
+V=151936) at B=64, T=2048. After the timed steps, 256 decode steps of that
+model run from the prefilled cache (Tmax = 2304) and are reported as
+``decode``. Inputs are seeded and synthetic; weights are N(0, 0.02) with unit
+norm gains.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+path has no exchange step); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from cross_layer_kv_pool_b300 import synth  # noqa: E402
+
+METRIC = "prefill tok/s (3 cyclic passes, g=16) at 1.3B k=14"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_1p3b",
+                    choices=["prefill_1p3b", "half_small", "full_small"])
+    ap.add_argument("--decode-steps", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--k", type=int, default=None, help="override the channel count k")
+    return ap.parse_args()
+
+
+def workload(args):
+    wl = dict(synth.WORKLOADS[args.workload])
+    if args.k is not None:
+        wl["shape"] = wl["shape"].replace(k=args.k)
+    return wl
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_weights(shape, seed: int = 0):
+    W = synth.make_weights(shape, seed=seed, device="cpu")
+    return {n: t.float().numpy() for n, t in W.items()}
+
+
+def cpu_sample(shape, rows: int, Wn, seed: int = 0):
+    """Time the CPU oracle on ``rows`` token rows of one cyclic group: the
+    layer stack plus the pool, against a cache of the workload's length.
+    Returns (seconds, rows, threads)."""
+    import oracle.whitematter as O
+    from types import SimpleNamespace
+    import dataclasses
+    oc = SimpleNamespace(**dataclasses.asdict(shape))
+    oc.storage = "bf16"
+    T, g = 2048, 16
+    q = g - 1
+    pos = np.arange(q, T, g)[:rows]
+    toks = np.random.default_rng(seed).integers(0, shape.V, size=rows)
+    ck, cv = O.new_cache(oc, 1, T)
+    threads = torch.get_num_threads()
+    t0 = time.perf_counter()
+    O.run_rows(oc, Wn, toks, np.zeros(rows, dtype=np.int64), pos, ck, cv, want_logits=False)
+    return time.perf_counter() - t0, rows, threads
+
+
+def cpu_baseline_record(shape, passes: int, rows: int):
+    secs, n, threads = cpu_sample(shape, rows, oracle_weights(shape))
+    tok_s = n / secs / passes
+    return {"value": tok_s, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": (f"{n} token rows of one cyclic group (positions 15, 31, ... of a "
+                       f"2048-token sequence) through the {shape.L}-layer stack and the pool, "
+                       f"fp64 NumPy, {secs:.1f} s; tok/s = rows / time / {passes} passes")}
+
+
+def run_reference(args, ws, rank):
+    """The CPU oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    wl = workload(args)
+    shape = wl["shape"]
+    rows = 2
+    samples = []
+    Wn = oracle_weights(shape)
+    for i in range(args.warmup + args.steps):
+        secs, n, threads = cpu_sample(shape, rows, Wn, seed=i)
+        if i >= args.warmup:
+            samples.append(n / secs / wl["passes"])
+    value = statistics.mean(samples)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * rows / (value * wl["passes"]),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": config_dict(args, wl),
+        "cpu_baseline": {"value": value, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step {rows} token rows of one cyclic group through the "
+                                   f"{shape.L}-layer stack and pool (fp64 NumPy), extrapolated "
+                                   f"to {wl['passes']} passes"},
+        "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(args, wl):
+    s = wl["shape"]
+    return {"workload": f"{args.workload}: 3 cyclic passes g={wl['g']} + last-position logits",
+            "L": s.L, "D": s.D, "k": s.k, "p": s.p, "Hq": s.Hq, "Hkv": s.Hkv, "d": s.d,
+            "F": s.F, "V": s.V, "global_batch": wl["B"] * args.gpus, "seq_len": wl["T"],
+            "g": wl["g"], "passes": wl["passes"], "parallelism": f"replicas x{args.gpus}",
+            "l2": "inputs larger than L2 (weights 2.9 GB, 0.8 GB layer-state stash per group)"
+                  if args.workload == "prefill_1p3b" else "inputs larger than L2"}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args, ws, rank, local):
+    from cross_layer_kv_pool_b300 import wm
+
+    wl = workload(args)
+    s = wl["shape"]
+    B, T, g, passes = wl["B"], wl["T"], wl["g"], wl["passes"]
+    nd = args.decode_steps
+    Tmax = T + nd
+    dev = torch.device("cuda", torch.cuda.current_device())
+    W = synth.make_weights(s, seed=0, device=dev)
+    m = wm.Model(s, W)
+    tok = synth.make_tokens(s, B, T, seed=1 + rank, device=dev)
+    dec_tok = synth.make_tokens(s, B, max(nd, 1), seed=2 + rank, device=dev)
+    ck, cv = m.new_cache(B, Tmax)
+    wsp = m.workspace(max(wm.rows_for_pass(B, T, g), B), Tmax)
+    lg = torch.empty((B, s.V), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(tokens):
+        ck.zero_()
+        cv.zero_()
+        for n in range(passes):
+            last = n == passes - 1
+            wm.wm_cyclic_pass(m, tokens, g, ck, cv, wsp, logits=lg if last else None,
+                              logits_mode="last" if last else "none")
+
+    for _ in range(args.warmup):
+        step(tok)
+    torch.cuda.synchronize()
+    if wm.wm_check_flags(wsp) != 0:
+        raise RuntimeError("device-side checks failed during warm-up")
+
+    # ---- timed region: K steps; per-kernel events on three of them ----
+    tracers = [wm.Tracer(wm.WM_TRACE_GEMM, 512), wm.Tracer(wm.WM_TRACE_MIX, 64),
+               wm.Tracer(wm.WM_TRACE_ATTN, 256)]
+    launches = wm.Tracer(wm.WM_TRACE_GEMM, 1)  # launch counting only
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        tr = tracers[i] if i < len(tracers) else launches
+        tr.attach(m)
+        step(tok)
+        wm.Tracer.detach(m)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(ws)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, ws)
+    gpu_launches = int(sum(t.t.launches for t in tracers[:args.steps]) + launches.t.launches)
+    value = ws * B * T / (ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers ----
+    tok_host = tok.cpu().pin_memory()
+    lg_host = torch.empty((B, s.V), dtype=torch.float32).pin_memory()
+    tok_dev = torch.empty_like(tok)
+    for _ in range(max(1, args.warmup // 2)):
+        tok_dev.copy_(tok_host, non_blocking=True)
+        step(tok_dev)
+        lg_host.copy_(lg, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier(ws)
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        tok_dev.copy_(tok_host, non_blocking=True)
+        step(tok_dev)
+        lg_host.copy_(lg, non_blocking=True)
+    x1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(x0.elapsed_time(x1) / args.steps, ws)
+    e2e = {"value": ws * B * T / (ms_e2e / 1e3), "unit": "tok/s",
+           "h2d_bytes_per_step": tok_host.numel() * 4, "d2h_bytes_per_step": lg_host.numel() * 4}
+
+    # ---- decode from the prefilled cache ----
+    decode = None
+    if nd > 0:
+        dlg = torch.empty((B, s.V), dtype=torch.float32, device=dev)
+        step(tok)
+        for t in range(3):  # warm-up, overwritten below
+            wm.wm_decode_step(m, dec_tok[:, t].contiguous(), T + t, ck, cv, dlg, wsp)
+        cols = [dec_tok[:, t].contiguous() for t in range(nd)]
+        torch.cuda.synchronize()
+        barrier(ws)
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for t in range(nd):
+            wm.wm_decode_step(m, cols[t], T + t, ck, cv, dlg, wsp)
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dms = max_over_ranks(d0.elapsed_time(d1), ws)
+        cache_bytes = 2 * B * s.k * s.Hkv * Tmax * s.d * 2
+        decode = {"value": ws * B * nd / (dms / 1e3), "unit": "tok/s", "steps": nd, "batch": B,
+                  "prefix": T, "ms_per_step": dms / nd, "peak_cache_bytes": cache_bytes,
+                  "cache_bytes_L_channels": cache_bytes // s.k * s.L}
+    if wm.wm_check_flags(wsp) != 0:
+        raise RuntimeError("device-side checks failed")
+
+    # ---- per-kernel rooflines from the traced launches ----
+    pk, pk_kind = peaks()
+
+    def summarise(tr, unit):
+        res = tr.results()
+        if not res:
+            return None
+        tot_ms = sum(r[0] for r in res)
+        tot_w = sum(r[1] for r in res)
+        return {"launches": len(res), "avg_ms": tot_ms / len(res), "work_per_launch": tot_w / len(res),
+                "achieved": tot_w / (tot_ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)}
+
+    gemm = summarise(tracers[0], "TFLOP/s") if args.steps >= 1 else None
+    mix = summarise(tracers[1], "GB/s") if args.steps >= 2 else None
+    attn = summarise(tracers[2], "TFLOP/s") if args.steps >= 3 else None
+    tc_peak = pk.get("bf16_tflops_sustained", 1400.0)
+    roofline = None
+    if gemm:
+        roofline = {"kernel": "gemm_tc_kernel (tcgen05 GEMM engine, all stack/router/projection/"
+                              "LM-head contractions)",
+                    "bound": "tensor", "achieved": gemm["achieved"], "peak": tc_peak,
+                    "unit": "TFLOP/s", "frac": gemm["achieved"] / tc_peak, "traffic": None,
+                    "peak_source": f"{pk_kind} bf16_tflops_sustained",
+                    "launches_timed": gemm["launches"], "avg_launch_ms": gemm["avg_ms"],
+                    "flops_per_launch": gemm["work_per_launch"]}
+    mixer = None
+    if mix:
+        hbm = pk.get("hbm_gbs", 6400.0)
+        mixer = {"bound": "hbm", "achieved": mix["achieved"], "peak": hbm, "unit": "GB/s",
+                 "frac": mix["achieved"] / hbm, "peak_source": f"{pk_kind} hbm_gbs",
+                 "launches_timed": mix["launches"], "avg_launch_ms": mix["avg_ms"],
+                 "bytes_per_launch": mix["work_per_launch"]}
+    attention = None
+    if attn:
+        attention = {"bound": "tensor", "achieved": attn["achieved"], "peak": tc_peak,
+                     "unit": "TFLOP/s", "frac": attn["achieved"] / tc_peak,
+                     "flops": "causal only (4*Hq*d per visible key)",
+                     "launches_timed": attn["launches"], "avg_launch_ms": attn["avg_ms"]}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_record(s, passes, rows=2)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded tokens, N(0,0.02) weights)",
+        "config": config_dict(args, wl), "e2e": e2e, "gpu_launches": gpu_launches,
+        "roofline": roofline, "mixer": mixer, "attention": attention, "decode": decode,
+        "cpu_baseline": cpu, "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -88,6 +88,7 @@ wm_status check_ws(const wm_config& c, void* ws, size_t ws_bytes, long long N, l
 
 struct Ctx {
   mutable cudaError_t err = cudaSuccess;   // first failed launch of this call
+  mutable long long launches = 0;          // kernels launched by this call
   const wm_config* c;
   const wm_weights* w;
   char* ws;
@@ -117,15 +118,32 @@ Ctx make_ctx(const wm_config* c, const wm_weights* w, void* ws, long long N, lon
   return x;
 }
 
+// Measurement hook: event pair around one launch of the traced kernel class.
+int trace_begin(const Ctx& x, int kind) {
+  wm_trace* t = x.c->trace;
+  if (!t || t->kind != kind || t->count >= t->capacity || !t->begin || !t->end) return -1;
+  cudaEventRecord(static_cast<cudaEvent_t>(t->begin[t->count]), x.st);
+  return t->count;
+}
+void trace_end(const Ctx& x, int idx, double work) {
+  if (idx < 0) return;
+  wm_trace* t = x.c->trace;
+  cudaEventRecord(static_cast<cudaEvent_t>(t->end[idx]), x.st);
+  if (t->work) t->work[idx] = work;
+  t->count = idx + 1;
+}
+
 // bf16 contractions run on the tensor-core engine; shapes it cannot express
 // (operand strides not 16-byte multiples) and the fp32 mode run on CUDA cores.
 void gemm(const Ctx& x, const GemmDesc& g) {
+  const int tr = trace_begin(x, WM_TRACE_GEMM);
   if (x.tc && gemm_tc_supported(g)) {
     const cudaError_t e = launch_gemm_tc(g, x.st);
     if (e != cudaSuccess && x.err == cudaSuccess) x.err = e;
-    return;
+  } else {
+    launch_gemm_simt(x.c->dtype, g, x.st);
   }
-  launch_gemm_simt(x.c->dtype, g, x.st);
+  trace_end(x, tr, 2.0 * g.M * g.N * (double)g.K * g.batch * (g.B2 ? 2 : 1));
 }
 
 Epi base_epi(const Ctx& x) {
@@ -140,8 +158,8 @@ Epi base_epi(const Ctx& x) {
 // Layer stack of N rows whose h^0 is already in stash[:, 0]. Layer l reads
 // stash[:, l], writes stash[:, l+1] (or h^L), and emits inv_rms / router
 // inputs of its input state. The last layer's body runs only if requested.
-void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void* cache_v, int B,
-               int Tmax, bool emit_rin) {
+void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, void* cache_k,
+               void* cache_v, int B, int Tmax, bool emit_rin) {
   const wm_config& c = *x.c;
   const wm_weights& w = *x.w;
   const long long LD = (long long)c.L * c.D;
@@ -150,6 +168,7 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
   for (int l = 0; l < c.L; ++l) {
     const bool body = l < c.L - 1 || last_layer;
     char* h_in = stash + (long long)l * c.D * x.es;
+    ++x.launches;
     launch_norm_emit(c.dtype, stash, LD, c.D, N, l, 1, c.D, c.L, w.in_norm,
                      body ? x.buf<void>(B_XN) : nullptr, x.buf<float>(B_INV), w.src_norm,
                      emit_rin ? x.buf<void>(B_RIN) : nullptr, x.nR, c.p, c.p_offset, c.eps, x.st);
@@ -165,6 +184,7 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
       g.epi.gain = x.wp(w.q_norm, (long long)l * c.d);
       g.epi.pos = x.buf<int>(B_POS);
       g.epi.Tmax = Tmax;
+      ++x.launches;
       gemm(x, g);
     }
     {  // attention to channel l mod k over s < pos
@@ -173,7 +193,10 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
       a.channel = l % c.k; a.cache_k = cache_k; a.cache_v = cache_v;
       a.B = B; a.k = c.k; a.Hq = c.Hq; a.Hkv = c.Hkv; a.d = c.d; a.Tmax = Tmax;
       a.out = x.buf<void>(B_O); a.flags = x.flags();
+      const int tr = trace_begin(x, WM_TRACE_ATTN);
+      ++x.launches;
       launch_attention(c.dtype, a, !x.tc, x.st, nq);
+      trace_end(x, tr, 4.0 * c.Hq * c.d * pos_sum);
     }
     {  // O projection + residual
       GemmDesc g;
@@ -184,8 +207,10 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
       g.epi.mode = EPI_RESID;
       g.epi.R = h_in; g.epi.ldr = LD;
       g.epi.C = x.buf<void>(B_HMID); g.epi.ldc = c.D;
+      ++x.launches;
       gemm(x, g);
     }
+    ++x.launches;
     launch_rmsnorm(c.dtype, x.buf<void>(B_HMID), c.D, 0, 1, N, c.D,
                    x.wp(w.post_norm, (long long)l * c.D), x.buf<void>(B_XN), c.eps, x.st);
     {  // gate/up + SwiGLU
@@ -197,6 +222,7 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
       g.epi = base_epi(x);
       g.epi.mode = EPI_SWIGLU;
       g.epi.C = x.buf<void>(B_ACT); g.epi.ldc = c.F;
+      ++x.launches;
       gemm(x, g);
     }
     {  // down + residual -> next state
@@ -212,6 +238,7 @@ void run_stack(const Ctx& x, int N, int nq, bool last_layer, void* cache_k, void
       } else {
         g.epi.C = x.buf<void>(B_HL); g.epi.ldc = c.D;
       }
+      ++x.launches;
       gemm(x, g);
     }
   }
@@ -225,6 +252,7 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   const wm_weights& w = *x.w;
   const int kL = c.k * c.L;
   if (w.static_coeff) {
+    ++x.launches;
     launch_broadcast_coeff(w.static_coeff, N, 2 * kL, coeff, x.st);
   } else {
     GemmDesc g;
@@ -235,13 +263,18 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
     g.epi.mode = EPI_STORE;
     g.epi.out_f32 = 1;
     g.epi.C = coeff; g.epi.ldc = 2LL * kL; g.epi.c_bstride = kL;
+    ++x.launches;
     gemm(x, g);
   }
   MixArgs m;
   m.stash = states; m.ld_row = ld_row; m.inv = x.buf<float>(B_INV); m.coeff = coeff;
   m.src_norm = w.src_norm; m.chan_norm = w.chan_norm; m.mixed = mixed;
   m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
+  const int tr = trace_begin(x, WM_TRACE_MIX);
+  ++x.launches;
   launch_mix(c.dtype, m, !x.tc, x.st);
+  trace_end(x, tr, (double)N * ((double)c.L * c.D * x.es + 2.0 * c.k * c.L * 4 + c.L * 4.0 +
+                                 2.0 * c.k * c.D * x.es));
   for (int branch = 0; branch < 2; ++branch) {
     GemmDesc g;
     g.M = N; g.N = c.Hkv * c.d; g.K = c.D; g.batch = c.k;
@@ -255,11 +288,13 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
     g.epi.pos = x.buf<int>(B_POS); g.epi.seq = x.buf<int>(B_SEQ);
     g.epi.cache_k = cache_k; g.epi.cache_v = cache_v;
     g.epi.k = c.k; g.epi.Hkv = c.Hkv; g.epi.Tmax = Tmax; g.epi.B = B;
+    ++x.launches;
     gemm(x, g);
   }
 }
 
 wm_status finish(const Ctx& x) {
+  if (x.c->trace) x.c->trace->launches += x.launches;
   const cudaError_t e = cudaGetLastError();
   return (e == cudaSuccess && x.err == cudaSuccess) ? WM_OK : WM_ERR_CUDA;
 }
@@ -305,7 +340,9 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
   const wm_config& c = *cfg;
   cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
   cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
+  ++x.launches;
   launch_norm_emit(c.dtype, states, (long long)c.L * c.D, c.D, N, 0, c.L, c.D, c.L, nullptr,
                    nullptr, x.buf<float>(B_INV), w->src_norm,
                    w->static_coeff ? nullptr : x.buf<void>(B_RIN), x.nR, c.p, c.p_offset, c.eps,
@@ -332,7 +369,10 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.q = q; a.N = N; a.seq = seq; a.pos = pos; a.channel = channel;
   a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
+  const int tr = trace_begin(x, WM_TRACE_ATTN);
+  ++x.launches;
   launch_attention(cfg->dtype, a, !x.tc, x.st, 0);
+  trace_end(x, tr, 0.0);  // visible-key count is not known on the host here
   return finish(x);
 }
 
@@ -354,17 +394,21 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
   if ((s = check_ws(*cfg, ws, ws_bytes, B * nq_max, Tmax)) != WM_OK) return s;
   Ctx x = make_ctx(cfg, w, ws, B * nq_max, Tmax, stream);
   const wm_config& c = *cfg;
+  ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, T, c.d, c.rope_base, x.st);
   for (int q = q_begin; q < q_end; ++q) {
     const int nq = (T - q + g - 1) / g;
     const int N = B * nq;
+    ++x.launches;
     launch_group_rows(tokens, B, T, g, q, nq, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
                       x.buf<int32_t>(B_POS), x.buf<int32_t>(B_ROWMAP), x.st);
+    ++x.launches;
     launch_embed(c.dtype, x.buf<int32_t>(B_TOK), N, w->embed, c.V, c.D, x.buf<void>(B_STASH),
                  (long long)c.L * c.D, x.flags(), x.st);
     const bool has_last = (T - 1) % g == q;
     const bool want = logits_mode == WM_LOGITS_ALL || (logits_mode == WM_LOGITS_LAST && has_last);
-    run_stack(x, N, nq, want, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+    const double pos_sum = (double)B * ((double)nq * q + (double)g * nq * (nq - 1) / 2.0);
+    run_stack(x, N, nq, pos_sum, want, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
     if (want) {
       GemmDesc lg;
       lg.N = c.V; lg.K = c.D; lg.B = w->lm_head; lg.ldb = c.D;
@@ -373,15 +417,18 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
       lg.epi.out_f32 = 1;
       lg.epi.C = logits; lg.epi.ldc = c.V;
       if (logits_mode == WM_LOGITS_ALL) {
+        ++x.launches;
         launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, N, c.D, w->final_norm,
                        x.buf<void>(B_LASTX), c.eps, x.st);
         lg.M = N; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
         lg.epi.rowmap = x.buf<int>(B_ROWMAP);
       } else {
+        ++x.launches;
         launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, (T - 1 - q) / g, nq, B, c.D,
                        w->final_norm, x.buf<void>(B_LASTX), c.eps, x.st);
         lg.M = B; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
       }
+      ++x.launches;
       gemm(x, lg);
     }
     run_pool(x, N, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
@@ -402,12 +449,16 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
   if ((s = check_ws(*cfg, ws, ws_bytes, B, Tmax)) != WM_OK) return s;
   Ctx x = make_ctx(cfg, w, ws, B, Tmax, stream);
   const wm_config& c = *cfg;
+  ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), pos, pos + 1, c.d, c.rope_base, x.st);
+  ++x.launches;
   launch_decode_rows(tokens, B, pos, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
                      x.buf<int32_t>(B_POS), x.st);
+  ++x.launches;
   launch_embed(c.dtype, x.buf<int32_t>(B_TOK), B, w->embed, c.V, c.D, x.buf<void>(B_STASH),
                (long long)c.L * c.D, x.flags(), x.st);
-  run_stack(x, B, 1, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+  run_stack(x, B, 1, (double)B * pos, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+  ++x.launches;
   launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, B, c.D, w->final_norm,
                  x.buf<void>(B_LASTX), c.eps, x.st);
   GemmDesc lg;
@@ -418,6 +469,7 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
   lg.epi.mode = EPI_STORE;
   lg.epi.out_f32 = 1;
   lg.epi.C = logits; lg.epi.ldc = c.V;
+  ++x.launches;
   gemm(x, lg);
   run_pool(x, B, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
            x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);

@@ -1,6 +1,8 @@
 // Strictly causal channel attention: row n (sequence seq[n], position pos[n])
 // attends to keys s < pos[n] of one cache channel; query head h reads KV head
 // h*Hkv/Hq; a row with no visible key gets 0.
+#include <cuda_fp16.h>
+
 #include "kernels.h"
 
 namespace wm {
@@ -94,8 +96,16 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 }  // namespace
@@ -203,6 +213,16 @@ __global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, in
         cp_async_wait<0>();
       }
       __syncthreads();
+      // values to fp16 in place (exact for bf16 inputs of normal range), so
+      // that P V runs with P in fp16 instead of bf16
+      {
+        __nv_bfloat162* vb2 = reinterpret_cast<__nv_bfloat162*>(sV + buf * AKV * LDS);
+        for (int c = threadIdx.x; c < AKV * (LDS / 2); c += ATHREADS) {
+          const float2 f = __bfloat1622float2(vb2[c]);
+          reinterpret_cast<__half2*>(vb2)[c] = __floats2half2_rn(f.x, f.y);
+        }
+      }
+      __syncthreads();
       const __nv_bfloat16* Kb = sK + buf * AKV * LDS;
       const __nv_bfloat16* Vb = sV + buf * AKV * LDS;
       // S = Q K^T for 16 rows x 64 keys
@@ -250,8 +270,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, in
         const float e2 = exp2f(sc[nt][2] - base1), e3 = exp2f(sc[nt][3] - base1);
         rs0 += e0 + e1;
         rs1 += e2 + e3;
-        pf[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16(e0, e1);
-        pf[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16(e2, e3);
+        pf[nt >> 1][(nt & 1) * 2 + 0] = pack_f16(e0, e1);
+        pf[nt >> 1][(nt & 1) * 2 + 1] = pack_f16(e2, e3);
       }
       l0 = l0 * corr0 + rs0;
       l1 = l1 * corr1 + rs1;
@@ -270,8 +290,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, in
           ldsm_x4_t(smem_addr(Vb + (j * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + dn * 8 +
                               (lane >> 4) * 8),
                     b0, b1, b2, b3);
-          mma_bf16(o[dn], pa, b0, b1);
-          mma_bf16(o[dn + 1], pa, b2, b3);
+          mma_f16(o[dn], pa, b0, b1);
+          mma_f16(o[dn + 1], pa, b2, b3);
         }
       }
       __syncthreads();  // this buffer may be overwritten by the next prefetch

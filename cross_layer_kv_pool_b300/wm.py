@@ -35,12 +35,59 @@ class WMError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} (status {status})")
 
 
+WM_TRACE_GEMM, WM_TRACE_MIX, WM_TRACE_ATTN = 0, 1, 2
+
+
+class WMTrace(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("capacity", ctypes.c_int32),
+                ("count", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("begin", ctypes.POINTER(ctypes.c_void_p)), ("end", ctypes.POINTER(ctypes.c_void_p)),
+                ("work", ctypes.POINTER(ctypes.c_double)), ("launches", ctypes.c_int64)]
+
+
 class WMConfig(ctypes.Structure):
     _fields_ = [("L", ctypes.c_int32), ("D", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("p", ctypes.c_int32), ("p_offset", ctypes.c_int32), ("Hq", ctypes.c_int32),
                 ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("V", ctypes.c_int32), ("eps", ctypes.c_float), ("rope_base", ctypes.c_float),
-                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("trace", ctypes.POINTER(WMTrace))]
+
+
+class Tracer:
+    """Event pairs for the measurement hook: ``attach(model)`` makes the
+    library bracket each launch of ``kind`` with these torch CUDA events."""
+
+    def __init__(self, kind: int, capacity: int):
+        self.events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                       for _ in range(capacity)]
+        for b, e in self.events:       # create the driver handles
+            b.record()
+            e.record()
+        torch.cuda.synchronize()
+        n = capacity
+        self._b = (ctypes.c_void_p * n)(*[b.cuda_event for b, _ in self.events])
+        self._e = (ctypes.c_void_p * n)(*[e.cuda_event for _, e in self.events])
+        self._w = (ctypes.c_double * n)()
+        self.t = WMTrace(kind, n, 0, 0, ctypes.cast(self._b, ctypes.POINTER(ctypes.c_void_p)),
+                         ctypes.cast(self._e, ctypes.POINTER(ctypes.c_void_p)),
+                         ctypes.cast(self._w, ctypes.POINTER(ctypes.c_double)), 0)
+
+    def attach(self, model: "Model"):
+        model.cfg.trace = ctypes.pointer(self.t)
+
+    @staticmethod
+    def detach(model: "Model"):
+        model.cfg.trace = ctypes.POINTER(WMTrace)()
+
+    def reset(self):
+        self.t.count = 0
+        self.t.launches = 0
+
+    def results(self):
+        """[(milliseconds, work)] of the traced launches (after a sync)."""
+        return [(self.events[i][0].elapsed_time(self.events[i][1]), self._w[i])
+                for i in range(self.t.count)]
 
 
 class WMWeights(ctypes.Structure):
@@ -93,7 +140,7 @@ def _check(status, where):
 def make_config(shape: ModelShape, flags: int = 0) -> WMConfig:
     return WMConfig(shape.L, shape.D, shape.k, shape.p, shape.p_offset, shape.Hq, shape.Hkv,
                     shape.d, shape.F, shape.V, shape.eps, shape.rope_base,
-                    WM_F32 if shape.dtype == "f32" else WM_BF16, flags)
+                    WM_F32 if shape.dtype == "f32" else WM_BF16, flags, None)
 
 
 def _ptr(t):

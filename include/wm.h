@@ -62,6 +62,26 @@ typedef enum {
 /* Engine flags (wm_config.flags). */
 #define WM_FLAG_SIMT_GEMM 1u  /* run every contraction on CUDA cores (debug aid) */
 
+/* Optional measurement hook (wm_config.trace, nullable). While entries
+ * remain, an entry point records begin[i] / end[i] (caller-created
+ * cudaEvent_t handles) on its stream immediately before and after each launch
+ * of the selected kernel class, stores the launch's algorithmic work in
+ * work[i] and advances ``count``. Work is FLOPs for the contraction engine
+ * (2*M*N*K per product) and for attention (4*Hq*d per visible key of every
+ * row), and bytes read plus written for the mixer. */
+typedef enum { WM_TRACE_GEMM = 0, WM_TRACE_MIX = 1, WM_TRACE_ATTN = 2 } wm_trace_kind;
+typedef struct {
+    int32_t kind;        /* wm_trace_kind                                       */
+    int32_t capacity;    /* event pairs available                               */
+    int32_t count;       /* in/out: entries used                                */
+    int32_t reserved;
+    void* const* begin;  /* cudaEvent_t[capacity]                               */
+    void* const* end;    /* cudaEvent_t[capacity]                               */
+    double* work;        /* [capacity] algorithmic work of each traced launch   */
+    int64_t launches;    /* in/out: every kernel launched by calls that carry
+                          * this trace (all classes) is counted here          */
+} wm_trace;
+
 /* Model shape. The router reads the source states l < L with
  * l % p == p_offset ([OD How it works]: the router reads every p-th layer's
  * state, stride p = 2, yet emits weights for all L layers). */
@@ -80,6 +100,7 @@ typedef struct {
     float rope_base;    /* RoPE base                                           */
     int32_t dtype;      /* wm_dtype: storage and GEMM operand type             */
     uint32_t flags;     /* WM_FLAG_* engine flags                              */
+    wm_trace* trace;    /* nullable measurement hook (host memory)            */
 } wm_config;
 
 /* Weights (device pointers, storage type). nR = number of router sources.
