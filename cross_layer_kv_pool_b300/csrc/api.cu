@@ -272,7 +272,7 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
   const int tr = trace_begin(x, WM_TRACE_MIX);
   ++x.launches;
-  launch_mix(c.dtype, m, !x.tc, x.st);
+  launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
   trace_end(x, tr, (double)N * ((double)c.L * c.D * x.es + 2.0 * c.k * c.L * 4 + c.L * 4.0 +
                                  2.0 * c.k * c.D * x.es));
   for (int branch = 0; branch < 2; ++branch) {

@@ -72,6 +72,6 @@ struct MixArgs {
   int N, L, D, k;
   float eps;
 };
-void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st);
+void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags);
 
 }  // namespace wm

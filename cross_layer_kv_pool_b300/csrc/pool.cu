@@ -39,9 +39,212 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
   }
 }
 
-void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st) {
+// ---------------------------------------------------------------------------
+// Streaming engine (bf16 storage): one persistent CTA per SM walks token rows.
+// Each row's contiguous L x D stack is staged into shared memory by one bulk
+// TMA copy (double-buffered, so the next row streams in while this one is
+// mixed); inv_rms folds into the coefficients; every thread owns 4 adjacent
+// columns and all 2k channel accumulators for them (packed f32x2 FMAs), so
+// each state element is read once for all 2k outputs; the channel RMSNorm is a
+// block reduction; the output is written channel-major with 8-byte stores.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int MIX_C = 4;  // columns per thread
+
+__device__ __forceinline__ uint32_t sa32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ bool mix_mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t addr = sa32(bar);
+  unsigned long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (it == 0) t0 = t;
+    else if (t - t0 > 4000000000ull) return false;
+  }
+}
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rd, {%0, %1};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rd;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void ld4_bf16(const __nv_bfloat16* p, float* v) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+}  // namespace
+
+template <int K, int NT>
+__global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint32_t* flags) {
+  extern __shared__ __align__(128) uint8_t msm[];
+  constexpr int HALF = NT / 2;  // threads per branch
+  const int L = a.L, D = a.D;
+  const size_t stage = (size_t)L * D * 2;
+  __nv_bfloat16* buf[2] = {reinterpret_cast<__nv_bfloat16*>(msm),
+                           reinterpret_cast<__nv_bfloat16*>(msm + stage)};
+  float* coef = reinterpret_cast<float*>(msm + 2 * stage);   // [2][L][K]
+  float* red = coef + (size_t)2 * L * K;                       // [2K][32]
+  float* scale = red + 2 * K * 32;                             // [2K]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(scale + 2 * K + (2 * K & 1));  // [2]
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int beta = tid / HALF, bt = tid % HALF, wb = bt >> 5;  // branch, thread and warp in branch
+  const int t0 = bt * MIX_C;
+  const __nv_bfloat16* src = (const __nv_bfloat16*)a.stash;
+  const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm + (size_t)beta * L * D;
+  const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm + (size_t)beta * K * D;
+  __nv_bfloat16* out = (__nv_bfloat16*)a.mixed + (size_t)beta * K * a.N * D;
+
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa32(&bar[0])) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa32(&bar[1])) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+  auto issue = [&](int r, int b) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&bar[b])),
+                 "r"((uint32_t)stage)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            sa32(buf[b])),
+        "l"(src + (long long)r * a.ld_row), "r"((uint32_t)stage), "r"(sa32(&bar[b]))
+        : "memory");
+  };
+  if (tid == 0 && (int)blockIdx.x < a.N) issue(blockIdx.x, 0);
+  uint32_t phase[2] = {0, 0};
+  bool ok = true;
+  int it = 0;
+  for (int r = blockIdx.x; r < a.N; r += gridDim.x, ++it) {
+    const int b = it & 1;
+    const int rn = r + gridDim.x;
+    if (tid == 0 && rn < a.N) issue(rn, b ^ 1);  // its buffer was released last iteration
+    // coefficients of this row, scaled by the inverse RMS of each source
+    for (int i = tid; i < 2 * L * K; i += NT) {
+      const int be = i / (L * K), l = (i / K) % L, j = i % K;
+      coef[i] = a.coeff[(((long long)r * 2 + be) * K + j) * L + l] * a.inv[(long long)r * L + l];
+    }
+    if (!mix_mbar_wait(&bar[b], phase[b])) ok = false;
+    phase[b] ^= 1;
+    __syncthreads();
+    float acc[K][MIX_C];
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+#pragma unroll
+      for (int c = 0; c < MIX_C; ++c) acc[j][c] = 0.f;
+    if (t0 < D) {
+      const __nv_bfloat16* hb = buf[b] + t0;
+      const float* cf = coef + (size_t)beta * L * K;
+      const __nv_bfloat16* sp = sn + t0;
+#pragma unroll 1
+      for (int l = 0; l < L; ++l, hb += D, sp += D, cf += K) {
+        float h[MIX_C], sg[MIX_C];
+        ld4_bf16(hb, h);
+        ld4_bf16(sp, sg);
+#pragma unroll
+        for (int c = 0; c < MIX_C; ++c) h[c] *= sg[c];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+          const float cj = cf[j];
+          ffma2(acc[j][0], acc[j][1], cj, h[0], h[1]);
+          ffma2(acc[j][2], acc[j][3], cj, h[2], h[3]);
+        }
+      }
+    }
+    // channel norms: sum of squares over D for each (beta, j)
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+      float ss = 0.f;
+#pragma unroll
+      for (int c = 0; c < MIX_C; ++c) ss += acc[j][c] * acc[j][c];
+      ss = warp_sum(ss);
+      if (lane == 0) red[(beta * K + j) * 32 + wb] = ss;
+    }
+    __syncthreads();
+    if (tid < 2 * K) {
+      float ss = 0.f;
+      for (int w = 0; w < HALF / 32; ++w) ss += red[tid * 32 + w];
+      scale[tid] = rsqrtf(ss / (float)D + a.eps);
+    }
+    __syncthreads();
+    if (t0 < D) {
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        float g[MIX_C];
+        ld4_bf16(cn + (size_t)j * D + t0, g);
+        const float sc = scale[beta * K + j];
+        __nv_bfloat162 o0 = __floats2bfloat162_rn(acc[j][0] * sc * g[0], acc[j][1] * sc * g[1]);
+        __nv_bfloat162 o1 = __floats2bfloat162_rn(acc[j][2] * sc * g[2], acc[j][3] * sc * g[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t*>(&o0);
+        u.y = *reinterpret_cast<uint32_t*>(&o1);
+        *reinterpret_cast<uint2*>(out + ((size_t)j * a.N + r) * D + t0) = u;
+      }
+    }
+    __syncthreads();  // buffer b and coef are free for reuse
+  }
+  if (!ok && tid == 0) atomicOr(flags, FLAG_TIMEOUT);
+}
+
+template <int K, int NT>
+bool launch_mix_stream_nt(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
+  const size_t smem = 2 * (size_t)a.L * a.D * 2 + (size_t)2 * a.L * K * 4 + 2 * K * 32 * 4 +
+                      (2 * K + 2) * 4 + 16 + 128;
+  if (smem > 227 * 1024) return false;
+  if (cudaFuncSetAttribute(mix_stream_kernel<K, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem) != cudaSuccess)
+    return false;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = a.N < sms ? a.N : sms;
+  mix_stream_kernel<K, NT><<<grid, NT, smem, st>>>(a, flags);
+  return true;
+}
+
+// Smallest block whose halves (one per branch) cover D/4 columns each and
+// still leave registers for 4k accumulators per thread (one block per SM).
+template <int K>
+bool launch_mix_stream(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
+  const int need = 2 * (a.D / MIX_C);
+  if (need <= 256) return launch_mix_stream_nt<K, 256>(a, flags, st);
+  if (need <= 512) return launch_mix_stream_nt<K, 512>(a, flags, st);
+  if (need <= 896 && K <= 14) return launch_mix_stream_nt<K, 896>(a, flags, st);
+  if (need <= 1024 && K <= 8) return launch_mix_stream_nt<K, 1024>(a, flags, st);
+  return false;
+}
+
+void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags) {
   if (a.N <= 0) return;
-  (void)simt;
+  const bool stream_ok = dtype == WM_BF16 && !simt && a.D % (8 * MIX_C) == 0 &&
+                         ((uintptr_t)a.stash % 16 == 0) && (a.ld_row % 8 == 0);
+  if (stream_ok) {
+    bool done = false;
+    switch (a.k) {
+      case 1: done = launch_mix_stream<1>(a, flags, st); break;
+      case 2: done = launch_mix_stream<2>(a, flags, st); break;
+      case 4: done = launch_mix_stream<4>(a, flags, st); break;
+      case 8: done = launch_mix_stream<8>(a, flags, st); break;
+      case 12: done = launch_mix_stream<12>(a, flags, st); break;
+      case 14: done = launch_mix_stream<14>(a, flags, st); break;
+      case 16: done = launch_mix_stream<16>(a, flags, st); break;
+      default: break;
+    }
+    if (done) return;
+  }
   WM_DISPATCH_S(dtype, mix_simt_kernel<S><<<a.N, 256, a.D * sizeof(float), st>>>(a));
 }
 

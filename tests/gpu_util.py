@@ -17,8 +17,9 @@ from cross_layer_kv_pool_b300 import build, synth, wm
 # oracle in bf16-storage mode, run against itself with weights perturbed by
 # 1e-7..1e-5 (the scale of fp32-vs-fp64 arithmetic), already differs by
 # 2.5-3.8% max-element and 1.0-1.6% in norm on those entries, because single
-# bf16 rounding flips are amplified by the signed mixing; the bounds are about
-# 2.5x that spread. Logits keep 2e-2 in every case.
+# bf16 rounding flips are amplified by the signed mixing. Whole bf16 group
+# steps are therefore also allowed SPREAD_FACTOR times the oracle's own spread
+# on the same instance (``within``), measured in the test itself.
 TOL = {"f32": dict(logits=1e-4, cache=1e-4, mixed=1e-4, coeff=1e-4, attn=1e-4,
                    cache_step=1e-4, cache_step_norm=1e-4),
        "bf16": dict(logits=2e-2, cache=2e-2, mixed=1e-2, coeff=2e-2, attn=1e-2,
@@ -70,7 +71,25 @@ def small_shape(dtype="f32", **kw):
     return synth.ModelShape(**base)
 
 
-def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", check=None):
+def perturbed(Wn, eps, seed=12345):
+    """Weights with independent relative perturbations of size eps: the
+    oracle run on them measures how far the instance itself moves under
+    arithmetic-level differences (its conditioning)."""
+    rng = np.random.default_rng(seed)
+    return {k: v * (1.0 + eps * rng.standard_normal(v.shape)) for k, v in Wn.items()}
+
+
+SPREAD_EPS = 1e-5     # relative size of fp32-vs-fp64 differences in long reductions
+SPREAD_FACTOR = 2.5   # the GPU may move at most this many times the oracle's own spread
+
+
+def within(err, base, spread):
+    """err <= max(base tolerance, SPREAD_FACTOR x measured oracle spread)."""
+    return err <= max(base, SPREAD_FACTOR * spread)
+
+
+def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", check=None,
+                    spread=False):
     """Run ``passes`` cyclic passes on the GPU one group at a time. Before each
     checked group (``check(n, q)``), copy the GPU cache to the host, run the
     oracle's same group from that snapshot, and compare what the group wrote
@@ -89,7 +108,9 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
     ws = m.workspace(wm.rows_for_pass(B, T, g), Tmax)
     lg = torch.zeros((B, T, s.V) if logits_mode == "all" else (B, s.V), dtype=torch.float32,
                      device="cuda")
-    worst = {"cache": 0.0, "cache_norm": 0.0, "logits": 0.0, "checked": 0}
+    worst = {"cache": 0.0, "cache_norm": 0.0, "logits": 0.0, "checked": 0,
+             "spread_cache": 0.0, "spread_cache_norm": 0.0, "spread_logits": 0.0}
+    Wp = perturbed(Wn, SPREAD_EPS) if spread else None
     for n in range(passes):
         mode = logits_mode if n == passes - 1 else "none"
         for q in range(g):
@@ -97,6 +118,7 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
             if do:
                 torch.cuda.synchronize()
                 sk, sv = host(ck), host(cv)
+                pk, pv = sk.copy(), sv.copy()
             wm.wm_cyclic_pass(m, tok, g, ck, cv, ws, q_begin=q, q_end=q + 1,
                               logits=None if mode == "none" else lg, logits_mode=mode)
             if not do:
@@ -106,6 +128,19 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
                                logits=None if mode == "none" else mode)
             P = np.arange(q, T, g)
             gk, gv = host(ck), host(cv)
+            if spread:
+                pl = O.cyclic_pass(oc, Wp, tokens_h, g, pk, pv, q_begin=q, q_end=q + 1,
+                                   logits=None if mode == "none" else mode)
+                worst["spread_cache"] = max(worst["spread_cache"],
+                                            relerr(pk[:, :, :, P], sk[:, :, :, P]),
+                                            relerr(pv[:, :, :, P], sv[:, :, :, P]))
+                worst["spread_cache_norm"] = max(worst["spread_cache_norm"],
+                                                 normerr(pk[:, :, :, P], sk[:, :, :, P]),
+                                                 normerr(pv[:, :, :, P], sv[:, :, :, P]))
+                if mode == "all":
+                    worst["spread_logits"] = max(worst["spread_logits"], relerr(pl[:, P], rl[:, P]))
+                elif mode == "last" and (T - 1) % g == q:
+                    worst["spread_logits"] = max(worst["spread_logits"], relerr(pl, rl))
             worst["cache"] = max(worst["cache"], relerr(gk[:, :, :, P], sk[:, :, :, P]),
                                  relerr(gv[:, :, :, P], sv[:, :, :, P]))
             worst["cache_norm"] = max(worst["cache_norm"], normerr(gk[:, :, :, P], sk[:, :, :, P]),
