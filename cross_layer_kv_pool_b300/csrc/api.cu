@@ -2,6 +2,7 @@
 // drivers of the pool, the cyclic Gauss-Seidel pass and the decode step.
 // Every arithmetic step runs in the kernels launched from here.
 #include <cstring>
+#include <mutex>
 
 #include "kernels.h"
 
@@ -491,3 +492,96 @@ wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* s
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// wm_pool_mix_static: the pool without a caller workspace.
+//
+// For callers that cannot allocate device memory themselves: a plug-in host
+// that hands the library nothing but its input and output pointers, or a
+// latency-bound loop that must not call cudaMalloc (which synchronises the
+// device). The pool's scratch (router inputs, per-source inverse RMS,
+// coefficients, mixed channels, RoPE table, flag word) lives instead in one
+// file-scope device array of WM_POOL_STATIC_SCRATCH_BYTES, which every GPU
+// that loads the library holds until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+__device__ __align__(256) unsigned char g_pool_scratch[WM_POOL_STATIC_SCRATCH_BYTES];
+
+// Device address of g_pool_scratch on the current device. In host code the
+// symbol is only a host-side stand-in, so the address is looked up with
+// cudaGetSymbolAddress, once per device, with that device current.
+void* pool_scratch_address() {
+  static std::mutex mu;
+  static void* addr[256] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pool_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+// Compact layout: only the buffers the pool touches.
+Layout pool_static_layout(const wm_config& c, long long N, long long Tmax) {
+  const size_t es = elem_size(c.dtype);
+  const long long nR = count_nR(c);
+  Layout lay;
+  for (int i = 0; i < NBUF; ++i) lay.off[i] = 0;
+  size_t o = 0;
+  auto put = [&](Buf b, size_t bytes) {
+    lay.off[b] = o;
+    o += align256(bytes);
+  };
+  put(B_FLAGS, 256);
+  put(B_ROPE, (size_t)Tmax * (c.d / 2) * sizeof(float2));
+  put(B_SEQ, (size_t)N * 4);
+  put(B_POS, (size_t)N * 4);
+  put(B_RIN, (size_t)2 * N * nR * c.D * es);
+  put(B_INV, (size_t)N * c.L * 4);
+  put(B_COEFF, (size_t)N * 2 * c.k * c.L * 4);
+  put(B_MIXED, (size_t)N * 2 * c.k * c.D * es);
+  lay.total = o;
+  return lay;
+}
+
+}  // namespace
+
+extern "C" wm_status wm_pool_mix_static(const wm_config* cfg, const wm_weights* w,
+                                        const void* states, int32_t N, const int32_t* seq,
+                                        const int32_t* pos, void* cache_k, void* cache_v,
+                                        int32_t B, int32_t Tmax, float* coeff_out,
+                                        void* mixed_out, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (N < 1 || B < 1 || Tmax < 1 || !states || !seq || !pos || !cache_k || !cache_v)
+    return WM_ERR_INVALID_ARG;
+  if (!aligned16(states) || !aligned16(cache_k) || !aligned16(cache_v) ||
+      (coeff_out && !aligned16(coeff_out)) || (mixed_out && !aligned16(mixed_out)))
+    return WM_ERR_INVALID_ARG;
+  const Layout lay = pool_static_layout(*cfg, N, Tmax);
+  if (lay.total > (size_t)WM_POOL_STATIC_SCRATCH_BYTES) return WM_ERR_WORKSPACE;
+  void* base = pool_scratch_address();
+  if (!base) return WM_ERR_CUDA;
+  Ctx x = make_ctx(cfg, w, base, N, Tmax, stream);
+  x.lay = lay;
+  const wm_config& c = *cfg;
+  // the previous call's flag bits must not leak into this one
+  if (cudaMemsetAsync(x.flags(), 0, 256, x.st) != cudaSuccess) return WM_ERR_CUDA;
+  cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  ++x.launches;
+  launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
+  ++x.launches;
+  launch_norm_emit(c.dtype, states, (long long)c.L * c.D, c.D, N, 0, c.L, c.D, c.L, nullptr,
+                   nullptr, x.buf<float>(B_INV), w->src_norm,
+                   w->static_coeff ? nullptr : x.buf<void>(B_RIN), x.nR, c.p, c.p_offset, c.eps,
+                   x.st);
+  run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
+           mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  return finish(x);
+}

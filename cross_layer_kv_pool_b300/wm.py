@@ -26,7 +26,8 @@ LOGITS = {"none": 0, None: 0, "last": 1, "all": 2}
 WM_FLAG_SIMT_GEMM = 1
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
-            "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version")
+            "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version",
+            "wm_pool_mix_static")
 
 
 class WMError(RuntimeError):
@@ -118,6 +119,8 @@ def lib():
                                      vp, sz, vp]
         L.wm_decode_step.restype = ctypes.c_int
         L.wm_decode_step.argtypes = [cfgp, wp, vp, i32, i32, vp, vp, i32, vp, vp, sz, vp]
+        L.wm_pool_mix_static.restype = ctypes.c_int
+        L.wm_pool_mix_static.argtypes = [cfgp, wp, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp, vp]
         L.wm_check_flags.restype = ctypes.c_int
         L.wm_check_flags.argtypes = [vp, sz, ctypes.POINTER(ctypes.c_uint32), vp]
         L.wm_status_string.restype = ctypes.c_char_p
@@ -201,6 +204,18 @@ def wm_pool_mix(m: Model, states, seq, pos, cache_k, cache_v, ws, coeff_out=None
                            B, Tmax, _ptr(coeff_out), _ptr(mixed_out), _ptr(ws), ws.numel(),
                            _stream(stream))
     _check(st, "wm_pool_mix")
+
+
+def wm_pool_mix_static(m: Model, states, seq, pos, cache_k, cache_v, coeff_out=None,
+                       mixed_out=None, stream=None):
+    """wm_pool_mix with the library's fixed internal scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    B, Tmax = cache_k.shape[0], cache_k.shape[3]
+    st = lib().wm_pool_mix_static(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(states),
+                                  states.shape[0], _ptr(seq), _ptr(pos), _ptr(cache_k),
+                                  _ptr(cache_v), B, Tmax, _ptr(coeff_out), _ptr(mixed_out),
+                                  _stream(stream))
+    _check(st, "wm_pool_mix_static")
 
 
 def wm_channel_attn(cfg: WMConfig, q, seq, pos, channel: int, cache_k, cache_v, out, ws,

@@ -198,6 +198,34 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w,
  * WM_ERR_TIMEOUT if a bounded wait gave up since the last call. */
 wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream);
 
+/* wm_pool_mix without a workspace, for callers that cannot allocate device
+ * memory: a plug-in host that hands the library only its input and output
+ * pointers, or a loop that must not call cudaMalloc because that
+ * synchronises the device. (The pages have no counterpart of this call; it
+ * computes exactly what wm_pool_mix computes, with the same arguments minus
+ * ws / ws_bytes.)
+ *
+ * Scratch: one device array of WM_POOL_STATIC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * Rows beyond what fits (RoPE table of Tmax positions, then per row about
+ * 4*nR*D + 4*k*D + 8*k*L + 4*L + 8 bytes in bf16 storage) return
+ * WM_ERR_WORKSPACE before anything is launched. The call itself allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the one array and finds the
+ * previous call's contents there; the call clears what must start at zero
+ * (its flag word) itself. Calls that overlap on the GPU - on different
+ * streams, or from different host threads - race on the array and must be
+ * serialised by the caller. Device-side index checks of this call are not
+ * reported (its flag word is internal). */
+#define WM_POOL_STATIC_SCRATCH_BYTES (32u << 20)
+wm_status wm_pool_mix_static(const wm_config* cfg, const wm_weights* w,
+                             const void* states, int32_t N,
+                             const int32_t* seq, const int32_t* pos,
+                             void* cache_k, void* cache_v, int32_t B, int32_t Tmax,
+                             float* coeff_out, void* mixed_out, void* stream);
+
 const char* wm_status_string(wm_status s);
 int32_t wm_abi_version(void);
 
