@@ -41,12 +41,15 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
 
 // ---------------------------------------------------------------------------
 // Streaming engine (bf16 storage): one persistent CTA per SM walks token rows.
-// Each row's contiguous L x D stack is staged into shared memory by one bulk
-// TMA copy (double-buffered, so the next row streams in while this one is
-// mixed); inv_rms folds into the coefficients; every thread owns 4 adjacent
-// columns and all 2k channel accumulators for them (packed f32x2 FMAs), so
-// each state element is read once for all 2k outputs; the channel RMSNorm is a
-// block reduction; the output is written channel-major with 8-byte stores.
+// Each row's contiguous L x D stack streams through shared memory in chunks of
+// MIX_LC layers, each chunk together with both branches' source-norm gains of
+// those layers, by bulk TMA copies into a ring of MIX_STAGES stages (so the
+// next chunks, also of the next row, load while this one is mixed). inv_rms
+// folds into the coefficients. The block's two halves take one branch each;
+// every thread owns 4 adjacent columns and all k channel accumulators of its
+// branch (packed f32x2 FMAs), so each staged element is read once per branch
+// for all k outputs. The channel RMSNorm is a block reduction; the output is
+// written channel-major with 8-byte stores.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr int MIX_C = 4;  // columns per thread
@@ -87,89 +90,105 @@ __device__ __forceinline__ void ld4_bf16(const __nv_bfloat16* p, float* v) {
 }
 }  // namespace
 
+constexpr int MIX_LC = 4;      // source layers per staged chunk
+constexpr int MIX_STAGES = 4;  // chunks in flight
+
 template <int K, int NT>
 __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint32_t* flags) {
   extern __shared__ __align__(128) uint8_t msm[];
   constexpr int HALF = NT / 2;  // threads per branch
   const int L = a.L, D = a.D;
-  const size_t stage = (size_t)L * D * 2;
-  __nv_bfloat16* buf[2] = {reinterpret_cast<__nv_bfloat16*>(msm),
-                           reinterpret_cast<__nv_bfloat16*>(msm + stage)};
-  float* coef = reinterpret_cast<float*>(msm + 2 * stage);   // [2][L][K]
-  float* red = coef + (size_t)2 * L * K;                       // [2K][32]
-  float* scale = red + 2 * K * 32;                             // [2K]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(scale + 2 * K + (2 * K & 1));  // [2]
+  const int nc = (L + MIX_LC - 1) / MIX_LC;
+  // stage s: [MIX_LC][D] states, then [2][MIX_LC][D] source-norm gains
+  const size_t stage_elems = (size_t)3 * MIX_LC * D;
+  __nv_bfloat16* stages = reinterpret_cast<__nv_bfloat16*>(msm);
+  float* coef = reinterpret_cast<float*>(msm + MIX_STAGES * stage_elems * 2);  // [2][L][K]
+  float* red = coef + (size_t)2 * L * K;                                        // [2K][32]
+  float* scale = red + 2 * K * 32;                                              // [2K]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(scale + 2 * K + (2 * K & 1));     // [MIX_STAGES]
   const int tid = threadIdx.x, lane = tid & 31;
   const int beta = tid / HALF, bt = tid % HALF, wb = bt >> 5;  // branch, thread and warp in branch
   const int t0 = bt * MIX_C;
   const __nv_bfloat16* src = (const __nv_bfloat16*)a.stash;
-  const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm + (size_t)beta * L * D;
+  const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm;
   const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm + (size_t)beta * K * D;
   __nv_bfloat16* out = (__nv_bfloat16*)a.mixed + (size_t)beta * K * a.N * D;
 
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa32(&bar[0])) : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa32(&bar[1])) : "memory");
+    for (int i = 0; i < MIX_STAGES; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(sa32(&bar[i])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  auto issue = [&](int r, int b) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa32(&bar[b])),
-                 "r"((uint32_t)stage)
+  // Chunk q of this block: row blockIdx.x + (q / nc) * gridDim.x, layers of chunk q % nc.
+  auto issue = [&](int q) {
+    const long long r = blockIdx.x + (long long)(q / nc) * gridDim.x;
+    if (r >= a.N) return;
+    const int c = (int)(q % nc), l0 = c * MIX_LC, lc = min(MIX_LC, L - l0);
+    const int st = (int)(q % MIX_STAGES);
+    const uint32_t bytes = (uint32_t)lc * D * 2;
+    __nv_bfloat16* dst = stages + st * stage_elems;
+    const uint32_t b = sa32(&bar[st]);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(3 * bytes)
                  : "memory");
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            sa32(buf[b])),
-        "l"(src + (long long)r * a.ld_row), "r"((uint32_t)stage), "r"(sa32(&bar[b]))
-        : "memory");
+    const __nv_bfloat16* srcs[3] = {src + r * a.ld_row + (long long)l0 * D,
+                                    sn + (long long)l0 * D, sn + ((long long)L + l0) * D};
+    for (int i = 0; i < 3; ++i)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              sa32(dst + (size_t)i * MIX_LC * D)),
+          "l"(srcs[i]), "r"(bytes), "r"(b)
+          : "memory");
   };
-  if (tid == 0 && (int)blockIdx.x < a.N) issue(blockIdx.x, 0);
-  uint32_t phase[2] = {0, 0};
+  if (tid == 0)
+    for (int q = 0; q < MIX_STAGES; ++q) issue(q);
   bool ok = true;
-  int it = 0;
-  for (int r = blockIdx.x; r < a.N; r += gridDim.x, ++it) {
-    const int b = it & 1;
-    const int rn = r + gridDim.x;
-    if (tid == 0 && rn < a.N) issue(rn, b ^ 1);  // its buffer was released last iteration
+  float acc[K][MIX_C];
+  int q = 0;
+  for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
     // coefficients of this row, scaled by the inverse RMS of each source
     for (int i = tid; i < 2 * L * K; i += NT) {
       const int be = i / (L * K), l = (i / K) % L, j = i % K;
       coef[i] = a.coeff[(((long long)r * 2 + be) * K + j) * L + l] * a.inv[(long long)r * L + l];
     }
-    if (!mix_mbar_wait(&bar[b], phase[b])) ok = false;
-    phase[b] ^= 1;
-    __syncthreads();
-    float acc[K][MIX_C];
 #pragma unroll
     for (int j = 0; j < K; ++j)
 #pragma unroll
       for (int c = 0; c < MIX_C; ++c) acc[j][c] = 0.f;
-    if (t0 < D) {
-      const __nv_bfloat16* hb = buf[b] + t0;
-      const float* cf = coef + (size_t)beta * L * K;
-      const __nv_bfloat16* sp = sn + t0;
+    for (int c = 0; c < nc; ++c, ++q) {
+      const int st = q % MIX_STAGES;
+      if (!mix_mbar_wait(&bar[st], (uint32_t)((q / MIX_STAGES) & 1))) ok = false;
+      __syncthreads();
+      if (t0 < D) {
+        const int l0 = c * MIX_LC, lc = min(MIX_LC, L - l0);
+        const __nv_bfloat16* hs = stages + st * stage_elems + t0;
+        const __nv_bfloat16* gs = hs + (size_t)(1 + beta) * MIX_LC * D;
+        const float* cf = coef + ((size_t)beta * L + l0) * K;
 #pragma unroll 1
-      for (int l = 0; l < L; ++l, hb += D, sp += D, cf += K) {
-        float h[MIX_C], sg[MIX_C];
-        ld4_bf16(hb, h);
-        ld4_bf16(sp, sg);
+        for (int ll = 0; ll < lc; ++ll, hs += D, gs += D, cf += K) {
+          float h[MIX_C], sg[MIX_C];
+          ld4_bf16(hs, h);
+          ld4_bf16(gs, sg);
 #pragma unroll
-        for (int c = 0; c < MIX_C; ++c) h[c] *= sg[c];
+          for (int e = 0; e < MIX_C; ++e) h[e] *= sg[e];
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-          const float cj = cf[j];
-          ffma2(acc[j][0], acc[j][1], cj, h[0], h[1]);
-          ffma2(acc[j][2], acc[j][3], cj, h[2], h[3]);
+          for (int j = 0; j < K; ++j) {
+            const float cj = cf[j];
+            ffma2(acc[j][0], acc[j][1], cj, h[0], h[1]);
+            ffma2(acc[j][2], acc[j][3], cj, h[2], h[3]);
+          }
         }
       }
+      __syncthreads();  // stage st is free: refill it
+      if (tid == 0) issue(q + MIX_STAGES);
     }
     // channel norms: sum of squares over D for each (beta, j)
 #pragma unroll
     for (int j = 0; j < K; ++j) {
       float ss = 0.f;
 #pragma unroll
-      for (int c = 0; c < MIX_C; ++c) ss += acc[j][c] * acc[j][c];
+      for (int e = 0; e < MIX_C; ++e) ss += acc[j][e] * acc[j][e];
       ss = warp_sum(ss);
       if (lane == 0) red[(beta * K + j) * 32 + wb] = ss;
     }
@@ -194,15 +213,15 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
         *reinterpret_cast<uint2*>(out + ((size_t)j * a.N + r) * D + t0) = u;
       }
     }
-    __syncthreads();  // buffer b and coef are free for reuse
+    __syncthreads();  // coef, red and scale are free for the next row
   }
   if (!ok && tid == 0) atomicOr(flags, FLAG_TIMEOUT);
 }
 
 template <int K, int NT>
 bool launch_mix_stream_nt(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
-  const size_t smem = 2 * (size_t)a.L * a.D * 2 + (size_t)2 * a.L * K * 4 + 2 * K * 32 * 4 +
-                      (2 * K + 2) * 4 + 16 + 128;
+  const size_t smem = (size_t)MIX_STAGES * 3 * MIX_LC * a.D * 2 + (size_t)2 * a.L * K * 4 +
+                      2 * K * 32 * 4 + (2 * K + 2) * 4 + 8 * MIX_STAGES + 128;
   if (smem > 227 * 1024) return false;
   if (cudaFuncSetAttribute(mix_stream_kernel<K, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
