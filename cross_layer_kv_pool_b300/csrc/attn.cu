@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const AttnArgs a) {
 // softmax is online in fp32 (exp2 with the 1/sqrt(d) scale folded in).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int AQ = 64, AKV = 64, ATHREADS = 128;
+constexpr int AWARPS = 8, AQ = 16 * AWARPS, AKV = 32, ATHREADS = 32 * AWARPS;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -111,7 +111,7 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 }  // namespace
 
 template <int HD>
-__global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, int rpt, int nq) {
+__global__ void __launch_bounds__(ATHREADS, 2) attn_mma_kernel(const AttnArgs a, int rpt, int nq) {
   constexpr int LDS = HD + 8;  // padded smem row (elements): conflict-free ldmatrix
   extern __shared__ __align__(16) uint8_t sm[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm);
@@ -194,15 +194,9 @@ __global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, in
 #pragma unroll
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    uint32_t qf[HD / 16][4];
     cp_async_wait<0>();  // Q (and the first K/V block) landed
     __syncthreads();
-    {
-      const int row = warp * 16 + (lane & 15), col = (lane >> 4) * 8;
-#pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks)
-        ldsm_x4(smem_addr(sQ + row * LDS + ks * 16 + col), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
-    }
+    const uint32_t qaddr = smem_addr(sQ + (warp * 16 + (lane & 15)) * LDS + (lane >> 4) * 8);
 
     for (int kb = 0; kb < nkb; ++kb) {
       const int buf = kb & 1;
@@ -230,14 +224,17 @@ __global__ void __launch_bounds__(ATHREADS) attn_mma_kernel(const AttnArgs a, in
 #pragma unroll
       for (int nt = 0; nt < AKV / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < AKV / 8; ++nt) {
+      for (int ks = 0; ks < HD / 16; ks += 2) {
+        uint32_t qa[4], qb[4];
+        ldsm_x4(qaddr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
+        ldsm_x4(qaddr + ks * 32 + 32, qb[0], qb[1], qb[2], qb[3]);
 #pragma unroll
-        for (int ks = 0; ks < HD / 16; ks += 2) {
+        for (int nt = 0; nt < AKV / 8; ++nt) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4(smem_addr(Kb + (nt * 8 + (lane & 7)) * LDS + ks * 16 + (lane >> 3) * 8), b0, b1,
                   b2, b3);
-          mma_bf16(sc[nt], qf[ks], b0, b1);
-          mma_bf16(sc[nt], qf[ks + 1], b2, b3);
+          mma_bf16(sc[nt], qa, b0, b1);
+          mma_bf16(sc[nt], qb, b2, b3);
         }
       }
       // mask keys s >= pos of the row, online softmax

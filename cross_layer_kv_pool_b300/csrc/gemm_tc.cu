@@ -129,6 +129,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -227,39 +236,49 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
       for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);
     }
   } else {
+    constexpr int CW = (BN % 32 == 0) ? 32 : 16;  // columns per TMEM load
 #pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 32) {
-      uint32_t r[32];
-      float v[32];
+    for (int c0 = 0; c0 < BN; c0 += CW) {
+      uint32_t r[CW];
+      float v[CW];
       __syncwarp();
-      tmem_ld32(taddr + c0, r);
+      if constexpr (CW == 32) tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(r));
+      else tmem_ld16(taddr + c0, r);
       if constexpr (DUAL) {
-        uint32_t r2[32];
-        tmem_ld32(taddr + BN + c0, r2);
+        uint32_t r2[CW];
+        if constexpr (CW == 32) tmem_ld32(taddr + BN + c0, *reinterpret_cast<uint32_t(*)[32]>(r2));
+        else tmem_ld16(taddr + BN + c0, r2);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < CW; ++i) {
           const float gt = __uint_as_float(r[i]);
           v[i] = gt / (1.f + __expf(-gt)) * __uint_as_float(r2[i]);
         }
       } else {
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        for (int i = 0; i < CW; ++i) v[i] = __uint_as_float(r[i]);
       }
       const int col = n0 + c0;
       if (!row_ok || col >= p.N) continue;
-      const bool full = col + 32 <= p.N;
+      const bool full = col + CW <= p.N;
       if constexpr (MODE == EPI_RESID) {
         const __nv_bfloat16* rp = (const __nv_bfloat16*)e.R + (long long)row * e.ldr + col;
         if (full && p.vec_res) {
-          float rv[32];
-          ld_bf16x32(rp, rv);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] += rv[i];
+          for (int q = 0; q < CW / 8; ++q) {
+            const uint4 u = reinterpret_cast<const uint4*>(rp)[q];
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __bfloat1622float2(h[i]);
+              v[8 * q + 2 * i] += f.x;
+              v[8 * q + 2 * i + 1] += f.y;
+            }
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < CW; ++i)
             if (col + i < p.N) v[i] += __bfloat162float(rp[i]);
         }
       }
@@ -269,20 +288,28 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
         float* cp = (float*)e.C + off;
         if (full && p.vec_out) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
+          for (int i = 0; i < CW; i += 4)
             *reinterpret_cast<float4*>(cp + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < CW; ++i)
             if (col + i < p.N) cp[i] = v[i];
         }
       } else {
         __nv_bfloat16* cp = (__nv_bfloat16*)e.C + off;
         if (full && p.vec_out) {
-          st_bf16x32(cp, v);
+#pragma unroll
+          for (int q = 0; q < CW / 8; ++q) {
+            uint4 u;
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              h[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+            reinterpret_cast<uint4*>(cp)[q] = u;
+          }
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
+          for (int i = 0; i < CW; ++i)
             if (col + i < p.N) cp[i] = __float2bfloat16_rn(v[i]);
         }
       }
@@ -290,14 +317,24 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
   }
 }
 
+constexpr int pow2_at_least(int x) {
+  int p = 32;
+  while (p < x) p *= 2;
+  return p;
+}
+
 template <int BN, bool DUAL>
 struct Cfg {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES * (DUAL ? 2 : 1);
-  static constexpr int STAGES = (DUAL || BN == 256) ? 4 : 6;
+  static_assert(STAGE_BYTES % 1024 == 0, "operand tiles stay 1024-byte aligned");
+  static constexpr int STAGES_RAW = (220 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int ACC_COLS = BN * (DUAL ? 2 : 1);
-  static constexpr int TMEM_COLS = 2 * ACC_COLS;
+  static constexpr int ACC_STRIDE = pow2_at_least(ACC_COLS);  // accumulator 1 column offset
+  static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
 };
 
@@ -399,7 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         }
         fence_after();
-        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
@@ -452,7 +489,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int bidx = (int)(t / tiles_per_batch);
       const int rem = (int)(t % tiles_per_batch);
       const int mt = rem % p.m_tiles, nt = rem / p.m_tiles;
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_COLS;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
       epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
       fence_before();
       __syncwarp();
@@ -552,19 +589,56 @@ bool gemm_tc_supported(const GemmDesc& g) {
   return tc::encode_fn() != nullptr;
 }
 
+namespace {
+// Tile width with the fewest waves of tiles over the SMs, weighing each wave
+// by the tile width plus a fixed per-tile cost (tiles of one GEMM run
+// concurrently, one per SM, so the last partial wave sets the time).
+int pick_bn(const GemmDesc& g, const int* cands, int n) {
+  const long long m_tiles = (g.M + tc::BM - 1) / tc::BM;
+  const long long sms = tc::num_sms();
+  int best = cands[0];
+  long long best_cost = -1;
+  for (int i = 0; i < n; ++i) {
+    const long long bn = cands[i];
+    const long long tiles = m_tiles * ((g.N + bn - 1) / bn) * g.batch;
+    const long long waves = (tiles + sms - 1) / sms;
+    const long long cost = waves * (bn + 16);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = (int)bn;
+    }
+  }
+  return best;
+}
+}  // namespace
+
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
+  static const int kPlain[] = {256, 224, 128, 112};
   switch (g.epi.mode) {
     case EPI_SWIGLU:
       return tc::run<128, true, EPI_SWIGLU, 0>(g, st);
     case EPI_STORE:
-      return g.N >= 256 ? tc::run<256, false, EPI_STORE, 0>(g, st)
-                        : tc::run<128, false, EPI_STORE, 0>(g, st);
-    case EPI_RESID:
-      return g.N >= 256 ? tc::run<256, false, EPI_RESID, 0>(g, st)
-                        : tc::run<128, false, EPI_RESID, 0>(g, st);
+    case EPI_RESID: {
+      const int bn = pick_bn(g, kPlain, 4);
+      if (g.epi.mode == EPI_STORE) {
+        switch (bn) {
+          case 256: return tc::run<256, false, EPI_STORE, 0>(g, st);
+          case 224: return tc::run<224, false, EPI_STORE, 0>(g, st);
+          case 128: return tc::run<128, false, EPI_STORE, 0>(g, st);
+          default: return tc::run<112, false, EPI_STORE, 0>(g, st);
+        }
+      }
+      switch (bn) {
+        case 256: return tc::run<256, false, EPI_RESID, 0>(g, st);
+        case 224: return tc::run<224, false, EPI_RESID, 0>(g, st);
+        case 128: return tc::run<128, false, EPI_RESID, 0>(g, st);
+        default: return tc::run<112, false, EPI_RESID, 0>(g, st);
+      }
+    }
     case EPI_QNORM_ROPE:
     case EPI_KV: {
-      const bool wide = g.N % 256 == 0;
+      static const int kHeads[] = {256, 128};
+      const bool wide = g.N % 256 == 0 && pick_bn(g, kHeads, 2) == 256;
       if (g.epi.mode == EPI_QNORM_ROPE) {
         if (g.epi.d == 128)
           return wide ? tc::run<256, false, EPI_QNORM_ROPE, 128>(g, st)
