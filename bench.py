@@ -356,6 +356,13 @@ def run_ours(args, ws, rank, local):
                 "achieved": tot_w / (tot_ms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9)}
 
     gemm = summarise(tracers[0], "TFLOP/s") if args.steps >= 1 else None
+    shapes = {}
+    for ms_, w_ in tracers[0].results():
+        d = shapes.setdefault(f"{w_:.4g}", [0, 0.0])
+        d[0] += 1
+        d[1] += ms_
+    gemm_shapes = {k: {"launches": v[0], "avg_ms": v[1] / v[0],
+                       "tflops": float(k) / (v[1] / v[0] / 1e3) / 1e12} for k, v in shapes.items()}
     mix = summarise(tracers[1], "GB/s") if args.steps >= 2 else None
     attn = summarise(tracers[2], "TFLOP/s") if args.steps >= 3 else None
     tc_peak = pk.get("bf16_tflops_sustained", 1400.0)
@@ -367,7 +374,7 @@ def run_ours(args, ws, rank, local):
                     "unit": "TFLOP/s", "frac": gemm["achieved"] / tc_peak, "traffic": None,
                     "peak_source": f"{pk_kind} bf16_tflops_sustained",
                     "launches_timed": gemm["launches"], "avg_launch_ms": gemm["avg_ms"],
-                    "flops_per_launch": gemm["work_per_launch"]}
+                    "flops_per_launch": gemm["work_per_launch"], "by_flops_per_launch": gemm_shapes}
     mixer = None
     if mix:
         hbm = pk.get("hbm_gbs", 6400.0)

@@ -355,13 +355,14 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
 
 wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const int32_t* seq,
                           const int32_t* pos, int32_t channel, const void* cache_k,
-                          const void* cache_v, int32_t B, int32_t Tmax, void* out, void* ws,
-                          size_t ws_bytes, void* stream) {
+                          const void* cache_v, int32_t B, int32_t Tmax, void* out,
+                          int32_t rows_per_seq, void* ws, size_t ws_bytes, void* stream) {
   wm_status s;
   if ((s = check_config(cfg)) != WM_OK) return s;
   if (N < 1 || B < 1 || Tmax < 1 || !q || !seq || !pos || !cache_k || !cache_v || !out)
     return WM_ERR_INVALID_ARG;
   if (channel < 0 || channel >= cfg->k) return WM_ERR_INVALID_ARG;
+  if (rows_per_seq < 0 || (rows_per_seq > 0 && N % rows_per_seq)) return WM_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || !aligned16(cache_k) || !aligned16(cache_v))
     return WM_ERR_INVALID_ARG;
   if ((s = check_ws(*cfg, ws, ws_bytes, N, Tmax)) != WM_OK) return s;
@@ -372,7 +373,7 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
   const int tr = trace_begin(x, WM_TRACE_ATTN);
   ++x.launches;
-  launch_attention(cfg->dtype, a, !x.tc, x.st, 0);
+  launch_attention(cfg->dtype, a, !x.tc, x.st, rows_per_seq);
   trace_end(x, tr, 0.0);  // visible-key count is not known on the host here
   return finish(x);
 }

@@ -338,6 +338,12 @@ void launch_attn_mma(const AttnArgs& a, int nq, cudaStream_t st) {
 void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq) {
   if (a.N <= 0) return;
   const int G = a.Hq / a.Hkv;
+  // prefill groups (several rows per sequence) run on tcgen05; single-row
+  // sequences (decode) and unstructured row lists run on mma.sync
+  if (dtype == WM_BF16 && !simt && nq >= 8 && attention_tc_supported(a, nq)) {
+    launch_attention_tc(a, nq, st);
+    return;
+  }
   if (dtype == WM_BF16 && !simt && G <= AQ) {
     if (nq > 0 && a.N % nq) nq = 0;
     if (a.d == 128) launch_attn_mma<128>(a, nq, st);

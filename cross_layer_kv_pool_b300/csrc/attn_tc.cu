@@ -1,0 +1,545 @@
+// Strictly causal channel attention on tcgen05 tensor cores (bf16, prefill).
+//
+// A CTA owns one KV head and a tile of up to 128 query rows (M): R consecutive
+// token rows of one sequence times the G = Hq/Hkv query heads that read this
+// KV head, packed in (row, head) order. The Q tile is one 3-D TMA box
+// {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly in that
+// order. Keys and values stream in blocks of 128 positions of the channel.
+//
+//   warp 0     TMA: Q once, then K and V blocks into two-stage rings;
+//   warp 1     tcgen05.mma: S_j = Q K_j^T (K-major operands) into one of two
+//              TMEM score buffers, and O_j = P_j V_j (P from shared memory,
+//              V as an MN-major operand) into one of two TMEM output buffers;
+//   warps 2-5  one query row per thread: masked online softmax on S_j read
+//              from TMEM (keys s < pos of the row), P_j written to shared
+//              memory in the 128-byte-swizzled K-major layout, and O
+//              accumulated in registers one block behind (O = O*corr + O_j).
+// Every wait is bounded: on timeout the CTA raises FLAG_TIMEOUT, stops issuing,
+// drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+
+namespace wm {
+namespace atc {
+
+constexpr int BQ = 128, BKEY = 128, NTHREADS = 192;
+constexpr unsigned long long WAIT_NS = 4000000000ull;
+
+struct Params {
+  const int* seq;
+  const int* pos;
+  void* out;          // [N][Hq][HD] bf16
+  uint32_t* flags;
+  int N, Hq, Hkv, G, rpt, nq, Tmax, k, channel, B;
+  float scale_log2;   // log2(e) / sqrt(d)
+};
+
+__device__ __forceinline__ uint32_t su32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try(b, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  while (true) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > WAIT_NS) return false;
+  }
+}
+__device__ __forceinline__ void tma3(const CUtensorMap* m, uint64_t* bar, void* dst, int c0, int c1,
+                                     int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
+      "l"(m), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+// 128-byte swizzled operand tile: rows of 128 B, 8-row groups 1024 B apart
+// (SBO); for the MN-major value operand, LBO is the distance between its
+// 64-column chunks.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(lbo >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16, bf16 A/B, fp32 D, M = 128; b_mn: B is MN-major.
+__host__ __device__ constexpr uint32_t idesc(int n, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn ? (1u << 16) : 0u) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int HD>
+struct Smem {
+  static constexpr int QB = BQ * HD * 2;     // Q tile
+  static constexpr int KB = BKEY * HD * 2;   // one K (or V) block
+  static constexpr int PB = BQ * BKEY * 2;   // P tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;           // 2 stages
+  static constexpr int OFF_V = OFF_K + 2 * KB;       // 2 stages
+  static constexpr int OFF_P = OFF_V + 2 * KB;
+  static constexpr int OFF_BAR = OFF_P + PB;
+  static constexpr int BYTES = 1024 + OFF_BAR + 256;
+  static constexpr int TMEM_COLS = 512;  // 2 score + 2 output buffers of 128 columns
+};
+
+template <int HD>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using SM = Smem<HD>;
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bar = (uint64_t*)(sm + SM::OFF_BAR);
+  uint64_t* q_full = bar + 0;
+  uint64_t* k_full = bar + 1;   // [2]
+  uint64_t* k_empty = bar + 3;  // [2]
+  uint64_t* v_full = bar + 5;   // [2]
+  uint64_t* v_empty = bar + 7;  // [2]
+  uint64_t* s_full = bar + 9;   // [2]
+  uint64_t* s_empty = bar + 11; // [2]
+  uint64_t* p_full = bar + 13;
+  uint64_t* p_empty = bar + 14;
+  uint64_t* o_full = bar + 15;  // [2]
+  uint64_t* o_empty = bar + 17; // [2]
+  uint64_t* mma_done = bar + 19;
+  uint32_t* tmem_holder = (uint32_t*)(bar + 20);
+  volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
+  int* s_meta = (int*)(tmem_holder + 2);  // [0] = number of key blocks, [1] = sequence
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int hk = blockIdx.y;
+  // rows of this tile: late positions first
+  const int tps = (p.nq + p.rpt - 1) / p.rpt;
+  const int b = blockIdx.x / tps, t = tps - 1 - blockIdx.x % tps;
+  const int r0 = b * p.nq + t * p.rpt;
+  const int r1 = min(r0 + p.rpt, (b + 1) * p.nq);
+  const int mrows = (r1 - r0) * p.G;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_empty[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(p_empty, 1);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    // key blocks: enough for the largest visible position of the tile
+    int maxp = 0;
+    for (int r = r0; r < r1; ++r) maxp = max(maxp, p.pos[r]);
+    maxp = min(maxp, p.Tmax);
+    s_meta[0] = (maxp + BKEY - 1) / BKEY;
+    s_meta[1] = p.seq[r0];
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(tmem_holder)),
+                 "r"((uint32_t)SM::TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const int sq = s_meta[1];
+  const bool seq_ok = sq >= 0 && sq < p.B;
+  const int nkb = seq_ok ? s_meta[0] : 0;  // an invalid sequence reads no keys
+  if (!seq_ok && threadIdx.x == 0) atomicOr(p.flags, FLAG_BAD_SEQ);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      bool ok = true;
+      uint8_t* sQ = sm + SM::OFF_Q;
+      // the box fills R*G rows of each 128-row operand chunk; rows past them
+      // feed only accumulator rows that are never read back
+      mbar_expect_tx(q_full, (uint32_t)(HD / 64) * p.G * p.rpt * 128);
+      for (int c = 0; c < HD / 64; ++c) tma3(&tmQ, q_full, sQ + c * BQ * 128, c * 64, hk * p.G, r0);
+      const int zc = ((sq * p.k) + p.channel) * p.Hkv + hk;
+      uint32_t used = 0, lastk = 0, lastv = 0;
+      for (int j = 0; j < nkb && ok; ++j) {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+        mbar_expect_tx(&k_full[s], (uint32_t)SM::KB);
+        for (int c = 0; c < HD / 64; ++c)
+          tma3(&tmK, &k_full[s], sm + SM::OFF_K + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
+        if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+        mbar_expect_tx(&v_full[s], (uint32_t)SM::KB);
+        for (int c = 0; c < HD / 64; ++c)
+          tma3(&tmV, &v_full[s], sm + SM::OFF_V + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
+        used |= 1u << s;
+        lastk = (lastk & ~(1u << s)) | (ph << s);
+        lastv = lastk;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.flags, FLAG_TIMEOUT);
+      }
+      volatile int no_abort = 0;
+      mbar_wait(q_full, 0, &no_abort);
+      for (int s = 0; s < 2; ++s)
+        if (used & (1u << s)) {
+          mbar_wait(&k_full[s], (lastk >> s) & 1, &no_abort);
+          mbar_wait(&v_full[s], (lastv >> s) & 1, &no_abort);
+        }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      fence_after();
+      const uint32_t sQ = su32(sm + SM::OFF_Q), sP = su32(sm + SM::OFF_P);
+      constexpr uint32_t id_qk = idesc(BKEY, false);
+      constexpr uint32_t id_pv = idesc(HD, true);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&k_full[s], ph, abort_flag)) return false;
+        if (!mbar_wait(&s_empty[s], ph ^ 1, abort_flag)) return false;
+        fence_after();
+        const uint32_t sK = su32(sm + SM::OFF_K + s * SM::KB);
+#pragma unroll
+        for (int k16 = 0; k16 < HD / 16; ++k16) {
+          const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
+          const uint32_t offk = (k16 >> 2) * BKEY * 128 + (k16 & 3) * 32;
+          umma(tmem + s * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
+        }
+        commit(&s_full[s]);
+        commit(&k_empty[s]);
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
+        if (!mbar_wait(&v_full[s], ph, abort_flag)) return false;
+        if (!mbar_wait(&o_empty[s], ph ^ 1, abort_flag)) return false;
+        fence_after();
+        const uint32_t sV = su32(sm + SM::OFF_V + s * SM::KB);
+#pragma unroll
+        for (int k16 = 0; k16 < BKEY / 16; ++k16) {
+          const uint32_t offp = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
+          umma(tmem + 256 + s * 128, sdesc(sP + offp, 16),
+               sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, k16 > 0);
+        }
+        commit(&o_full[s]);
+        commit(p_empty);
+        commit(&v_empty[s]);
+        return true;
+      };
+      if (ok && nkb > 0) ok = issue_qk(0);
+      for (int j = 0; j < nkb && ok; ++j) {
+        if (j + 1 < nkb) ok = issue_qk(j + 1);
+        if (ok) ok = issue_pv(j);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(p.flags, FLAG_TIMEOUT);
+      }
+      commit(mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(mma_done, 0, &no_abort);
+    }
+  } else {
+    // ---------------- softmax / output warps: one query row per thread ----------------
+    const int quarter = warp & 3;
+    const int m = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const bool valid = m < mrows;
+    const int r = r0 + (valid ? m / p.G : 0);
+    const int h = hk * p.G + (valid ? m % p.G : 0);
+    int ps = valid ? p.pos[r] : 0;
+    if (valid && (ps < 0 || ps >= p.Tmax)) {
+      atomicOr(p.flags, FLAG_BAD_POS);
+      ps = 0;
+    }
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* prow = sm + SM::OFF_P + m * 128;
+    float o[HD];
+#pragma unroll
+    for (int i = 0; i < HD; ++i) o[i] = 0.f;
+    float mrun = -INFINITY, l = 0.f, corr_prev = 1.f;
+    bool ok = true;
+    auto accumulate = [&](int jj, float corr) -> bool {
+      const int s = jj & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&o_full[s], (jj >> 1) & 1, abort_flag) ? 1 : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) return false;
+      fence_after();
+#pragma unroll
+      for (int c = 0; c < HD / 16; ++c) {
+        float v[16];
+        tmem_ld16(lane_base + 256 + s * 128 + c * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[c * 16 + i] = o[c * 16 + i] * corr + v[i];
+      }
+      fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[s]);
+      return true;
+    };
+    for (int j = 0; j < nkb && ok; ++j) {
+      const int s = j & 1;
+      int w = 1;
+      if (lane == 0) w = mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag) ? 1 : 0;
+      w = __shfl_sync(0xffffffffu, w, 0);
+      if (!w) { ok = false; break; }
+      fence_after();
+      const uint32_t sa = lane_base + s * 128;
+      const int kbase = j * BKEY;
+      const bool need_mask = kbase + BKEY > ps;
+      // pass 1: row max of the scaled, masked scores
+      float mx = mrun;
+#pragma unroll
+      for (int c = 0; c < BKEY / 16; ++c) {
+        float v[16];
+        tmem_ld16(sa + c * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const bool vis = !need_mask || (kbase + c * 16 + i < ps);
+          if (vis) mx = fmaxf(mx, v[i] * p.scale_log2);
+        }
+      }
+      const float base = mx == -INFINITY ? 0.f : mx;
+      const float corr = exp2f(mrun - base);
+      mrun = mx;
+      // P may be overwritten once the previous block's P V product has read it
+      if (j > 0) {
+        if (lane == 0) w = mbar_wait(p_empty, (j - 1) & 1, abort_flag) ? 1 : 0;
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) { ok = false; break; }
+      }
+      // pass 2: probabilities, row sum, P (bf16) into the swizzled K-major tile
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < BKEY / 16; ++c) {
+        float v[16];
+        tmem_ld16(sa + c * 16, v);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const bool v0 = !need_mask || (kbase + c * 16 + i < ps);
+          const bool v1 = !need_mask || (kbase + c * 16 + i + 1 < ps);
+          const float e0 = v0 ? exp2f(v[i] * p.scale_log2 - base) : 0.f;
+          const float e1 = v1 ? exp2f(v[i + 1] * p.scale_log2 - base) : 0.f;
+          rs += e0 + e1;
+          __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
+          pk[i / 2] = *reinterpret_cast<uint32_t*>(&hh);
+        }
+        // keys c*16 .. c*16+15 are 16-byte units 2*(c%4), +1 of 64-key chunk c/4
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int unit = (c & 3) * 2 + u;
+          uint8_t* dst = prow + (c >> 2) * BQ * 128 + ((unit ^ (m & 7)) << 4);
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+      l = l * corr + rs;
+      fence_before();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(p_full);
+        mbar_arrive(&s_empty[s]);
+      }
+      // output of the previous block, scaled to the max before this block
+      if (j > 0 && !accumulate(j - 1, corr_prev)) { ok = false; break; }
+      corr_prev = corr;
+    }
+    if (ok && nkb > 0 && !accumulate(nkb - 1, corr_prev)) ok = false;
+    if (!ok) {
+      if (lane == 0) {
+        *abort_flag = 1;
+        atomicOr(p.flags, FLAG_TIMEOUT);
+      }
+    } else if (valid) {
+      const float inv = (ps > 0 && l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD;
+#pragma unroll
+      for (int i = 0; i < HD; i += 8) {
+        uint4 u;
+        __nv_bfloat162* hh = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hh[e] = __floats2bfloat162_rn(o[i + 2 * e] * inv, o[i + 2 * e + 1] * inv);
+        *reinterpret_cast<uint4*>(dst + i) = u;
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"((uint32_t)SM::TMEM_COLS)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool map3(CUtensorMap* m, const void* ptr, cuuint64_t d0, cuuint64_t d1, cuuint64_t d2,
+          cuuint64_t s1, cuuint64_t s2, cuuint32_t b0, cuuint32_t b1, cuuint32_t b2) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HD>
+cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
+  using SM = Smem<HD>;
+  const int G = a.Hq / a.Hkv;
+  const int rpt = BQ / G;
+  CUtensorMap mq, mk, mv;
+  // q as [N][Hq][HD]: box {64 dims, G heads, rpt rows}
+  if (!map3(&mq, a.q, HD, a.Hq, a.N, (cuuint64_t)HD * 2, (cuuint64_t)a.Hq * HD * 2, 64, G, rpt))
+    return cudaErrorInvalidValue;
+  // cache as [B*k*Hkv][Tmax][HD]: box {64 dims, 128 positions, 1}
+  const cuuint64_t planes = (cuuint64_t)a.B * a.k * a.Hkv;
+  if (!map3(&mk, a.cache_k, HD, a.Tmax, planes, (cuuint64_t)HD * 2, (cuuint64_t)a.Tmax * HD * 2, 64,
+            BKEY, 1))
+    return cudaErrorInvalidValue;
+  if (!map3(&mv, a.cache_v, HD, a.Tmax, planes, (cuuint64_t)HD * 2, (cuuint64_t)a.Tmax * HD * 2, 64,
+            BKEY, 1))
+    return cudaErrorInvalidValue;
+  Params p;
+  p.seq = a.seq; p.pos = a.pos; p.out = a.out; p.flags = a.flags;
+  p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rpt = rpt; p.nq = nq; p.Tmax = a.Tmax;
+  p.k = a.k; p.channel = a.channel; p.B = a.B;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
+  const int B = a.N / nq;
+  const int tiles = B * ((nq + rpt - 1) / rpt);
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(tiles, a.Hkv);
+  attn_tc_kernel<HD><<<grid, NTHREADS, SM::BYTES, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace atc
+
+// The tensor-core path takes structured calls (rows = B sequences of nq
+// consecutive rows, one sequence per tile) whose G heads fit a 128-row tile.
+bool attention_tc_supported(const AttnArgs& a, int nq) {
+  if (nq <= 0 || a.N % nq) return false;
+  const int G = a.Hq / a.Hkv;
+  if (G > atc::BQ || (a.d != 64 && a.d != 128)) return false;
+  if (((uintptr_t)a.q | (uintptr_t)a.cache_k | (uintptr_t)a.cache_v | (uintptr_t)a.out) & 15u)
+    return false;
+  return atc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st) {
+  return a.d == 128 ? atc::run<128>(a, nq, st) : atc::run<64>(a, nq, st);
+}
+
+}  // namespace wm

@@ -602,7 +602,7 @@ int pick_bn(const GemmDesc& g, const int* cands, int n) {
     const long long bn = cands[i];
     const long long tiles = m_tiles * ((g.N + bn - 1) / bn) * g.batch;
     const long long waves = (tiles + sms - 1) / sms;
-    const long long cost = waves * (bn + 16);
+    const long long cost = waves * (bn + 48);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = (int)bn;
@@ -613,13 +613,13 @@ int pick_bn(const GemmDesc& g, const int* cands, int n) {
 }  // namespace
 
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
-  static const int kPlain[] = {256, 224, 128, 112};
+  static const int kPlain[] = {256, 224, 128};
   switch (g.epi.mode) {
     case EPI_SWIGLU:
       return tc::run<128, true, EPI_SWIGLU, 0>(g, st);
     case EPI_STORE:
     case EPI_RESID: {
-      const int bn = pick_bn(g, kPlain, 4);
+      const int bn = pick_bn(g, kPlain, 3);
       if (g.epi.mode == EPI_STORE) {
         switch (bn) {
           case 256: return tc::run<256, false, EPI_STORE, 0>(g, st);

@@ -59,6 +59,8 @@ struct AttnArgs {
   uint32_t* flags;
 };
 void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq);
+bool attention_tc_supported(const AttnArgs& a, int nq);
+cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st);
 
 // ---- pool.cu ---------------------------------------------------------------
 struct MixArgs {

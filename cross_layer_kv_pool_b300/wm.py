@@ -113,7 +113,8 @@ def lib():
         L.wm_pool_mix.restype = ctypes.c_int
         L.wm_pool_mix.argtypes = [cfgp, wp, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp, vp, sz, vp]
         L.wm_channel_attn.restype = ctypes.c_int
-        L.wm_channel_attn.argtypes = [cfgp, vp, i32, vp, vp, i32, vp, vp, i32, i32, vp, vp, sz, vp]
+        L.wm_channel_attn.argtypes = [cfgp, vp, i32, vp, vp, i32, vp, vp, i32, i32, vp, i32, vp, sz,
+                                      vp]
         L.wm_cyclic_pass.restype = ctypes.c_int
         L.wm_cyclic_pass.argtypes = [cfgp, wp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32,
                                      vp, sz, vp]
@@ -219,11 +220,11 @@ def wm_pool_mix_static(m: Model, states, seq, pos, cache_k, cache_v, coeff_out=N
 
 
 def wm_channel_attn(cfg: WMConfig, q, seq, pos, channel: int, cache_k, cache_v, out, ws,
-                    stream=None):
+                    rows_per_seq: int = 0, stream=None):
     B, Tmax = cache_k.shape[0], cache_k.shape[3]
     st = lib().wm_channel_attn(ctypes.byref(cfg), _ptr(q), q.shape[0], _ptr(seq), _ptr(pos),
                                int(channel), _ptr(cache_k), _ptr(cache_v), B, Tmax, _ptr(out),
-                               _ptr(ws), ws.numel(), _stream(stream))
+                               int(rows_per_seq), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "wm_channel_attn")
 
 

@@ -159,11 +159,15 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w,
  * selection"]: layer l reads channel l mod k, which the caller passes here).
  * q: [N][Hq][d], already q-normed and rotated; row n sees keys s < pos[n] of
  * sequence seq[n]; query head h reads KV head h*Hkv/Hq; scale 1/sqrt(d); a row
- * with pos = 0 gets 0. out: [N][Hq*d]. */
+ * with pos = 0 gets 0. out: [N][Hq*d].
+ * rows_per_seq: 0, or a declaration that the rows come as N / rows_per_seq
+ * runs of rows_per_seq consecutive rows of one sequence each (the shape of a
+ * cyclic group); it selects the tensor-core kernel. If the declaration is
+ * false the results are unspecified, but no access leaves the given arrays. */
 wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N,
                           const int32_t* seq, const int32_t* pos, int32_t channel,
                           const void* cache_k, const void* cache_v,
-                          int32_t B, int32_t Tmax, void* out,
+                          int32_t B, int32_t Tmax, void* out, int32_t rows_per_seq,
                           void* ws, size_t ws_bytes, void* stream);
 
 /* Groups q_begin..q_end-1 of one cyclic Gauss-Seidel pass over tokens [B][T]

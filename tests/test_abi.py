@@ -116,7 +116,10 @@ def test_other_entry_points_validate(L):
     assert L.wm_decode_step(ctypes.byref(c), ctypes.byref(w), vp, 1, 3, vp, vp, 64, None, vp,
                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
     # attention: channel out of range
-    assert L.wm_channel_attn(ctypes.byref(c), vp, 4, vp, vp, 2, vp, vp, 1, 64, vp, vp, 1 << 40,
+    assert L.wm_channel_attn(ctypes.byref(c), vp, 4, vp, vp, 2, vp, vp, 1, 64, vp, 0, vp, 1 << 40,
+                             None) == wm.WM_ERR_INVALID_ARG
+    # rows_per_seq must divide N
+    assert L.wm_channel_attn(ctypes.byref(c), vp, 6, vp, vp, 0, vp, vp, 1, 64, vp, 4, vp, 1 << 40,
                              None) == wm.WM_ERR_INVALID_ARG
     # pool: N = 0, misaligned states
     assert L.wm_pool_mix(ctypes.byref(c), ctypes.byref(w), vp, 0, vp, vp, vp, vp, 1, 64, None,

@@ -21,9 +21,10 @@ def _lib():
 # Channel attention
 # ---------------------------------------------------------------------------
 
+@pytest.mark.parametrize("rps", [0, 200])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d,Hq,Hkv", [(64, 4, 2), (128, 14, 2), (64, 8, 8)])
-def test_attention_uniform_closed_form(dtype, d, Hq, Hkv):
+def test_attention_uniform_closed_form(dtype, d, Hq, Hkv, rps):
     """Zero keys: the output is the mean of the visible values, which encode
     channel, sequence, position and KV head; checked exactly."""
     s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=3)
@@ -43,7 +44,7 @@ def test_attention_uniform_closed_form(dtype, d, Hq, Hkv):
     out = torch.empty((N, Hq * d), dtype=s.torch_dtype, device="cuda")
     ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
     for c in range(s.k):
-        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws)
+        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws, rows_per_seq=rps)
         torch.cuda.synchronize()
         o = host(out).reshape(N, Hq, d)
         P = host(pos)
@@ -88,6 +89,39 @@ def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax):
                         for r in range(N)])
         err = relerr(host(out).reshape(N, Hq, d), ref)
         assert err <= TOL[dtype]["attn"], err
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,Hq,Hkv,Tmax,g", [(128, 14, 2, 2304, 16), (64, 8, 8, 700, 4),
+                                             (128, 4, 1, 300, 7)])
+def test_attention_group_rows_vs_oracle(dtype, d, Hq, Hkv, Tmax, g):
+    """Rows shaped like a cyclic group (per sequence, positions q + u*g), the
+    tensor-core path, including key blocks past Tmax and a ragged last tile."""
+    s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=3)
+    cfg = wm.make_config(s)
+    B, q = 3, g - 1
+    P = np.arange(q, Tmax, g)
+    nq = len(P)
+    ck = synth.make_normal((B, s.k, Hkv, Tmax, d), 21, "cuda", 2.0, s.torch_dtype)
+    cv = synth.make_normal((B, s.k, Hkv, Tmax, d), 22, "cuda", 1.0, s.torch_dtype)
+    seq_h = np.repeat(np.arange(B), nq)
+    pos_h = np.tile(P, B)
+    N = B * nq
+    seq = torch.tensor(seq_h, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(pos_h, dtype=torch.int32, device="cuda")
+    qt = synth.make_normal((N, Hq, d), 23, "cuda", 1.0, s.torch_dtype)
+    out = torch.empty((N, Hq * d), dtype=s.torch_dtype, device="cuda")
+    ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
+    c = 2
+    wm.wm_channel_attn(cfg, qt, seq, pos, c, ck, cv, out, ws, rows_per_seq=nq)
+    torch.cuda.synchronize()
+    assert wm.wm_check_flags(ws) == 0
+    K, Vv, Q = host(ck), host(cv), host(qt)
+    rows = np.r_[0:8, nq - 8:nq + 8, N - 8:N]
+    ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
+                    for r in rows])
+    err = relerr(host(out).reshape(N, Hq, d)[rows], ref)
+    assert err <= TOL[dtype]["attn"], err
 
 
 # ---------------------------------------------------------------------------
