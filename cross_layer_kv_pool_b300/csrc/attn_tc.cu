@@ -10,10 +10,13 @@
 //   warp 1     tcgen05.mma: S_j = Q K_j^T (K-major operands) into one of two
 //              TMEM score buffers, and O_j = P_j V_j (P from shared memory,
 //              V as an MN-major operand) into one of two TMEM output buffers;
-//   warps 2-5  one query row per thread: masked online softmax on S_j read
-//              from TMEM (keys s < pos of the row), P_j written to shared
-//              memory in the 128-byte-swizzled K-major layout, and O
-//              accumulated in registers one block behind (O = O*corr + O_j).
+//   warps 2-9  two threads per query row (warps w and w + 4 share a TMEM lane
+//              quarter and take one half of the keys and of the output dims
+//              each): masked online softmax on S_j read from TMEM (keys
+//              s < pos of the row; the halves exchange row maxima through
+//              shared memory), P_j written to shared memory in the
+//              128-byte-swizzled K-major layout, and O accumulated in
+//              registers one block behind (O = O*corr + O_j).
 // Every wait is bounded: on timeout the CTA raises FLAG_TIMEOUT, stops issuing,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -24,7 +27,7 @@
 namespace wm {
 namespace atc {
 
-constexpr int BQ = 128, BKEY = 128, NTHREADS = 192;
+constexpr int BQ = 128, BKEY = 128, NTHREADS = 320;  // 2 + 8 warps
 constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 struct Params {
@@ -148,6 +151,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_ld32_nw(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+// 64 consecutive columns of this thread's TMEM lane, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  tmem_ld32_nw(taddr, r);
+  tmem_ld32_nw(taddr + 32, r + 32);
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 template <int HD>
 struct Smem {
   static constexpr int QB = BQ * HD * 2;     // Q tile
@@ -157,7 +182,8 @@ struct Smem {
   static constexpr int OFF_K = OFF_Q + QB;           // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * KB;       // 2 stages
   static constexpr int OFF_P = OFF_V + 2 * KB;
-  static constexpr int OFF_BAR = OFF_P + PB;
+  static constexpr int OFF_X = OFF_P + PB;  // row-statistic exchange [3][2][128]
+  static constexpr int OFF_BAR = OFF_X + 3 * 2 * BQ * 4;
   static constexpr int BYTES = 1024 + OFF_BAR + 256;
   static constexpr int TMEM_COLS = 512;  // 2 score + 2 output buffers of 128 columns
 };
@@ -182,7 +208,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* o_full = bar + 15;  // [2]
   uint64_t* o_empty = bar + 17; // [2]
   uint64_t* mma_done = bar + 19;
-  uint32_t* tmem_holder = (uint32_t*)(bar + 20);
+  uint64_t* xbar = bar + 20;    // [4] row-statistic exchange per TMEM lane quarter
+  uint32_t* tmem_holder = (uint32_t*)(bar + 24);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   int* s_meta = (int*)(tmem_holder + 2);  // [0] = number of key blocks, [1] = sequence
 
@@ -203,13 +230,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&s_empty[i], 8);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 4);
+      mbar_init(&o_empty[i], 8);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(p_empty, 1);
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
     *abort_flag = 0;
     // key blocks: enough for the largest visible position of the tile
     int maxp = 0;
@@ -332,24 +360,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_wait(mma_done, 0, &no_abort);
     }
   } else {
-    // ---------------- softmax / output warps: one query row per thread ----------------
+    // ------------- softmax / output warps: two threads per query row -------------
+    constexpr int HO = HD / 2;  // output dims per thread
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;  // which 64 keys of S and which half of O
     const int m = quarter * 32 + lane;  // query row of the tile = TMEM lane
     const bool valid = m < mrows;
     const int r = r0 + (valid ? m / p.G : 0);
     const int h = hk * p.G + (valid ? m % p.G : 0);
     int ps = valid ? p.pos[r] : 0;
     if (valid && (ps < 0 || ps >= p.Tmax)) {
-      atomicOr(p.flags, FLAG_BAD_POS);
+      if (half == 0) atomicOr(p.flags, FLAG_BAD_POS);
       ps = 0;
     }
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* prow = sm + SM::OFF_P + m * 128;
-    float o[HD];
+    uint8_t* prow = sm + SM::OFF_P + half * BQ * 128 + m * 128;
+    float* xch = reinterpret_cast<float*>(sm + SM::OFF_X);  // [parity][half][row]
+    float o[HO];
 #pragma unroll
-    for (int i = 0; i < HD; ++i) o[i] = 0.f;
+    for (int i = 0; i < HO; ++i) o[i] = 0.f;
     float mrun = -INFINITY, l = 0.f, corr_prev = 1.f;
     bool ok = true;
+    uint32_t xph = 0;
+    // both threads of a row publish a value, then read the other's (bounded)
+    auto exchange = [&]() -> bool {
+      mbar_arrive(&xbar[quarter]);
+      const bool r = mbar_wait(&xbar[quarter], xph, abort_flag);
+      xph ^= 1;
+      return r;
+    };
     auto accumulate = [&](int jj, float corr) -> bool {
       const int s = jj & 1;
       int w = 1;
@@ -357,12 +396,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) return false;
       fence_after();
+      if constexpr (HO == 64) {
+        float v[64];
+        tmem_ld64(lane_base + 256 + s * 128 + half * HO, v);
 #pragma unroll
-      for (int c = 0; c < HD / 16; ++c) {
-        float v[16];
-        tmem_ld16(lane_base + 256 + s * 128 + c * 16, v);
+        for (int i = 0; i < 64; ++i) o[i] = o[i] * corr + v[i];
+      } else {
+        float v[32];
+        tmem_ld32(lane_base + 256 + s * 128 + half * HO, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o[c * 16 + i] = o[c * 16 + i] * corr + v[i];
+        for (int i = 0; i < 32; ++i) o[i] = o[i] * corr + v[i];
       }
       fence_before();
       __syncwarp();
@@ -376,21 +419,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       w = __shfl_sync(0xffffffffu, w, 0);
       if (!w) { ok = false; break; }
       fence_after();
-      const uint32_t sa = lane_base + s * 128;
-      const int kbase = j * BKEY;
-      const bool need_mask = kbase + BKEY > ps;
-      // pass 1: row max of the scaled, masked scores
-      float mx = mrun;
+      // this thread's 64 keys: kbase .. kbase + 63; visible are those < ps
+      const int kbase = j * BKEY + half * 64;
+      const int nvis = min(max(ps - kbase, 0), 64);
+      float sv[64];
+      tmem_ld64(lane_base + s * 128 + half * 64, sv);
+      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BKEY / 16; ++c) {
-        float v[16];
-        tmem_ld16(sa + c * 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const bool vis = !need_mask || (kbase + c * 16 + i < ps);
-          if (vis) mx = fmaxf(mx, v[i] * p.scale_log2);
-        }
+      for (int i = 0; i < 64; ++i) {
+        sv[i] = i < nvis ? sv[i] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sv[i]);
       }
+      // row max over both halves
+      xch[(s * 2 + half) * BQ + m] = mx;
+      if (!exchange()) { ok = false; break; }
+      mx = fmaxf(fmaxf(mx, xch[(s * 2 + (half ^ 1)) * BQ + m]), mrun);
       const float base = mx == -INFINITY ? 0.f : mx;
       const float corr = exp2f(mrun - base);
       mrun = mx;
@@ -400,31 +443,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         w = __shfl_sync(0xffffffffu, w, 0);
         if (!w) { ok = false; break; }
       }
-      // pass 2: probabilities, row sum, P (bf16) into the swizzled K-major tile
       float rs = 0.f;
 #pragma unroll
-      for (int c = 0; c < BKEY / 16; ++c) {
-        float v[16];
-        tmem_ld16(sa + c * 16, v);
-        uint32_t pk[8];
+      for (int u = 0; u < 8; ++u) {
+        uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          const bool v0 = !need_mask || (kbase + c * 16 + i < ps);
-          const bool v1 = !need_mask || (kbase + c * 16 + i + 1 < ps);
-          const float e0 = v0 ? exp2f(v[i] * p.scale_log2 - base) : 0.f;
-          const float e1 = v1 ? exp2f(v[i + 1] * p.scale_log2 - base) : 0.f;
+        for (int e = 0; e < 4; ++e) {
+          const float e0 = exp2f(sv[8 * u + 2 * e] - base);
+          const float e1 = exp2f(sv[8 * u + 2 * e + 1] - base);
           rs += e0 + e1;
           __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
-          pk[i / 2] = *reinterpret_cast<uint32_t*>(&hh);
+          pk[e] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        // keys c*16 .. c*16+15 are 16-byte units 2*(c%4), +1 of 64-key chunk c/4
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int unit = (c & 3) * 2 + u;
-          uint8_t* dst = prow + (c >> 2) * BQ * 128 + ((unit ^ (m & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-        }
+        *reinterpret_cast<uint4*>(prow + ((u ^ (m & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       l = l * corr + rs;
       fence_before();
@@ -439,16 +470,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       corr_prev = corr;
     }
     if (ok && nkb > 0 && !accumulate(nkb - 1, corr_prev)) ok = false;
+    // total row sum over both halves
+    xch[(4 + half) * BQ + m] = l;
+    if (ok && !exchange()) ok = false;
+    const float lt = l + xch[(4 + (half ^ 1)) * BQ + m];
     if (!ok) {
       if (lane == 0) {
         *abort_flag = 1;
         atomicOr(p.flags, FLAG_TIMEOUT);
       }
     } else if (valid) {
-      const float inv = (ps > 0 && l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD;
+      const float inv = (ps > 0 && lt > 0.f) ? 1.f / lt : 0.f;
+      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD + half * HO;
 #pragma unroll
-      for (int i = 0; i < HD; i += 8) {
+      for (int i = 0; i < HO; i += 8) {
         uint4 u;
         __nv_bfloat162* hh = reinterpret_cast<__nv_bfloat162*>(&u);
 #pragma unroll
