@@ -167,6 +167,7 @@ __device__ __forceinline__ void ld_bf16x32(const __nv_bfloat16* p, float* v) {
 }
 
 // RMSNorm over one head held in registers, gain, then rotate-half RoPE.
+// Gains are read 8 at a time and the (cos, sin) table 2 pairs at a time.
 template <int HD>
 __device__ __forceinline__ void norm_rope(float (&v)[HD], const __nv_bfloat16* gain, float eps,
                                           const float2* rt) {
@@ -175,13 +176,27 @@ __device__ __forceinline__ void norm_rope(float (&v)[HD], const __nv_bfloat16* g
   for (int i = 0; i < HD; ++i) ss += v[i] * v[i];
   const float inv = rsqrtf(ss / (float)HD + eps);
 #pragma unroll
-  for (int i = 0; i < HD; ++i) v[i] *= inv * __bfloat162float(gain[i]);
+  for (int i = 0; i < HD; i += 8) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(gain + i));
+    const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
-  for (int t = 0; t < HD / 2; ++t) {
-    const float2 cs = rt[t];
-    const float x1 = v[t], x2 = v[t + HD / 2];
+    for (int e = 0; e < 4; ++e) {
+      const float2 g = __bfloat1622float2(g2[e]);
+      v[i + 2 * e] *= inv * g.x;
+      v[i + 2 * e + 1] *= inv * g.y;
+    }
+  }
+  const float4* rt4 = reinterpret_cast<const float4*>(rt);
+#pragma unroll
+  for (int t = 0; t < HD / 2; t += 2) {
+    const float4 cs = __ldg(rt4 + t / 2);
+    float x1 = v[t], x2 = v[t + HD / 2];
     v[t] = x1 * cs.x - x2 * cs.y;
     v[t + HD / 2] = x2 * cs.x + x1 * cs.y;
+    x1 = v[t + 1];
+    x2 = v[t + 1 + HD / 2];
+    v[t + 1] = x1 * cs.z - x2 * cs.w;
+    v[t + 1 + HD / 2] = x2 * cs.z + x1 * cs.w;
   }
 }
 
@@ -393,7 +408,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
         const int bidx = (int)(t / tiles_per_batch);
         const int rem = (int)(t % tiles_per_batch);
-        const int mt = rem % p.m_tiles, nt = rem / p.m_tiles;
+        const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
@@ -488,7 +503,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_after();
       const int bidx = (int)(t / tiles_per_batch);
       const int rem = (int)(t % tiles_per_batch);
-      const int mt = rem % p.m_tiles, nt = rem / p.m_tiles;
+      const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
       epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
       fence_before();
