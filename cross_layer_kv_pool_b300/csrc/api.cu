@@ -12,7 +12,7 @@ namespace {
 
 enum Buf {
   B_FLAGS, B_ROPE, B_TOK, B_SEQ, B_POS, B_ROWMAP, B_STASH, B_HMID, B_HL, B_XN, B_Q, B_O,
-  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_LASTX, NBUF
+  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_LASTX, B_PARTIAL, B_ATTNP, B_END, NBUF
 };
 
 struct Layout {
@@ -43,6 +43,17 @@ Layout make_layout(const wm_config& c, long long N, long long Tmax) {
   sz[B_INV] = (size_t)N * c.L * 4;
   sz[B_COEFF] = (size_t)N * 2 * c.k * c.L * 4;
   sz[B_MIXED] = (size_t)N * 2 * c.k * c.D * es;
+  {  // split-K partial sums for GEMMs of at most 128 rows
+    const long long rows = N < 128 ? N : 128;
+    long long w = 2LL * c.F;
+    const long long cand[] = {(long long)c.Hq * c.d, c.D, 2LL * c.k * c.L,
+                              (long long)c.k * c.Hkv * c.d};
+    for (long long v : cand) w = v > w ? v : w;
+    sz[B_PARTIAL] = (size_t)rows * w * 4;
+  }
+  // decode attention key-split partials (at most 16 splits, rows <= 1024)
+  sz[B_ATTNP] = (size_t)(N < 1024 ? N : 1024) * c.Hq * 16 * (c.d + 2) * 4;
+  sz[B_END] = 0;
   Layout lay;
   size_t o = 0;
   for (int i = 0; i < NBUF; ++i) {
@@ -136,10 +147,16 @@ void trace_end(const Ctx& x, int idx, double work) {
 
 // bf16 contractions run on the tensor-core engine; shapes it cannot express
 // (operand strides not 16-byte multiples) and the fp32 mode run on CUDA cores.
-void gemm(const Ctx& x, const GemmDesc& g) {
+void gemm(const Ctx& x, const GemmDesc& gd) {
   const int tr = trace_begin(x, WM_TRACE_GEMM);
+  GemmDesc g = gd;
+  g.partial = x.buf<float>(B_PARTIAL);
+  g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
+  if (g.partial_elems <= 0) g.partial = nullptr;
   if (x.tc && gemm_tc_supported(g)) {
-    const cudaError_t e = launch_gemm_tc(g, x.st);
+    int n = 0;
+    const cudaError_t e = launch_gemm_tc(g, x.st, &n);
+    x.launches += n - 1;  // the caller counted one launch
     if (e != cudaSuccess && x.err == cudaSuccess) x.err = e;
   } else {
     launch_gemm_simt(x.c->dtype, g, x.st);
@@ -195,8 +212,9 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
       a.B = B; a.k = c.k; a.Hq = c.Hq; a.Hkv = c.Hkv; a.d = c.d; a.Tmax = Tmax;
       a.out = x.buf<void>(B_O); a.flags = x.flags();
       const int tr = trace_begin(x, WM_TRACE_ATTN);
-      ++x.launches;
-      launch_attention(c.dtype, a, !x.tc, x.st, nq);
+      const long long pe = (long long)(x.lay.off[B_ATTNP + 1] - x.lay.off[B_ATTNP]) / 4;
+      x.launches += launch_attention(c.dtype, a, !x.tc, x.st, nq, nq == 1 ? (int)(pos_sum / B) : 0,
+                                     x.buf<float>(B_ATTNP), pe);
       trace_end(x, tr, 4.0 * c.Hq * c.d * pos_sum);
     }
     {  // O projection + residual
@@ -294,6 +312,12 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   }
 }
 
+// The split-K partial sums start at zero in every call (finalize re-zeroes).
+void zero_partials(const Ctx& x) {
+  const size_t n = x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL];
+  if (n) cudaMemsetAsync(x.buf<char>(B_PARTIAL), 0, n, x.st);
+}
+
 wm_status finish(const Ctx& x) {
   if (x.c->trace) x.c->trace->launches += x.launches;
   const cudaError_t e = cudaGetLastError();
@@ -343,6 +367,7 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
   cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
+  zero_partials(x);
   ++x.launches;
   launch_norm_emit(c.dtype, states, (long long)c.L * c.D, c.D, N, 0, c.L, c.D, c.L, nullptr,
                    nullptr, x.buf<float>(B_INV), w->src_norm,
@@ -372,8 +397,10 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
   const int tr = trace_begin(x, WM_TRACE_ATTN);
-  ++x.launches;
-  launch_attention(cfg->dtype, a, !x.tc, x.st, rows_per_seq);
+  // one row per sequence: the decode engine, with Tmax as the bound on visible keys
+  const long long pe = (long long)(x.lay.off[B_ATTNP + 1] - x.lay.off[B_ATTNP]) / 4;
+  x.launches += launch_attention(cfg->dtype, a, !x.tc, x.st, rows_per_seq,
+                                 rows_per_seq == 1 ? Tmax : 0, x.buf<float>(B_ATTNP), pe);
   trace_end(x, tr, 0.0);  // visible-key count is not known on the host here
   return finish(x);
 }
@@ -398,6 +425,7 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
   const wm_config& c = *cfg;
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, T, c.d, c.rope_base, x.st);
+  zero_partials(x);
   for (int q = q_begin; q < q_end; ++q) {
     const int nq = (T - q + g - 1) / g;
     const int N = B * nq;
@@ -453,6 +481,7 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
   const wm_config& c = *cfg;
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), pos, pos + 1, c.d, c.rope_base, x.st);
+  zero_partials(x);
   ++x.launches;
   launch_decode_rows(tokens, B, pos, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
                      x.buf<int32_t>(B_POS), x.st);

@@ -333,26 +333,271 @@ void launch_attn_mma(const AttnArgs& a, int nq, cudaStream_t st) {
   attn_mma_kernel<HD><<<grid, ATHREADS, smem, st>>>(a, rpt, nq);
 }
 
+// ---------------------------------------------------------------------------
+// Decode engine (bf16, one query row per sequence): flash-decoding. A CTA owns
+// (row, KV head, key split); its G query heads form one 16-row MMA tile. Four
+// warps take every 4th block of 32 keys of the split with warp-private,
+// double-buffered cp.async tiles (no block-wide barrier in the loop), keep
+// their own online-softmax state, and merge through shared memory at the end.
+// With several splits, each writes (max, sum, unnormalised output) and
+// attn_combine_kernel merges them.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int DWARPS = 4, DKEYS = 32;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs a, int nsplit,
+                                                                  float* part) {
+  constexpr int LDS = HD + 8;
+  extern __shared__ __align__(16) uint8_t sm[];
+  __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm);          // [16][LDS]
+  __nv_bfloat16* sKV = sQ + 16 * LDS;                                 // [warp][2][K,V][DKEYS][LDS]
+  float* sO = reinterpret_cast<float*>(sm);                           // [warp][16][HD + 2], reused
+  const int G = a.Hq / a.Hkv;
+  const int n = blockIdx.x / a.Hkv, hk = blockIdx.x % a.Hkv, z = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sq = a.seq[n], ps = a.pos[n];
+  const bool ok = sq >= 0 && sq < a.B && ps >= 0 && ps < a.Tmax;
+  if (!ok && threadIdx.x == 0) atomicOr(a.flags, (sq < 0 || sq >= a.B) ? FLAG_BAD_SEQ : FLAG_BAD_POS);
+  const int visible = ok ? ps : 0;
+  int span = (visible + nsplit - 1) / nsplit;
+  span = (span + DKEYS - 1) / DKEYS * DKEYS;
+  const int k0 = min(visible, z * span), k1 = min(visible, k0 + span);
+  const int nblk = (k1 - k0 + DKEYS - 1) / DKEYS;
+  const long long kvbase = ok ? (((long long)sq * a.k + a.channel) * a.Hkv + hk) * a.Tmax * HD : 0;
+  const __nv_bfloat16* Kg = (const __nv_bfloat16*)a.cache_k + kvbase;
+  const __nv_bfloat16* Vg = (const __nv_bfloat16*)a.cache_v + kvbase;
+  const __nv_bfloat16* qg = (const __nv_bfloat16*)a.q;
+  // Q rows: the G heads of this KV head (rows >= G are zero)
+  for (int c = threadIdx.x; c < 16 * (HD / 8); c += 32 * DWARPS) {
+    const int m = c / (HD / 8), part8 = c % (HD / 8);
+    const bool v = m < G;
+    cp_async16(sQ + m * LDS + part8 * 8,
+               qg + ((long long)n * a.Hq + hk * G + (v ? m : 0)) * HD + part8 * 8, v);
+  }
+  cp_async_commit();
+  __nv_bfloat16* myKV = sKV + warp * 2 * 2 * DKEYS * LDS;
+  auto load_blk = [&](int blk, int buf) {
+    __nv_bfloat16* dK = myKV + (buf * 2 + 0) * DKEYS * LDS;
+    __nv_bfloat16* dV = myKV + (buf * 2 + 1) * DKEYS * LDS;
+    for (int c = lane; c < DKEYS * (HD / 8); c += 32) {
+      const int rr = c / (HD / 8), part8 = c % (HD / 8);
+      const int s = k0 + blk * DKEYS + rr;
+      const bool v = s < k1;
+      const long long off = (long long)(v ? s : 0) * HD + part8 * 8;
+      cp_async16(dK + rr * LDS + part8 * 8, Kg + off, v);
+      cp_async16(dV + rr * LDS + part8 * 8, Vg + off, v);
+    }
+    cp_async_commit();
+  };
+  const float sl2 = 1.4426950408889634f / sqrtf((float)HD);
+  float o[HD / 8][4];
+#pragma unroll
+  for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int blk = warp, buf = 0;
+  if (blk < nblk) load_blk(blk, 0);
+  cp_async_wait<0>();
+  __syncthreads();  // Q visible to every warp
+  const uint32_t qaddr = smem_addr(sQ + (lane & 15) * LDS + (lane >> 4) * 8);
+  for (; blk < nblk; blk += DWARPS, buf ^= 1) {
+    if (blk + DWARPS < nblk) {
+      load_blk(blk + DWARPS, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncwarp();
+    const __nv_bfloat16* Kb = myKV + (buf * 2 + 0) * DKEYS * LDS;
+    const __nv_bfloat16* Vb = myKV + (buf * 2 + 1) * DKEYS * LDS;
+    float sc[DKEYS / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < DKEYS / 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ks += 2) {
+      uint32_t qa[4], qb[4];
+      ldsm_x4(qaddr + ks * 32, qa[0], qa[1], qa[2], qa[3]);
+      ldsm_x4(qaddr + ks * 32 + 32, qb[0], qb[1], qb[2], qb[3]);
+#pragma unroll
+      for (int nt = 0; nt < DKEYS / 8; ++nt) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(smem_addr(Kb + (nt * 8 + (lane & 7)) * LDS + ks * 16 + (lane >> 3) * 8), b0, b1, b2, b3);
+        mma_bf16(sc[nt], qa, b0, b1);
+        mma_bf16(sc[nt], qb, b2, b3);
+      }
+    }
+    float mx0 = m0, mx1 = m1;
+#pragma unroll
+    for (int nt = 0; nt < DKEYS / 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool vis = k0 + blk * DKEYS + nt * 8 + 2 * (lane & 3) + e < k1;
+        sc[nt][e] = vis ? sc[nt][e] * sl2 : -INFINITY;
+        sc[nt][2 + e] = vis ? sc[nt][2 + e] * sl2 : -INFINITY;
+        mx0 = fmaxf(mx0, sc[nt][e]);
+        mx1 = fmaxf(mx1, sc[nt][2 + e]);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float base0 = mx0 == -INFINITY ? 0.f : mx0, base1 = mx1 == -INFINITY ? 0.f : mx1;
+    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+    m0 = mx0;
+    m1 = mx1;
+    float rs0 = 0.f, rs1 = 0.f;
+    uint32_t pf[DKEYS / 16][4];
+#pragma unroll
+    for (int nt = 0; nt < DKEYS / 8; ++nt) {
+      const float e0 = exp2f(sc[nt][0] - base0), e1 = exp2f(sc[nt][1] - base0);
+      const float e2 = exp2f(sc[nt][2] - base1), e3 = exp2f(sc[nt][3] - base1);
+      rs0 += e0 + e1;
+      rs1 += e2 + e3;
+      __nv_bfloat162 p01 = __floats2bfloat162_rn(e0, e1), p23 = __floats2bfloat162_rn(e2, e3);
+      pf[nt >> 1][(nt & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&p01);
+      pf[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&p23);
+    }
+    l0 = l0 * corr0 + rs0;
+    l1 = l1 * corr1 + rs1;
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) {
+      o[i][0] *= corr0; o[i][1] *= corr0;
+      o[i][2] *= corr1; o[i][3] *= corr1;
+    }
+#pragma unroll
+    for (int j = 0; j < DKEYS / 16; ++j) {
+      const uint32_t pa[4] = {pf[j][0], pf[j][1], pf[j][2], pf[j][3]};
+#pragma unroll
+      for (int dn = 0; dn < HD / 8; dn += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_addr(Vb + (j * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + dn * 8 +
+                            (lane >> 4) * 8), b0, b1, b2, b3);
+        mma_bf16(o[dn], pa, b0, b1);
+        mma_bf16(o[dn + 1], pa, b2, b3);
+      }
+    }
+    __syncwarp();  // this buffer may be refilled two blocks later
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  __syncthreads();  // all warps are done with their tiles: reuse shared memory
+  // per-warp state: sO[w][row][0..HD) = o, [HD] = m, [HD + 1] = l
+  float* mine = sO + (size_t)warp * 16 * (HD + 2);
+  const int g0 = lane >> 2, g1 = g0 + 8;
+#pragma unroll
+  for (int dn = 0; dn < HD / 8; ++dn) {
+    const int d0 = dn * 8 + 2 * (lane & 3);
+    mine[g0 * (HD + 2) + d0] = o[dn][0];
+    mine[g0 * (HD + 2) + d0 + 1] = o[dn][1];
+    mine[g1 * (HD + 2) + d0] = o[dn][2];
+    mine[g1 * (HD + 2) + d0 + 1] = o[dn][3];
+  }
+  if ((lane & 3) == 0) {
+    mine[g0 * (HD + 2) + HD] = m0;
+    mine[g0 * (HD + 2) + HD + 1] = l0;
+    mine[g1 * (HD + 2) + HD] = m1;
+    mine[g1 * (HD + 2) + HD + 1] = l1;
+  }
+  __syncthreads();
+  // merge the warps: thread (head h, dims) for h < G
+  for (int idx = threadIdx.x; idx < G * HD; idx += 32 * DWARPS) {
+    const int h = idx / HD, d = idx % HD;
+    float M = -INFINITY;
+    for (int w = 0; w < DWARPS; ++w) M = fmaxf(M, sO[((size_t)w * 16 + h) * (HD + 2) + HD]);
+    const float base = M == -INFINITY ? 0.f : M;
+    float L = 0.f, acc = 0.f;
+    for (int w = 0; w < DWARPS; ++w) {
+      const float* st = sO + ((size_t)w * 16 + h) * (HD + 2);
+      const float f = exp2f(st[HD] - base);
+      L += f * st[HD + 1];
+      acc += f * st[d];
+    }
+    const int head = hk * G + h;
+    if (nsplit == 1) {
+      const float v = (visible > 0 && L > 0.f) ? acc / L : 0.f;
+      ((__nv_bfloat16*)a.out)[((long long)n * a.Hq + head) * HD + d] = __float2bfloat16_rn(v);
+    } else {
+      float* dst = part + (((long long)n * a.Hq + head) * nsplit + z) * (HD + 2);
+      dst[d] = acc;
+      if (d == 0) {
+        dst[HD] = M;
+        dst[HD + 1] = L;
+      }
+    }
+  }
+}
+
+template <int HD>
+__global__ void attn_combine_kernel(const AttnArgs a, int nsplit, const float* part) {
+  const long long nh = blockIdx.x;  // (row, head)
+  const int d = threadIdx.x;
+  if (d >= HD) return;
+  const float* src = part + nh * nsplit * (HD + 2);
+  float M = -INFINITY;
+  for (int z = 0; z < nsplit; ++z) M = fmaxf(M, src[z * (HD + 2) + HD]);
+  const float base = M == -INFINITY ? 0.f : M;
+  float L = 0.f, acc = 0.f;
+  for (int z = 0; z < nsplit; ++z) {
+    const float f = exp2f(src[z * (HD + 2) + HD] - base);
+    L += f * src[z * (HD + 2) + HD + 1];
+    acc += f * src[z * (HD + 2) + d];
+  }
+  ((__nv_bfloat16*)a.out)[nh * HD + d] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+}
+
+template <int HD>
+int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long part_elems,
+                       cudaStream_t st) {
+  int sms = 148, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long ctas = (long long)a.N * a.Hkv;
+  int nsplit = (int)((2LL * sms + ctas - 1) / ctas);
+  nsplit = max(1, min(nsplit, min(16, (kv_len + 4 * DKEYS - 1) / (4 * DKEYS))));
+  if (nsplit > 1 && (long long)a.N * a.Hq * nsplit * (HD + 2) > part_elems) nsplit = 1;
+  const size_t smem_loop = (size_t)(16 + DWARPS * 2 * 2 * DKEYS) * (HD + 8) * 2;
+  const size_t smem_merge = (size_t)DWARPS * 16 * (HD + 2) * 4;
+  const size_t smem = smem_loop > smem_merge ? smem_loop : smem_merge;
+  cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  dim3 grid((unsigned)ctas, nsplit);
+  attn_decode_kernel<HD><<<grid, 32 * DWARPS, smem, st>>>(a, nsplit, part);
+  if (nsplit > 1) {
+    attn_combine_kernel<HD><<<(unsigned)((long long)a.N * a.Hq), HD, 0, st>>>(a, nsplit, part);
+    return 2;
+  }
+  return 1;
+}
+
 // nq > 0 declares the rows as B = N / nq sequences of nq consecutive rows
 // (cyclic groups and decode steps); 0 = no structure assumed.
-void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq) {
-  if (a.N <= 0) return;
+int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq, int kv_len,
+                     float* part, long long part_elems) {
+  if (a.N <= 0) return 0;
   const int G = a.Hq / a.Hkv;
+  // one row per sequence (decode steps): split the keys across CTAs
+  if (dtype == WM_BF16 && !simt && nq == 1 && G <= 16 && kv_len > 0) {
+    return a.d == 128 ? launch_attn_decode<128>(a, kv_len, part, part_elems, st)
+                      : launch_attn_decode<64>(a, kv_len, part, part_elems, st);
+  }
   // prefill groups (several rows per sequence) run on tcgen05; single-row
   // sequences (decode) and unstructured row lists run on mma.sync
   if (dtype == WM_BF16 && !simt && nq >= 8 && attention_tc_supported(a, nq)) {
     launch_attention_tc(a, nq, st);
-    return;
+    return 1;
   }
   if (dtype == WM_BF16 && !simt && G <= AQ) {
     if (nq > 0 && a.N % nq) nq = 0;
     if (a.d == 128) launch_attn_mma<128>(a, nq, st);
     else launch_attn_mma<64>(a, nq, st);
-    return;
+    return 1;
   }
   const long long warps = (long long)a.N * a.Hq;
   const int blocks = (int)((warps + 3) / 4);
   WM_DISPATCH_S(dtype, attn_simt_kernel<S><<<blocks, 128, 0, st>>>(a));
+  return 1;
 }
 
 }  // namespace wm

@@ -96,6 +96,11 @@ struct GemmDesc {
   long long ldb = 0, b_bstride = 0;
   const void* B2 = nullptr;      // EPI_SWIGLU second operand (same strides as B)
   Epi epi;
+  // Zero-filled fp32 scratch for split-K (nullable): when a GEMM has too few
+  // output tiles to occupy the GPU, K is split across CTAs that add their
+  // partial tiles here; a finalize kernel applies the epilogue and re-zeroes.
+  float* partial = nullptr;
+  long long partial_elems = 0;
 };
 
 // Per-head epilogue on one row's d values (EPI_QNORM_ROPE and the key branch

@@ -27,8 +27,10 @@ constexpr unsigned long long WAIT_NS = 4000000000ull;  // 4 s bound on any wait
 struct Params {
   int M, N, K, batch;
   int m_tiles, n_tiles, num_kb;
-  long long total_tiles;
+  int ksplit, kb_per;     // split-K: K slices per output tile, k-blocks per slice
+  long long total_tiles;  // output tiles x ksplit
   int vec_out, vec_res;
+  float* partial;         // split-K accumulation target [batch][M][N] (x2 when DUAL)
   Epi epi;
 };
 
@@ -332,6 +334,106 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
   }
 }
 
+// Split-K: add this slice's accumulator row into the fp32 partial sums.
+template <int BN, bool DUAL>
+__device__ __forceinline__ void partial_tile(const Params& p, uint32_t taddr, int row, int bidx,
+                                             int n0) {
+  constexpr int CW = (BN % 32 == 0) ? 32 : 16;
+  const bool row_ok = row < p.M;
+  const long long plane = (long long)p.batch * p.M * p.N;
+#pragma unroll 1
+  for (int half = 0; half < (DUAL ? 2 : 1); ++half) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < BN; c0 += CW) {
+      uint32_t r[CW];
+      __syncwarp();
+      if constexpr (CW == 32) tmem_ld32(taddr + half * BN + c0, *reinterpret_cast<uint32_t(*)[32]>(r));
+      else tmem_ld16(taddr + half * BN + c0, r);
+      tmem_wait_ld();
+      const int col = n0 + c0;
+      if (!row_ok || col >= p.N) continue;
+      float* dst = p.partial + half * plane + ((long long)bidx * p.M + row) * p.N + col;
+      if (col + CW <= p.N && (p.N % 4) == 0) {
+#pragma unroll
+        for (int i = 0; i < CW; i += 4)
+          atomicAdd(reinterpret_cast<float4*>(dst + i),
+                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+      } else {
+        for (int i = 0; i < CW && col + i < p.N; ++i) atomicAdd(dst + i, __uint_as_float(r[i]));
+      }
+    }
+  }
+}
+
+// Epilogue applied to summed split-K partials: one thread per output element
+// (plain modes) or per (row, head) (norm modes); re-zeroes what it read.
+template <int MODE, int HD>
+__global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
+  const Epi& e = p.epi;
+  const long long plane = (long long)p.batch * p.M * p.N;
+  if constexpr (MODE == EPI_QNORM_ROPE || MODE == EPI_KV) {
+    const int heads = p.N / HD;
+    const long long task = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    if (task >= (long long)p.batch * p.M * heads) return;
+    const int hh = (int)(task % heads);
+    const int row = (int)((task / heads) % p.M);
+    const int bidx = (int)(task / ((long long)heads * p.M));
+    float* src = p.partial + ((long long)bidx * p.M + row) * p.N + hh * HD;
+    float v[HD];
+#pragma unroll
+    for (int i = 0; i < HD; i += 4) {
+      const float4 f = *reinterpret_cast<const float4*>(src + i);
+      v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
+      *reinterpret_cast<float4*>(src + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int ps = e.pos[row];
+    if (ps < 0 || ps >= e.Tmax) {
+      atomicOr(e.flags, FLAG_BAD_POS);
+      return;
+    }
+    const float2* rt = e.rope + (long long)ps * (HD / 2);
+    __nv_bfloat16* dst;
+    if constexpr (MODE == EPI_QNORM_ROPE) {
+      norm_rope<HD>(v, (const __nv_bfloat16*)e.gain, e.eps, rt);
+      dst = (__nv_bfloat16*)e.C + (long long)row * e.ldc + hh * HD;
+    } else {
+      const int sq = e.seq[row];
+      if (sq < 0 || sq >= e.B) {
+        atomicOr(e.flags, FLAG_BAD_SEQ);
+        return;
+      }
+      if (e.kv_branch == 0)
+        norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps, rt);
+      dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
+            ((((long long)sq * e.k + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
+    }
+#pragma unroll
+    for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);
+  } else {
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane;
+         i += (long long)gridDim.x * blockDim.x) {
+      const int col = (int)(i % p.N);
+      const int row = (int)((i / p.N) % p.M);
+      const int bidx = (int)(i / ((long long)p.N * p.M));
+      float v = p.partial[i];
+      p.partial[i] = 0.f;
+      if constexpr (MODE == EPI_SWIGLU) {
+        const float u = p.partial[plane + i];
+        p.partial[plane + i] = 0.f;
+        v = v / (1.f + __expf(-v)) * u;
+      }
+      if constexpr (MODE == EPI_RESID) v += __bfloat162float(((const __nv_bfloat16*)e.R)[(long long)row * e.ldr + col]);
+      const long long orow = (MODE == EPI_STORE && e.rowmap) ? e.rowmap[row] : row;
+      const long long off = (long long)bidx * e.c_bstride + orow * e.ldc + col;
+      if (e.out_f32)
+        ((float*)e.C)[off] = v;
+      else
+        ((__nv_bfloat16*)e.C)[off] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
 constexpr int pow2_at_least(int x) {
   int p = 32;
   while (p < x) p *= 2;
@@ -406,10 +508,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t phase = 0, used = 0, last_phase = 0;
       bool ok = true;
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const int bidx = (int)(t / tiles_per_batch);
-        const int rem = (int)(t % tiles_per_batch);
+        const long long ot = t / p.ksplit;
+        const int ks = (int)(t % p.ksplit);
+        const int bidx = (int)(ot / tiles_per_batch);
+        const int rem = (int)(ot % tiles_per_batch);
         const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
@@ -452,7 +557,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         fence_after();
         const uint32_t d_tmem = tmem_base + acc * C::ACC_STRIDE;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb0 = (int)(t % p.ksplit) * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -462,7 +568,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16) {
-            const uint32_t accum = (kb | k16) != 0;
+            const uint32_t accum = (kb != kb0) || (k16 != 0);
             umma(d_tmem, sdesc(sa + 32 * k16), sdesc(sb + 32 * k16), idesc, accum);
             if (DUAL) umma(d_tmem + BN, sdesc(sa + 32 * k16), sdesc(sb + C::B_BYTES + 32 * k16), idesc, accum);
           }
@@ -501,11 +607,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         break;
       }
       fence_after();
-      const int bidx = (int)(t / tiles_per_batch);
-      const int rem = (int)(t % tiles_per_batch);
+      const long long ot = t / p.ksplit;
+      const int bidx = (int)(ot / tiles_per_batch);
+      const int rem = (int)(ot % tiles_per_batch);
       const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
-      epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
+      if (p.partial)
+        partial_tile<BN, DUAL>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
+      else
+        epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
       fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -559,7 +669,7 @@ int num_sms() {
 }
 
 template <int BN, bool DUAL, int MODE, int HD>
-cudaError_t run(const GemmDesc& g, cudaStream_t st) {
+cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   using C = Cfg<BN, DUAL>;
   CUtensorMap ta, tb, tb2;
   if (!make_map(&ta, g.A, g.K, g.M, g.batch, g.lda, g.a_bstride, BM)) return cudaErrorInvalidValue;
@@ -575,7 +685,22 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st) {
   p.m_tiles = (g.M + BM - 1) / BM;
   p.n_tiles = (g.N + BN - 1) / BN;
   p.num_kb = (g.K + BK - 1) / BK;
-  p.total_tiles = (long long)p.m_tiles * p.n_tiles * g.batch;
+  const long long out_tiles = (long long)p.m_tiles * p.n_tiles * g.batch;
+  p.ksplit = 1;
+  p.kb_per = p.num_kb;
+  p.partial = nullptr;
+  const int sms = num_sms();
+  const long long need = (long long)g.batch * g.M * g.N * (DUAL ? 2 : 1);
+  if (g.partial && need <= g.partial_elems && out_tiles * 2 <= sms && p.num_kb >= 4 &&
+      (MODE != EPI_QNORM_ROPE && MODE != EPI_KV ? true : (g.N % HD == 0))) {
+    int ks = (int)((sms + out_tiles - 1) / out_tiles);
+    ks = min(ks, p.num_kb / 2);
+    p.kb_per = (p.num_kb + ks - 1) / ks;
+    p.ksplit = (p.num_kb + p.kb_per - 1) / p.kb_per;
+    if (p.ksplit > 1) p.partial = g.partial;
+    else p.kb_per = p.num_kb;
+  }
+  p.total_tiles = out_tiles * p.ksplit;
   p.epi = g.epi;
   const size_t osz = g.epi.out_f32 ? 4 : 2;
   p.vec_out = ((uintptr_t)g.epi.C % 16 == 0) && ((g.epi.ldc * osz) % 16 == 0) &&
@@ -584,8 +709,18 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st) {
   auto kern = gemm_tc_kernel<BN, DUAL, MODE, HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const long long grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
   kern<<<(int)grid, NTHREADS, C::SMEM, st>>>(ta, tb, tb2, p);
+  if (launches) ++*launches;
+  if (p.partial) {
+    long long work = (MODE == EPI_QNORM_ROPE || MODE == EPI_KV)
+                         ? (long long)g.batch * g.M * (g.N / (HD > 0 ? HD : 1))
+                         : (long long)g.batch * g.M * g.N;
+    long long blocks = (work + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    finalize_kernel<MODE, (HD > 0 ? HD : 64)><<<(int)blocks, 256, 0, st>>>(p);
+    if (launches) ++*launches;
+  }
   return cudaGetLastError();
 }
 
@@ -627,27 +762,27 @@ int pick_bn(const GemmDesc& g, const int* cands, int n) {
 }
 }  // namespace
 
-cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int* launches) {
   static const int kPlain[] = {256, 224, 128};
   switch (g.epi.mode) {
     case EPI_SWIGLU:
-      return tc::run<128, true, EPI_SWIGLU, 0>(g, st);
+      return tc::run<128, true, EPI_SWIGLU, 0>(g, st, launches);
     case EPI_STORE:
     case EPI_RESID: {
       const int bn = pick_bn(g, kPlain, 3);
       if (g.epi.mode == EPI_STORE) {
         switch (bn) {
-          case 256: return tc::run<256, false, EPI_STORE, 0>(g, st);
-          case 224: return tc::run<224, false, EPI_STORE, 0>(g, st);
-          case 128: return tc::run<128, false, EPI_STORE, 0>(g, st);
-          default: return tc::run<112, false, EPI_STORE, 0>(g, st);
+          case 256: return tc::run<256, false, EPI_STORE, 0>(g, st, launches);
+          case 224: return tc::run<224, false, EPI_STORE, 0>(g, st, launches);
+          case 128: return tc::run<128, false, EPI_STORE, 0>(g, st, launches);
+          default: return tc::run<112, false, EPI_STORE, 0>(g, st, launches);
         }
       }
       switch (bn) {
-        case 256: return tc::run<256, false, EPI_RESID, 0>(g, st);
-        case 224: return tc::run<224, false, EPI_RESID, 0>(g, st);
-        case 128: return tc::run<128, false, EPI_RESID, 0>(g, st);
-        default: return tc::run<112, false, EPI_RESID, 0>(g, st);
+        case 256: return tc::run<256, false, EPI_RESID, 0>(g, st, launches);
+        case 224: return tc::run<224, false, EPI_RESID, 0>(g, st, launches);
+        case 128: return tc::run<128, false, EPI_RESID, 0>(g, st, launches);
+        default: return tc::run<112, false, EPI_RESID, 0>(g, st, launches);
       }
     }
     case EPI_QNORM_ROPE:
@@ -656,15 +791,15 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st) {
       const bool wide = g.N % 256 == 0 && pick_bn(g, kHeads, 2) == 256;
       if (g.epi.mode == EPI_QNORM_ROPE) {
         if (g.epi.d == 128)
-          return wide ? tc::run<256, false, EPI_QNORM_ROPE, 128>(g, st)
-                      : tc::run<128, false, EPI_QNORM_ROPE, 128>(g, st);
-        return wide ? tc::run<256, false, EPI_QNORM_ROPE, 64>(g, st)
-                    : tc::run<128, false, EPI_QNORM_ROPE, 64>(g, st);
+          return wide ? tc::run<256, false, EPI_QNORM_ROPE, 128>(g, st, launches)
+                      : tc::run<128, false, EPI_QNORM_ROPE, 128>(g, st, launches);
+        return wide ? tc::run<256, false, EPI_QNORM_ROPE, 64>(g, st, launches)
+                    : tc::run<128, false, EPI_QNORM_ROPE, 64>(g, st, launches);
       }
       if (g.epi.d == 128)
-        return wide ? tc::run<256, false, EPI_KV, 128>(g, st)
-                    : tc::run<128, false, EPI_KV, 128>(g, st);
-      return wide ? tc::run<256, false, EPI_KV, 64>(g, st) : tc::run<128, false, EPI_KV, 64>(g, st);
+        return wide ? tc::run<256, false, EPI_KV, 128>(g, st, launches)
+                    : tc::run<128, false, EPI_KV, 128>(g, st, launches);
+      return wide ? tc::run<256, false, EPI_KV, 64>(g, st, launches) : tc::run<128, false, EPI_KV, 64>(g, st, launches);
     }
   }
   return cudaErrorNotSupported;

@@ -43,7 +43,7 @@ void launch_broadcast_coeff(const float* stat, int N, int n_per_row, float* coef
 // ---- gemm_simt.cu / gemm_tc.cu --------------------------------------------
 void launch_gemm_simt(int dtype, const GemmDesc& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
-cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st);
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int* launches);
 
 // ---- attn.cu ---------------------------------------------------------------
 struct AttnArgs {
@@ -58,7 +58,11 @@ struct AttnArgs {
   void* out;              // [N][Hq*d]
   uint32_t* flags;
 };
-void launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq);
+// Returns the number of kernels launched. kv_len: the largest visible key
+// count when the host knows it (decode), else 0. part: fp32 scratch for the
+// decode engine's key splits (part_elems floats), nullable.
+int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq, int kv_len,
+                     float* part, long long part_elems);
 bool attention_tc_supported(const AttnArgs& a, int nq);
 cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st);
 

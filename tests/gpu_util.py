@@ -154,7 +154,7 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
     return worst
 
 
-def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None):
+def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None, start_pos=0):
     """Decode steps t = 0..T-1 on the GPU; each step is compared with the
     oracle's step from the GPU's cache snapshot. Returns worst errors."""
     import oracle.whitematter as O
@@ -166,12 +166,13 @@ def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None):
     lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
     tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
     worst = {"cache": 0.0, "logits": 0.0}
-    for t in range(T):
+    for i in range(T):
+        t = start_pos + i
         torch.cuda.synchronize()
         sk, sv = host(ck), host(cv)
-        wm.wm_decode_step(m, tok[:, t].contiguous(), t, ck, cv, lg, ws)
+        wm.wm_decode_step(m, tok[:, i].contiguous(), t, ck, cv, lg, ws)
         torch.cuda.synchronize()
-        rl = O.decode_step(oc, Wn, tokens_h[:, t], t, sk, sv)
+        rl = O.decode_step(oc, Wn, tokens_h[:, i], t, sk, sv)
         worst["logits"] = max(worst["logits"], relerr(host(lg), rl))
         worst["cache"] = max(worst["cache"], relerr(host(ck)[:, :, :, t], sk[:, :, :, t]),
                              relerr(host(cv)[:, :, :, t], sv[:, :, :, t]))

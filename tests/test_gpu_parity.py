@@ -21,7 +21,7 @@ def _lib():
 # Channel attention
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("rps", [0, 200])
+@pytest.mark.parametrize("rps", [0, 200, 1])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d,Hq,Hkv", [(64, 4, 2), (128, 14, 2), (64, 8, 8)])
 def test_attention_uniform_closed_form(dtype, d, Hq, Hkv, rps):
@@ -63,9 +63,12 @@ def test_attention_uniform_closed_form(dtype, d, Hq, Hkv, rps):
     assert wm.wm_check_flags(ws) == 0
 
 
+@pytest.mark.parametrize("rps", [0, 1])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("d,Hq,Hkv,Tmax", [(64, 4, 2, 300), (128, 14, 2, 257), (64, 8, 8, 130)])
-def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax):
+@pytest.mark.parametrize("d,Hq,Hkv,Tmax", [(64, 4, 2, 300), (128, 14, 2, 257), (64, 8, 8, 130),
+                                           (128, 14, 2, 2304)])
+def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax, rps):
+    """Random rows; rows_per_seq = 1 takes the decode engine (key splits)."""
     s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=2)
     cfg = wm.make_config(s)
     B = 2
@@ -82,7 +85,7 @@ def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax):
     out = torch.empty((N, Hq * d), dtype=s.torch_dtype, device="cuda")
     ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
     for c in range(s.k):
-        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws)
+        wm.wm_channel_attn(cfg, q, seq, pos, c, ck, cv, out, ws, rows_per_seq=rps)
         torch.cuda.synchronize()
         K, Vv, Q = host(ck), host(cv), host(q)
         ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
@@ -246,6 +249,24 @@ def test_decode_steps_isolated(dtype, shape_kw):
     w = isolated_decode(m, Wn, tokens, Tmax=T + 5)
     tol = TOL[dtype]
     assert w["logits"] <= tol["logits"] and w["cache"] <= tol["cache"], w
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape_kw", [dict(d=128, Hq=14, Hkv=2, D=256, L=3, k=3),
+                                      dict(L=4, k=2, Hq=8, Hkv=8)])
+def test_decode_long_context_isolated(dtype, shape_kw):
+    """Decode steps at positions near 700 and 2000 over a random prefix: the
+    decode engine splits the keys across CTAs and merges the splits."""
+    s = small_shape(dtype, **shape_kw)
+    m, Wn = model(s, seed=12)
+    B, Tmax = 3, 2100
+    for start in (700, 2001):
+        ck = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 40 + start, "cuda", 1.0, s.torch_dtype)
+        cv = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 41 + start, "cuda", 1.0, s.torch_dtype)
+        tokens = np.random.default_rng(start).integers(0, s.V, size=(B, 3))
+        w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start)
+        tol = TOL[dtype]
+        assert w["logits"] <= tol["logits"] and w["cache"] <= tol["cache"], (start, w)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
