@@ -336,10 +336,29 @@ def run_ours(args, ws, rank, local):
         d1.record(stream)
         torch.cuda.synchronize()
         dms = max_over_ranks(d0.elapsed_time(d1), ws)
+        # per-kernel shares of one decode step (separate, traced steps)
+        dtr = {}
+        for kind, name in ((wm.WM_TRACE_GEMM, "gemm"), (wm.WM_TRACE_ATTN, "attention"),
+                           (wm.WM_TRACE_MIX, "mixer")):
+            tr = wm.Tracer(kind, 256)
+            tr.attach(m)
+            wm.wm_decode_step(m, cols[0], T, ck, cv, dlg, wsp)
+            wm.Tracer.detach(m)
+            torch.cuda.synchronize()
+            res = tr.results()
+            dtr[name] = {"launches": len(res), "total_ms": sum(r[0] for r in res),
+                         "launches_per_step_traced": tr.t.launches}
+            if kind == wm.WM_TRACE_GEMM:
+                by = {}
+                for ms_, w_ in res:
+                    d_ = by.setdefault(f"{w_:.4g}", [0, 0.0])
+                    d_[0] += 1
+                    d_[1] += ms_
+                dtr[name]["by_flops"] = {k: [v[0], v[1] / v[0]] for k, v in by.items()}
         cache_bytes = 2 * B * s.k * s.Hkv * Tmax * s.d * 2
         decode = {"value": ws * B * nd / (dms / 1e3), "unit": "tok/s", "steps": nd, "batch": B,
                   "prefix": T, "ms_per_step": dms / nd, "peak_cache_bytes": cache_bytes,
-                  "cache_bytes_L_channels": cache_bytes // s.k * s.L}
+                  "cache_bytes_L_channels": cache_bytes // s.k * s.L, "kernels": dtr}
     if wm.wm_check_flags(wsp) != 0:
         raise RuntimeError("device-side checks failed")
 

@@ -154,7 +154,7 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
     return worst
 
 
-def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None, start_pos=0):
+def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None, start_pos=0, spread=False):
     """Decode steps t = 0..T-1 on the GPU; each step is compared with the
     oracle's step from the GPU's cache snapshot. Returns worst errors."""
     import oracle.whitematter as O
@@ -165,14 +165,22 @@ def isolated_decode(m, Wn, tokens_h, Tmax, start_cache=None, start_pos=0):
     ws = m.workspace(B, Tmax)
     lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
     tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
-    worst = {"cache": 0.0, "logits": 0.0}
+    worst = {"cache": 0.0, "logits": 0.0, "spread_cache": 0.0, "spread_logits": 0.0}
+    Wp = perturbed(Wn, SPREAD_EPS) if spread else None
     for i in range(T):
         t = start_pos + i
         torch.cuda.synchronize()
         sk, sv = host(ck), host(cv)
         wm.wm_decode_step(m, tok[:, i].contiguous(), t, ck, cv, lg, ws)
         torch.cuda.synchronize()
+        if spread:
+            pk, pv = sk.copy(), sv.copy()
         rl = O.decode_step(oc, Wn, tokens_h[:, i], t, sk, sv)
+        if spread:
+            pl = O.decode_step(oc, Wp, tokens_h[:, i], t, pk, pv)
+            worst["spread_logits"] = max(worst["spread_logits"], relerr(pl, rl))
+            worst["spread_cache"] = max(worst["spread_cache"], relerr(pk[:, :, :, t], sk[:, :, :, t]),
+                                        relerr(pv[:, :, :, t], sv[:, :, :, t]))
         worst["logits"] = max(worst["logits"], relerr(host(lg), rl))
         worst["cache"] = max(worst["cache"], relerr(host(ck)[:, :, :, t], sk[:, :, :, t]),
                              relerr(host(cv)[:, :, :, t], sv[:, :, :, t]))

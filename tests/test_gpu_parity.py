@@ -246,9 +246,10 @@ def test_decode_steps_isolated(dtype, shape_kw):
     m, Wn = model(s, seed=2)
     B, T = 3, 10
     tokens = np.random.default_rng(3).integers(0, s.V, size=(B, T))
-    w = isolated_decode(m, Wn, tokens, Tmax=T + 5)
+    w = isolated_decode(m, Wn, tokens, Tmax=T + 5, spread=dtype == "bf16")
     tol = TOL[dtype]
-    assert w["logits"] <= tol["logits"] and w["cache"] <= tol["cache"], w
+    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
+    assert within(w["cache"], tol["cache"], w["spread_cache"]), w
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -264,9 +265,11 @@ def test_decode_long_context_isolated(dtype, shape_kw):
         ck = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 40 + start, "cuda", 1.0, s.torch_dtype)
         cv = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 41 + start, "cuda", 1.0, s.torch_dtype)
         tokens = np.random.default_rng(start).integers(0, s.V, size=(B, 3))
-        w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start)
+        w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start,
+                            spread=dtype == "bf16")
         tol = TOL[dtype]
-        assert w["logits"] <= tol["logits"] and w["cache"] <= tol["cache"], (start, w)
+        assert within(w["logits"], tol["logits"], w["spread_logits"]), (start, w)
+        assert within(w["cache"], tol["cache"], w["spread_cache"]), (start, w)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
