@@ -153,10 +153,15 @@ void gemm(const Ctx& x, const GemmDesc& gd) {
   g.partial = x.buf<float>(B_PARTIAL);
   g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
   if (g.partial_elems <= 0) g.partial = nullptr;
-  if (x.tc && gemm_tc_supported(g)) {
+  // Few rows and enough column blocks (decode steps): the mma.sync engine
+  // spreads the weight stream over many CTAs without a TMEM pipeline to set up.
+  const bool skinny = g.M <= 64 && (long long)((g.N + 15) / 16) * g.batch >= 96 && g.N < 32768;
+  if (x.tc && skinny && gemm_skinny_supported(g)) {
+    x.launches += launch_gemm_skinny(g, x.st) - 1;  // the caller counted one launch
+  } else if (x.tc && gemm_tc_supported(g)) {
     int n = 0;
     const cudaError_t e = launch_gemm_tc(g, x.st, &n);
-    x.launches += n - 1;  // the caller counted one launch
+    x.launches += n - 1;
     if (e != cudaSuccess && x.err == cudaSuccess) x.err = e;
   } else {
     launch_gemm_simt(x.c->dtype, g, x.st);

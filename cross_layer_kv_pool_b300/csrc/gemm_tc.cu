@@ -726,6 +726,26 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
 
 }  // namespace tc
 
+// Per-head epilogue over fp32 sums that another engine left in g.partial.
+int launch_finalize_head(const GemmDesc& g, cudaStream_t st) {
+  tc::Params p;
+  p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
+  p.m_tiles = p.n_tiles = p.num_kb = p.ksplit = p.kb_per = 1;
+  p.total_tiles = 0; p.vec_out = p.vec_res = 0;
+  p.partial = g.partial;
+  p.epi = g.epi;
+  const long long work = (long long)g.batch * g.M * (g.N / g.epi.d);
+  const unsigned blocks = (unsigned)((work + 255) / 256);
+  if (g.epi.mode == EPI_QNORM_ROPE) {
+    if (g.epi.d == 128) tc::finalize_kernel<EPI_QNORM_ROPE, 128><<<blocks, 256, 0, st>>>(p);
+    else tc::finalize_kernel<EPI_QNORM_ROPE, 64><<<blocks, 256, 0, st>>>(p);
+  } else {
+    if (g.epi.d == 128) tc::finalize_kernel<EPI_KV, 128><<<blocks, 256, 0, st>>>(p);
+    else tc::finalize_kernel<EPI_KV, 64><<<blocks, 256, 0, st>>>(p);
+  }
+  return 1;
+}
+
 bool gemm_tc_supported(const GemmDesc& g) {
   auto a16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batch <= 0) return false;

@@ -272,6 +272,23 @@ def test_decode_long_context_isolated(dtype, shape_kw):
         assert within(w["cache"], tol["cache"], w["spread_cache"]), (start, w)
 
 
+def test_decode_1p3b_widths_isolated():
+    """Decode steps with the 1.3B model's widths (D 1792, 14 query heads of 128,
+    2 KV heads, F 4608), 8 layers and 8 channels: the few-row contraction
+    engine (fused residual and SwiGLU, head epilogues through fp32 sums) and
+    the split-key decode attention."""
+    s = synth.HALF_1P3B.replace(L=8, k=8, V=2000)
+    m, Wn = model(s, seed=21, jitter=0.1)
+    B, Tmax, start = 8, 300, 250
+    ck = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 51, "cuda", 1.0, s.torch_dtype)
+    cv = synth.make_normal((B, s.k, s.Hkv, Tmax, s.d), 52, "cuda", 1.0, s.torch_dtype)
+    tokens = np.random.default_rng(5).integers(0, s.V, size=(B, 3))
+    w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start, spread=True)
+    tol = TOL["bf16"]
+    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
+    assert within(w["cache"], tol["cache"], w["spread_cache"]), w
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_partial_pass_writes_exact_positions(dtype):
     s = small_shape(dtype)
