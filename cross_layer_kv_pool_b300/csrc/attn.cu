@@ -555,7 +555,7 @@ int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long par
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long ctas = (long long)a.N * a.Hkv;
-  int nsplit = (int)((6LL * sms + ctas - 1) / ctas);
+  int nsplit = (int)((2LL * sms + ctas - 1) / ctas);
   nsplit = max(1, min(nsplit, min(16, (kv_len + 4 * DKEYS - 1) / (4 * DKEYS))));
   if (nsplit > 1 && (long long)a.N * a.Hq * nsplit * (HD + 2) > part_elems) nsplit = 1;
   const size_t smem_loop = (size_t)(16 + DWARPS * 2 * 2 * DKEYS) * (HD + 8) * 2;
