@@ -58,6 +58,13 @@ Readings where the pages are silent (each listed again in the design notes):
       router input, the mixed channels and the cached K/V. Arithmetic between
       those points stays fp64; router coefficients and logits stay unrounded.
       Without ``storage`` (the default) nothing is rounded.
+  R17 Where the mixed channel is stored. c = RMSNorm(m; tau) feeds only the
+      linear K/V projection, so W c = s * W (tau (.) m) with the scalar
+      s = rsqrt(mean(m^2) + eps). ``cfg.mixed_storage == "gained"`` models a
+      pipeline that stores u = tau (.) m and applies s to the projection
+      output; the default "normed" stores c. In exact arithmetic the two are
+      the same function (pinned); they differ only in which tensor bf16
+      storage rounds, and ``mixed`` is then bf16(s * u).
 
 Parity pins for every function below live in tests/test_oracle_pins.py and
 tests/test_oracle_mutants.py (closed forms, special cases, brute force and an
@@ -251,6 +258,8 @@ def pool(cfg, W, states, pos, static_coeff=None):
     R = router_sources(cfg)
     coeff = np.zeros((N, 2, k, L), dtype=np.float64)
     mixed = np.zeros((N, 2, k, D), dtype=np.float64)
+    stored = np.zeros((N, 2, k, D), dtype=np.float64)  # projection input (R17)
+    scale = np.ones((N, 2, k), dtype=np.float64)        # applied to its output
     for beta in range(2):
         n = rmsnorm(states, W["src_norm"][beta], cfg.eps)          # [N, L, D]
         if static_coeff is None:
@@ -261,13 +270,18 @@ def pool(cfg, W, states, pos, static_coeff=None):
         m = np.einsum("njl,nld->njd", a, n)
         coeff[:, beta] = a
         mixed[:, beta] = _st(cfg, rmsnorm(m, W["chan_norm"][beta], cfg.eps))
+        stored[:, beta] = mixed[:, beta]
+        if getattr(cfg, "mixed_storage", "normed") == "gained":
+            scale[:, beta] = 1.0 / np.sqrt(np.mean(m * m, axis=-1) + cfg.eps)
+            stored[:, beta] = _st(cfg, m * _f64(W["chan_norm"][beta]))
+            mixed[:, beta] = _st(cfg, stored[:, beta] * scale[:, beta, :, None])
     K = np.zeros((N, k, Hkv, d), dtype=np.float64)
     V = np.zeros((N, k, Hkv, d), dtype=np.float64)
     for j in range(k):
-        kt = (mixed[:, 0, j] @ _f64(W["Wk"][j]).T).reshape(N, Hkv, d)
+        kt = ((stored[:, 0, j] @ _f64(W["Wk"][j]).T) * scale[:, 0, j, None]).reshape(N, Hkv, d)
         kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)
         K[:, j] = _st(cfg, rope(kt, _f64(pos)[:, None], cfg.rope_base))
-        V[:, j] = _st(cfg, (mixed[:, 1, j] @ _f64(W["Wv"][j]).T).reshape(N, Hkv, d))
+        V[:, j] = _st(cfg, ((stored[:, 1, j] @ _f64(W["Wv"][j]).T) * scale[:, 1, j, None]).reshape(N, Hkv, d))
     return {"K": K, "V": V, "coeff": coeff, "mixed": mixed}
 
 

@@ -57,11 +57,16 @@ def model(shape, seed=0, jitter=0.1, static=None, flags=0):
 def ocfg(shape):
     """The oracle's view of a model: bf16 workloads use its bf16-storage mode
     (activations rounded where a bf16 pipeline stores them), fp32 workloads
-    the plain fp64 arithmetic."""
+    the plain fp64 arithmetic. The bf16 pipeline's mixer stores the gained
+    channel tau (.) m and leaves the norm factor to the K/V projection, so the
+    oracle rounds at that tensor too (reading R17; every bf16 test shape is
+    inside that mixer's envelope: k <= 16, L <= 64, D/32 divisible into
+    slices of at most 14 warps)."""
     ns = SimpleNamespace(**dataclasses.asdict(shape))
     ns.nR = shape.nR
     if shape.dtype == "bf16":
         ns.storage = "bf16"
+        ns.mixed_storage = "gained"
     return ns
 
 

@@ -522,9 +522,35 @@ def check_bf16_storage_mode(O):
     assert np.max(np.abs(lgb - lg)) > 0
 
 
+def check_gained_storage_equivalence(O):
+    """R17: storing u = tau (.) m and scaling the projection output by
+    rsqrt(mean(m^2) + eps) is the same function as storing c = RMSNorm(m; tau)
+    in exact arithmetic (to 1e-10); under bf16 storage the two placements
+    round different tensors, so they differ, but only at bf16 level, and all
+    stored values are bf16 numbers."""
+    c = _cfg(L=5, D=16, k=3, Hq=4, Hkv=2, d=8)
+    W = _weights(c, seed=31)
+    rng = np.random.default_rng(32)
+    states = rng.standard_normal((6, c.L, c.D)) * np.exp(rng.uniform(-1, 1, (6, c.L, 1)))
+    pos = rng.integers(0, 50, 6)
+    ref = O.pool(c, W, states, pos)
+    cg = SimpleNamespace(**vars(c), mixed_storage="gained")
+    got = O.pool(cg, W, states, pos)
+    for key in ("K", "V", "mixed", "coeff"):
+        _close(got[key], ref[key], RTOL, f"gained {key}")
+    cb = SimpleNamespace(**vars(c), storage="bf16")
+    cgb = SimpleNamespace(**vars(cg), storage="bf16")
+    rb, gb = O.pool(cb, W, states, pos), O.pool(cgb, W, states, pos)
+    for key in ("K", "V", "mixed"):
+        assert np.array_equal(O.round_bf16(gb[key]), gb[key]), key
+        _close(gb[key], rb[key], 2.0 ** -6, f"bf16 gained {key}")
+    assert not np.array_equal(gb["mixed"], rb["mixed"])
+
+
 ALL_CHECKS = [
     check_round_bf16,
     check_bf16_storage_mode,
+    check_gained_storage_equivalence,
     check_rmsnorm_closed_forms,
     check_rope_closed_forms,
     check_silu,

@@ -40,6 +40,11 @@ MUTANTS = [
      'kt = rmsnorm(kt, W["k_norm"][j], cfg.eps)\n        K[:, j] = _st(cfg, rope(kt, _f64(pos)[:, None], cfg.rope_base))',
      'kt = rope(kt, _f64(pos)[:, None], cfg.rope_base)\n        K[:, j] = _st(cfg, rmsnorm(kt, W["k_norm"][j], cfg.eps))'),
     ("pool_v_uses_wk", "pool", 'W["Wv"][j]', 'W["Wk"][j]'),
+    ("pool_gained_scale_no_eps", "pool", "np.mean(m * m, axis=-1) + cfg.eps)", "np.mean(m * m, axis=-1))"),
+    ("pool_gained_scale_sum", "pool", "np.mean(m * m, axis=-1)", "np.sum(m * m, axis=-1)"),
+    ("pool_gained_no_tau", "pool", 'stored[:, beta] = _st(cfg, m * _f64(W["chan_norm"][beta]))',
+     'stored[:, beta] = _st(cfg, m)'),
+    ("pool_gained_scale_branch", "pool", "* scale[:, 1, j, None]", "* scale[:, 0, j, None]"),
     ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
      'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
     ("states_are_outputs", "run_rows", "        states[:, l] = h\n        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)",
