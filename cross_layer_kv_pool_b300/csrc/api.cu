@@ -12,7 +12,7 @@ namespace {
 
 enum Buf {
   B_FLAGS, B_ROPE, B_TOK, B_SEQ, B_POS, B_ROWMAP, B_STASH, B_HMID, B_HL, B_XN, B_Q, B_O,
-  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_LASTX, B_PARTIAL, B_ATTNP, B_END, NBUF
+  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_CHSS, B_LASTX, B_PARTIAL, B_ATTNP, B_END, NBUF
 };
 
 struct Layout {
@@ -43,6 +43,7 @@ Layout make_layout(const wm_config& c, long long N, long long Tmax) {
   sz[B_INV] = (size_t)N * c.L * 4;
   sz[B_COEFF] = (size_t)N * 2 * c.k * c.L * 4;
   sz[B_MIXED] = (size_t)N * 2 * c.k * c.D * es;
+  sz[B_CHSS] = (size_t)N * 2 * c.k * 8 * 4;  // deferred channel-norm partial sums
   {  // split-K partial sums for GEMMs of at most 128 rows
     const long long rows = N < 128 ? N : 128;
     long long w = 2LL * c.F;
@@ -273,8 +274,11 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
 
 // Router (or static weights) -> coefficients; mix + channel norm; channel
 // projections with K-norm + RoPE; scatter into the cache at (seq, pos).
-void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* coeff,
-              void* mixed, void* cache_k, void* cache_v, int B, int Tmax) {
+// Router, mixer and K/V projections for N rows. Returns the mixer's deferred
+// norm part count (0: ``mixed`` holds the normed channels; P > 0: it holds
+// u = tau (.) m and the projections applied the norm factor).
+int run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* coeff,
+             void* mixed, void* cache_k, void* cache_v, int B, int Tmax) {
   const wm_config& c = *x.c;
   const wm_weights& w = *x.w;
   const int kL = c.k * c.L;
@@ -296,10 +300,11 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
   MixArgs m;
   m.stash = states; m.ld_row = ld_row; m.inv = x.buf<float>(B_INV); m.coeff = coeff;
   m.src_norm = w.src_norm; m.chan_norm = w.chan_norm; m.mixed = mixed;
+  m.chan_ss = x.buf<float>(B_CHSS);
   m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
   const int tr = trace_begin(x, WM_TRACE_MIX);
   ++x.launches;
-  launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  const int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
   trace_end(x, tr, (double)N * ((double)c.L * c.D * x.es + 2.0 * c.k * c.L * 4 + c.L * 4.0 +
                                  2.0 * c.k * c.D * x.es));
   for (int branch = 0; branch < 2; ++branch) {
@@ -315,9 +320,25 @@ void run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* 
     g.epi.pos = x.buf<int>(B_POS); g.epi.seq = x.buf<int>(B_SEQ);
     g.epi.cache_k = cache_k; g.epi.cache_v = cache_v;
     g.epi.k = c.k; g.epi.Hkv = c.Hkv; g.epi.Tmax = Tmax; g.epi.B = B;
+    if (parts) {
+      g.epi.chan_ss = x.buf<float>(B_CHSS);
+      g.epi.chan_parts = parts;
+      g.epi.chan_D = (float)c.D;
+    }
     ++x.launches;
     gemm(x, g);
   }
+  return parts;
+}
+
+// The caller asked for the channels themselves: apply a deferred norm in place.
+void finish_mixed(const Ctx& x, int N, void* mixed, int parts) {
+  if (!parts) return;
+  MixArgs m{};
+  m.mixed = mixed; m.chan_ss = x.buf<float>(B_CHSS);
+  m.N = N; m.D = x.c->D; m.k = x.c->k; m.L = x.c->L; m.eps = x.c->eps;
+  ++x.launches;
+  launch_mix_normalize(m, parts, x.st);
 }
 
 // The split-K partial sums start at zero in every call (finalize re-zeroes).
@@ -381,8 +402,10 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
                    nullptr, x.buf<float>(B_INV), w->src_norm,
                    w->static_coeff ? nullptr : x.buf<void>(B_RIN), x.nR, c.p, c.p_offset, c.eps,
                    x.st);
-  run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
-           mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  const int parts =
+      run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
+               mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  if (mixed_out) finish_mixed(x, N, mixed_out, parts);
   return finish(x);
 }
 
@@ -582,6 +605,7 @@ Layout pool_static_layout(const wm_config& c, long long N, long long Tmax) {
   put(B_INV, (size_t)N * c.L * 4);
   put(B_COEFF, (size_t)N * 2 * c.k * c.L * 4);
   put(B_MIXED, (size_t)N * 2 * c.k * c.D * es);
+  put(B_CHSS, (size_t)N * 2 * c.k * 8 * 4);
   lay.total = o;
   return lay;
 }
@@ -619,7 +643,9 @@ extern "C" wm_status wm_pool_mix_static(const wm_config* cfg, const wm_weights* 
                    nullptr, x.buf<float>(B_INV), w->src_norm,
                    w->static_coeff ? nullptr : x.buf<void>(B_RIN), x.nR, c.p, c.p_offset, c.eps,
                    x.st);
-  run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
-           mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  const int parts =
+      run_pool(x, N, states, (long long)c.L * c.D, coeff_out ? coeff_out : x.buf<float>(B_COEFF),
+               mixed_out ? mixed_out : x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  if (mixed_out) finish_mixed(x, N, mixed_out, parts);
   return finish(x);
 }

@@ -85,8 +85,22 @@ struct Epi {
   void* cache_v = nullptr;
   int k = 0, Hkv = 0, Tmax = 0, B = 0;
   int kv_branch = 0;             // EPI_KV: 0 = keys (norm + RoPE), 1 = values (raw)
+  // EPI_KV with a deferred channel norm (nullable): the input rows are
+  // u = tau (.) m and output row ``row`` of channel b is scaled by
+  // rsqrt(sum_c chan_ss[row][kv_branch][b][c] / chan_D + eps), the channel
+  // RMSNorm's factor (the projection is linear in its input).
+  const float* chan_ss = nullptr;
+  int chan_parts = 0;
+  float chan_D = 1.f;
   uint32_t* flags = nullptr;
 };
+
+__device__ __forceinline__ float chan_scale(const Epi& e, long long row, int channel) {
+  const float* p = e.chan_ss + ((row * 2 + e.kv_branch) * e.k + channel) * e.chan_parts;
+  float s = 0.f;
+  for (int c = 0; c < e.chan_parts; ++c) s += p[c];
+  return rsqrtf(s / e.chan_D + e.eps);
+}
 
 struct GemmDesc {
   int M = 0, N = 0, K = 0, batch = 1;

@@ -32,6 +32,10 @@ __device__ void epi_store_head(const Epi& e, int b, int gm, int gn0, float* v) {
     atomicOr(e.flags, FLAG_BAD_SEQ);
     return;
   }
+  if (e.chan_ss) {
+    const float cs = chan_scale(e, gm, b);
+    for (int t = 0; t < d; ++t) v[t] *= cs;
+  }
   if (e.kv_branch == 0)
     head_norm_rope<S>(v, d, (const S*)e.gain + (long long)b * e.gain_bstride, e.eps,
                       e.rope + (long long)p * (d >> 1));

@@ -243,6 +243,11 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
           atomicOr(e.flags, FLAG_BAD_SEQ);
           continue;
         }
+        if (e.chan_ss) {
+          const float cs = chan_scale(e, row, bidx);
+#pragma unroll
+          for (int t = 0; t < HD; ++t) v[t] *= cs;
+        }
         if (e.kv_branch == 0)
           norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps,
                         rt);
@@ -402,6 +407,11 @@ __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
       if (sq < 0 || sq >= e.B) {
         atomicOr(e.flags, FLAG_BAD_SEQ);
         return;
+      }
+      if (e.chan_ss) {
+        const float cs = chan_scale(e, row, bidx);
+#pragma unroll
+        for (int t = 0; t < HD; ++t) v[t] *= cs;
       }
       if (e.kv_branch == 0)
         norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps, rt);

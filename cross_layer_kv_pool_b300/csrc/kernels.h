@@ -79,9 +79,19 @@ struct MixArgs {
   const void* src_norm;   // [2][L][D]
   const void* chan_norm;  // [2][k][D]
   void* mixed;            // [2][k][N][D]
+  float* chan_ss;         // [N][2][k][8] slice sums of squares (deferred-norm output)
   int N, L, D, k;
   float eps;
 };
-void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags);
+// Runs the mixer. Returns 0 if ``mixed`` holds the channel-normed c, or P > 0
+// if it holds u = tau (.) m with the norm deferred: chan_ss then holds P
+// partial sums of squares per (row, branch, channel) and the norm factor is
+// rsqrt(sum / D + eps) (applied by the projection epilogue, or in place by
+// launch_mix_normalize).
+int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags);
+// Tensor-core mixer (bf16, deferred norm); returns P, or 0 if the shape is
+// outside its envelope (k > 16, L > 64, 2kL > 1024, misaligned operands).
+int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
+void launch_mix_normalize(const MixArgs& a, int parts, cudaStream_t st);
 
 }  // namespace wm

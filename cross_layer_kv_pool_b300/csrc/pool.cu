@@ -246,10 +246,14 @@ bool launch_mix_stream(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
   return false;
 }
 
-void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags) {
-  if (a.N <= 0) return;
+int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags) {
+  if (a.N <= 0) return 0;
   const bool stream_ok = dtype == WM_BF16 && !simt && a.D % (8 * MIX_C) == 0 &&
                          ((uintptr_t)a.stash % 16 == 0) && (a.ld_row % 8 == 0);
+  if (dtype == WM_BF16 && !simt) {
+    const int parts = launch_mix_tc(a, st, flags);
+    if (parts) return parts;
+  }
   if (stream_ok) {
     bool done = false;
     switch (a.k) {
@@ -262,9 +266,10 @@ void launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_
       case 16: done = launch_mix_stream<16>(a, flags, st); break;
       default: break;
     }
-    if (done) return;
+    if (done) return 0;
   }
   WM_DISPATCH_S(dtype, mix_simt_kernel<S><<<a.N, 256, a.D * sizeof(float), st>>>(a));
+  return 0;
 }
 
 }  // namespace wm
