@@ -8,15 +8,18 @@
 //
 //   warp 0     TMA: Q once, then K and V blocks into two-stage rings;
 //   warp 1     tcgen05.mma: S_j = Q K_j^T (K-major operands) into one of two
-//              TMEM score buffers, and O_j = P_j V_j (P from shared memory,
-//              V as an MN-major operand) into one of two TMEM output buffers;
+//              TMEM score buffers, and O += P_j V_j (P from shared memory, V
+//              as an MN-major operand) into one TMEM output accumulator;
 //   warps 2-9  two threads per query row (warps w and w + 4 share a TMEM lane
 //              quarter and take one half of the keys and of the output dims
-//              each): masked online softmax on S_j read from TMEM (keys
-//              s < pos of the row; the halves exchange row maxima through
-//              shared memory), P_j written to shared memory in the
-//              128-byte-swizzled K-major layout, and O accumulated in
-//              registers one block behind (O = O*corr + O_j).
+//              each): online softmax on S_j read from TMEM (keys s < pos of
+//              the row, masked only in blocks that are partly visible; the
+//              halves exchange row maxima through shared memory), P_j
+//              written to shared memory in the 128-byte-swizzled K-major
+//              layout. The exponent base is raised lazily, only when a row
+//              maximum exceeds it by more than 8 (P stays below 2^8); then
+//              the thread rescales its half of O in TMEM, after the previous
+//              P V product has landed. O is read once, at the end.
 // Every wait is bounded: on timeout the CTA raises FLAG_TIMEOUT, stops issuing,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -173,6 +176,19 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]),
+      "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]),
+      "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
 template <int HD>
 struct Smem {
   static constexpr int QB = BQ * HD * 2;     // Q tile
@@ -185,7 +201,7 @@ struct Smem {
   static constexpr int OFF_X = OFF_P + PB;  // row-statistic exchange [3][2][128]
   static constexpr int OFF_BAR = OFF_X + 3 * 2 * BQ * 4;
   static constexpr int BYTES = 1024 + OFF_BAR + 256;
-  static constexpr int TMEM_COLS = 512;  // 2 score + 2 output buffers of 128 columns
+  static constexpr int TMEM_COLS = 512;  // 2 score buffers of 128 columns + the HD-column output
 };
 
 template <int HD>
@@ -204,9 +220,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* s_full = bar + 9;   // [2]
   uint64_t* s_empty = bar + 11; // [2]
   uint64_t* p_full = bar + 13;
-  uint64_t* p_empty = bar + 14;
-  uint64_t* o_full = bar + 15;  // [2]
-  uint64_t* o_empty = bar + 17; // [2]
+  uint64_t* pv_done = bar + 14; // P V product j complete (P free, O current)
   uint64_t* mma_done = bar + 19;
   uint64_t* xbar = bar + 20;    // [4] row-statistic exchange per TMEM lane quarter
   uint32_t* tmem_holder = (uint32_t*)(bar + 24);
@@ -231,11 +245,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_empty[i], 8);
-      mbar_init(&o_full[i], 1);
-      mbar_init(&o_empty[i], 8);
     }
     mbar_init(p_full, 8);
-    mbar_init(p_empty, 1);
+    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
     *abort_flag = 0;
@@ -332,17 +344,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
         if (!mbar_wait(&v_full[s], ph, abort_flag)) return false;
-        if (!mbar_wait(&o_empty[s], ph ^ 1, abort_flag)) return false;
         fence_after();
         const uint32_t sV = su32(sm + SM::OFF_V + s * SM::KB);
 #pragma unroll
         for (int k16 = 0; k16 < BKEY / 16; ++k16) {
           const uint32_t offp = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
-          umma(tmem + 256 + s * 128, sdesc(sP + offp, 16),
-               sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, k16 > 0);
+          umma(tmem + 256, sdesc(sP + offp, 16), sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv,
+               (j > 0 || k16 > 0) ? 1u : 0u);
         }
-        commit(&o_full[s]);
-        commit(p_empty);
+        commit(pv_done);
         commit(&v_empty[s]);
         return true;
       };
@@ -376,10 +386,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* prow = sm + SM::OFF_P + half * BQ * 128 + m * 128;
     float* xch = reinterpret_cast<float*>(sm + SM::OFF_X);  // [parity][half][row]
-    float o[HO];
-#pragma unroll
-    for (int i = 0; i < HO; ++i) o[i] = 0.f;
-    float mrun = -INFINITY, l = 0.f, corr_prev = 1.f;
+    float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and row sum
     bool ok = true;
     uint32_t xph = 0;
     // both threads of a row publish a value, then read the other's (bounded)
@@ -389,35 +396,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       xph ^= 1;
       return r;
     };
-    auto accumulate = [&](int jj, float corr) -> bool {
-      const int s = jj & 1;
+    // lane 0 waits, the warp follows
+    auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
       int w = 1;
-      if (lane == 0) w = mbar_wait(&o_full[s], (jj >> 1) & 1, abort_flag) ? 1 : 0;
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (!w) return false;
-      fence_after();
-      if constexpr (HO == 64) {
-        float v[64];
-        tmem_ld64(lane_base + 256 + s * 128 + half * HO, v);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) o[i] = o[i] * corr + v[i];
-      } else {
-        float v[32];
-        tmem_ld32(lane_base + 256 + s * 128 + half * HO, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = o[i] * corr + v[i];
-      }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[s]);
-      return true;
+      if (lane == 0) w = mbar_wait(b, parity, abort_flag) ? 1 : 0;
+      return __shfl_sync(0xffffffffu, w, 0) != 0;
     };
+    const float sl2 = p.scale_log2;
+    const uint32_t o_addr = lane_base + 256 + half * HO;
     for (int j = 0; j < nkb && ok; ++j) {
       const int s = j & 1;
-      int w = 1;
-      if (lane == 0) w = mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag) ? 1 : 0;
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (!w) { ok = false; break; }
+      if (!warp_wait(&s_full[s], (j >> 1) & 1)) { ok = false; break; }
       fence_after();
       // this thread's 64 keys: kbase .. kbase + 63; visible are those < ps
       const int kbase = j * BKEY + half * 64;
@@ -425,23 +414,46 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float sv[64];
       tmem_ld64(lane_base + s * 128 + half * 64, sv);
       float mx = -INFINITY;
+      if (__all_sync(0xffffffffu, nvis == 64)) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        sv[i] = i < nvis ? sv[i] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[i]);
+        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          if (i >= nvis) sv[i] = -INFINITY;
+          mx = fmaxf(mx, sv[i]);
+        }
       }
-      // row max over both halves
-      xch[(s * 2 + half) * BQ + m] = mx;
+      // row max over both halves, in scaled log2 units (the scale is positive)
+      xch[(s * 2 + half) * BQ + m] = mx * sl2;
       if (!exchange()) { ok = false; break; }
-      mx = fmaxf(fmaxf(mx, xch[(s * 2 + (half ^ 1)) * BQ + m]), mrun);
-      const float base = mx == -INFINITY ? 0.f : mx;
-      const float corr = exp2f(mrun - base);
-      mrun = mx;
-      // P may be overwritten once the previous block's P V product has read it
-      if (j > 0) {
-        if (lane == 0) w = mbar_wait(p_empty, (j - 1) & 1, abort_flag) ? 1 : 0;
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) { ok = false; break; }
+      mx = fmaxf(mx * sl2, xch[(s * 2 + (half ^ 1)) * BQ + m]);
+      float corr = 1.f;
+      bool resc = false;
+      if (mx > mrun + 8.f) {
+        // O and l hold blocks < j taken against the old base (nothing if the
+        // row had no visible key yet)
+        if (j > 0 && mrun != -INFINITY) {
+          resc = true;
+          corr = exp2f(mrun - mx);
+        }
+        mrun = mx;
+      }
+      const float base = mrun == -INFINITY ? 0.f : mrun;
+      // the previous P V product must be complete: it reads P, and O holds it
+      if (j > 0 && !warp_wait(pv_done, (j - 1) & 1)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, resc)) {
+        fence_after();
+        l *= corr;
+        uint32_t r[HO];
+        tmem_ld32_nw(o_addr, r);
+        if constexpr (HO == 64) tmem_ld32_nw(o_addr + 32, r + 32);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < HO; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
+        tmem_st32(o_addr, r);
+        if constexpr (HO == 64) tmem_st32(o_addr + 32, r + 32);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
       float rs = 0.f;
 #pragma unroll
@@ -449,15 +461,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float e0 = exp2f(sv[8 * u + 2 * e] - base);
-          const float e1 = exp2f(sv[8 * u + 2 * e + 1] - base);
+          const float e0 = exp2f(fmaf(sv[8 * u + 2 * e], sl2, -base));
+          const float e1 = exp2f(fmaf(sv[8 * u + 2 * e + 1], sl2, -base));
           rs += e0 + e1;
           __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
           pk[e] = *reinterpret_cast<uint32_t*>(&hh);
         }
         *reinterpret_cast<uint4*>(prow + ((u ^ (m & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l = l * corr + rs;
+      l += rs;
       fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
@@ -465,15 +477,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(p_full);
         mbar_arrive(&s_empty[s]);
       }
-      // output of the previous block, scaled to the max before this block
-      if (j > 0 && !accumulate(j - 1, corr_prev)) { ok = false; break; }
-      corr_prev = corr;
     }
-    if (ok && nkb > 0 && !accumulate(nkb - 1, corr_prev)) ok = false;
     // total row sum over both halves
     xch[(4 + half) * BQ + m] = l;
     if (ok && !exchange()) ok = false;
     const float lt = l + xch[(4 + (half ^ 1)) * BQ + m];
+    float o[HO];
+#pragma unroll
+    for (int i = 0; i < HO; ++i) o[i] = 0.f;
+    if (ok && nkb > 0) {
+      if (!warp_wait(pv_done, (nkb - 1) & 1)) {
+        ok = false;
+      } else {
+        fence_after();
+        if constexpr (HO == 64) tmem_ld64(o_addr, o);
+        else tmem_ld32(o_addr, o);
+      }
+    }
     if (!ok) {
       if (lane == 0) {
         *abort_flag = 1;
