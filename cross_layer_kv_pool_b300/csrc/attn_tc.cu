@@ -189,6 +189,41 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// 2^x on the special-function unit (inputs here are <= 8; results below the
+// smallest normal flush to zero, far below bf16 resolution of the row sum)
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// packed pairs of fp32 (one instruction for two lanes of arithmetic)
+__device__ __forceinline__ unsigned long long f2pack(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 template <int HD>
 struct Smem {
   static constexpr int QB = BQ * HD * 2;     // Q tile
@@ -414,15 +449,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float sv[64];
       tmem_ld64(lane_base + s * 128 + half * 64, sv);
       float mx = -INFINITY;
-      if (__all_sync(0xffffffffu, nvis == 64)) {
+      if (!__all_sync(0xffffffffu, nvis == 64)) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, sv[i]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
+        for (int i = 0; i < 64; ++i)
           if (i >= nvis) sv[i] = -INFINITY;
-          mx = fmaxf(mx, sv[i]);
-        }
+      }
+      {  // four independent chains of three-input maxima
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int i = 0; i < 64; i += 8)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) m4[c] = fmax3(m4[c], sv[i + 2 * c], sv[i + 2 * c + 1]);
+        mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
       }
       // row max over both halves, in scaled log2 units (the scale is positive)
       xch[(s * 2 + half) * BQ + m] = mx * sl2;
@@ -455,21 +493,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if constexpr (HO == 64) tmem_st32(o_addr + 32, r + 32);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      float rs = 0.f;
+      // P = 2^(s * scale - base), two lanes per instruction; row sum in two
+      // packed partial sums
+      const unsigned long long sc2 = f2pack(sl2, sl2), nb2 = f2pack(-base, -base);
+      unsigned long long rs2[2] = {0ull, 0ull};
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float e0 = exp2f(fmaf(sv[8 * u + 2 * e], sl2, -base));
-          const float e1 = exp2f(fmaf(sv[8 * u + 2 * e + 1], sl2, -base));
-          rs += e0 + e1;
+          float x0, x1;
+          f2unpack(ffma2(f2pack(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]), sc2, nb2), x0, x1);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          rs2[e & 1] = fadd2(rs2[e & 1], f2pack(e0, e1));
           __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
           pk[e] = *reinterpret_cast<uint32_t*>(&hh);
         }
         *reinterpret_cast<uint4*>(prow + ((u ^ (m & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l += rs;
+      {
+        float a0, a1, b0, b1;
+        f2unpack(rs2[0], a0, a1);
+        f2unpack(rs2[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+      }
       fence_before();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
