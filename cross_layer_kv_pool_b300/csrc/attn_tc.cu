@@ -1,25 +1,27 @@
 // Strictly causal channel attention on tcgen05 tensor cores (bf16, prefill).
 //
-// A CTA owns one KV head and a tile of up to 128 query rows (M): R consecutive
-// token rows of one sequence times the G = Hq/Hkv query heads that read this
-// KV head, packed in (row, head) order. The Q tile is one 3-D TMA box
-// {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly in that
-// order. Keys and values stream in blocks of 128 positions of the channel.
+// A CTA owns one KV head and two tiles of up to 128 query rows (M) each: R
+// consecutive token rows of one sequence per tile times the G = Hq/Hkv query
+// heads that read this KV head, packed in (row, head) order. A Q tile is one
+// 3-D TMA box {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly
+// in that order. Keys and values stream in blocks of 128 positions of the
+// channel and serve both tiles.
 //
-//   warp 0     TMA: Q once, then K and V blocks into two-stage rings;
-//   warp 1     tcgen05.mma: S_j = Q K_j^T (K-major operands) into one of two
-//              TMEM score buffers, and O += P_j V_j (P from shared memory, V
-//              as an MN-major operand) into one TMEM output accumulator;
-//   warps 2-9  two threads per query row (warps w and w + 4 share a TMEM lane
-//              quarter and take one half of the keys and of the output dims
-//              each): online softmax on S_j read from TMEM (keys s < pos of
-//              the row, masked only in blocks that are partly visible; the
-//              halves exchange row maxima through shared memory), P_j
-//              written to shared memory in the 128-byte-swizzled K-major
-//              layout. The exponent base is raised lazily, only when a row
-//              maximum exceeds it by more than 8 (P stays below 2^8); then
-//              the thread rescales its half of O in TMEM, after the previous
-//              P V product has landed. O is read once, at the end.
+//   warp 0       TMA: both Q tiles once, then K and V blocks into two-stage rings;
+//   warp 1       tcgen05.mma, per key block j and tile t:
+//                  S_t = Q_t K_j^T  (K-major smem operands, fp32 in TMEM),
+//                  O_t += P_t V_j   (P from TMEM, V an MN-major smem operand),
+//                issued as O_0, S_0(j+1), O_1, S_1(j+1) so that one tile's
+//                MMAs run while the other tile's softmax works;
+//   warps 4-11   one softmax warpgroup per tile, one thread per query row
+//                (TMEM lane): the row's 128 scores are read once; keys s >= pos
+//                are masked only in partly visible blocks; P = 2^(s*scale -
+//                base) goes back into TMEM as bf16 pairs over S's first
+//                columns. The base is raised lazily, only when a row maximum
+//                exceeds it by more than 8 (P stays below 2^8); then the
+//                thread rescales its row of O in TMEM. O is read once, at the
+//                end. The control warpgroup gives registers to the softmax
+//                warpgroups (setmaxnreg).
 // Every wait is bounded: on timeout the CTA raises FLAG_TIMEOUT, stops issuing,
 // drains its copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -30,7 +32,11 @@
 namespace wm {
 namespace atc {
 
-constexpr int BQ = 128, BKEY = 128, NTHREADS = 320;  // 2 + 8 warps
+constexpr int BQ = 128, BKEY = 128, NTHREADS = 384;  // 3 warpgroups: control, tile 0, tile 1
+// Register split: 384 threads x 168 at launch = 64512; the control warpgroup
+// keeps 88, each softmax warpgroup takes 208: 128 x 88 + 256 x 208 = 64512
+// (per SM sub-partition, one control and two softmax warps: 32 x 504 <= 16384).
+constexpr int REG_CTRL = 88, REG_SOFTMAX = 208;
 constexpr unsigned long long WAIT_NS = 4000000000ull;
 
 struct Params {
@@ -224,20 +230,38 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
   return d;
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 template <int HD>
 struct Smem {
-  static constexpr int QB = BQ * HD * 2;     // Q tile
+  static constexpr int QB = BQ * HD * 2;     // one Q tile
   static constexpr int KB = BKEY * HD * 2;   // one K (or V) block
-  static constexpr int PB = BQ * BKEY * 2;   // P tile
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB;           // 2 stages
+  static constexpr int OFF_Q = 0;                    // 2 tiles
+  static constexpr int OFF_K = OFF_Q + 2 * QB;       // 2 stages
   static constexpr int OFF_V = OFF_K + 2 * KB;       // 2 stages
-  static constexpr int OFF_P = OFF_V + 2 * KB;
-  static constexpr int OFF_X = OFF_P + PB;  // row-statistic exchange [3][2][128]
-  static constexpr int OFF_BAR = OFF_X + 3 * 2 * BQ * 4;
+  static constexpr int OFF_BAR = OFF_V + 2 * KB;
   static constexpr int BYTES = 1024 + OFF_BAR + 256;
-  static constexpr int TMEM_COLS = 512;  // 2 score buffers of 128 columns + the HD-column output
+  // per tile t: S_t (128 fp32 columns; P_t, bf16 pairs, overwrites its first
+  // 64 after S_t is read) at t * 256, O_t (HD columns) at t * 256 + 128
+  static constexpr int TMEM_COLS = 512;
 };
+
+// A from tensor memory (P), B from shared memory (V), D in tensor memory.
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                        uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+      : "memory");
+}
 
 template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -248,28 +272,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
   uint64_t* bar = (uint64_t*)(sm + SM::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;   // [2]
-  uint64_t* k_empty = bar + 3;  // [2]
-  uint64_t* v_full = bar + 5;   // [2]
-  uint64_t* v_empty = bar + 7;  // [2]
-  uint64_t* s_full = bar + 9;   // [2]
-  uint64_t* s_empty = bar + 11; // [2]
-  uint64_t* p_full = bar + 13;
-  uint64_t* pv_done = bar + 14; // P V product j complete (P free, O current)
-  uint64_t* mma_done = bar + 19;
-  uint64_t* xbar = bar + 20;    // [4] row-statistic exchange per TMEM lane quarter
-  uint32_t* tmem_holder = (uint32_t*)(bar + 24);
+  uint64_t* k_full = bar + 1;    // [2]
+  uint64_t* k_empty = bar + 3;   // [2]
+  uint64_t* v_full = bar + 5;    // [2]
+  uint64_t* v_empty = bar + 7;   // [2]
+  uint64_t* s_full = bar + 9;    // [2] per tile: S_t of the current block is in TMEM
+  uint64_t* p_full = bar + 11;   // [2] per tile: P_t written (4 warps arrive)
+  uint64_t* pv_done = bar + 13;  // [2] per tile: O_t += P_t V_j complete
+  uint64_t* mma_done = bar + 15;
+  uint32_t* tmem_holder = (uint32_t*)(bar + 16);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   int* s_meta = (int*)(tmem_holder + 2);  // [0] = number of key blocks, [1] = sequence
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
-  // rows of this tile: late positions first
-  const int tps = (p.nq + p.rpt - 1) / p.rpt;
+  // token rows of this CTA (two tiles of rpt rows each): late positions first
+  const int span = 2 * p.rpt;
+  const int tps = (p.nq + span - 1) / span;
   const int b = blockIdx.x / tps, t = tps - 1 - blockIdx.x % tps;
-  const int r0 = b * p.nq + t * p.rpt;
-  const int r1 = min(r0 + p.rpt, (b + 1) * p.nq);
-  const int mrows = (r1 - r0) * p.G;
+  const int r0 = b * p.nq + t * span;
+  const int rend = (b + 1) * p.nq;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -279,16 +301,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, 8);
-    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 64);
     *abort_flag = 0;
-    // key blocks: enough for the largest visible position of the tile
+    // key blocks: enough for the largest visible position of the CTA
     int maxp = 0;
-    for (int r = r0; r < r1; ++r) maxp = max(maxp, p.pos[r]);
+    for (int r = r0; r < min(r0 + span, rend); ++r) maxp = max(maxp, p.pos[r]);
     maxp = min(maxp, p.Tmax);
     s_meta[0] = (maxp + BKEY - 1) / BKEY;
     s_meta[1] = p.seq[r0];
@@ -310,18 +330,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const bool seq_ok = sq >= 0 && sq < p.B;
   const int nkb = seq_ok ? s_meta[0] : 0;  // an invalid sequence reads no keys
   if (!seq_ok && threadIdx.x == 0) atomicOr(p.flags, FLAG_BAD_SEQ);
-
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       bool ok = true;
-      uint8_t* sQ = sm + SM::OFF_Q;
-      // the box fills R*G rows of each 128-row operand chunk; rows past them
-      // feed only accumulator rows that are never read back
-      mbar_expect_tx(q_full, (uint32_t)(HD / 64) * p.G * p.rpt * 128);
-      for (int c = 0; c < HD / 64; ++c) tma3(&tmQ, q_full, sQ + c * BQ * 128, c * 64, hk * p.G, r0);
+      // each tile's box fills R*G rows of each 128-row operand chunk; rows
+      // past them feed only accumulator rows that are never read back
+      mbar_expect_tx(q_full, (uint32_t)(2 * (HD / 64) * p.G * p.rpt * 128));
+      for (int tt = 0; tt < 2; ++tt)
+        for (int c = 0; c < HD / 64; ++c)
+          tma3(&tmQ, q_full, sm + SM::OFF_Q + tt * SM::QB + c * BQ * 128, c * 64, hk * p.G,
+               r0 + tt * p.rpt);
       const int zc = ((sq * p.k) + p.channel) * p.Hkv + hk;
-      uint32_t used = 0, lastk = 0, lastv = 0;
+      uint32_t used = 0, lastk = 0;
       for (int j = 0; j < nkb && ok; ++j) {
         const int s = j & 1;
         const uint32_t ph = (j >> 1) & 1;
@@ -335,7 +358,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tma3(&tmV, &v_full[s], sm + SM::OFF_V + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
         used |= 1u << s;
         lastk = (lastk & ~(1u << s)) | (ph << s);
-        lastv = lastk;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -346,55 +368,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int s = 0; s < 2; ++s)
         if (used & (1u << s)) {
           mbar_wait(&k_full[s], (lastk >> s) & 1, &no_abort);
-          mbar_wait(&v_full[s], (lastv >> s) & 1, &no_abort);
+          mbar_wait(&v_full[s], (lastk >> s) & 1, &no_abort);
         }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
+      // tcgen05.mma operations of this thread execute in issue order, so
+      // S_t(j + 1) (issued after O_t += P_t(j) V_j) cannot overwrite P_t(j)
+      // before the product has read it.
       bool ok = mbar_wait(q_full, 0, abort_flag);
       fence_after();
-      const uint32_t sQ = su32(sm + SM::OFF_Q), sP = su32(sm + SM::OFF_P);
+      const uint32_t sQ = su32(sm + SM::OFF_Q);
       constexpr uint32_t id_qk = idesc(BKEY, false);
       constexpr uint32_t id_pv = idesc(HD, true);
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_full[s], ph, abort_flag)) return false;
-        if (!mbar_wait(&s_empty[s], ph ^ 1, abort_flag)) return false;
-        fence_after();
-        const uint32_t sK = su32(sm + SM::OFF_K + s * SM::KB);
+      auto qk = [&](int tt, int j) {
+        const uint32_t sK = su32(sm + SM::OFF_K + (j & 1) * SM::KB);
+        const uint32_t q = sQ + tt * SM::QB;
 #pragma unroll
         for (int k16 = 0; k16 < HD / 16; ++k16) {
           const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
           const uint32_t offk = (k16 >> 2) * BKEY * 128 + (k16 & 3) * 32;
-          umma(tmem + s * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
+          umma(tmem + tt * 256, sdesc(q + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
         }
-        commit(&s_full[s]);
-        commit(&k_empty[s]);
-        return true;
+        commit(&s_full[tt]);
       };
-      auto issue_pv = [&](int j) -> bool {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(p_full, j & 1, abort_flag)) return false;
-        if (!mbar_wait(&v_full[s], ph, abort_flag)) return false;
+      auto pv = [&](int tt, int j) -> bool {
+        if (!mbar_wait(&p_full[tt], j & 1, abort_flag)) return false;
         fence_after();
-        const uint32_t sV = su32(sm + SM::OFF_V + s * SM::KB);
+        const uint32_t sV = su32(sm + SM::OFF_V + (j & 1) * SM::KB);
 #pragma unroll
-        for (int k16 = 0; k16 < BKEY / 16; ++k16) {
-          const uint32_t offp = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
-          umma(tmem + 256, sdesc(sP + offp, 16), sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv,
-               (j > 0 || k16 > 0) ? 1u : 0u);
-        }
-        commit(pv_done);
-        commit(&v_empty[s]);
+        for (int k16 = 0; k16 < BKEY / 16; ++k16)
+          umma_ts(tmem + tt * 256 + 128, tmem + tt * 256 + k16 * 8,
+                  sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, (j > 0 || k16 > 0) ? 1u : 0u);
+        commit(&pv_done[tt]);
         return true;
       };
-      if (ok && nkb > 0) ok = issue_qk(0);
+      if (ok && nkb > 0) {
+        ok = mbar_wait(&k_full[0], 0, abort_flag);
+        if (ok) {
+          fence_after();
+          qk(0, 0);
+          qk(1, 0);
+          commit(&k_empty[0]);
+        }
+      }
       for (int j = 0; j < nkb && ok; ++j) {
-        if (j + 1 < nkb) ok = issue_qk(j + 1);
-        if (ok) ok = issue_pv(j);
+        const bool next = j + 1 < nkb;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!pv(0, j)) { ok = false; break; }
+        if (next) {
+          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+          fence_after();
+          qk(0, j + 1);
+        }
+        if (!pv(1, j)) { ok = false; break; }
+        commit(&v_empty[j & 1]);
+        if (next) {
+          qk(1, j + 1);
+          commit(&k_empty[(j + 1) & 1]);
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -404,68 +437,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       volatile int no_abort = 0;
       mbar_wait(mma_done, 0, &no_abort);
     }
+  }
   } else {
-    // ------------- softmax / output warps: two threads per query row -------------
-    constexpr int HO = HD / 2;  // output dims per thread
-    const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;  // which 64 keys of S and which half of O
-    const int m = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_SOFTMAX));
+    // ------------- softmax warps: tile tt, one thread per query row -------------
+    const int tt = (warp - 4) >> 2;
+    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+    const int m = quarter * 32 + lane;   // query row of the tile = TMEM lane
+    const int rt0 = r0 + tt * p.rpt;
+    const int mrows = max(0, min(p.rpt, rend - rt0)) * p.G;
     const bool valid = m < mrows;
-    const int r = r0 + (valid ? m / p.G : 0);
+    const int r = rt0 + (valid ? m / p.G : 0);
     const int h = hk * p.G + (valid ? m % p.G : 0);
     int ps = valid ? p.pos[r] : 0;
     if (valid && (ps < 0 || ps >= p.Tmax)) {
-      if (half == 0) atomicOr(p.flags, FLAG_BAD_POS);
+      atomicOr(p.flags, FLAG_BAD_POS);
       ps = 0;
     }
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* prow = sm + SM::OFF_P + half * BQ * 128 + m * 128;
-    float* xch = reinterpret_cast<float*>(sm + SM::OFF_X);  // [parity][half][row]
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + tt * 256;
     float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and row sum
     bool ok = true;
-    uint32_t xph = 0;
-    // both threads of a row publish a value, then read the other's (bounded)
-    auto exchange = [&]() -> bool {
-      mbar_arrive(&xbar[quarter]);
-      const bool r = mbar_wait(&xbar[quarter], xph, abort_flag);
-      xph ^= 1;
-      return r;
-    };
-    // lane 0 waits, the warp follows
-    auto warp_wait = [&](uint64_t* b, uint32_t parity) -> bool {
+    auto warp_wait = [&](uint64_t* bb, uint32_t parity) -> bool {
       int w = 1;
-      if (lane == 0) w = mbar_wait(b, parity, abort_flag) ? 1 : 0;
+      if (lane == 0) w = mbar_wait(bb, parity, abort_flag) ? 1 : 0;
       return __shfl_sync(0xffffffffu, w, 0) != 0;
     };
     const float sl2 = p.scale_log2;
-    const uint32_t o_addr = lane_base + 256 + half * HO;
     for (int j = 0; j < nkb && ok; ++j) {
-      const int s = j & 1;
-      if (!warp_wait(&s_full[s], (j >> 1) & 1)) { ok = false; break; }
+      if (!warp_wait(&s_full[tt], j & 1)) { ok = false; break; }
       fence_after();
-      // this thread's 64 keys: kbase .. kbase + 63; visible are those < ps
-      const int kbase = j * BKEY + half * 64;
-      const int nvis = min(max(ps - kbase, 0), 64);
-      float sv[64];
-      tmem_ld64(lane_base + s * 128 + half * 64, sv);
-      float mx = -INFINITY;
-      if (!__all_sync(0xffffffffu, nvis == 64)) {
+      // The row's 128 scores, one TMEM load wait.
+      const int nvis = min(max(ps - j * BKEY, 0), BKEY);
+      float sv[BKEY];
+      {
+        uint32_t* ru = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int c = 0; c < BKEY / 32; ++c) tmem_ld32_nw(lane_base + c * 32, ru + 32 * c);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      }
+      if (!__all_sync(0xffffffffu, nvis == BKEY)) {
+#pragma unroll
+        for (int i = 0; i < BKEY; ++i)
           if (i >= nvis) sv[i] = -INFINITY;
       }
-      {  // four independent chains of three-input maxima
+      float mx;
+      {
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 64; i += 8)
+        for (int i = 0; i < BKEY; i += 8)
 #pragma unroll
-          for (int c = 0; c < 4; ++c) m4[c] = fmax3(m4[c], sv[i + 2 * c], sv[i + 2 * c + 1]);
-        mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+          for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], sv[i + 2 * q], sv[i + 2 * q + 1]);
+        mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;  // scaled log2 units
       }
-      // row max over both halves, in scaled log2 units (the scale is positive)
-      xch[(s * 2 + half) * BQ + m] = mx * sl2;
-      if (!exchange()) { ok = false; break; }
-      mx = fmaxf(mx * sl2, xch[(s * 2 + (half ^ 1)) * BQ + m]);
       float corr = 1.f;
       bool resc = false;
       if (mx > mrun + 8.f) {
@@ -473,44 +496,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // row had no visible key yet)
         if (j > 0 && mrun != -INFINITY) {
           resc = true;
-          corr = exp2f(mrun - mx);
+          corr = ex2(mrun - mx);
         }
         mrun = mx;
       }
       const float base = mrun == -INFINITY ? 0.f : mrun;
-      // the previous P V product must be complete: it reads P, and O holds it
-      if (j > 0 && !warp_wait(pv_done, (j - 1) & 1)) { ok = false; break; }
       if (__any_sync(0xffffffffu, resc)) {
+        // O_t holds the products of blocks < j once the previous one landed
+        if (!warp_wait(&pv_done[tt], (j - 1) & 1)) { ok = false; break; }
         fence_after();
         l *= corr;
-        uint32_t r[HO];
-        tmem_ld32_nw(o_addr, r);
-        if constexpr (HO == 64) tmem_ld32_nw(o_addr + 32, r + 32);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int i = 0; i < HO; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * corr);
-        tmem_st32(o_addr, r);
-        if constexpr (HO == 64) tmem_st32(o_addr + 32, r + 32);
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t ro[32];
+          tmem_ld32_nw(lane_base + 128 + c * 32, ro);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * corr);
+          tmem_st32(lane_base + 128 + c * 32, ro);
+        }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      // P = 2^(s * scale - base), two lanes per instruction; row sum in two
-      // packed partial sums
+      // P = 2^(s * scale - base) as bf16 pairs over S_t's first 64 columns (16
+      // at a time); row sum in two packed partial sums.
       const unsigned long long sc2 = f2pack(sl2, sl2), nb2 = f2pack(-base, -base);
       unsigned long long rs2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        uint32_t pk[4];
+      for (int c = 0; c < BKEY / 32; ++c) {
+        uint32_t pw[16];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 16; ++e) {
+          const int i = 32 * c + 2 * e;
           float x0, x1;
-          f2unpack(ffma2(f2pack(sv[8 * u + 2 * e], sv[8 * u + 2 * e + 1]), sc2, nb2), x0, x1);
+          f2unpack(ffma2(f2pack(sv[i], sv[i + 1]), sc2, nb2), x0, x1);
           const float e0 = ex2(x0), e1 = ex2(x1);
           rs2[e & 1] = fadd2(rs2[e & 1], f2pack(e0, e1));
           __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
-          pk[e] = *reinterpret_cast<uint32_t*>(&hh);
+          pw[e] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        *reinterpret_cast<uint4*>(prow + ((u ^ (m & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        tmem_st16(lane_base + 16 * c, pw);
       }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       {
         float a0, a1, b0, b1;
         f2unpack(rs2[0], a0, a1);
@@ -518,44 +544,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         l += (a0 + a1) + (b0 + b1);
       }
       fence_before();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(p_full);
-        mbar_arrive(&s_empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&p_full[tt]);
     }
-    // total row sum over both halves
-    xch[(4 + half) * BQ + m] = l;
-    if (ok && !exchange()) ok = false;
-    const float lt = l + xch[(4 + (half ^ 1)) * BQ + m];
-    float o[HO];
-#pragma unroll
-    for (int i = 0; i < HO; ++i) o[i] = 0.f;
-    if (ok && nkb > 0) {
-      if (!warp_wait(pv_done, (nkb - 1) & 1)) {
-        ok = false;
-      } else {
-        fence_after();
-        if constexpr (HO == 64) tmem_ld64(o_addr, o);
-        else tmem_ld32(o_addr, o);
-      }
+    const bool have_o = ok && nkb > 0;
+    if (have_o) {
+      if (!warp_wait(&pv_done[tt], (nkb - 1) & 1)) ok = false;
+      else fence_after();
     }
     if (!ok) {
       if (lane == 0) {
         *abort_flag = 1;
         atomicOr(p.flags, FLAG_TIMEOUT);
       }
-    } else if (valid) {
-      const float inv = (ps > 0 && lt > 0.f) ? 1.f / lt : 0.f;
-      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD + half * HO;
+    } else {
+      // O / l, 32 dims at a time (the TMEM loads are warp-collective)
+      const float inv = (valid && ps > 0 && l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD;
 #pragma unroll
-      for (int i = 0; i < HO; i += 8) {
-        uint4 u;
-        __nv_bfloat162* hh = reinterpret_cast<__nv_bfloat162*>(&u);
+      for (int c = 0; c < HD / 32; ++c) {
+        float o[32];
+        if (have_o) tmem_ld32(lane_base + 128 + c * 32, o);
+        else
 #pragma unroll
-        for (int e = 0; e < 4; ++e) hh[e] = __floats2bfloat162_rn(o[i + 2 * e] * inv, o[i + 2 * e + 1] * inv);
-        *reinterpret_cast<uint4*>(dst + i) = u;
+          for (int i = 0; i < 32; ++i) o[i] = 0.f;
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 u;
+            __nv_bfloat162* hh = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              hh[e] = __floats2bfloat162_rn(o[i + 2 * e] * inv, o[i + 2 * e + 1] * inv);
+            *reinterpret_cast<uint4*>(dst + 32 * c + i) = u;
+          }
+        }
       }
     }
   }
@@ -618,7 +641,7 @@ cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
   p.k = a.k; p.channel = a.channel; p.B = a.B;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const int B = a.N / nq;
-  const int tiles = B * ((nq + rpt - 1) / rpt);
+  const int tiles = B * ((nq + 2 * rpt - 1) / (2 * rpt));
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES);
   if (e != cudaSuccess) return e;
