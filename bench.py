@@ -13,6 +13,12 @@ norm gains.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
+``--kernel mixer|attention`` instead times one kernel of the path alone, through
+the C ABI (``wm_pool_mix`` on ``--rows`` token rows of the 1.3B pool, or
+``wm_channel_attn`` on one prefill group of ``--batch`` sequences), and prints
+one JSON line with its CUDA-event time and roofline fraction; the profiles
+under profiles/ capture these invocations.
+
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -52,6 +58,11 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k", type=int, default=None, help="override the channel count k")
+    ap.add_argument("--kernel", choices=["mixer", "attention"], default=None,
+                    help="time one kernel of the path alone (1.3B shapes)")
+    ap.add_argument("--rows", type=int, default=8192, help="--kernel mixer: token rows")
+    ap.add_argument("--batch", type=int, default=64, help="--kernel attention: sequences")
+    ap.add_argument("--group", type=int, default=15, help="--kernel attention: group index q")
     return ap.parse_args()
 
 
@@ -424,8 +435,74 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_kernel(args):
+    """One kernel alone at 1.3B shapes, timed by the library's CUDA events on
+    its stream (warm-up launches first; inputs above L2 size for the mixer)."""
+    from cross_layer_kv_pool_b300 import wm
+
+    s = synth.HALF_1P3B.replace(V=1024)  # the pool and attention do not read the vocabulary
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m = wm.Model(s, synth.make_weights(s, seed=0, device=dev, gain_jitter=0.1))
+    pk, pk_src = peaks()
+    if args.kernel == "mixer":
+        N, B, Tmax = args.rows, 4, max(2048, -(-args.rows // 4))
+        flat = torch.randperm(B * Tmax, generator=torch.Generator().manual_seed(0))[:N]
+        seq = (flat // Tmax).to(torch.int32).to(dev)
+        pos = (flat % Tmax).to(torch.int32).to(dev)
+        states = synth.make_normal((N, s.L, s.D), 31, dev, 1.0, s.torch_dtype)
+        ck, cv = m.new_cache(B, Tmax)
+        wsp = m.workspace(N, Tmax)
+        kind = wm.WM_TRACE_MIX
+
+        def call():
+            wm.wm_pool_mix(m, states, seq, pos, ck, cv, wsp)
+        work = N * (s.L * s.D * 2 + 2 * s.k * s.L * 4 + s.L * 4 + 2 * s.k * s.D * 2)
+        unit, peak, bound = "GB/s", pk["hbm_gbs"], "hbm"
+        desc = f"wm_pool_mix, {N} rows of the 1.3B pool (L=28, D=1792, k=14)"
+    else:
+        B, T, g, Tmax = args.batch, 2048, 16, 2048
+        nq = T // g
+        pos = torch.arange(args.group, T, g, dtype=torch.int32).repeat(B).to(dev)
+        seq = torch.arange(B, dtype=torch.int32).repeat_interleave(nq).to(dev)
+        N = B * nq
+        q = synth.make_normal((N, s.Hq, s.d), 3, dev, 1.0, torch.bfloat16)
+        ck, cv = m.new_cache(B, Tmax)
+        ck.copy_(synth.make_normal(tuple(ck.shape), 4, dev, 1.0, torch.bfloat16))
+        cv.copy_(synth.make_normal(tuple(cv.shape), 5, dev, 1.0, torch.bfloat16))
+        out = torch.empty_like(q)
+        wsp = m.workspace(N, Tmax)
+        kind = wm.WM_TRACE_ATTN
+
+        def call():
+            wm.wm_channel_attn(m.cfg, q, seq, pos, 3, ck, cv, out, wsp, rows_per_seq=nq)
+        work = 4.0 * s.Hq * s.d * float(pos.double().sum())
+        unit, peak, bound = "TFLOP/s", pk["bf16_tflops"], "tensor"
+        desc = f"wm_channel_attn, group {args.group} of {B} sequences of 2048 (1.3B heads)"
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    tr = wm.Tracer(kind, max(args.steps, 1))
+    tr.attach(m)
+    for _ in range(args.steps):
+        call()
+    torch.cuda.synchronize()
+    wm.Tracer.detach(m)
+    ms = statistics.mean(r[0] for r in tr.results())
+    if wm.wm_check_flags(wsp) != 0:
+        raise RuntimeError("device-side checks failed")
+    achieved = work / (ms * 1e-3) / (1e9 if unit == "GB/s" else 1e12)
+    print(json.dumps({"kernel": args.kernel, "call": desc, "ms": ms, "achieved": achieved,
+                      "unit": unit, "bound": bound, "peak": peak, "frac": achieved / peak,
+                      "peak_source": f"{pk_src} {'hbm_gbs' if unit == 'GB/s' else 'bf16_tflops (burst)'}",
+                      "work_per_launch": work, "launches": args.steps, "warmup": args.warmup}),
+          flush=True)
+
+
 def main():
     args = parse()
+    if args.kernel:
+        run_kernel(args)
+        return
     ws, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, ws, rank)
