@@ -622,7 +622,10 @@ template <int HD>
 cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
   using SM = Smem<HD>;
   const int G = a.Hq / a.Hkv;
-  const int rpt = BQ / G;
+  // rows per tile: a full 128-row tile, or half of a short sequence's rows so
+  // that both tiles of the CTA have work
+  int rpt = BQ / G;
+  if (2 * rpt > nq) rpt = (nq + 1) / 2;
   CUtensorMap mq, mk, mv;
   // q as [N][Hq][HD]: box {64 dims, G heads, rpt rows}
   if (!map3(&mq, a.q, HD, a.Hq, a.N, (cuuint64_t)HD * 2, (cuuint64_t)a.Hq * HD * 2, 64, G, rpt))

@@ -701,7 +701,9 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   p.partial = nullptr;
   const int sms = num_sms();
   const long long need = (long long)g.batch * g.M * g.N * (DUAL ? 2 : 1);
-  if (g.partial && need <= g.partial_elems && out_tiles * 2 <= sms && p.num_kb >= 4 &&
+  // split-K only for one row tile (decode-sized M): for more rows the fp32
+  // atomics of the partial tiles cost more than the idle SMs it recovers
+  if (g.partial && g.M <= BM && need <= g.partial_elems && out_tiles * 2 <= sms && p.num_kb >= 4 &&
       (MODE != EPI_QNORM_ROPE && MODE != EPI_KV ? true : (g.N % HD == 0))) {
     int ks = (int)((sms + out_tiles - 1) / out_tiles);
     ks = min(ks, p.num_kb / 2);
