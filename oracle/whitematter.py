@@ -65,6 +65,12 @@ Readings where the pages are silent (each listed again in the design notes):
       output; the default "normed" stores c. In exact arithmetic the two are
       the same function (pinned); they differ only in which tensor bf16
       storage rounds, and ``mixed`` is then bf16(s * u).
+  R18 The feedback-free variant ([PL 5 ANALYSIS, "Deep-to-shallow feedback":
+      a 16-channel cache for 16 layers, costs like vanilla, no iteration) has
+      k = L and builds channel l from the token's states h^0..h^l only: the
+      router reads the sources of R inside 0..l (its other inputs unused)
+      through rows l*L + 0..l of W_R (or static_coeff[b][l][0..l]); the
+      channel is cached before layer l runs; layer l still attends to s < i.
 
 Parity pins for every function below live in tests/test_oracle_pins.py and
 tests/test_oracle_mutants.py (closed forms, special cases, brute force and an
@@ -81,7 +87,7 @@ __all__ = [
     "round_bf16", "rmsnorm", "rope", "silu", "router_sources", "channel_of_layer",
     "group_positions", "channel_attention", "consumer_layer", "pool",
     "run_rows", "new_cache", "cyclic_pass", "decode_step",
-    "autoregressive", "kv_residual",
+    "autoregressive", "kv_residual", "feedback_free_channel", "feedback_free_pass",
 ]
 
 
@@ -391,3 +397,82 @@ def kv_residual(prev_k, prev_v, cur_k, cur_v):
     num = np.sum((_f64(cur_k) - _f64(prev_k)) ** 2) + np.sum((_f64(cur_v) - _f64(prev_v)) ** 2)
     den = np.sum(_f64(cur_k) ** 2) + np.sum(_f64(cur_v) ** 2)
     return math.sqrt(num / den) if den > 0 else 0.0
+
+
+# ----------------------------------------------------------------------------
+# Feedback-free variant (R18)
+# ----------------------------------------------------------------------------
+
+def feedback_free_channel(cfg, W, states, pos, l, static_coeff=None):
+    """Channel l of the feedback-free variant ([PL 5 ANALYSIS, "Deep-to-shallow
+    feedback"]; reading R18): the pool of :func:`pool` with k = L, restricted
+    to the sources 0..l of each row. states: [N, l + 1, D] (h^0..h^l); pos: [N].
+    The router reads the sources of R inside 0..l, a prefix of its input, and
+    gives a^b_{l, 0..l} through rows l*L + 0..l of W_R^b; static_coeff gives
+    static_coeff[b][l][0..l] instead. Storage rounding as in :func:`pool` (R14,
+    R17). Returns K, V [N, Hkv, d] and coeff [N, 2, l + 1].
+    """
+    states = _f64(states)
+    N, D, L = states.shape[0], cfg.D, cfg.L
+    Hkv, d = cfg.Hkv, cfg.d
+    Rl = [s for s in router_sources(cfg) if s <= l]
+    gained = getattr(cfg, "mixed_storage", "normed") == "gained"
+    coeff = np.zeros((N, 2, l + 1), dtype=np.float64)
+    out = []
+    for beta in range(2):
+        n = rmsnorm(states, _f64(W["src_norm"][beta])[: l + 1], cfg.eps)   # [N, l+1, D]
+        if static_coeff is not None:
+            a = np.broadcast_to(_f64(static_coeff)[beta, l, : l + 1], (N, l + 1))
+        elif Rl:
+            x = _st(cfg, n[:, Rl, :].reshape(N, len(Rl) * D))
+            Wr = _f64(W["Wr"][beta])[l * L: l * L + l + 1, : len(Rl) * D]
+            a = x @ Wr.T
+        else:
+            a = np.zeros((N, l + 1))
+        coeff[:, beta] = a
+        m = np.einsum("nl,nld->nd", a, n)
+        tau = _f64(W["chan_norm"][beta][l])
+        if gained:
+            stored = _st(cfg, m * tau)
+            scale = 1.0 / np.sqrt(np.mean(m * m, axis=-1) + cfg.eps)
+        else:
+            stored = _st(cfg, rmsnorm(m, tau, cfg.eps))
+            scale = np.ones(N)
+        Wp = _f64(W["Wk"][l] if beta == 0 else W["Wv"][l])
+        out.append(((stored @ Wp.T) * scale[:, None]).reshape(N, Hkv, d))
+    kt = rmsnorm(out[0], W["k_norm"][l], cfg.eps)
+    K = _st(cfg, rope(kt, _f64(pos)[:, None], cfg.rope_base))
+    V = _st(cfg, out[1])
+    return K, V, coeff
+
+
+def feedback_free_pass(cfg, W, tokens, cache_k, cache_v, pos0=0, logits=None,
+                       static_coeff=None):
+    """Tokens [B, T] at positions pos0..pos0+T-1 through the feedback-free
+    variant in one layer-by-layer pass ([PL 5 ANALYSIS, "Deep-to-shallow
+    feedback"]: no iteration). For l = 0..L-1: every token's channel l is
+    pooled from its states 0..l and written to cache channel l at its
+    position, then layer l runs for every token and attends to channel l at
+    s < pos (keys of earlier calls included). k must equal L. ``logits``:
+    None, "last" (-> [B, V] at the last position) or "all" (-> [B, T, V]).
+    The cache arrays are updated in place.
+    """
+    assert cfg.k == cfg.L, "the feedback-free variant has one channel per layer"
+    tokens = np.asarray(tokens, dtype=np.int64)
+    B, T = tokens.shape
+    seq = np.repeat(np.arange(B), T)
+    pos = pos0 + np.tile(np.arange(T), B)
+    h = _f64(W["embed"])[tokens.reshape(-1)]
+    states = np.zeros((B * T, cfg.L, cfg.D), dtype=np.float64)
+    for l in range(cfg.L):
+        states[:, l] = h
+        K, V, _ = feedback_free_channel(cfg, W, states[:, : l + 1], pos, l, static_coeff)
+        for r in range(B * T):
+            cache_k[seq[r], l, :, pos[r], :] = K[r]
+            cache_v[seq[r], l, :, pos[r], :] = V[r]
+        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)
+    if logits is None:
+        return None
+    lg = _st(cfg, rmsnorm(h, W["final_norm"], cfg.eps)) @ _f64(W["lm_head"]).T
+    lg = lg.reshape(B, T, cfg.V)
+    return lg[:, -1] if logits == "last" else lg

@@ -134,6 +134,43 @@ def _vanilla_strict_causal(c, W, tokens):
     return _rms(h, W["final_norm"], c.eps) @ W["lm_head"].T
 
 
+def _source_select_strict_causal(c, W, tokens, src):
+    """Like _vanilla_strict_causal, but layer l's K/V are made from the stored
+    input h^{src[l]} of layer src[l] <= l (with the source norm of layer src[l]
+    and channel l's channel norm, projections and K-norm): the feedback-free
+    model under the one-hot constant mixture a_{l, src[l]} = 1. tokens [T]."""
+    T = len(tokens)
+    Hq, Hkv, d = c.Hq, c.Hkv, c.d
+    pos = np.arange(T)
+    vis = np.arange(T)[None, :] < np.arange(T)[:, None]
+    h = W["embed"][tokens]
+    saved = []
+    for l in range(c.L):
+        saved.append(h)
+        hs = saved[src[l]]
+        ck = _rms(_rms(hs, W["src_norm"][0][src[l]], c.eps), W["chan_norm"][0][l], c.eps)
+        cv = _rms(_rms(hs, W["src_norm"][1][src[l]], c.eps), W["chan_norm"][1][l], c.eps)
+        K = _rms((ck @ W["Wk"][l].T).reshape(T, Hkv, d), W["k_norm"][l], c.eps)
+        K = _rope_complex(K, pos[:, None], c.rope_base)
+        V = (cv @ W["Wv"][l].T).reshape(T, Hkv, d)
+        a = _rms(h, W["in_norm"][l], c.eps)
+        Q = _rms((a @ W["Wq"][l].T).reshape(T, Hq, d), W["q_norm"][l], c.eps)
+        Q = _rope_complex(Q, pos[:, None], c.rope_base)
+        O = np.zeros((T, Hq, d))
+        rep = Hq // Hkv
+        for hq in range(Hq):
+            hk = hq // rep
+            S = np.where(vis, (Q[:, hq, :] @ K[:, hk, :].T) / math.sqrt(d), -np.inf)
+            has = vis.any(axis=1)
+            P = np.zeros((T, T))
+            P[has] = scipy.special.softmax(S[has], axis=1)
+            O[:, hq, :] = P @ V[:, hk, :]
+        h = h + O.reshape(T, Hq * d) @ W["Wo"][l].T
+        f = _rms(h, W["post_norm"][l], c.eps)
+        h = h + (_swish(f @ W["Wgate"][l].T) * (f @ W["Wup"][l].T)) @ W["Wdown"][l].T
+    return _rms(h, W["final_norm"], c.eps) @ W["lm_head"].T
+
+
 def _ar(O, c, W, tokens, Tmax=None, static=None):
     B, T = tokens.shape
     ck, cv = O.new_cache(c, B, Tmax or T)
@@ -547,6 +584,83 @@ def check_gained_storage_equivalence(O):
     assert not np.array_equal(gb["mixed"], rb["mixed"])
 
 
+# ---------------------------------------------------------------------------
+# Feedback-free variant (R18)
+# ---------------------------------------------------------------------------
+
+def check_feedback_free_one_hot_static(O):
+    """Constant one-hot mixtures a_{l, src[l]} = 1 (src[l] <= l): the
+    feedback-free pass equals an independently written Transformer whose
+    layer l reads K/V built from the stored input of layer src[l]; src[l] = l
+    is the vanilla strict-causal Transformer."""
+    c = _cfg(L=3, D=16, k=3, Hq=4, Hkv=2, d=8)
+    W = _weights(c, seed=41)
+    tokens = _tokens(c, 2, 6, 42)
+    for src in ([0, 1, 2], [0, 0, 1], [0, 0, 0]):
+        static = np.zeros((2, c.k, c.L))
+        for beta in range(2):
+            for l in range(c.L):
+                static[beta, l, src[l]] = 1.0
+        ck, cv = O.new_cache(c, 2, 6)
+        lg = O.feedback_free_pass(c, W, tokens, ck, cv, logits="all", static_coeff=static)
+        for b in range(2):
+            _close(lg[b], _source_select_strict_causal(c, W, tokens[b], src), 1e-10, f"src {src}")
+    ck, cv = O.new_cache(c, 2, 6)
+    eye = np.zeros((2, c.k, c.L))
+    eye[0] = eye[1] = np.eye(c.L)
+    lg = O.feedback_free_pass(c, W, tokens, ck, cv, logits="all", static_coeff=eye)
+    for b in range(2):
+        _close(lg[b], _vanilla_strict_causal(c, W, tokens[b]), 1e-10, "vanilla")
+
+
+def check_feedback_free_one_pass_is_autoregressive(O):
+    """The variant needs no iteration: one pass over T tokens equals T
+    single-token calls at positions 0..T-1 (caches and logits), with the
+    router (p = 2, p_offset = 1, so channel 0 has no router source)."""
+    c = _cfg(L=4, D=16, k=4, p=2, p_offset=1, Hq=4, Hkv=2, d=8)
+    W = _weights(c, seed=43)
+    tokens = _tokens(c, 2, 7, 44)
+    ck1, cv1 = O.new_cache(c, 2, 7)
+    lg1 = O.feedback_free_pass(c, W, tokens, ck1, cv1, logits="all")
+    ck2, cv2 = O.new_cache(c, 2, 7)
+    lg2 = np.stack([O.feedback_free_pass(c, W, tokens[:, t:t + 1], ck2, cv2, pos0=t, logits="last")
+                    for t in range(7)], axis=1)
+    _close(lg2, lg1, 1e-10, "logits")
+    _close(ck2, ck1, 1e-10, "keys")
+    _close(cv2, cv1, 1e-10, "values")
+    assert np.max(np.abs(ck1[:, 0])) == 0.0  # channel 0: no router source, zero coefficients
+    assert np.max(np.abs(ck1[:, 1])) > 0.0
+
+
+def check_feedback_free_router_reads_prefix(O):
+    """Channel l reads only the router inputs of sources 0..l and only rows
+    l*L + 0..l of W_R: changing any other router weight leaves it unchanged,
+    changing a used one changes the coefficients (and, with two or more
+    sources, the channel)."""
+    c = _cfg(L=4, D=16, k=4, p=1, Hq=4, Hkv=2, d=8)
+    W = _weights(c, seed=45)
+    rng = np.random.default_rng(46)
+    states = rng.standard_normal((5, c.L, c.D))
+    pos = np.arange(5)
+    for l in range(c.L):
+        K, V, a = O.feedback_free_channel(c, W, states[:, : l + 1], pos, l)
+        W2 = dict(W)
+        W2["Wr"] = W["Wr"].copy()
+        for beta in range(2):
+            used = np.zeros(W["Wr"].shape[1:], dtype=bool)
+            used[l * c.L: l * c.L + l + 1, : (l + 1) * c.D] = True
+            W2["Wr"][beta][~used] = rng.standard_normal(int((~used).sum()))
+        K2, V2, a2 = O.feedback_free_channel(c, W2, states[:, : l + 1], pos, l)
+        assert np.array_equal(K2, K) and np.array_equal(V2, V) and np.array_equal(a2, a), l
+        W3 = dict(W)
+        W3["Wr"] = W["Wr"].copy()
+        W3["Wr"][1][l * c.L + l, l * c.D] += 1.0
+        _, V3, a3 = O.feedback_free_channel(c, W3, states[:, : l + 1], pos, l)
+        assert not np.allclose(a3[:, 1, l], a[:, 1, l]), l
+        # one source (l = 0): the channel norm removes the coefficient's scale
+        assert np.allclose(V3, V) == (l == 0), l
+
+
 ALL_CHECKS = [
     check_round_bf16,
     check_bf16_storage_mode,
@@ -568,4 +682,7 @@ ALL_CHECKS = [
     check_bruteforce_T4,
     check_partial_pass_positions,
     check_last_logits_and_decode,
+    check_feedback_free_one_hot_static,
+    check_feedback_free_one_pass_is_autoregressive,
+    check_feedback_free_router_reads_prefix,
 ]

@@ -45,6 +45,25 @@ MUTANTS = [
     ("pool_gained_no_tau", "pool", 'stored[:, beta] = _st(cfg, m * _f64(W["chan_norm"][beta]))',
      'stored[:, beta] = _st(cfg, m)'),
     ("pool_gained_scale_branch", "pool", "* scale[:, 1, j, None]", "* scale[:, 0, j, None]"),
+    ("ff_router_rows_shifted", "feedback_free_channel", "[l * L: l * L + l + 1, : len(Rl) * D]",
+     "[l * L + 1: l * L + l + 2, : len(Rl) * D]"),
+    ("ff_router_all_rows_of_channel", "feedback_free_channel", "Rl = [s for s in router_sources(cfg) if s <= l]",
+     "Rl = [s for s in router_sources(cfg) if s <= max(l, 1)]"),
+    ("ff_static_transposed", "feedback_free_channel", "static_coeff)[beta, l, : l + 1]",
+     "static_coeff)[beta, : l + 1, l]"),
+    ("ff_cache_after_layer", "feedback_free_pass",
+     """        K, V, _ = feedback_free_channel(cfg, W, states[:, : l + 1], pos, l, static_coeff)
+        for r in range(B * T):
+            cache_k[seq[r], l, :, pos[r], :] = K[r]
+            cache_v[seq[r], l, :, pos[r], :] = V[r]
+        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)""",
+     """        K, V, _ = feedback_free_channel(cfg, W, states[:, : l + 1], pos, l, static_coeff)
+        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)
+        for r in range(B * T):
+            cache_k[seq[r], l, :, pos[r], :] = K[r]
+            cache_v[seq[r], l, :, pos[r], :] = V[r]"""),
+    ("ff_no_prefix_states", "feedback_free_pass", "states[:, : l + 1], pos, l, static_coeff)",
+     "states[:, : max(l, 1)], pos, max(l - 1, 0), static_coeff)"),
     ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
      'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
     ("states_are_outputs", "run_rows", "        states[:, l] = h\n        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)",
