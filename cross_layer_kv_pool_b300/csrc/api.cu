@@ -185,8 +185,12 @@ Epi base_epi(const Ctx& x) {
 // Layer stack of N rows whose h^0 is already in stash[:, 0]. Layer l reads
 // stash[:, l], writes stash[:, l+1] (or h^L), and emits inv_rms / router
 // inputs of its input state. The last layer's body runs only if requested.
+void run_pool_channel(const Ctx& x, int N, int l, void* cache_k, void* cache_v, int B, int Tmax);
+
+// The consumer stack over N rows. With ``feedback_free``, channel l of every
+// row is pooled from its states 0..l right before layer l (k = L).
 void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, void* cache_k,
-               void* cache_v, int B, int Tmax, bool emit_rin) {
+               void* cache_v, int B, int Tmax, bool emit_rin, bool feedback_free = false) {
   const wm_config& c = *x.c;
   const wm_weights& w = *x.w;
   const long long LD = (long long)c.L * c.D;
@@ -199,6 +203,7 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
     launch_norm_emit(c.dtype, stash, LD, c.D, N, l, 1, c.D, c.L, w.in_norm,
                      body ? x.buf<void>(B_XN) : nullptr, x.buf<float>(B_INV), w.src_norm,
                      emit_rin ? x.buf<void>(B_RIN) : nullptr, x.nR, c.p, c.p_offset, c.eps, x.st);
+    if (feedback_free) run_pool_channel(x, N, l, cache_k, cache_v, B, Tmax);
     if (!body) break;
     {  // Q projection + per-head q-norm + RoPE
       GemmDesc g;
@@ -272,8 +277,6 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
   }
 }
 
-// Router (or static weights) -> coefficients; mix + channel norm; channel
-// projections with K-norm + RoPE; scatter into the cache at (seq, pos).
 // Router, mixer and K/V projections for N rows. Returns the mixer's deferred
 // norm part count (0: ``mixed`` holds the normed channels; P > 0: it holds
 // u = tau (.) m and the projections applied the norm factor).
@@ -302,6 +305,7 @@ int run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* c
   m.src_norm = w.src_norm; m.chan_norm = w.chan_norm; m.mixed = mixed;
   m.chan_ss = x.buf<float>(B_CHSS);
   m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
+  m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
   const int tr = trace_begin(x, WM_TRACE_MIX);
   ++x.launches;
   const int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
@@ -323,6 +327,7 @@ int run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* c
     if (parts) {
       g.epi.chan_ss = x.buf<float>(B_CHSS);
       g.epi.chan_parts = parts;
+      g.epi.chan_ss_k = c.k;
       g.epi.chan_D = (float)c.D;
     }
     ++x.launches;
@@ -337,8 +342,81 @@ void finish_mixed(const Ctx& x, int N, void* mixed, int parts) {
   MixArgs m{};
   m.mixed = mixed; m.chan_ss = x.buf<float>(B_CHSS);
   m.N = N; m.D = x.c->D; m.k = x.c->k; m.L = x.c->L; m.eps = x.c->eps;
+  m.inv_ld = x.c->L; m.sn_layers = x.c->L; m.cn_channels = x.c->k;
   ++x.launches;
   launch_mix_normalize(m, parts, x.st);
+}
+
+// Feedback-free channel l (k = L; [PL 5 ANALYSIS, "Deep-to-shallow feedback"]):
+// the pool restricted to the sources 0..l of each row, computed before layer
+// l runs, so that layer l reads only states its own pass has produced. The
+// router reads the sources of R inside 0..l (a prefix of its input) through
+// rows l*L + 0..l of W_R; the mixer takes the first l + 1 states; channel l's
+// projections write cache channel l.
+void run_pool_channel(const Ctx& x, int N, int l, void* cache_k, void* cache_v, int B, int Tmax) {
+  const wm_config& c = *x.c;
+  const wm_weights& w = *x.w;
+  const int Ls = l + 1;
+  float* coeff = x.buf<float>(B_COEFF);  // [N][2][1][Ls]
+  if (w.static_coeff) {
+    // the row's constants static[b][l][0..l], gathered once, then broadcast
+    float* tmp = x.buf<float>(B_CHSS);
+    for (int b = 0; b < 2; ++b)
+      cudaMemcpyAsync(tmp + b * Ls, w.static_coeff + ((long long)b * c.k + l) * c.L,
+                      (size_t)Ls * sizeof(float), cudaMemcpyDeviceToDevice, x.st);
+    ++x.launches;
+    launch_broadcast_coeff(tmp, N, 2 * Ls, coeff, x.st);
+  } else {
+    int r = 0;  // router sources inside 0..l
+    for (int s = 0; s <= l; ++s) r += (s % c.p) == c.p_offset;
+    if (r == 0) {
+      cudaMemsetAsync(coeff, 0, (size_t)N * 2 * Ls * sizeof(float), x.st);
+    } else {
+      const long long in = (long long)x.nR * c.D;
+      GemmDesc g;
+      g.M = N; g.N = Ls; g.K = r * c.D; g.batch = 2;
+      g.A = x.buf<void>(B_RIN); g.lda = in; g.a_bstride = (long long)N * in;
+      g.B = x.wp(w.Wr, (long long)l * c.L * in); g.ldb = in; g.b_bstride = (long long)c.k * c.L * in;
+      g.epi = base_epi(x);
+      g.epi.mode = EPI_STORE;
+      g.epi.out_f32 = 1;
+      g.epi.C = coeff; g.epi.ldc = 2LL * Ls; g.epi.c_bstride = Ls;
+      ++x.launches;
+      gemm(x, g);
+    }
+  }
+  MixArgs m;
+  m.stash = x.buf<void>(B_STASH); m.ld_row = (long long)c.L * c.D; m.inv = x.buf<float>(B_INV);
+  m.coeff = coeff; m.src_norm = w.src_norm; m.chan_norm = x.wp(w.chan_norm, (long long)l * c.D);
+  m.mixed = x.buf<void>(B_MIXED); m.chan_ss = x.buf<float>(B_CHSS);
+  m.N = N; m.L = Ls; m.D = c.D; m.k = 1; m.eps = c.eps;
+  m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
+  const int tr = trace_begin(x, WM_TRACE_MIX);
+  ++x.launches;
+  const int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  trace_end(x, tr, (double)N * ((double)Ls * c.D * x.es + 2.0 * Ls * 4 + Ls * 4.0 + 2.0 * c.D * x.es));
+  for (int branch = 0; branch < 2; ++branch) {
+    GemmDesc g;
+    g.M = N; g.N = c.Hkv * c.d; g.K = c.D; g.batch = 1;
+    g.A = x.buf<char>(B_MIXED) + (long long)branch * N * c.D * x.es; g.lda = c.D;
+    g.B = x.wp(branch == 0 ? w.Wk : w.Wv, (long long)l * c.Hkv * c.d * c.D); g.ldb = c.D;
+    g.epi = base_epi(x);
+    g.epi.mode = EPI_KV;
+    g.epi.kv_branch = branch;
+    g.epi.gain = x.wp(w.k_norm, (long long)l * c.d); g.epi.gain_bstride = c.d;
+    g.epi.pos = x.buf<int>(B_POS); g.epi.seq = x.buf<int>(B_SEQ);
+    g.epi.cache_k = cache_k; g.epi.cache_v = cache_v;
+    g.epi.k = c.k; g.epi.Hkv = c.Hkv; g.epi.Tmax = Tmax; g.epi.B = B;
+    g.epi.chan0 = l;
+    if (parts) {
+      g.epi.chan_ss = x.buf<float>(B_CHSS);
+      g.epi.chan_parts = parts;
+      g.epi.chan_ss_k = 1;
+      g.epi.chan_D = (float)c.D;
+    }
+    ++x.launches;
+    gemm(x, g);
+  }
 }
 
 // The split-K partial sums start at zero in every call (finalize re-zeroes).
@@ -494,6 +572,73 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w, const int32_
     }
     run_pool(x, N, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
              x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  }
+  return finish(x);
+}
+
+wm_status wm_feedforward_pass(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
+                              int32_t B, int32_t T, int32_t pos0, void* cache_k, void* cache_v,
+                              int32_t Tmax, float* logits, int32_t logits_mode, void* ws,
+                              size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (cfg->k != cfg->L) return WM_ERR_INVALID_ARG;  // one channel per layer
+  if (!tokens || !cache_k || !cache_v || B < 1 || T < 1 || pos0 < 0 || (long long)pos0 + T > Tmax)
+    return WM_ERR_INVALID_ARG;
+  if (logits_mode < WM_LOGITS_NONE || logits_mode > WM_LOGITS_ALL) return WM_ERR_INVALID_ARG;
+  if (logits_mode != WM_LOGITS_NONE && (!logits || !aligned16(logits))) return WM_ERR_INVALID_ARG;
+  if (!aligned16(cache_k) || !aligned16(cache_v)) return WM_ERR_INVALID_ARG;
+  if ((long long)T > (1LL << 26)) return WM_ERR_INVALID_ARG;
+  // sequences per chunk: as many as the workspace holds rows for (at least one)
+  int nb = B;
+  while (nb > 1 && make_layout(*cfg, (long long)nb * T, Tmax).total > ws_bytes) nb = (nb + 1) / 2;
+  if ((s = check_ws(*cfg, ws, ws_bytes, (long long)nb * T, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, w, ws, (long long)nb * T, Tmax, stream);
+  const wm_config& c = *cfg;
+  ++x.launches;
+  launch_rope_table(x.buf<float2>(B_ROPE), pos0, pos0 + T, c.d, c.rope_base, x.st);
+  zero_partials(x);
+  const long long seq_bytes = (long long)c.k * c.Hkv * Tmax * c.d * x.es;
+  for (int b0 = 0; b0 < B; b0 += nb) {
+    const int nbc = B - b0 < nb ? B - b0 : nb;
+    const int N = nbc * T;
+    char* ck = static_cast<char*>(cache_k) + b0 * seq_bytes;
+    char* cv = static_cast<char*>(cache_v) + b0 * seq_bytes;
+    ++x.launches;
+    launch_group_rows(tokens + (long long)b0 * T, nbc, T, 1, 0, T, x.buf<int32_t>(B_TOK),
+                      x.buf<int32_t>(B_SEQ), x.buf<int32_t>(B_POS), x.buf<int32_t>(B_ROWMAP), x.st,
+                      pos0);
+    ++x.launches;
+    launch_embed(c.dtype, x.buf<int32_t>(B_TOK), N, w->embed, c.V, c.D, x.buf<void>(B_STASH),
+                 (long long)c.L * c.D, x.flags(), x.st);
+    const bool want = logits_mode != WM_LOGITS_NONE;
+    const double pos_sum = (double)nbc * ((double)T * pos0 + (double)T * (T - 1) / 2.0);
+    run_stack(x, N, T, pos_sum, want, ck, cv, nbc, Tmax, w->static_coeff == nullptr, true);
+    if (want) {
+      GemmDesc lg;
+      lg.N = c.V; lg.K = c.D; lg.B = w->lm_head; lg.ldb = c.D;
+      lg.epi = base_epi(x);
+      lg.epi.mode = EPI_STORE;
+      lg.epi.out_f32 = 1;
+      lg.epi.ldc = c.V;
+      if (logits_mode == WM_LOGITS_ALL) {
+        ++x.launches;
+        launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, N, c.D, w->final_norm,
+                       x.buf<void>(B_LASTX), c.eps, x.st);
+        lg.M = N; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+        lg.epi.rowmap = x.buf<int>(B_ROWMAP);
+        lg.epi.C = logits + (long long)b0 * T * c.V;
+      } else {
+        ++x.launches;
+        launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, T - 1, T, nbc, c.D, w->final_norm,
+                       x.buf<void>(B_LASTX), c.eps, x.st);
+        lg.M = nbc; lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+        lg.epi.C = logits + (long long)b0 * c.V;
+      }
+      ++x.launches;
+      gemm(x, lg);
+    }
   }
   return finish(x);
 }

@@ -91,12 +91,14 @@ struct Epi {
   // RMSNorm's factor (the projection is linear in its input).
   const float* chan_ss = nullptr;
   int chan_parts = 0;
+  int chan_ss_k = 0;             // channels per branch in the chan_ss layout
   float chan_D = 1.f;
+  int chan0 = 0;                 // EPI_KV: cache channel of batch 0 (channel = chan0 + batch)
   uint32_t* flags = nullptr;
 };
 
 __device__ __forceinline__ float chan_scale(const Epi& e, long long row, int channel) {
-  const float* p = e.chan_ss + ((row * 2 + e.kv_branch) * e.k + channel) * e.chan_parts;
+  const float* p = e.chan_ss + ((row * 2 + e.kv_branch) * e.chan_ss_k + channel) * e.chan_parts;
   float s = 0.f;
   for (int c = 0; c < e.chan_parts; ++c) s += p[c];
   return rsqrtf(s / e.chan_D + e.eps);

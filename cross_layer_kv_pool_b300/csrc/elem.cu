@@ -58,21 +58,22 @@ void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStrea
 // Rows of cyclic group q: row r = b * nq + u holds position i = q + u * g.
 // ---------------------------------------------------------------------------
 __global__ void group_rows_kernel(const int32_t* __restrict__ tokens, int B, int T, int g, int q,
-                                  int nq, int32_t* tok, int32_t* seq, int32_t* pos,
+                                  int nq, int pos0, int32_t* tok, int32_t* seq, int32_t* pos,
                                   int32_t* rowmap) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B * nq) return;
   const int b = r / nq, u = r % nq, i = q + u * g;
   tok[r] = tokens[(long long)b * T + i];
   seq[r] = b;
-  pos[r] = i;
+  pos[r] = pos0 + i;
   if (rowmap) rowmap[r] = b * T + i;
 }
 
 void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq, int32_t* tok,
-                       int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st) {
+                       int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st, int pos0) {
   const int n = B * nq;
-  group_rows_kernel<<<(n + 255) / 256, 256, 0, st>>>(tokens, B, T, g, q, nq, tok, seq, pos, rowmap);
+  group_rows_kernel<<<(n + 255) / 256, 256, 0, st>>>(tokens, B, T, g, q, nq, pos0, tok, seq, pos,
+                                                     rowmap);
 }
 
 __global__ void decode_rows_kernel(const int32_t* __restrict__ tokens, int B, int t, int32_t* tok,

@@ -41,7 +41,7 @@ __device__ void epi_store_head(const Epi& e, int b, int gm, int gn0, float* v) {
                       e.rope + (long long)p * (d >> 1));
   const int h = gn0 / d;
   S* c = (S*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
-         ((((long long)sq * e.k + b) * e.Hkv + h) * e.Tmax + p) * d;
+         ((((long long)sq * e.k + e.chan0 + b) * e.Hkv + h) * e.Tmax + p) * d;
   for (int t = 0; t < d; ++t) c[t] = from_f<S>(v[t]);
 }
 

@@ -252,7 +252,7 @@ __device__ __forceinline__ void epilogue_tile(const Params& p, uint32_t taddr, i
           norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps,
                         rt);
         dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
-              ((((long long)sq * e.k + bidx) * e.Hkv + col0 / HD) * e.Tmax + ps) * HD;
+              ((((long long)sq * e.k + e.chan0 + bidx) * e.Hkv + col0 / HD) * e.Tmax + ps) * HD;
       }
 #pragma unroll
       for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
       if (e.kv_branch == 0)
         norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps, rt);
       dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
-            ((((long long)sq * e.k + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
+            ((((long long)sq * e.k + e.chan0 + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
     }
 #pragma unroll
     for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);

@@ -21,8 +21,10 @@ inline size_t elem_size(int dtype) { return dtype == WM_F32 ? 4 : 2; }
 
 // ---- elem.cu ---------------------------------------------------------------
 void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStream_t st);
+// Rows of group q (positions pos0 + q + g*u) of B sequences of T tokens.
 void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq,
-                       int32_t* tok, int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st);
+                       int32_t* tok, int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st,
+                       int pos0 = 0);
 void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32_t* seq,
                         int32_t* pos, cudaStream_t st);
 void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V, int D,
@@ -80,7 +82,10 @@ struct MixArgs {
   const void* chan_norm;  // [2][k][D]
   void* mixed;            // [2][k][N][D]
   float* chan_ss;         // [N][2][k][8] slice sums of squares (deferred-norm output)
-  int N, L, D, k;
+  int N, L, D, k;         // rows, source layers mixed (the first L of each row), width, channels
+  int inv_ld;             // floats between rows of inv (>= L)
+  int sn_layers;          // layers per branch in src_norm (>= L)
+  int cn_channels;        // channels per branch in chan_norm (>= k)
   float eps;
 };
 // Runs the mixer. Returns 0 if ``mixed`` holds the channel-normed c, or P > 0

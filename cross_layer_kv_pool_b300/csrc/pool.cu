@@ -14,7 +14,7 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
   __shared__ float red[32];
   const int r = blockIdx.x;
   const S* hs = (const S*)a.stash + (long long)r * a.ld_row;
-  const float* inv = a.inv + (long long)r * a.L;
+  const float* inv = a.inv + (long long)r * a.inv_ld;
   const S* sn = (const S*)a.src_norm;
   const S* cn = (const S*)a.chan_norm;
   S* out = (S*)a.mixed;
@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
       for (int t = threadIdx.x; t < a.D; t += blockDim.x) {
         float acc = 0.f;
         for (int l = 0; l < a.L; ++l)
-          acc += cf[l] * (inv[l] * to_f(sn[((long long)beta * a.L + l) * a.D + t]) *
+          acc += cf[l] * (inv[l] * to_f(sn[((long long)beta * a.sn_layers + l) * a.D + t]) *
                           to_f(hs[(long long)l * a.D + t]));
         mbuf[t] = acc;
         ss += acc * acc;
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
       const float im = rsqrtf(ss / (float)a.D + a.eps);
       for (int t = threadIdx.x; t < a.D; t += blockDim.x)
         out[(((long long)beta * a.k + j) * a.N + r) * a.D + t] =
-            from_f<S>(mbuf[t] * im * to_f(cn[((long long)beta * a.k + j) * a.D + t]));
+            from_f<S>(mbuf[t] * im * to_f(cn[((long long)beta * a.cn_channels + j) * a.D + t]));
     }
   }
 }
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
   const int t0 = bt * MIX_C;
   const __nv_bfloat16* src = (const __nv_bfloat16*)a.stash;
   const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm;
-  const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm + (size_t)beta * K * D;
+  const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm + (size_t)beta * a.cn_channels * D;
   __nv_bfloat16* out = (__nv_bfloat16*)a.mixed + (size_t)beta * K * a.N * D;
 
   if (tid == 0) {
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(3 * bytes)
                  : "memory");
     const __nv_bfloat16* srcs[3] = {src + r * a.ld_row + (long long)l0 * D,
-                                    sn + (long long)l0 * D, sn + ((long long)L + l0) * D};
+                                    sn + (long long)l0 * D, sn + ((long long)a.sn_layers + l0) * D};
     for (int i = 0; i < 3; ++i)
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
     // coefficients of this row, scaled by the inverse RMS of each source
     for (int i = tid; i < 2 * L * K; i += NT) {
       const int be = i / (L * K), l = (i / K) % L, j = i % K;
-      coef[i] = a.coeff[(((long long)r * 2 + be) * K + j) * L + l] * a.inv[(long long)r * L + l];
+      coef[i] = a.coeff[(((long long)r * 2 + be) * K + j) * L + l] * a.inv[(long long)r * a.inv_ld + l];
     }
 #pragma unroll
     for (int j = 0; j < K; ++j)

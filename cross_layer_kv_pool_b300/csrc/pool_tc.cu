@@ -142,7 +142,7 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
     for (int i = tid; i < 2 * per_b; i += blockDim.x) {
       const int be = i / per_b, rem = i - be * per_b, l = rem / w8, c8 = (rem - l * w8) * 8;
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (l < L) v = *reinterpret_cast<const uint4*>(sn + ((size_t)be * L + l) * D + c0 + c8);
+      if (l < L) v = *reinterpret_cast<const uint4*>(sn + ((size_t)be * a.sn_layers + l) * D + c0 + c8);
       *reinterpret_cast<uint4*>(gains + ((size_t)be * LP + l) * SROW + c8) = v;
     }
     for (unsigned o = g.off_stage + 16u * tid; o < g.off_bar; o += 16u * blockDim.x)
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
       for (int i = 0; i < MAXV; ++i) {
         const bool v = row < a.N && pk[i] != 0xffffffffu;
         pc[i] = v ? a.coeff[row * ncoef + tid + NC * i] : 0.f;
-        pi[i] = v ? a.inv[row * L + (pk[i] >> 16)] : 0.f;
+        pi[i] = v ? a.inv[row * a.inv_ld + (pk[i] >> 16)] : 0.f;
       }
     };
     auto convert = [&](long long it_dst) {  // prefetched values -> tile of iteration it_dst
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
         for (int h = 0; h < 2; ++h) {
           const int j = gq + 8 * h;
           tau[be][nt][h] =
-              j < K ? *reinterpret_cast<const uint32_t*>(cn + ((size_t)be * K + j) * D + c0 + wcol +
+              j < K ? *reinterpret_cast<const uint32_t*>(cn + ((size_t)be * a.cn_channels + j) * D + c0 + wcol +
                                                          nt * 8 + 2 * tq)
                     : 0u;
         }

@@ -27,7 +27,7 @@ WM_FLAG_SIMT_GEMM = 1
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
             "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version",
-            "wm_pool_mix_static")
+            "wm_pool_mix_static", "wm_feedforward_pass")
 
 
 class WMError(RuntimeError):
@@ -118,6 +118,9 @@ def lib():
         L.wm_cyclic_pass.restype = ctypes.c_int
         L.wm_cyclic_pass.argtypes = [cfgp, wp, vp, i32, i32, i32, i32, i32, vp, vp, i32, vp, i32,
                                      vp, sz, vp]
+        L.wm_feedforward_pass.restype = ctypes.c_int
+        L.wm_feedforward_pass.argtypes = [cfgp, wp, vp, i32, i32, i32, vp, vp, i32, vp, i32, vp,
+                                          sz, vp]
         L.wm_decode_step.restype = ctypes.c_int
         L.wm_decode_step.argtypes = [cfgp, wp, vp, i32, i32, vp, vp, i32, vp, vp, sz, vp]
         L.wm_pool_mix_static.restype = ctypes.c_int
@@ -238,6 +241,18 @@ def wm_cyclic_pass(m: Model, tokens, g: int, cache_k, cache_v, ws, q_begin: int 
                               Tmax, _ptr(logits), LOGITS[logits_mode], _ptr(ws), ws.numel(),
                               _stream(stream))
     _check(st, "wm_cyclic_pass")
+
+
+def wm_feedforward_pass(m: Model, tokens, cache_k, cache_v, ws, pos0: int = 0, logits=None,
+                        logits_mode="none", stream=None):
+    """Feedback-free variant (k = L): tokens [B][T] at positions pos0.. in
+    one exact pass; the workspace may hold fewer than B*T rows (at least T)."""
+    B, T = tokens.shape
+    Tmax = cache_k.shape[3]
+    st = lib().wm_feedforward_pass(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(tokens), B,
+                                   T, int(pos0), _ptr(cache_k), _ptr(cache_v), Tmax, _ptr(logits),
+                                   LOGITS[logits_mode], _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "wm_feedforward_pass")
 
 
 def wm_decode_step(m: Model, tokens, pos: int, cache_k, cache_v, logits, ws, stream=None):

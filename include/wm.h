@@ -188,6 +188,25 @@ wm_status wm_cyclic_pass(const wm_config* cfg, const wm_weights* w,
                          float* logits, int32_t logits_mode,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* The feedback-free variant ([PL 5 ANALYSIS, "Deep-to-shallow feedback"]: a
+ * full cache, one channel per layer, no deep-to-shallow pathway, no
+ * iteration). Requires k = L. Channel l of a token mixes only its states
+ * h^0..h^l: the router reads the sources of R inside 0..l (rows l*L + 0..l of
+ * W_R, the other inputs unused) or static_coeff[b][l][0..l], and the channel is
+ * pooled and written to the cache right before layer l runs, for all rows;
+ * layer l then attends to channel l at positions s < pos. One call is one
+ * exact evaluation of tokens [B][T] at positions pos0..pos0+T-1 against a
+ * cache already holding positions < pos0 (T = 1 is a decode step).
+ * logits as for wm_cyclic_pass (LAST -> [B][V] at pos0+T-1, ALL -> [B][T][V]).
+ * The workspace may hold fewer rows than B*T: whole sequences are processed
+ * in chunks that fit (at least one sequence, T rows). Errors as for
+ * wm_cyclic_pass; k != L is WM_ERR_INVALID_ARG. */
+wm_status wm_feedforward_pass(const wm_config* cfg, const wm_weights* w,
+                              const int32_t* tokens, int32_t B, int32_t T, int32_t pos0,
+                              void* cache_k, void* cache_v, int32_t Tmax,
+                              float* logits, int32_t logits_mode,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* One autoregressive decode step at position ``pos`` for tokens [B]
  * ([PL 3 METHOD, "Execution schedules"]: a token's pooled channels are
  * appended only after its layer stack). The stack attends to s < pos, then

@@ -129,3 +129,19 @@ def test_other_entry_points_validate(L):
     # flags: null workspace
     f = ctypes.c_uint32()
     assert L.wm_check_flags(None, 256, ctypes.byref(f), None) == wm.WM_ERR_INVALID_ARG
+
+
+def test_feedforward_pass_validates(L):
+    """The feedback-free pass needs k = L and the usual argument checks."""
+    vp = FAKE
+    c = _cfg()                      # k = 2 < L = 4
+    w = _weights_struct()
+    assert L.wm_feedforward_pass(ctypes.byref(c), ctypes.byref(w), vp, 1, 8, 0, vp, vp, 16, None, 0,
+                                 vp, 1 << 40, None) == wm.WM_ERR_INVALID_ARG
+    c4 = _cfg(k=4)
+    assert L.wm_feedforward_pass(ctypes.byref(c4), ctypes.byref(w), vp, 1, 8, 9, vp, vp, 16, None,
+                                 0, vp, 1 << 40, None) == wm.WM_ERR_INVALID_ARG   # pos0 + T > Tmax
+    assert L.wm_feedforward_pass(ctypes.byref(c4), ctypes.byref(w), vp, 1, 8, 0, vp, vp, 16, None,
+                                 1, vp, 1 << 40, None) == wm.WM_ERR_INVALID_ARG   # LAST, no logits
+    assert L.wm_feedforward_pass(ctypes.byref(c4), ctypes.byref(w), vp, 1, 8, 0, vp, vp, 16, None,
+                                 0, None, 1 << 40, None) == wm.WM_ERR_WORKSPACE
