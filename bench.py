@@ -63,6 +63,10 @@ def parse():
     ap.add_argument("--rows", type=int, default=8192, help="--kernel mixer: token rows")
     ap.add_argument("--batch", type=int, default=64, help="--kernel attention: sequences")
     ap.add_argument("--group", type=int, default=15, help="--kernel attention: group index q")
+    ap.add_argument("--variant", choices=["feedback_free"], default=None,
+                    help="time the feedback-free variant (k = L, one pass) at the workload's shape")
+    ap.add_argument("--chunk", type=int, default=8,
+                    help="--variant feedback_free: sequences per workspace chunk")
     return ap.parse_args()
 
 
@@ -498,10 +502,74 @@ def run_kernel(args):
           flush=True)
 
 
+def run_variant(args):
+    """The feedback-free variant ([PL 5 ANALYSIS, "Deep-to-shallow feedback"])
+    at the workload's model shape with k = L: one exact layer-by-layer pass
+    over B x T tokens through ``wm_feedforward_pass``, last-position logits;
+    the workspace holds ``--chunk`` sequences at a time."""
+    from cross_layer_kv_pool_b300 import wm
+
+    wl = workload(args)
+    s = wl["shape"].replace(k=wl["shape"].L)
+    B, T = wl["B"], wl["T"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m = wm.Model(s, synth.make_weights(s, seed=0, device=dev))
+    tok = synth.make_tokens(s, B, T, seed=1, device=dev)
+    ck, cv = m.new_cache(B, T)
+    chunk = max(1, min(args.chunk, B))
+    wsp = m.workspace(chunk * T, T)
+    lg = torch.empty((B, s.V), dtype=torch.float32, device=dev)
+
+    def step():
+        ck.zero_()
+        cv.zero_()
+        wm.wm_feedforward_pass(m, tok, ck, cv, wsp, logits=lg, logits_mode="last")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if wm.wm_check_flags(wsp) != 0:
+        raise RuntimeError("device-side checks failed during warm-up")
+    tr = [wm.Tracer(wm.WM_TRACE_GEMM, 4096), wm.Tracer(wm.WM_TRACE_MIX, 512),
+          wm.Tracer(wm.WM_TRACE_ATTN, 512)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    # one more step with the per-kernel events on
+    kinds = {}
+    for t, name in zip(tr, ("gemm", "mixer", "attention")):
+        t.attach(m)
+        step()
+        torch.cuda.synchronize()
+        wm.Tracer.detach(m)
+        res = t.results()
+        kinds[name] = {"launches": len(res), "total_ms": sum(r[0] for r in res),
+                       "work": sum(r[1] for r in res)}
+    pk, pk_src = peaks()
+    kinds["gemm"]["tflops"] = kinds["gemm"]["work"] / (kinds["gemm"]["total_ms"] * 1e9)
+    kinds["attention"]["tflops_causal"] = kinds["attention"]["work"] / (kinds["attention"]["total_ms"] * 1e9)
+    kinds["mixer"]["gbs"] = kinds["mixer"]["work"] / (kinds["mixer"]["total_ms"] * 1e6)
+    print(json.dumps({
+        "metric": "prefill tok/s (feedback-free variant, k = L, one pass)", "value": B * T / (ms / 1e3),
+        "unit": "tok/s", "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded tokens, N(0,0.02) weights)",
+        "config": {"workload": f"{args.workload} shape with k = L = {s.L}, one feedback-free pass",
+                   "global_batch": B, "seq_len": T, "chunk_sequences": chunk},
+        "kernels": kinds, "peaks": {"source": pk_src, **pk},
+        "cache_bytes": 2 * B * s.k * T * s.Hkv * s.d * 2}), flush=True)
+
+
 def main():
     args = parse()
     if args.kernel:
         run_kernel(args)
+        return
+    if args.variant:
+        run_variant(args)
         return
     ws, rank, local = dist_init()
     if args.impl == "reference":

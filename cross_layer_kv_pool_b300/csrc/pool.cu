@@ -246,8 +246,102 @@ bool launch_mix_stream(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
   return false;
 }
 
+// ---------------------------------------------------------------------------
+// One channel (k = 1, the feedback-free variant's per-layer pool): a weighted
+// sum of the row's L states, about 1 FMA per byte, so CUDA cores keep pace
+// with HBM. One block per row, 8 columns per thread (16-byte loads of the
+// state and both gains), fp32 sums of the exact state x gain products. Like
+// the tensor-core mixer it writes u = tau (.) m and the row's sum of squares
+// (one part) for the projection epilogue.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void unpack8(const uint4& u, float* v) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+__global__ void __launch_bounds__(1024) mix1_kernel(const MixArgs a) {
+  __shared__ float coef[2][64];
+  __shared__ float red[2][32];
+  const long long r = blockIdx.x;
+  const int L = a.L, D = a.D;
+  const int t0 = threadIdx.x * 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  for (int i = threadIdx.x; i < 2 * L; i += blockDim.x) {
+    const int be = i / L, l = i % L;
+    coef[be][l] = a.coeff[(r * 2 + be) * L + l] * a.inv[r * a.inv_ld + l];
+  }
+  __syncthreads();
+  const __nv_bfloat16* hs = (const __nv_bfloat16*)a.stash + r * a.ld_row + t0;
+  const __nv_bfloat16* gk = (const __nv_bfloat16*)a.src_norm + t0;
+  const __nv_bfloat16* gv = gk + (size_t)a.sn_layers * D;
+  float mk[8], mv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) mk[e] = mv[e] = 0.f;
+  if (t0 < D) {
+#pragma unroll 4
+    for (int l = 0; l < L; ++l) {
+      float h[8], sk[8], sv[8];
+      unpack8(*reinterpret_cast<const uint4*>(hs + (size_t)l * D), h);
+      unpack8(*reinterpret_cast<const uint4*>(gk + (size_t)l * D), sk);
+      unpack8(*reinterpret_cast<const uint4*>(gv + (size_t)l * D), sv);
+      const float ck = coef[0][l], cv = coef[1][l];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        mk[e] = fmaf(ck, sk[e] * h[e], mk[e]);
+        mv[e] = fmaf(cv, sv[e] * h[e], mv[e]);
+      }
+    }
+  }
+  float ssk = 0.f, ssv = 0.f;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    ssk += mk[e] * mk[e];
+    ssv += mv[e] * mv[e];
+  }
+  ssk = warp_sum(ssk);
+  ssv = warp_sum(ssv);
+  if (lane == 0) {
+    red[0][warp] = ssk;
+    red[1][warp] = ssv;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {
+    float s2 = 0.f;
+    for (int w = 0; w < nw; ++w) s2 += red[threadIdx.x][w];
+    a.chan_ss[r * 2 + threadIdx.x] = s2;  // [N][2][1][1]
+  }
+  if (t0 < D) {
+#pragma unroll
+    for (int be = 0; be < 2; ++be) {
+      float g[8];
+      unpack8(*reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.chan_norm +
+                                              (size_t)be * a.cn_channels * D + t0),
+              g);
+      const float* m = be ? mv : mk;
+      uint4 o;
+      __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(m[2 * i] * g[2 * i], m[2 * i + 1] * g[2 * i + 1]);
+      *reinterpret_cast<uint4*>((__nv_bfloat16*)a.mixed + ((size_t)be * a.N + r) * D + t0) = o;
+    }
+  }
+}
+
 int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags) {
   if (a.N <= 0) return 0;
+  if (dtype == WM_BF16 && !simt && a.k == 1 && a.chan_ss && a.L <= 64 && a.D % 8 == 0 &&
+      a.D <= 8 * 1024 && (uintptr_t)a.stash % 16 == 0 && a.ld_row % 8 == 0 &&
+      (uintptr_t)a.src_norm % 16 == 0 && (uintptr_t)a.chan_norm % 16 == 0 &&
+      (uintptr_t)a.mixed % 16 == 0) {
+    const int threads = ((a.D / 8 + 31) / 32) * 32;
+    mix1_kernel<<<a.N, threads, 0, st>>>(a);
+    return 1;
+  }
   const bool stream_ok = dtype == WM_BF16 && !simt && a.D % (8 * MIX_C) == 0 &&
                          ((uintptr_t)a.stash % 16 == 0) && (a.ld_row % 8 == 0);
   if (dtype == WM_BF16 && !simt) {
