@@ -88,6 +88,7 @@ __all__ = [
     "group_positions", "channel_attention", "consumer_layer", "pool",
     "run_rows", "new_cache", "cyclic_pass", "decode_step",
     "autoregressive", "kv_residual", "feedback_free_channel", "feedback_free_pass",
+    "rmsnorm_backward", "pool_backward",
 ]
 
 
@@ -476,3 +477,80 @@ def feedback_free_pass(cfg, W, tokens, cache_k, cache_v, pos0=0, logits=None,
     lg = _st(cfg, rmsnorm(h, W["final_norm"], cfg.eps)) @ _f64(W["lm_head"]).T
     lg = lg.reshape(B, T, cfg.V)
     return lg[:, -1] if logits == "last" else lg
+
+
+# ----------------------------------------------------------------------------
+# Backward pass of the pool (gradients for training schedules)
+# ----------------------------------------------------------------------------
+
+def rmsnorm_backward(x, w, eps, dy):
+    """Gradients of y = w * x / sqrt(mean(x^2) + eps) over the last axis.
+    Returns (dx, xdy): with r = sqrt(mean(x^2) + eps) and g = w * dy,
+    dx = g / r - x * sum(g * x) / (n * r^3); xdy = (x / r) * dy, whose sum
+    over the axes that share a gain is that gain's gradient."""
+    x, dy = _f64(x), _f64(dy)
+    n = x.shape[-1]
+    r = np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+    g = _f64(w) * dy
+    dx = g / r - x * np.sum(g * x, axis=-1, keepdims=True) / (n * r ** 3)
+    return dx, (x / r) * dy
+
+
+def pool_backward(cfg, W, states, pos, dK, dV, static_coeff=None):
+    """Reverse-mode gradients of :func:`pool` (exact arithmetic, no storage
+    rounding) for upstream gradients dK, dV [N, k, Hkv, d] of its outputs K, V.
+    The steps of :func:`pool` are undone in reverse: RoPE (a rotation, whose
+    transpose rotates by -pos), the K-norm, the channel projections, the channel
+    norm, the mix m_j = sum_l a_{j,l} n_l, the router a = W_R x (skipped with
+    ``static_coeff``) and the per-source norms; the two branches' state
+    gradients add up. Returns a dict of fp64 arrays: dstates [N, L, D], dWr
+    [2, k*L, nR*D] (zeros with static_coeff), dWk, dWv [k, Hkv*d, D],
+    dsrc_norm [2, L, D], dchan_norm [2, k, D], dk_norm [k, d].
+    """
+    states = _f64(states)
+    N, L, D = states.shape
+    k, Hkv, d = cfg.k, cfg.Hkv, cfg.d
+    R = router_sources(cfg)
+    dK, dV = _f64(dK), _f64(dV)
+    g = {"dstates": np.zeros((N, L, D)), "dWr": np.zeros((2, k * L, len(R) * D)),
+         "dWk": np.zeros((k, Hkv * d, D)), "dWv": np.zeros((k, Hkv * d, D)),
+         "dsrc_norm": np.zeros((2, L, D)), "dchan_norm": np.zeros((2, k, D)),
+         "dk_norm": np.zeros((k, d))}
+    for beta in range(2):
+        sig = _f64(W["src_norm"][beta])
+        n = rmsnorm(states, sig, cfg.eps)                              # [N, L, D]
+        x = n[:, R, :].reshape(N, len(R) * D)
+        if static_coeff is None:
+            a = (x @ _f64(W["Wr"][beta]).T).reshape(N, k, L)
+        else:
+            a = np.broadcast_to(_f64(static_coeff)[beta], (N, k, L))
+        m = np.einsum("njl,nld->njd", a, n)                           # [N, k, D]
+        tau = _f64(W["chan_norm"][beta])
+        c = rmsnorm(m, tau, cfg.eps)
+        dc = np.zeros((N, k, D))
+        for j in range(k):
+            if beta == 0:
+                Wp = _f64(W["Wk"][j])
+                kt = (c[:, j] @ Wp.T).reshape(N, Hkv, d)
+                dkn = rope(dK[:, j], -_f64(pos)[:, None], cfg.rope_base)
+                dkt, kdy = rmsnorm_backward(kt, W["k_norm"][j], cfg.eps, dkn)
+                g["dk_norm"][j] += kdy.reshape(-1, d).sum(axis=0)
+                dy = dkt.reshape(N, Hkv * d)
+                g["dWk"][j] += dy.T @ c[:, j]
+            else:
+                Wp = _f64(W["Wv"][j])
+                dy = dV[:, j].reshape(N, Hkv * d)
+                g["dWv"][j] += dy.T @ c[:, j]
+            dc[:, j] = dy @ Wp
+        dm, mdy = rmsnorm_backward(m, tau, cfg.eps, dc)
+        g["dchan_norm"][beta] += mdy.sum(axis=0)
+        da = np.einsum("njd,nld->njl", dm, n)                         # [N, k, L]
+        dn = np.einsum("njl,njd->nld", a, dm)                         # [N, L, D]
+        if static_coeff is None:
+            daf = da.reshape(N, k * L)
+            g["dWr"][beta] += daf.T @ x
+            dn[:, R, :] += (daf @ _f64(W["Wr"][beta])).reshape(N, len(R), D)
+        dh, hdy = rmsnorm_backward(states, sig, cfg.eps, dn)
+        g["dstates"] += dh
+        g["dsrc_norm"][beta] += hdy.sum(axis=0)
+    return g

@@ -661,6 +661,62 @@ def check_feedback_free_router_reads_prefix(O):
         assert np.allclose(V3, V) == (l == 0), l
 
 
+# ---------------------------------------------------------------------------
+# Backward pass of the pool
+# ---------------------------------------------------------------------------
+
+def _fd_check(O, c, W, states, pos, static, seed):
+    """Central differences of L = <G_K, K> + <G_V, V> against pool_backward,
+    for every entry of every parameter and state (tiny shapes)."""
+    rng = np.random.default_rng(seed)
+    N = states.shape[0]
+    GK = rng.standard_normal((N, c.k, c.Hkv, c.d))
+    GV = rng.standard_normal((N, c.k, c.Hkv, c.d))
+
+    def loss(Wx, st):
+        r = O.pool(c, Wx, st, pos, static)
+        return np.sum(GK * r["K"]) + np.sum(GV * r["V"])
+
+    g = O.pool_backward(c, W, states, pos, GK, GV, static)
+    h = 1e-6
+    names = [("Wk", "dWk"), ("Wv", "dWv"), ("src_norm", "dsrc_norm"), ("chan_norm", "dchan_norm"),
+             ("k_norm", "dk_norm")] + ([] if static is not None else [("Wr", "dWr")])
+    for name, key in names:
+        fd = np.zeros_like(W[name])
+        for idx in np.ndindex(W[name].shape):
+            W1 = dict(W)
+            W1[name] = W[name].copy()
+            W1[name][idx] += h
+            lp = loss(W1, states)
+            W1[name][idx] -= 2 * h
+            fd[idx] = (lp - loss(W1, states)) / (2 * h)
+        _close(g[key], fd, 1e-7, key)
+    fd = np.zeros_like(states)
+    for idx in np.ndindex(states.shape):
+        s1 = states.copy()
+        s1[idx] += h
+        lp = loss(W, s1)
+        s1[idx] -= 2 * h
+        fd[idx] = (lp - loss(W, s1)) / (2 * h)
+    _close(g["dstates"], fd, 1e-7, "dstates")
+    if static is not None:
+        assert not np.any(g["dWr"])
+
+
+def check_pool_backward_finite_differences(O):
+    """pool_backward is the gradient of pool: central differences agree to
+    1e-7 for every router, projection, norm-gain and state entry, with the
+    router (p = 2, offset 1) and with constant mixing weights."""
+    c = _cfg(L=3, D=8, k=2, p=2, p_offset=1, Hq=4, Hkv=2, d=4)
+    W = _weights(c, seed=51)
+    rng = np.random.default_rng(52)
+    states = rng.standard_normal((3, c.L, c.D)) * np.exp(rng.uniform(-1, 1, (3, c.L, 1)))
+    pos = rng.integers(0, 40, 3)
+    _fd_check(O, c, W, states, pos, None, 53)
+    static = rng.standard_normal((2, c.k, c.L))
+    _fd_check(O, c, W, states, pos, static, 54)
+
+
 ALL_CHECKS = [
     check_round_bf16,
     check_bf16_storage_mode,
@@ -685,4 +741,5 @@ ALL_CHECKS = [
     check_feedback_free_one_hot_static,
     check_feedback_free_one_pass_is_autoregressive,
     check_feedback_free_router_reads_prefix,
+    check_pool_backward_finite_differences,
 ]

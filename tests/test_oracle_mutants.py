@@ -45,6 +45,12 @@ MUTANTS = [
     ("pool_gained_no_tau", "pool", 'stored[:, beta] = _st(cfg, m * _f64(W["chan_norm"][beta]))',
      'stored[:, beta] = _st(cfg, m)'),
     ("pool_gained_scale_branch", "pool", "* scale[:, 1, j, None]", "* scale[:, 0, j, None]"),
+    ("bwd_rms_no_cross_term", "rmsnorm_backward", "dx = g / r - x * np.sum(g * x, axis=-1, keepdims=True) / (n * r ** 3)",
+     "dx = g / r"),
+    ("bwd_rope_forward_rotation", "pool_backward", "rope(dK[:, j], -_f64(pos)[:, None]", "rope(dK[:, j], _f64(pos)[:, None]"),
+    ("bwd_no_router_to_states", "pool_backward", "dn[:, R, :] += (daf @", "dn[:, R, :] -= 0 * (daf @"),
+    ("bwd_mix_transposed", "pool_backward", 'dn = np.einsum("njl,njd->nld", a, dm)', 'dn = np.einsum("njl,njd->nld", a[:, ::-1], dm)'),
+    ("bwd_branch_grads_overwrite", "pool_backward", 'g["dstates"] += dh', 'g["dstates"] = dh'),
     ("ff_router_rows_shifted", "feedback_free_channel", "[l * L: l * L + l + 1, : len(Rl) * D]",
      "[l * L + 1: l * L + l + 2, : len(Rl) * D]"),
     ("ff_router_all_rows_of_channel", "feedback_free_channel", "Rl = [s for s in router_sources(cfg) if s <= l]",
