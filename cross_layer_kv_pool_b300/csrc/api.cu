@@ -643,6 +643,33 @@ wm_status wm_feedforward_pass(const wm_config* cfg, const wm_weights* w, const i
   return finish(x);
 }
 
+size_t wm_pool_backward_workspace_size(const wm_config* cfg, int32_t max_rows) {
+  if (check_config(cfg) != WM_OK || max_rows < 1) return 0;
+  return pool_bwd_layout(*cfg, max_rows).total;
+}
+
+wm_status wm_pool_backward(const wm_config* cfg, const wm_weights* w, const void* states,
+                           int32_t N, const int32_t* pos, const void* dK, const void* dV,
+                           float* dstates, const wm_pool_grads* grads, void* ws, size_t ws_bytes,
+                           void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (N < 1 || !states || !pos || !dK || !dV || !dstates || !grads) return WM_ERR_INVALID_ARG;
+  if (!grads->dWk || !grads->dWv || !grads->dsrc_norm || !grads->dchan_norm || !grads->dk_norm)
+    return WM_ERR_INVALID_ARG;
+  if ((long long)cfg->k * cfg->L > 1024 || cfg->D > 8192) return WM_ERR_INVALID_ARG;
+  if (!aligned16(states) || !aligned16(dK) || !aligned16(dV) || !aligned16(dstates))
+    return WM_ERR_INVALID_ARG;
+  const PoolBwdLayout lay = pool_bwd_layout(*cfg, N);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < lay.total) return WM_ERR_WORKSPACE;
+  PoolBwdArgs q;
+  q.cfg = cfg; q.w = w; q.states = states; q.N = N; q.pos = pos; q.dK = dK; q.dV = dV;
+  q.dstates = dstates; q.g = *grads; q.ws = ws; q.lay = lay;
+  const cudaError_t e = run_pool_backward(q, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? WM_OK : WM_ERR_CUDA;
+}
+
 wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
                          int32_t B, int32_t pos, void* cache_k, void* cache_v, int32_t Tmax,
                          float* logits, void* ws, size_t ws_bytes, void* stream) {

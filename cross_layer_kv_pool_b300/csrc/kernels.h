@@ -97,6 +97,30 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
 // Tensor-core mixer (bf16, deferred norm); returns P, or 0 if the shape is
 // outside its envelope (k > 16, L > 64, 2kL > 1024, misaligned operands).
 int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
+
+// ---------------------------------------------------------------------------
+// Backward pass of the pool (pool_bwd.cu)
+// ---------------------------------------------------------------------------
+struct PoolBwdLayout {
+  enum { INV, N_, X, A, M, RJ, C, KT, DY, DC, DN, DX, WR, WP, G, AK, NB };
+  size_t off[NB];
+  size_t total;
+};
+PoolBwdLayout pool_bwd_layout(const wm_config& c, long long N);
+struct PoolBwdArgs {
+  const wm_config* cfg;
+  const wm_weights* w;
+  const void* states;  // [N][L][D] storage type
+  int N;
+  const int* pos;      // [N]
+  const void* dK;      // [N][k][Hkv][d] storage type
+  const void* dV;
+  float* dstates;      // [N][L][D] fp32, overwritten
+  wm_pool_grads g;     // fp32 accumulators
+  void* ws;
+  PoolBwdLayout lay;
+};
+cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st);
 void launch_mix_normalize(const MixArgs& a, int parts, cudaStream_t st);
 
 }  // namespace wm

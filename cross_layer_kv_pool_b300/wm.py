@@ -27,7 +27,8 @@ WM_FLAG_SIMT_GEMM = 1
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
             "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version",
-            "wm_pool_mix_static", "wm_feedforward_pass")
+            "wm_pool_mix_static", "wm_feedforward_pass", "wm_pool_backward",
+            "wm_pool_backward_workspace_size")
 
 
 class WMError(RuntimeError):
@@ -91,6 +92,11 @@ class Tracer:
                 for i in range(self.t.count)]
 
 
+class WMPoolGrads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("dWr", "dWk", "dWv", "dsrc_norm", "dchan_norm", "dk_norm")]
+
+
 class WMWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in WEIGHT_ORDER] + [("static_coeff", ctypes.c_void_p)]
 
@@ -121,6 +127,11 @@ def lib():
         L.wm_feedforward_pass.restype = ctypes.c_int
         L.wm_feedforward_pass.argtypes = [cfgp, wp, vp, i32, i32, i32, vp, vp, i32, vp, i32, vp,
                                           sz, vp]
+        L.wm_pool_backward_workspace_size.restype = sz
+        L.wm_pool_backward_workspace_size.argtypes = [cfgp, i32]
+        L.wm_pool_backward.restype = ctypes.c_int
+        L.wm_pool_backward.argtypes = [cfgp, wp, vp, i32, vp, vp, vp, vp,
+                                       ctypes.POINTER(WMPoolGrads), vp, sz, vp]
         L.wm_decode_step.restype = ctypes.c_int
         L.wm_decode_step.argtypes = [cfgp, wp, vp, i32, i32, vp, vp, i32, vp, vp, sz, vp]
         L.wm_pool_mix_static.restype = ctypes.c_int
@@ -253,6 +264,32 @@ def wm_feedforward_pass(m: Model, tokens, cache_k, cache_v, ws, pos0: int = 0, l
                                    T, int(pos0), _ptr(cache_k), _ptr(cache_v), Tmax, _ptr(logits),
                                    LOGITS[logits_mode], _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "wm_feedforward_pass")
+
+
+def pool_grads(m: Model, router: bool = True) -> dict:
+    """Zeroed fp32 gradient accumulators for wm_pool_backward."""
+    s = m.shape
+    dev = m.W["embed"].device
+    z = lambda *shape: torch.zeros(shape, dtype=torch.float32, device=dev)  # noqa: E731
+    g = {"dWk": z(s.k, s.Hkv * s.d, s.D), "dWv": z(s.k, s.Hkv * s.d, s.D),
+         "dsrc_norm": z(2, s.L, s.D), "dchan_norm": z(2, s.k, s.D), "dk_norm": z(s.k, s.d)}
+    g["dWr"] = z(2, s.k * s.L, s.nR * s.D) if router else None
+    return g
+
+
+def wm_pool_backward(m: Model, states, pos, dK, dV, dstates, grads: dict, ws=None, stream=None):
+    """Backward pass of the pool for N rows: writes dstates, adds to grads."""
+    N = states.shape[0]
+    if ws is None:
+        n = lib().wm_pool_backward_workspace_size(ctypes.byref(m.cfg), N)
+        ws = torch.zeros(n, dtype=torch.uint8, device=states.device)
+    gs = WMPoolGrads(*[_ptr(grads.get(k)) for k in
+                       ("dWr", "dWk", "dWv", "dsrc_norm", "dchan_norm", "dk_norm")])
+    st = lib().wm_pool_backward(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(states), N,
+                                _ptr(pos), _ptr(dK), _ptr(dV), _ptr(dstates), ctypes.byref(gs),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "wm_pool_backward")
+    return ws
 
 
 def wm_decode_step(m: Model, tokens, pos: int, cache_k, cache_v, logits, ws, stream=None):

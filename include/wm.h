@@ -207,6 +207,39 @@ wm_status wm_feedforward_pass(const wm_config* cfg, const wm_weights* w,
                               float* logits, int32_t logits_mode,
                               void* ws, size_t ws_bytes, void* stream);
 
+/* Gradient accumulators of the pool's parameters (fp32 device pointers, added
+ * to, so a caller may sum over groups and steps; zero them to start). */
+typedef struct {
+    float* dWr;          /* [2][k*L][nR*D]  nullable: router gradient skipped  */
+    float* dWk;          /* [k][Hkv*d][D]                                      */
+    float* dWv;          /* [k][Hkv*d][D]                                      */
+    float* dsrc_norm;    /* [2][L][D]                                          */
+    float* dchan_norm;   /* [2][k][D]                                          */
+    float* dk_norm;      /* [k][d]                                             */
+} wm_pool_grads;
+
+/* Bytes of workspace wm_pool_backward needs for up to ``max_rows`` rows; 0
+ * for an invalid configuration. */
+size_t wm_pool_backward_workspace_size(const wm_config* cfg, int32_t max_rows);
+
+/* Backward pass of the pool ([PL 3 METHOD, "Cross-layer KV pool"]; the
+ * gradients of a training schedule, [PL 4 EXPERIMENTS]) for N token rows:
+ * given the layer states the pool read (states [N][L][D], storage type), the
+ * rows' positions (pos [N], for RoPE) and the upstream gradients of their
+ * cached channels (dK, dV [N][k][Hkv][d], storage type), recompute the pool in
+ * fp32 and write dstates [N][L][D] (fp32, overwritten: the gradient of the
+ * pool's outputs with respect to every layer state of each row) and add the
+ * parameter gradients to ``grads``. With static_coeff set the router is not
+ * used and dWr is left alone. Plain products run as cuBLAS fp32 GEMMs, the
+ * rest in this library's kernels. Errors: WM_ERR_INVALID_ARG (null or
+ * misaligned pointers, N < 1, k * L > 1024, D > 8192), WM_ERR_WORKSPACE,
+ * WM_ERR_CUDA (a failed launch or cuBLAS call). */
+wm_status wm_pool_backward(const wm_config* cfg, const wm_weights* w,
+                           const void* states, int32_t N, const int32_t* pos,
+                           const void* dK, const void* dV, float* dstates,
+                           const wm_pool_grads* grads,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* One autoregressive decode step at position ``pos`` for tokens [B]
  * ([PL 3 METHOD, "Execution schedules"]: a token's pooled channels are
  * appended only after its layer stack). The stack attends to s < pos, then
