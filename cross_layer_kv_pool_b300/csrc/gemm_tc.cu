@@ -371,58 +371,119 @@ __device__ __forceinline__ void partial_tile(const Params& p, uint32_t taddr, in
   }
 }
 
-// Epilogue applied to summed split-K partials: one thread per output element
-// (plain modes) or per (row, head) (norm modes); re-zeroes what it read.
+// Epilogue applied to summed split-K partials; re-zeroes what it read. Norm
+// modes: one warp per (row, head), lane l holding dims l + 32c, so that every
+// RoPE pair (t, t + HD/2) sits in one lane. Plain modes: four outputs per
+// thread where the width allows.
 template <int MODE, int HD>
 __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
   const Epi& e = p.epi;
   const long long plane = (long long)p.batch * p.M * p.N;
   if constexpr (MODE == EPI_QNORM_ROPE || MODE == EPI_KV) {
+    constexpr int VPL = HD / 32;
+    const int lane = threadIdx.x & 31;
     const int heads = p.N / HD;
-    const long long task = blockIdx.x * (long long)blockDim.x + threadIdx.x;
-    if (task >= (long long)p.batch * p.M * heads) return;
+    const long long task = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+    if (task >= (long long)p.batch * p.M * heads) return;  // warp-uniform
     const int hh = (int)(task % heads);
     const int row = (int)((task / heads) % p.M);
     const int bidx = (int)(task / ((long long)heads * p.M));
     float* src = p.partial + ((long long)bidx * p.M + row) * p.N + hh * HD;
-    float v[HD];
+    float v[VPL];
 #pragma unroll
-    for (int i = 0; i < HD; i += 4) {
-      const float4 f = *reinterpret_cast<const float4*>(src + i);
-      v[i] = f.x; v[i + 1] = f.y; v[i + 2] = f.z; v[i + 3] = f.w;
-      *reinterpret_cast<float4*>(src + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < VPL; ++c) {
+      v[c] = src[lane + 32 * c];
+      src[lane + 32 * c] = 0.f;
     }
     const int ps = e.pos[row];
     if (ps < 0 || ps >= e.Tmax) {
-      atomicOr(e.flags, FLAG_BAD_POS);
+      if (lane == 0) atomicOr(e.flags, FLAG_BAD_POS);
       return;
     }
-    const float2* rt = e.rope + (long long)ps * (HD / 2);
+    const __nv_bfloat16* gain;
     __nv_bfloat16* dst;
+    bool rotate = true;
     if constexpr (MODE == EPI_QNORM_ROPE) {
-      norm_rope<HD>(v, (const __nv_bfloat16*)e.gain, e.eps, rt);
+      gain = (const __nv_bfloat16*)e.gain;
       dst = (__nv_bfloat16*)e.C + (long long)row * e.ldc + hh * HD;
     } else {
       const int sq = e.seq[row];
       if (sq < 0 || sq >= e.B) {
-        atomicOr(e.flags, FLAG_BAD_SEQ);
+        if (lane == 0) atomicOr(e.flags, FLAG_BAD_SEQ);
         return;
       }
       if (e.chan_ss) {
         const float cs = chan_scale(e, row, bidx);
 #pragma unroll
-        for (int t = 0; t < HD; ++t) v[t] *= cs;
+        for (int c = 0; c < VPL; ++c) v[c] *= cs;
       }
-      if (e.kv_branch == 0)
-        norm_rope<HD>(v, (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride, e.eps, rt);
+      rotate = e.kv_branch == 0;
+      gain = (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride;
       dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
             ((((long long)sq * e.k + e.chan0 + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
     }
+    if (rotate) {
+      float ss = 0.f;
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) st_bf16x32(dst + 32 * c, v + 32 * c);
+      for (int c = 0; c < VPL; ++c) ss += v[c] * v[c];
+      ss = warp_sum(ss);
+      const float inv = rsqrtf(ss / (float)HD + e.eps);
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) v[c] *= inv * __bfloat162float(gain[lane + 32 * c]);
+      const float2* rt = e.rope + (long long)ps * (HD / 2);
+#pragma unroll
+      for (int c = 0; c < VPL / 2; ++c) {  // pair (lane + 32c, lane + 32c + HD/2)
+        const float2 cs = rt[lane + 32 * c];
+        const float x1 = v[c], x2 = v[c + VPL / 2];
+        v[c] = x1 * cs.x - x2 * cs.y;
+        v[c + VPL / 2] = x2 * cs.x + x1 * cs.y;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(v[c]);
   } else {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane;
-         i += (long long)gridDim.x * blockDim.x) {
+    const bool vec = (p.N % 4) == 0 && (e.ldc % 4) == 0 && (e.c_bstride % 4) == 0 &&
+                     ((uintptr_t)e.C % 16) == 0 &&
+                     (MODE != EPI_RESID || ((e.ldr % 4) == 0 && ((uintptr_t)e.R % 8) == 0)) &&
+                     !(MODE == EPI_STORE && e.rowmap);
+    const long long step = (long long)gridDim.x * blockDim.x;
+    if (vec) {
+      for (long long i4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i4 * 4 < plane; i4 += step) {
+        const long long i = i4 * 4;
+        const int col = (int)(i % p.N);
+        const int row = (int)((i / p.N) % p.M);
+        const int bidx = (int)(i / ((long long)p.N * p.M));
+        float4 v = *reinterpret_cast<float4*>(p.partial + i);
+        *reinterpret_cast<float4*>(p.partial + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+        float o[4] = {v.x, v.y, v.z, v.w};
+        if constexpr (MODE == EPI_SWIGLU) {
+          const float4 u = *reinterpret_cast<float4*>(p.partial + plane + i);
+          *reinterpret_cast<float4*>(p.partial + plane + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o[q] = o[q] / (1.f + __expf(-o[q])) * uu[q];
+        }
+        if constexpr (MODE == EPI_RESID) {
+          const uint2 rr = *reinterpret_cast<const uint2*>((const __nv_bfloat16*)e.R +
+                                                           (long long)row * e.ldr + col);
+          const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
+          const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
+          o[0] += r0.x; o[1] += r0.y; o[2] += r1.x; o[3] += r1.y;
+        }
+        const long long off = (long long)bidx * e.c_bstride + (long long)row * e.ldc + col;
+        if (e.out_f32) {
+          *reinterpret_cast<float4*>((float*)e.C + off) = make_float4(o[0], o[1], o[2], o[3]);
+        } else {
+          uint2 w;
+          __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+          w.x = *reinterpret_cast<uint32_t*>(&a);
+          w.y = *reinterpret_cast<uint32_t*>(&b);
+          *reinterpret_cast<uint2*>((__nv_bfloat16*)e.C + off) = w;
+        }
+      }
+      return;
+    }
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane; i += step) {
       const int col = (int)(i % p.N);
       const int row = (int)((i / p.N) % p.M);
       const int bidx = (int)(i / ((long long)p.N * p.M));
@@ -726,8 +787,8 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   if (launches) ++*launches;
   if (p.partial) {
     long long work = (MODE == EPI_QNORM_ROPE || MODE == EPI_KV)
-                         ? (long long)g.batch * g.M * (g.N / (HD > 0 ? HD : 1))
-                         : (long long)g.batch * g.M * g.N;
+                         ? 32LL * g.batch * g.M * (g.N / (HD > 0 ? HD : 1))
+                         : ((long long)g.batch * g.M * g.N + 3) / 4;
     long long blocks = (work + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     finalize_kernel<MODE, (HD > 0 ? HD : 64)><<<(int)blocks, 256, 0, st>>>(p);
@@ -746,7 +807,7 @@ int launch_finalize_head(const GemmDesc& g, cudaStream_t st) {
   p.total_tiles = 0; p.vec_out = p.vec_res = 0;
   p.partial = g.partial;
   p.epi = g.epi;
-  const long long work = (long long)g.batch * g.M * (g.N / g.epi.d);
+  const long long work = 32LL * g.batch * g.M * (g.N / g.epi.d);
   const unsigned blocks = (unsigned)((work + 255) / 256);
   if (g.epi.mode == EPI_QNORM_ROPE) {
     if (g.epi.d == 128) tc::finalize_kernel<EPI_QNORM_ROPE, 128><<<blocks, 256, 0, st>>>(p);
