@@ -12,7 +12,8 @@ namespace {
 
 enum Buf {
   B_FLAGS, B_ROPE, B_TOK, B_SEQ, B_POS, B_ROWMAP, B_STASH, B_HMID, B_HL, B_XN, B_Q, B_O,
-  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_CHSS, B_LASTX, B_PARTIAL, B_ATTNP, B_END, NBUF
+  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_CHSS, B_LASTX, B_PARTIAL, B_CNT, B_ATTNP, B_END,
+  NBUF
 };
 
 struct Layout {
@@ -21,6 +22,7 @@ struct Layout {
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
 
 int count_nR(const wm_config& c) {
   int n = 0;
@@ -52,6 +54,8 @@ Layout make_layout(const wm_config& c, long long N, long long Tmax) {
     for (long long v : cand) w = v > w ? v : w;
     sz[B_PARTIAL] = (size_t)rows * w * 4;
   }
+  // arrival counters of the decode attention's key splits, per (row, KV head)
+  sz[B_CNT] = (size_t)(N < 1024 ? N : 1024) * c.Hkv * 4;
   // decode attention key-split partials (at most 16 splits, rows <= 1024)
   sz[B_ATTNP] = (size_t)(N < 1024 ? N : 1024) * c.Hq * 16 * (c.d + 2) * 4;
   sz[B_END] = 0;
@@ -225,6 +229,8 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
       a.channel = l % c.k; a.cache_k = cache_k; a.cache_v = cache_v;
       a.B = B; a.k = c.k; a.Hq = c.Hq; a.Hkv = c.Hkv; a.d = c.d; a.Tmax = Tmax;
       a.out = x.buf<void>(B_O); a.flags = x.flags();
+      a.counters = x.buf<int>(B_CNT);
+      a.counter_elems = (long long)(x.lay.off[B_CNT + 1] - x.lay.off[B_CNT]) / 4;
       const int tr = trace_begin(x, WM_TRACE_ATTN);
       const long long pe = (long long)(x.lay.off[B_ATTNP + 1] - x.lay.off[B_ATTNP]) / 4;
       x.launches += launch_attention(c.dtype, a, !x.tc, x.st, nq, nq == 1 ? (int)(pos_sum / B) : 0,
@@ -419,9 +425,10 @@ void run_pool_channel(const Ctx& x, int N, int l, void* cache_k, void* cache_v, 
   }
 }
 
-// The split-K partial sums start at zero in every call (finalize re-zeroes).
+// The split-K partial sums and the arrival counters start at zero in every
+// call (their consumers re-zero what they used).
 void zero_partials(const Ctx& x) {
-  const size_t n = x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL];
+  const size_t n = x.lay.off[B_CNT + 1] - x.lay.off[B_PARTIAL];
   if (n) cudaMemsetAsync(x.buf<char>(B_PARTIAL), 0, n, x.st);
 }
 
@@ -505,6 +512,9 @@ wm_status wm_channel_attn(const wm_config* cfg, const void* q, int32_t N, const 
   a.q = q; a.N = N; a.seq = seq; a.pos = pos; a.channel = channel;
   a.cache_k = cache_k; a.cache_v = cache_v; a.B = B; a.k = cfg->k; a.Hq = cfg->Hq;
   a.Hkv = cfg->Hkv; a.d = cfg->d; a.Tmax = Tmax; a.out = out; a.flags = x.flags();
+  a.counters = x.buf<int>(B_CNT);
+  a.counter_elems = (long long)(x.lay.off[B_CNT + 1] - x.lay.off[B_CNT]) / 4;
+  cudaMemsetAsync(a.counters, 0, (size_t)a.counter_elems * 4, x.st);
   const int tr = trace_begin(x, WM_TRACE_ATTN);
   // one row per sequence: the decode engine, with Tmax as the bound on visible keys
   const long long pe = (long long)(x.lay.off[B_ATTNP + 1] - x.lay.off[B_ATTNP]) / 4;

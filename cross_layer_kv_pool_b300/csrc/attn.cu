@@ -343,7 +343,22 @@ void launch_attn_mma(const AttnArgs& a, int nq, cudaStream_t st) {
 // attn_combine_kernel merges them.
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int DWARPS = 4, DKEYS = 32;
+constexpr int DWARPS = 4, DKEYS = 32, DBUF = 3;
+}
+
+// Merge of nsplit (max, sum, unnormalised output) partials of one (row, head).
+template <int HD>
+__device__ __forceinline__ float merge_splits(const float* src, int nsplit, int d) {
+  float M = -INFINITY;
+  for (int z = 0; z < nsplit; ++z) M = fmaxf(M, __ldcg(src + z * (HD + 2) + HD));
+  const float base = M == -INFINITY ? 0.f : M;
+  float L = 0.f, acc = 0.f;
+  for (int z = 0; z < nsplit; ++z) {
+    const float f = exp2f(__ldcg(src + z * (HD + 2) + HD) - base);
+    L += f * __ldcg(src + z * (HD + 2) + HD + 1);
+    acc += f * __ldcg(src + z * (HD + 2) + d);
+  }
+  return L > 0.f ? acc / L : 0.f;
 }
 
 template <int HD>
@@ -351,8 +366,9 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
                                                                   float* part) {
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t sm[];
+  __shared__ int last_split;
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm);          // [16][LDS]
-  __nv_bfloat16* sKV = sQ + 16 * LDS;                                 // [warp][2][K,V][DKEYS][LDS]
+  __nv_bfloat16* sKV = sQ + 16 * LDS;                                 // [warp][DBUF][K,V][DKEYS][LDS]
   float* sO = reinterpret_cast<float*>(sm);                           // [warp][16][HD + 2], reused
   const int G = a.Hq / a.Hkv;
   const int n = blockIdx.x / a.Hkv, hk = blockIdx.x % a.Hkv, z = blockIdx.y;
@@ -377,7 +393,7 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
                qg + ((long long)n * a.Hq + hk * G + (v ? m : 0)) * HD + part8 * 8, v);
   }
   cp_async_commit();
-  __nv_bfloat16* myKV = sKV + warp * 2 * 2 * DKEYS * LDS;
+  __nv_bfloat16* myKV = sKV + warp * DBUF * 2 * DKEYS * LDS;
   auto load_blk = [&](int blk, int buf) {
     __nv_bfloat16* dK = myKV + (buf * 2 + 0) * DKEYS * LDS;
     __nv_bfloat16* dV = myKV + (buf * 2 + 1) * DKEYS * LDS;
@@ -396,18 +412,21 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
 #pragma unroll
   for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  // this warp's blocks: warp, warp + DWARPS, ...; DBUF - 1 of them in flight
   int blk = warp, buf = 0;
-  if (blk < nblk) load_blk(blk, 0);
-  cp_async_wait<0>();
+#pragma unroll
+  for (int i = 0; i < DBUF - 1; ++i) {
+    if (blk + i * DWARPS < nblk) load_blk(blk + i * DWARPS, i);
+    else cp_async_commit();
+  }
+  cp_async_wait<DBUF - 2>();
   __syncthreads();  // Q visible to every warp
   const uint32_t qaddr = smem_addr(sQ + (lane & 15) * LDS + (lane >> 4) * 8);
-  for (; blk < nblk; blk += DWARPS, buf ^= 1) {
-    if (blk + DWARPS < nblk) {
-      load_blk(blk + DWARPS, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+  for (; blk < nblk; blk += DWARPS, buf = (buf + 1 == DBUF ? 0 : buf + 1)) {
+    const int ahead = blk + (DBUF - 1) * DWARPS;
+    if (ahead < nblk) load_blk(ahead, buf == 0 ? DBUF - 1 : buf - 1);
+    else cp_async_commit();
+    cp_async_wait<DBUF - 1>();
     __syncwarp();
     const __nv_bfloat16* Kb = myKV + (buf * 2 + 0) * DKEYS * LDS;
     const __nv_bfloat16* Vb = myKV + (buf * 2 + 1) * DKEYS * LDS;
@@ -477,8 +496,9 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
         mma_bf16(o[dn + 1], pa, b2, b3);
       }
     }
-    __syncwarp();  // this buffer may be refilled two blocks later
+    __syncwarp();  // this buffer is refilled DBUF - 1 blocks later
   }
+  cp_async_wait<0>();
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
@@ -528,6 +548,24 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
       }
     }
   }
+  if (nsplit == 1 || !a.counters) return;
+  // The last split of this (row, KV head) to arrive merges all of them.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int prev = atomicAdd(a.counters + blockIdx.x, 1);
+    last_split = prev == nsplit - 1;
+    if (last_split) a.counters[blockIdx.x] = 0;  // ready for the next launch
+  }
+  __syncthreads();
+  if (!last_split) return;
+  __threadfence();
+  for (int idx = threadIdx.x; idx < G * HD; idx += 32 * DWARPS) {
+    const int head = hk * G + idx / HD, d = idx % HD;
+    const float* src = part + ((long long)n * a.Hq + head) * nsplit * (HD + 2);
+    ((__nv_bfloat16*)a.out)[((long long)n * a.Hq + head) * HD + d] =
+        __float2bfloat16_rn(merge_splits<HD>(src, nsplit, d));
+  }
 }
 
 template <int HD>
@@ -535,19 +573,13 @@ __global__ void attn_combine_kernel(const AttnArgs a, int nsplit, const float* p
   const long long nh = blockIdx.x;  // (row, head)
   const int d = threadIdx.x;
   if (d >= HD) return;
-  const float* src = part + nh * nsplit * (HD + 2);
-  float M = -INFINITY;
-  for (int z = 0; z < nsplit; ++z) M = fmaxf(M, src[z * (HD + 2) + HD]);
-  const float base = M == -INFINITY ? 0.f : M;
-  float L = 0.f, acc = 0.f;
-  for (int z = 0; z < nsplit; ++z) {
-    const float f = exp2f(src[z * (HD + 2) + HD] - base);
-    L += f * src[z * (HD + 2) + HD + 1];
-    acc += f * src[z * (HD + 2) + d];
-  }
-  ((__nv_bfloat16*)a.out)[nh * HD + d] = __float2bfloat16_rn(L > 0.f ? acc / L : 0.f);
+  ((__nv_bfloat16*)a.out)[nh * HD + d] =
+      __float2bfloat16_rn(merge_splits<HD>(part + nh * nsplit * (HD + 2), nsplit, d));
 }
 
+// One CTA per (row, KV head, key split), one CTA per SM (shared memory). The
+// split count keeps the grid within one wave: a second wave costs a full
+// CTA start-up and drain, more than the idle SMs of a short first wave.
 template <int HD>
 int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long part_elems,
                        cudaStream_t st) {
@@ -555,16 +587,19 @@ int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long par
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long ctas = (long long)a.N * a.Hkv;
-  int nsplit = (int)((2LL * sms + ctas - 1) / ctas);
+  int nsplit = (int)(sms / ctas);
   nsplit = max(1, min(nsplit, min(16, (kv_len + 4 * DKEYS - 1) / (4 * DKEYS))));
   if (nsplit > 1 && (long long)a.N * a.Hq * nsplit * (HD + 2) > part_elems) nsplit = 1;
-  const size_t smem_loop = (size_t)(16 + DWARPS * 2 * 2 * DKEYS) * (HD + 8) * 2;
+  const bool fused = nsplit > 1 && a.counters && ctas <= a.counter_elems;
+  AttnArgs aa = a;
+  if (!fused) aa.counters = nullptr;
+  const size_t smem_loop = (size_t)(16 + DWARPS * DBUF * 2 * DKEYS) * (HD + 8) * 2;
   const size_t smem_merge = (size_t)DWARPS * 16 * (HD + 2) * 4;
   const size_t smem = smem_loop > smem_merge ? smem_loop : smem_merge;
   cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((unsigned)ctas, nsplit);
-  attn_decode_kernel<HD><<<grid, 32 * DWARPS, smem, st>>>(a, nsplit, part);
-  if (nsplit > 1) {
+  attn_decode_kernel<HD><<<grid, 32 * DWARPS, smem, st>>>(aa, nsplit, part);
+  if (nsplit > 1 && !fused) {
     attn_combine_kernel<HD><<<(unsigned)((long long)a.N * a.Hq), HD, 0, st>>>(a, nsplit, part);
     return 2;
   }

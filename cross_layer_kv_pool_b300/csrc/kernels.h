@@ -63,6 +63,10 @@ struct AttnArgs {
   int B, k, Hq, Hkv, d, Tmax;
   void* out;              // [N][Hq*d]
   uint32_t* flags;
+  // Optional arrival counters (zero on entry, left zero): the decode
+  // engine's last key split of each (row, KV head) merges the splits itself.
+  int* counters = nullptr;
+  long long counter_elems = 0;
 };
 // Returns the number of kernels launched. kv_len: the largest visible key
 // count when the host knows it (decode), else 0. part: fp32 scratch for the
