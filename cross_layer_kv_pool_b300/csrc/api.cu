@@ -155,6 +155,7 @@ void trace_end(const Ctx& x, int idx, double work) {
 void gemm(const Ctx& x, const GemmDesc& gd) {
   const int tr = trace_begin(x, WM_TRACE_GEMM);
   GemmDesc g = gd;
+  g.b_const = true;  // every product of the model multiplies by a weight matrix
   g.partial = x.buf<float>(B_PARTIAL);
   g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
   if (g.partial_elems <= 0) g.partial = nullptr;

@@ -11,6 +11,8 @@ namespace wm {
 // visible keys, each lane owning d/32 of the head's dimensions.
 template <typename S>
 __global__ void __launch_bounds__(128) attn_simt_kernel(const AttnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   if (wid >= (long long)a.N * a.Hq) return;
@@ -112,6 +114,8 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 
 template <int HD>
 __global__ void __launch_bounds__(ATHREADS, 2) attn_mma_kernel(const AttnArgs a, int rpt, int nq) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int LDS = HD + 8;  // padded smem row (elements): conflict-free ldmatrix
   extern __shared__ __align__(16) uint8_t sm[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm);
@@ -330,7 +334,7 @@ void launch_attn_mma(const AttnArgs& a, int nq, cudaStream_t st) {
   const size_t smem = (size_t)(AQ + 4 * AKV) * (HD + 8) * 2;
   cudaFuncSetAttribute(attn_mma_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(tiles, a.Hkv);
-  attn_mma_kernel<HD><<<grid, ATHREADS, smem, st>>>(a, rpt, nq);
+  launch_k(attn_mma_kernel<HD>, dim3(grid), dim3(ATHREADS), smem, st, a, rpt, nq);
 }
 
 // ---------------------------------------------------------------------------
@@ -364,6 +368,8 @@ __device__ __forceinline__ float merge_splits(const float* src, int nsplit, int 
 template <int HD>
 __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs a, int nsplit,
                                                                   float* part) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ int last_split;
@@ -570,6 +576,8 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
 
 template <int HD>
 __global__ void attn_combine_kernel(const AttnArgs a, int nsplit, const float* part) {
+  pdl_wait();
+  pdl_trigger();
   const long long nh = blockIdx.x;  // (row, head)
   const int d = threadIdx.x;
   if (d >= HD) return;
@@ -598,9 +606,9 @@ int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long par
   const size_t smem = smem_loop > smem_merge ? smem_loop : smem_merge;
   cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((unsigned)ctas, nsplit);
-  attn_decode_kernel<HD><<<grid, 32 * DWARPS, smem, st>>>(aa, nsplit, part);
+  launch_k(attn_decode_kernel<HD>, dim3(grid), dim3(32 * DWARPS), smem, st, aa, nsplit, part);
   if (nsplit > 1 && !fused) {
-    attn_combine_kernel<HD><<<(unsigned)((long long)a.N * a.Hq), HD, 0, st>>>(a, nsplit, part);
+    launch_k(attn_combine_kernel<HD>, dim3((unsigned)((long long)a.N * a.Hq)), dim3(HD), 0, st, a, nsplit, part);
     return 2;
   }
   return 1;
@@ -631,7 +639,7 @@ int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, i
   }
   const long long warps = (long long)a.N * a.Hq;
   const int blocks = (int)((warps + 3) / 4);
-  WM_DISPATCH_S(dtype, attn_simt_kernel<S><<<blocks, 128, 0, st>>>(a));
+  WM_DISPATCH_S(dtype, launch_k(attn_simt_kernel<S>, dim3(blocks), dim3(128), 0, st, a));
   return 1;
 }
 

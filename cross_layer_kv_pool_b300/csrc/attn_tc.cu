@@ -267,6 +267,8 @@ template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+  pdl_wait();
+  pdl_trigger();
   using SM = Smem<HD>;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -649,7 +651,7 @@ cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(tiles, a.Hkv);
-  attn_tc_kernel<HD><<<grid, NTHREADS, SM::BYTES, st>>>(mq, mk, mv, p);
+  launch_k(attn_tc_kernel<HD>, dim3(grid), dim3(NTHREADS), SM::BYTES, st, mq, mk, mv, p);
   return cudaGetLastError();
 }
 

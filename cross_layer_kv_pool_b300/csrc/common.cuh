@@ -9,6 +9,37 @@
 
 namespace wm {
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. Kernels go out through launch_k, which lets
+// a kernel's CTAs start while its predecessor in the stream drains. Every
+// such kernel calls pdl_wait() in each thread before it reads or writes any
+// global memory that another kernel writes or reads (only shared-memory,
+// TMEM and barrier set-up, tensor-map prefetch and loads of constant weights
+// may come first), so that it sees the predecessor's results and its grid
+// cannot complete before the predecessor's. pdl_trigger() lets the
+// successor's CTAs be scheduled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = block;
+  lc.dynamicSmemBytes = smem;
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kern, static_cast<KArgs>(args)...);
+}
+
 // Device-side check bits, OR-ed into the workspace flag word.
 enum : uint32_t {
   FLAG_BAD_TOKEN = 1u,     // token id outside [0, V)
@@ -111,6 +142,9 @@ struct GemmDesc {
   const void* B = nullptr;
   long long ldb = 0, b_bstride = 0;
   const void* B2 = nullptr;      // EPI_SWIGLU second operand (same strides as B)
+  // B (and B2) are weights that no kernel writes: the tensor-core engine may
+  // request them before its predecessor in the stream has finished.
+  bool b_const = false;
   Epi epi;
   // Zero-filled fp32 scratch for split-K (nullable): when a GEMM has too few
   // output tiles to occupy the GPU, K is split across CTAs that add their

@@ -35,6 +35,8 @@ __device__ __forceinline__ void st_vec(__nv_bfloat16* p, const float* v) {
 // RoPE table: tab[pos][t] = (cos, sin)(pos * base^(-2t/d)), angles in fp64.
 // ---------------------------------------------------------------------------
 __global__ void rope_table_kernel(float2* tab, int p0, int p1, int d, double base) {
+  pdl_wait();
+  pdl_trigger();
   const int half = d >> 1;
   const long long n = (long long)(p1 - p0) * half;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
@@ -51,7 +53,7 @@ void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStrea
   const long long n = (long long)(p1 - p0) * (d / 2);
   if (n <= 0) return;
   const int blocks = (int)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184);
-  rope_table_kernel<<<blocks, 256, 0, st>>>(tab, p0, p1, d, (double)base);
+  launch_k(rope_table_kernel, dim3(blocks), dim3(256), 0, st, tab, p0, p1, d, (double)base);
 }
 
 // ---------------------------------------------------------------------------
@@ -60,6 +62,8 @@ void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStrea
 __global__ void group_rows_kernel(const int32_t* __restrict__ tokens, int B, int T, int g, int q,
                                   int nq, int pos0, int32_t* tok, int32_t* seq, int32_t* pos,
                                   int32_t* rowmap) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B * nq) return;
   const int b = r / nq, u = r % nq, i = q + u * g;
@@ -72,12 +76,14 @@ __global__ void group_rows_kernel(const int32_t* __restrict__ tokens, int B, int
 void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq, int32_t* tok,
                        int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st, int pos0) {
   const int n = B * nq;
-  group_rows_kernel<<<(n + 255) / 256, 256, 0, st>>>(tokens, B, T, g, q, nq, pos0, tok, seq, pos,
+  launch_k(group_rows_kernel, dim3((n + 255) / 256), dim3(256), 0, st, tokens, B, T, g, q, nq, pos0, tok, seq, pos,
                                                      rowmap);
 }
 
 __global__ void decode_rows_kernel(const int32_t* __restrict__ tokens, int B, int t, int32_t* tok,
                                    int32_t* seq, int32_t* pos) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= B) return;
   tok[r] = tokens[r];
@@ -87,7 +93,7 @@ __global__ void decode_rows_kernel(const int32_t* __restrict__ tokens, int B, in
 
 void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32_t* seq,
                         int32_t* pos, cudaStream_t st) {
-  decode_rows_kernel<<<(B + 255) / 256, 256, 0, st>>>(tokens, B, t, tok, seq, pos);
+  launch_k(decode_rows_kernel, dim3((B + 255) / 256), dim3(256), 0, st, tokens, B, t, tok, seq, pos);
 }
 
 // ---------------------------------------------------------------------------
@@ -96,6 +102,8 @@ void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32
 template <typename S>
 __global__ void embed_kernel(const int32_t* __restrict__ tok, const S* __restrict__ embed, int V,
                              int D, S* __restrict__ out, long long ld_out, uint32_t* flags) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VN = VecT<S>::N;
   const int r = blockIdx.x;
   const int id = tok[r];
@@ -115,7 +123,7 @@ __global__ void embed_kernel(const int32_t* __restrict__ tok, const S* __restric
 void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V, int D, void* out,
                   long long ld_out, uint32_t* flags, cudaStream_t st) {
   if (N <= 0) return;
-  WM_DISPATCH_S(dtype, embed_kernel<S><<<N, 128, 0, st>>>(tok, (const S*)embed, V, D, (S*)out,
+  WM_DISPATCH_S(dtype, launch_k(embed_kernel<S>, dim3(N), dim3(128), 0, st, tok, (const S*)embed, V, D, (S*)out,
                                                          ld_out, flags));
 }
 
@@ -128,6 +136,8 @@ __global__ void norm_emit_kernel(const S* __restrict__ X, long long ldx_row, lon
                                  S* __restrict__ xn, float* __restrict__ inv_out,
                                  const S* __restrict__ src_norm, S* __restrict__ rin, int N,
                                  int nR, int p, int p_off, float eps) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VN = VecT<S>::N;
   __shared__ float red[32];
   const int r = blockIdx.x, l = l0 + blockIdx.y;
@@ -173,7 +183,7 @@ void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx
                       cudaStream_t st) {
   if (N <= 0 || nl <= 0) return;
   dim3 grid(N, nl);
-  WM_DISPATCH_S(dtype, norm_emit_kernel<S><<<grid, 256, 0, st>>>(
+  WM_DISPATCH_S(dtype, launch_k(norm_emit_kernel<S>, dim3(grid), dim3(256), 0, st, 
                            (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in, (S*)xn, inv,
                            (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
 }
@@ -181,6 +191,8 @@ void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx
 template <typename S>
 __global__ void rmsnorm_kernel(const S* __restrict__ X, long long ldx, int row0, int rstride,
                                int D, const S* __restrict__ gain, S* __restrict__ y, float eps) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int VN = VecT<S>::N;
   __shared__ float red[32];
   const int r = blockIdx.x;
@@ -207,12 +219,14 @@ __global__ void rmsnorm_kernel(const S* __restrict__ X, long long ldx, int row0,
 void launch_rmsnorm(int dtype, const void* X, long long ldx, int row0, int rstride, int N, int D,
                     const void* gain, void* y, float eps, cudaStream_t st) {
   if (N <= 0) return;
-  WM_DISPATCH_S(dtype, rmsnorm_kernel<S><<<N, 256, 0, st>>>((const S*)X, ldx, row0, rstride, D,
+  WM_DISPATCH_S(dtype, launch_k(rmsnorm_kernel<S>, dim3(N), dim3(256), 0, st, (const S*)X, ldx, row0, rstride, D,
                                                            (const S*)gain, (S*)y, eps));
 }
 
 __global__ void broadcast_coeff_kernel(const float* __restrict__ stat, long long total, int n_per_row,
                                        float* __restrict__ coeff) {
+  pdl_wait();
+  pdl_trigger();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x)
     coeff[i] = stat[i % n_per_row];
@@ -222,7 +236,7 @@ void launch_broadcast_coeff(const float* stat, int N, int n_per_row, float* coef
   const long long total = (long long)N * n_per_row;
   if (total <= 0) return;
   const long long b = (total + 255) / 256;
-  broadcast_coeff_kernel<<<(int)(b < 4096 ? b : 4096), 256, 0, st>>>(stat, total, n_per_row, coeff);
+  launch_k(broadcast_coeff_kernel, dim3((int)(b < 4096 ? b : 4096)), dim3(256), 0, st, stat, total, n_per_row, coeff);
 }
 
 }  // namespace wm

@@ -47,6 +47,8 @@ __device__ void epi_store_head(const Epi& e, int b, int gm, int gn0, float* v) {
 
 template <typename S, bool DUAL>
 __global__ void __launch_bounds__(NT) gemm_simt_kernel(const GemmDesc g) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[BK][BM + 1];
   __shared__ float Bs[BK][BN + 4];
   __shared__ float B2s[DUAL ? BK : 1][BN + 4];
@@ -132,9 +134,9 @@ void launch_gemm_simt(int dtype, const GemmDesc& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0 || g.batch <= 0) return;
   dim3 grid((g.M + BM - 1) / BM, (g.N + BN - 1) / BN, g.batch);
   if (g.B2) {
-    WM_DISPATCH_S(dtype, gemm_simt_kernel<S, true><<<grid, NT, 0, st>>>(g));
+    WM_DISPATCH_S(dtype, launch_k(gemm_simt_kernel<S, true>, dim3(grid), dim3(NT), 0, st, g));
   } else {
-    WM_DISPATCH_S(dtype, gemm_simt_kernel<S, false><<<grid, NT, 0, st>>>(g));
+    WM_DISPATCH_S(dtype, launch_k(gemm_simt_kernel<S, false>, dim3(grid), dim3(NT), 0, st, g));
   }
 }
 

@@ -37,6 +37,8 @@ __device__ __forceinline__ void mma(float (&d)[4], const uint32_t (&a)[4], uint3
 // DUAL: B and B2 (SwiGLU gate and up) share the activation loads.
 template <bool DUAL>
 __global__ void __launch_bounds__(NT) skinny_kernel(const GemmDesc g, float* fp32_out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) __nv_bfloat16 sA[STAGES][64][LDS];
   __shared__ __align__(16) __nv_bfloat16 sB[STAGES][(DUAL ? 2 : 1) * BN][LDS];
   const int b = blockIdx.y;
@@ -145,9 +147,9 @@ int launch_gemm_skinny(const GemmDesc& g, cudaStream_t st) {
   dim3 grid((g.N + sk::BN - 1) / sk::BN, g.batch);
   float* f32 = head ? g.partial : nullptr;
   if (g.B2)
-    sk::skinny_kernel<true><<<grid, sk::NT, 0, st>>>(g, f32);
+    launch_k(sk::skinny_kernel<true>, dim3(grid), dim3(sk::NT), 0, st, g, f32);
   else
-    sk::skinny_kernel<false><<<grid, sk::NT, 0, st>>>(g, f32);
+    launch_k(sk::skinny_kernel<false>, dim3(grid), dim3(sk::NT), 0, st, g, f32);
   if (!head) return 1;
   return 1 + launch_finalize_head(g, st);
 }

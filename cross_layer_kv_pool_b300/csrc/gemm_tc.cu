@@ -29,8 +29,10 @@ struct Params {
   int m_tiles, n_tiles, num_kb;
   int ksplit, kb_per;     // split-K: K slices per output tile, k-blocks per slice
   long long total_tiles;  // output tiles x ksplit
-  int vec_out, vec_res;
+  int vec_out, vec_res, vec_fin;
   float* partial;         // split-K accumulation target [batch][M][N] (x2 when DUAL)
+  int cluster_red;        // split-K over a thread-block cluster, reduced in shared memory
+  int b_const;            // B tiles may be requested before the predecessor grid ends
   Epi epi;
 };
 
@@ -142,6 +144,30 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Thread-block cluster: full barrier (release/acquire) and loads from the
+// shared memory of CTA ``rank`` of this cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+__device__ __forceinline__ uint32_t peer_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_peer(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(a));
+  return v;
 }
 
 __device__ __forceinline__ void st_bf16x32(__nv_bfloat16* p, const float* v) {
@@ -371,13 +397,110 @@ __device__ __forceinline__ void partial_tile(const Params& p, uint32_t taddr, in
   }
 }
 
+// Per-head epilogue of one (row, head) whose HD sums sit in one warp, lane l
+// holding dims l + 32c (so every RoPE pair (t, t + HD/2) is in one lane).
+template <int MODE, int HD>
+__device__ __forceinline__ void head_out(const Params& p, int bidx, int row, int hh, int lane,
+                                         float (&v)[HD / 32]) {
+  constexpr int VPL = HD / 32;
+  const Epi& e = p.epi;
+  const int ps = e.pos[row];
+  if (ps < 0 || ps >= e.Tmax) {
+    if (lane == 0) atomicOr(e.flags, FLAG_BAD_POS);
+    return;
+  }
+  const __nv_bfloat16* gain;
+  __nv_bfloat16* dst;
+  bool rotate = true;
+  if constexpr (MODE == EPI_QNORM_ROPE) {
+    gain = (const __nv_bfloat16*)e.gain;
+    dst = (__nv_bfloat16*)e.C + (long long)row * e.ldc + hh * HD;
+  } else {
+    const int sq = e.seq[row];
+    if (sq < 0 || sq >= e.B) {
+      if (lane == 0) atomicOr(e.flags, FLAG_BAD_SEQ);
+      return;
+    }
+    if (e.chan_ss) {
+      const float cs = chan_scale(e, row, bidx);
+#pragma unroll
+      for (int c = 0; c < VPL; ++c) v[c] *= cs;
+    }
+    rotate = e.kv_branch == 0;
+    gain = (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride;
+    dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
+          ((((long long)sq * e.k + e.chan0 + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
+  }
+  if (rotate) {
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) ss += v[c] * v[c];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)HD + e.eps);
+#pragma unroll
+    for (int c = 0; c < VPL; ++c) v[c] *= inv * __bfloat162float(gain[lane + 32 * c]);
+    const float2* rt = e.rope + (long long)ps * (HD / 2);
+#pragma unroll
+    for (int c = 0; c < VPL / 2; ++c) {  // pair (lane + 32c, lane + 32c + HD/2)
+      const float2 cs = rt[lane + 32 * c];
+      const float x1 = v[c], x2 = v[c + VPL / 2];
+      v[c] = x1 * cs.x - x2 * cs.y;
+      v[c + VPL / 2] = x2 * cs.x + x1 * cs.y;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < VPL; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(v[c]);
+}
+
+// Plain-mode epilogue of outputs (row, col .. col + 3) (SwiGLU already
+// applied): residual, then store. ``vec``: one 4-wide access each (widths and
+// alignments allow it, no row map); else element by element up to N.
+template <int MODE>
+__device__ __forceinline__ void plain_out4(const Params& p, int bidx, int row, int col,
+                                           float (&o)[4], bool vec) {
+  const Epi& e = p.epi;
+  if (vec) {
+    if constexpr (MODE == EPI_RESID) {
+      const uint2 rr = *reinterpret_cast<const uint2*>((const __nv_bfloat16*)e.R +
+                                                       (long long)row * e.ldr + col);
+      const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
+      const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
+      o[0] += r0.x; o[1] += r0.y; o[2] += r1.x; o[3] += r1.y;
+    }
+    const long long off = (long long)bidx * e.c_bstride + (long long)row * e.ldc + col;
+    if (e.out_f32) {
+      *reinterpret_cast<float4*>((float*)e.C + off) = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      uint2 w;
+      __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+      w.x = *reinterpret_cast<uint32_t*>(&a);
+      w.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>((__nv_bfloat16*)e.C + off) = w;
+    }
+    return;
+  }
+  const long long orow = (MODE == EPI_STORE && e.rowmap) ? e.rowmap[row] : row;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (col + i >= p.N) break;
+    float v = o[i];
+    if constexpr (MODE == EPI_RESID) v += __bfloat162float(((const __nv_bfloat16*)e.R)[(long long)row * e.ldr + col + i]);
+    const long long off = (long long)bidx * e.c_bstride + orow * e.ldc + col + i;
+    if (e.out_f32)
+      ((float*)e.C)[off] = v;
+    else
+      ((__nv_bfloat16*)e.C)[off] = __float2bfloat16_rn(v);
+  }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + __expf(-g)) * u; }
+
 // Epilogue applied to summed split-K partials; re-zeroes what it read. Norm
-// modes: one warp per (row, head), lane l holding dims l + 32c, so that every
-// RoPE pair (t, t + HD/2) sits in one lane. Plain modes: four outputs per
-// thread where the width allows.
+// modes: one warp per (row, head). Plain modes: four outputs per thread.
 template <int MODE, int HD>
 __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
-  const Epi& e = p.epi;
+  pdl_wait();
+  pdl_trigger();
   const long long plane = (long long)p.batch * p.M * p.N;
   if constexpr (MODE == EPI_QNORM_ROPE || MODE == EPI_KV) {
     constexpr int VPL = HD / 32;
@@ -395,112 +518,112 @@ __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
       v[c] = src[lane + 32 * c];
       src[lane + 32 * c] = 0.f;
     }
-    const int ps = e.pos[row];
-    if (ps < 0 || ps >= e.Tmax) {
-      if (lane == 0) atomicOr(e.flags, FLAG_BAD_POS);
-      return;
-    }
-    const __nv_bfloat16* gain;
-    __nv_bfloat16* dst;
-    bool rotate = true;
-    if constexpr (MODE == EPI_QNORM_ROPE) {
-      gain = (const __nv_bfloat16*)e.gain;
-      dst = (__nv_bfloat16*)e.C + (long long)row * e.ldc + hh * HD;
-    } else {
-      const int sq = e.seq[row];
-      if (sq < 0 || sq >= e.B) {
-        if (lane == 0) atomicOr(e.flags, FLAG_BAD_SEQ);
-        return;
-      }
-      if (e.chan_ss) {
-        const float cs = chan_scale(e, row, bidx);
-#pragma unroll
-        for (int c = 0; c < VPL; ++c) v[c] *= cs;
-      }
-      rotate = e.kv_branch == 0;
-      gain = (const __nv_bfloat16*)e.gain + (long long)bidx * e.gain_bstride;
-      dst = (__nv_bfloat16*)(e.kv_branch == 0 ? e.cache_k : e.cache_v) +
-            ((((long long)sq * e.k + e.chan0 + bidx) * e.Hkv + hh) * e.Tmax + ps) * HD;
-    }
-    if (rotate) {
-      float ss = 0.f;
-#pragma unroll
-      for (int c = 0; c < VPL; ++c) ss += v[c] * v[c];
-      ss = warp_sum(ss);
-      const float inv = rsqrtf(ss / (float)HD + e.eps);
-#pragma unroll
-      for (int c = 0; c < VPL; ++c) v[c] *= inv * __bfloat162float(gain[lane + 32 * c]);
-      const float2* rt = e.rope + (long long)ps * (HD / 2);
-#pragma unroll
-      for (int c = 0; c < VPL / 2; ++c) {  // pair (lane + 32c, lane + 32c + HD/2)
-        const float2 cs = rt[lane + 32 * c];
-        const float x1 = v[c], x2 = v[c + VPL / 2];
-        v[c] = x1 * cs.x - x2 * cs.y;
-        v[c + VPL / 2] = x2 * cs.x + x1 * cs.y;
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < VPL; ++c) dst[lane + 32 * c] = __float2bfloat16_rn(v[c]);
+    head_out<MODE, HD>(p, bidx, row, hh, lane, v);
   } else {
+    const Epi& e = p.epi;
     const bool vec = (p.N % 4) == 0 && (e.ldc % 4) == 0 && (e.c_bstride % 4) == 0 &&
                      ((uintptr_t)e.C % 16) == 0 &&
                      (MODE != EPI_RESID || ((e.ldr % 4) == 0 && ((uintptr_t)e.R % 8) == 0)) &&
                      !(MODE == EPI_STORE && e.rowmap);
+    const int quads = (p.N + 3) / 4;  // four columns per thread, per row
     const long long step = (long long)gridDim.x * blockDim.x;
-    if (vec) {
-      for (long long i4 = blockIdx.x * (long long)blockDim.x + threadIdx.x; i4 * 4 < plane; i4 += step) {
-        const long long i = i4 * 4;
-        const int col = (int)(i % p.N);
-        const int row = (int)((i / p.N) % p.M);
-        const int bidx = (int)(i / ((long long)p.N * p.M));
-        float4 v = *reinterpret_cast<float4*>(p.partial + i);
+    for (long long tq = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+         tq < (long long)p.batch * p.M * quads; tq += step) {
+      const int col = (int)(tq % quads) * 4;
+      const int row = (int)((tq / quads) % p.M);
+      const int bidx = (int)(tq / ((long long)quads * p.M));
+      const long long i = ((long long)bidx * p.M + row) * p.N + col;
+      float o[4];
+      if (vec) {
+        const float4 v = *reinterpret_cast<float4*>(p.partial + i);
         *reinterpret_cast<float4*>(p.partial + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-        float o[4] = {v.x, v.y, v.z, v.w};
+        o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
         if constexpr (MODE == EPI_SWIGLU) {
           const float4 u = *reinterpret_cast<float4*>(p.partial + plane + i);
           *reinterpret_cast<float4*>(p.partial + plane + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float uu[4] = {u.x, u.y, u.z, u.w};
+          o[0] = silu_mul(o[0], u.x); o[1] = silu_mul(o[1], u.y);
+          o[2] = silu_mul(o[2], u.z); o[3] = silu_mul(o[3], u.w);
+        }
+      } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) o[q] = o[q] / (1.f + __expf(-o[q])) * uu[q];
-        }
-        if constexpr (MODE == EPI_RESID) {
-          const uint2 rr = *reinterpret_cast<const uint2*>((const __nv_bfloat16*)e.R +
-                                                           (long long)row * e.ldr + col);
-          const float2 r0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.x));
-          const float2 r1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rr.y));
-          o[0] += r0.x; o[1] += r0.y; o[2] += r1.x; o[3] += r1.y;
-        }
-        const long long off = (long long)bidx * e.c_bstride + (long long)row * e.ldc + col;
-        if (e.out_f32) {
-          *reinterpret_cast<float4*>((float*)e.C + off) = make_float4(o[0], o[1], o[2], o[3]);
-        } else {
-          uint2 w;
-          __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
-          w.x = *reinterpret_cast<uint32_t*>(&a);
-          w.y = *reinterpret_cast<uint32_t*>(&b);
-          *reinterpret_cast<uint2*>((__nv_bfloat16*)e.C + off) = w;
+        for (int q = 0; q < 4; ++q) {
+          o[q] = 0.f;
+          if (col + q < p.N) {
+            o[q] = p.partial[i + q];
+            p.partial[i + q] = 0.f;
+            if constexpr (MODE == EPI_SWIGLU) {
+              o[q] = silu_mul(o[q], p.partial[plane + i + q]);
+              p.partial[plane + i + q] = 0.f;
+            }
+          }
         }
       }
-      return;
+      plain_out4<MODE>(p, bidx, row, col, o, vec);
     }
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < plane; i += step) {
-      const int col = (int)(i % p.N);
-      const int row = (int)((i / p.N) % p.M);
-      const int bidx = (int)(i / ((long long)p.N * p.M));
-      float v = p.partial[i];
-      p.partial[i] = 0.f;
-      if constexpr (MODE == EPI_SWIGLU) {
-        const float u = p.partial[plane + i];
-        p.partial[plane + i] = 0.f;
-        v = v / (1.f + __expf(-v)) * u;
+  }
+}
+
+// Split-K over a cluster: the CTAs of one output tile each hold their K
+// slice's accumulator rows in shared memory (``red``, RS floats per row);
+// CTA ``rank`` sums rows rank, rank + ks, ... over the cluster in a fixed
+// order and applies the epilogue. Warp ``we`` of ``nw`` takes every nw-th of
+// those rows; each lane issues all its loads of a row before adding them.
+template <int BN, bool DUAL, int MODE, int HD, int RS>
+__device__ __forceinline__ void cluster_reduce(const Params& p, const float* red, int we, int nw,
+                                               int lane) {
+  constexpr int KS_MAX = 8;
+  const int ks = p.ksplit, rank = (int)(blockIdx.x % ks);
+  const long long ot = blockIdx.x / ks;
+  const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  const int bidx = (int)(ot / tiles_per_batch), rem = (int)(ot % tiles_per_batch);
+  const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;
+  const int n0 = nt * BN, rows = min(BM, p.M - mt * BM);
+  uint32_t peer[KS_MAX];
+#pragma unroll
+  for (int q = 0; q < KS_MAX; ++q) peer[q] = q < ks ? peer_addr(su32(red), q) : 0u;
+  for (int j = rank + we * ks; j < rows; j += nw * ks) {
+    const int row = mt * BM + j;
+    if constexpr (MODE == EPI_QNORM_ROPE || MODE == EPI_KV) {
+      constexpr int VPL = HD / 32;
+#pragma unroll 1
+      for (int h0 = 0; h0 < BN && n0 + h0 < p.N; h0 += HD) {
+        float a[KS_MAX][VPL];
+        const uint32_t off = (uint32_t)(j * RS + h0 + lane) * 4u;
+#pragma unroll
+        for (int q = 0; q < KS_MAX; ++q)
+#pragma unroll
+          for (int c = 0; c < VPL; ++c) a[q][c] = q < ks ? ld_peer(peer[q] + off + 128u * c) : 0.f;
+        float v[VPL];
+#pragma unroll
+        for (int c = 0; c < VPL; ++c) {
+          v[c] = a[0][c];
+#pragma unroll
+          for (int q = 1; q < KS_MAX; ++q) v[c] += a[q][c];
+        }
+        head_out<MODE, HD>(p, bidx, row, (n0 + h0) / HD, lane, v);
       }
-      if constexpr (MODE == EPI_RESID) v += __bfloat162float(((const __nv_bfloat16*)e.R)[(long long)row * e.ldr + col]);
-      const long long orow = (MODE == EPI_STORE && e.rowmap) ? e.rowmap[row] : row;
-      const long long off = (long long)bidx * e.c_bstride + orow * e.ldc + col;
-      if (e.out_f32)
-        ((float*)e.C)[off] = v;
-      else
-        ((__nv_bfloat16*)e.C)[off] = __float2bfloat16_rn(v);
+    } else {
+      for (int c = 4 * lane; c < BN && n0 + c < p.N; c += 128) {
+        const uint32_t off = (uint32_t)(j * RS + c) * 4u;
+        float4 a[KS_MAX], b[DUAL ? KS_MAX : 1];
+#pragma unroll
+        for (int q = 0; q < KS_MAX; ++q) {
+          a[q] = q < ks ? ld_peer4(peer[q] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+          if constexpr (DUAL) b[q] = q < ks ? ld_peer4(peer[q] + off + BN * 4u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4 g = a[0], u = b[0];
+#pragma unroll
+        for (int q = 1; q < KS_MAX; ++q) {
+          g.x += a[q].x; g.y += a[q].y; g.z += a[q].z; g.w += a[q].w;
+          if constexpr (DUAL) { u.x += b[q].x; u.y += b[q].y; u.z += b[q].z; u.w += b[q].w; }
+        }
+        float o[4] = {g.x, g.y, g.z, g.w};
+        if constexpr (DUAL) {
+          o[0] = silu_mul(g.x, u.x); o[1] = silu_mul(g.y, u.y);
+          o[2] = silu_mul(g.z, u.z); o[3] = silu_mul(g.w, u.w);
+        }
+        plain_out4<MODE>(p, bidx, row, n0 + c, o, p.vec_fin != 0 && n0 + c + 4 <= p.N);
+      }
     }
   }
 }
@@ -524,7 +647,32 @@ struct Cfg {
   static constexpr int ACC_STRIDE = pow2_at_least(ACC_COLS);  // accumulator 1 column offset
   static constexpr int TMEM_COLS = 2 * ACC_STRIDE;
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+  // cluster split-K: accumulator rows staged over the (then idle) stage ring
+  static constexpr int RED_STRIDE = ACC_COLS + 4;
+  static_assert(BM * RED_STRIDE * 4 <= STAGES * STAGE_BYTES, "staged rows fit the ring");
 };
+
+// Cluster split-K: copy this thread's accumulator row (tile row ``j``) into
+// the staging rows ``red`` (RS floats per row) of this CTA's shared memory.
+template <int BN, bool DUAL, int RS>
+__device__ __forceinline__ void stage_row(const Params& p, uint32_t taddr, int j, bool row_ok,
+                                          float* red) {
+  constexpr int CW = (BN % 32 == 0) ? 32 : 16;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN * (DUAL ? 2 : 1); c0 += CW) {
+    uint32_t r[CW];
+    __syncwarp();
+    if constexpr (CW == 32) tmem_ld32(taddr + c0, *reinterpret_cast<uint32_t(*)[32]>(r));
+    else tmem_ld16(taddr + c0, r);
+    tmem_wait_ld();
+    if (!row_ok) continue;
+    float4* dst = reinterpret_cast<float4*>(red + (long long)j * RS + c0);
+#pragma unroll
+    for (int i = 0; i < CW; i += 4)
+      dst[i / 4] = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+  }
+}
 
 template <int BN, bool DUAL, int MODE, int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -571,11 +719,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int tiles_per_batch = p.m_tiles * p.n_tiles;
+  if (!(warp == 0 && lane == 0)) pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      int stage = 0;
+      // Weight tiles of the first ring stages go out before the wait for the
+      // predecessor grid (its results are only read through A).
+      int pre = 0;
+      if (p.b_const && blockIdx.x < p.total_tiles) {
+        const long long ot = blockIdx.x / p.ksplit;
+        const int bidx = (int)(ot / tiles_per_batch);
+        const int nt = (int)(ot % tiles_per_batch) % p.n_tiles;
+        const int kb0 = (int)(blockIdx.x % p.ksplit) * p.kb_per;
+        const int kb1 = min(p.num_kb, kb0 + p.kb_per);
+        for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+          uint8_t* sa = smem + pre * C::STAGE_BYTES;
+          mbar_expect_tx(&full[pre], C::STAGE_BYTES);
+          tma_load3(&tmB, &full[pre], sa + C::A_BYTES, kb * BK, nt * BN, bidx);
+          if (DUAL) tma_load3(&tmB2, &full[pre], sa + C::A_BYTES + C::B_BYTES, kb * BK, nt * BN, bidx);
+        }
+      }
+      pdl_wait();
+      int stage = 0, issued = 0;
       uint32_t phase = 0, used = 0, last_phase = 0;
       bool ok = true;
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
@@ -585,16 +752,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int rem = (int)(ot % tiles_per_batch);
         const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
         const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb, ++issued) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
-          mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+          if (issued >= pre) {  // else its B tiles and byte count are already posted
+            mbar_expect_tx(&full[stage], C::STAGE_BYTES);
+            tma_load3(&tmB, &full[stage], sa + C::A_BYTES, kb * BK, nt * BN, bidx);
+            if (DUAL) tma_load3(&tmB2, &full[stage], sa + C::A_BYTES + C::B_BYTES, kb * BK, nt * BN, bidx);
+          }
           tma_load3(&tmA, &full[stage], sa, kb * BK, mt * BM, bidx);
-          tma_load3(&tmB, &full[stage], sa + C::A_BYTES, kb * BK, nt * BN, bidx);
-          if (DUAL) tma_load3(&tmB2, &full[stage], sa + C::A_BYTES + C::B_BYTES, kb * BK, nt * BN, bidx);
           used |= 1u << stage;
           last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == C::STAGES) {
@@ -683,7 +852,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int rem = (int)(ot % tiles_per_batch);
       const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * C::ACC_STRIDE;
-      if (p.partial)
+      if (p.cluster_red) {
+        // this CTA holds exactly one tile; the stage ring is idle from here on
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        stage_row<BN, DUAL, C::RED_STRIDE>(p, taddr, quarter * 32 + lane,
+                                           mt * BM + quarter * 32 + lane < p.M,
+                                           reinterpret_cast<float*>(smem));
+      } else if (p.partial)
         partial_tile<BN, DUAL>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
       else
         epilogue_tile<BN, DUAL, MODE, HD>(p, taddr, mt * BM + quarter * 32 + lane, bidx, nt * BN);
@@ -699,6 +874,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"((uint32_t)C::TMEM_COLS)
                  : "memory");
+  }
+  if (p.cluster_red) {
+    cluster_sync();  // every CTA of the cluster has staged its rows
+    cluster_reduce<BN, DUAL, MODE, HD, C::RED_STRIDE>(p, reinterpret_cast<const float*>(smem),
+                                                      warp, NTHREADS / 32, lane);
+    cluster_sync();  // no CTA leaves while a peer may still read its rows
   }
 }
 
@@ -732,6 +913,41 @@ bool make_map(CUtensorMap* m, const void* ptr, long long K, long long rows, long
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Plain-mode outputs may be moved four at a time (see plain_out4).
+bool fin_vectorisable(const GemmDesc& g) {
+  const Epi& e = g.epi;
+  return (g.N % 4) == 0 && (e.ldc % 4) == 0 && (e.c_bstride % 4) == 0 &&
+         ((uintptr_t)e.C % 16) == 0 &&
+         (e.mode != EPI_RESID || ((e.ldr % 4) == 0 && ((uintptr_t)e.R % 8) == 0)) &&
+         !(e.mode == EPI_STORE && e.rowmap);
+}
+
+// How many clusters of ``ks`` CTAs of this kernel can be resident at once
+// (asked once per kernel and size; the dynamic shared memory size is set).
+template <int BN, bool DUAL, int MODE, int HD>
+int max_clusters(int ks) {
+  static int known[9] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (ks < 2 || ks > 8) return 0;
+  if (known[ks] < 0) {
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)ks);
+    lc.blockDim = dim3(NTHREADS);
+    lc.dynamicSmemBytes = (size_t)Cfg<BN, DUAL>::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)ks;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<BN, DUAL, MODE, HD>, &lc);
+    known[ks] = e == cudaSuccess ? n : 0;
+    if (e != cudaSuccess) cudaGetLastError();  // clear the query's error
+  }
+  return known[ks];
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -760,11 +976,35 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   p.ksplit = 1;
   p.kb_per = p.num_kb;
   p.partial = nullptr;
+  p.cluster_red = 0;
   const int sms = num_sms();
+  auto kern = gemm_tc_kernel<BN, DUAL, MODE, HD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  // Few output tiles (decode-sized M): split K over a cluster of up to 8
+  // CTAs that sum their slices through distributed shared memory; the
+  // largest split whose clusters are all resident at once (one wave).
+  if (g.M <= BM && out_tiles * 2 <= sms && p.num_kb >= 4) {
+    long long ks0 = sms / out_tiles;
+    if (ks0 > 8) ks0 = 8;
+    if (ks0 > p.num_kb / 2) ks0 = p.num_kb / 2;
+    for (int ks = (int)ks0; ks >= 2; --ks) {
+      const int kb_per = (p.num_kb + ks - 1) / ks;
+      const int kse = (p.num_kb + kb_per - 1) / kb_per;
+      if (kse != ks) continue;
+      if (max_clusters<BN, DUAL, MODE, HD>(ks) >= out_tiles) {
+        p.ksplit = ks;
+        p.kb_per = kb_per;
+        p.cluster_red = 1;
+        break;
+      }
+    }
+  }
   const long long need = (long long)g.batch * g.M * g.N * (DUAL ? 2 : 1);
   // split-K only for one row tile (decode-sized M): for more rows the fp32
   // atomics of the partial tiles cost more than the idle SMs it recovers
-  if (g.partial && g.M <= BM && need <= g.partial_elems && out_tiles * 2 <= sms && p.num_kb >= 4 &&
+  if (!p.cluster_red && g.partial && g.M <= BM && need <= g.partial_elems && out_tiles * 2 <= sms &&
+      p.num_kb >= 4 &&
       (MODE != EPI_QNORM_ROPE && MODE != EPI_KV ? true : (g.N % HD == 0))) {
     int ks = (int)((sms + out_tiles - 1) / out_tiles);
     ks = min(ks, p.num_kb / 2);
@@ -779,11 +1019,30 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   p.vec_out = ((uintptr_t)g.epi.C % 16 == 0) && ((g.epi.ldc * osz) % 16 == 0) &&
               ((g.epi.c_bstride * osz) % 16 == 0);
   p.vec_res = ((uintptr_t)g.epi.R % 16 == 0) && ((g.epi.ldr * 2) % 16 == 0);
-  auto kern = gemm_tc_kernel<BN, DUAL, MODE, HD>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
+  p.vec_fin = fin_vectorisable(g);
+  p.b_const = g.b_const ? 1 : 0;
+  if (p.cluster_red) {
+    // one CTA per (output tile, K slice); a cluster holds one tile's slices
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)p.total_tiles);
+    lc.blockDim = dim3(NTHREADS);
+    lc.dynamicSmemBytes = C::SMEM;
+    lc.stream = st;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)p.ksplit;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 2;
+    e = cudaLaunchKernelEx(&lc, kern, ta, tb, tb2, p);
+    if (launches) ++*launches;
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const long long grid = p.total_tiles < sms ? p.total_tiles : sms;
-  kern<<<(int)grid, NTHREADS, C::SMEM, st>>>(ta, tb, tb2, p);
+  launch_k(kern, dim3((unsigned)grid), dim3(NTHREADS), C::SMEM, st, ta, tb, tb2, p);
   if (launches) ++*launches;
   if (p.partial) {
     long long work = (MODE == EPI_QNORM_ROPE || MODE == EPI_KV)
@@ -791,7 +1050,7 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
                          : ((long long)g.batch * g.M * g.N + 3) / 4;
     long long blocks = (work + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    finalize_kernel<MODE, (HD > 0 ? HD : 64)><<<(int)blocks, 256, 0, st>>>(p);
+    launch_k(finalize_kernel<MODE, (HD > 0 ? HD : 64)>, dim3((unsigned)blocks), dim3(256), 0, st, p);
     if (launches) ++*launches;
   }
   return cudaGetLastError();
@@ -804,17 +1063,17 @@ int launch_finalize_head(const GemmDesc& g, cudaStream_t st) {
   tc::Params p;
   p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
   p.m_tiles = p.n_tiles = p.num_kb = p.ksplit = p.kb_per = 1;
-  p.total_tiles = 0; p.vec_out = p.vec_res = 0;
+  p.total_tiles = 0; p.vec_out = p.vec_res = p.vec_fin = 0; p.cluster_red = 0;
   p.partial = g.partial;
   p.epi = g.epi;
   const long long work = 32LL * g.batch * g.M * (g.N / g.epi.d);
   const unsigned blocks = (unsigned)((work + 255) / 256);
   if (g.epi.mode == EPI_QNORM_ROPE) {
-    if (g.epi.d == 128) tc::finalize_kernel<EPI_QNORM_ROPE, 128><<<blocks, 256, 0, st>>>(p);
-    else tc::finalize_kernel<EPI_QNORM_ROPE, 64><<<blocks, 256, 0, st>>>(p);
+    if (g.epi.d == 128) launch_k(tc::finalize_kernel<EPI_QNORM_ROPE, 128>, dim3(blocks), dim3(256), 0, st, p);
+    else launch_k(tc::finalize_kernel<EPI_QNORM_ROPE, 64>, dim3(blocks), dim3(256), 0, st, p);
   } else {
-    if (g.epi.d == 128) tc::finalize_kernel<EPI_KV, 128><<<blocks, 256, 0, st>>>(p);
-    else tc::finalize_kernel<EPI_KV, 64><<<blocks, 256, 0, st>>>(p);
+    if (g.epi.d == 128) launch_k(tc::finalize_kernel<EPI_KV, 128>, dim3(blocks), dim3(256), 0, st, p);
+    else launch_k(tc::finalize_kernel<EPI_KV, 64>, dim3(blocks), dim3(256), 0, st, p);
   }
   return 1;
 }

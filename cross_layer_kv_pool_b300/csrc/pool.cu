@@ -10,6 +10,8 @@ namespace wm {
 // CUDA-core engine, one block per row.
 template <typename S>
 __global__ void __launch_bounds__(256) mix_simt_kernel(const MixArgs a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float mbuf[];  // [D]
   __shared__ float red[32];
   const int r = blockIdx.x;
@@ -121,6 +123,8 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   // Chunk q of this block: row blockIdx.x + (q / nc) * gridDim.x, layers of chunk q % nc.
   auto issue = [&](int q) {
     const long long r = blockIdx.x + (long long)(q / nc) * gridDim.x;
@@ -230,7 +234,7 @@ bool launch_mix_stream_nt(const MixArgs& a, uint32_t* flags, cudaStream_t st) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int grid = a.N < sms ? a.N : sms;
-  mix_stream_kernel<K, NT><<<grid, NT, smem, st>>>(a, flags);
+  launch_k(mix_stream_kernel<K, NT>, dim3(grid), dim3(NT), smem, st, a, flags);
   return true;
 }
 
@@ -265,6 +269,8 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* v) {
 }
 
 __global__ void __launch_bounds__(1024) mix1_kernel(const MixArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float coef[2][64];
   __shared__ float red[2][32];
   const long long r = blockIdx.x;
@@ -339,7 +345,7 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
       (uintptr_t)a.src_norm % 16 == 0 && (uintptr_t)a.chan_norm % 16 == 0 &&
       (uintptr_t)a.mixed % 16 == 0) {
     const int threads = ((a.D / 8 + 31) / 32) * 32;
-    mix1_kernel<<<a.N, threads, 0, st>>>(a);
+    launch_k(mix1_kernel, dim3(a.N), dim3(threads), 0, st, a);
     return 1;
   }
   const bool stream_ok = dtype == WM_BF16 && !simt && a.D % (8 * MIX_C) == 0 &&
@@ -362,7 +368,7 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
     }
     if (done) return 0;
   }
-  WM_DISPATCH_S(dtype, mix_simt_kernel<S><<<a.N, 256, a.D * sizeof(float), st>>>(a));
+  WM_DISPATCH_S(dtype, launch_k(mix_simt_kernel<S>, dim3(a.N), dim3(256), a.D * sizeof(float), st, a));
   return 0;
 }
 

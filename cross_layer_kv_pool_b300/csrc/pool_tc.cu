@@ -166,6 +166,9 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
   }
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   __syncthreads();
+  // everything above touched only weights and shared memory
+  pdl_wait();
+  pdl_trigger();
 
   bool ok = true;
   if (warp == g.nwc) {
@@ -408,6 +411,8 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
 __global__ void __launch_bounds__(256) mix_normalize_kernel(void* mixed, const float* chan_ss,
                                                             int parts, int N, int k, int D,
                                                             float eps) {
+  pdl_wait();
+  pdl_trigger();
   const long long r = blockIdx.x;  // (b * k + j) * N + row
   const int row = (int)(r % N);
   const long long bj = r / N;
@@ -494,13 +499,13 @@ int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags) {
   long long nrg = blocks / g.CS;
   if (nrg < 1) nrg = 1;
   if (nrg > a.N) nrg = a.N;
-  mix_tc_kernel<<<(unsigned)(nrg * g.CS), (g.nwc + 2) * 32, g.smem, st>>>(a, g, flags);
+  launch_k(mix_tc_kernel, dim3((unsigned)(nrg * g.CS)), dim3((g.nwc + 2) * 32), g.smem, st, a, g, flags);
   return cudaGetLastError() == cudaSuccess ? g.CS : 0;
 }
 
 void launch_mix_normalize(const MixArgs& a, int parts, cudaStream_t st) {
   if (a.N <= 0 || parts <= 0) return;
-  mix_normalize_kernel<<<(unsigned)(2LL * a.k * a.N), 256, 0, st>>>(a.mixed, a.chan_ss, parts, a.N,
+  launch_k(mix_normalize_kernel, dim3((unsigned)(2LL * a.k * a.N)), dim3(256), 0, st, a.mixed, a.chan_ss, parts, a.N,
                                                                     a.k, a.D, a.eps);
 }
 
