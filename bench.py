@@ -8,8 +8,9 @@ through the C ABI (``wm_cyclic_pass``). The default workload is the 1.3B-scale
 half-cache model (L=28, D=1792, k=14, p=2, Hq=14, Hkv=2, d=128, F=4608,
 V=151936) at B=64, T=2048. After the timed steps, 256 decode steps of that
 model run from the prefilled cache (Tmax = 2304) and are reported as
-``decode``. Inputs are seeded and synthetic; weights are N(0, 0.02) with unit
-norm gains.
+``decode``: replayed from one CUDA graph of ``wm_decode_batch`` (positions on
+the device), with the direct ``wm_decode_step`` calls as ``decode.eager``.
+Inputs are seeded and synthetic; weights are N(0, 0.02) with unit norm gains.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -350,6 +351,32 @@ def run_ours(args, ws, rank, local):
             wm.wm_decode_step(m, cols[t], T + t, ck, cv, dlg, wsp)
         d1.record(stream)
         torch.cuda.synchronize()
+        dms_eager = max_over_ranks(d0.elapsed_time(d1), ws)
+        # The same steps replayed from one CUDA graph of wm_decode_batch (positions
+        # on the device): per step a token copy, the replay and a position bump.
+        # The entries rewritten at T .. T + nd - 1 get the values they already hold.
+        tok_buf = cols[0].clone()
+        pos_buf = torch.full((B,), T, dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            wm.wm_decode_batch(m, tok_buf, pos_buf, ck, cv, dlg, wsp)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            wm.wm_decode_batch(m, tok_buf, pos_buf, ck, cv, dlg, wsp)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        barrier(ws)
+        d0.record(stream)
+        for t in range(nd):
+            tok_buf.copy_(cols[t])
+            graph.replay()
+            pos_buf += 1
+        d1.record(stream)
+        torch.cuda.synchronize()
         dms = max_over_ranks(d0.elapsed_time(d1), ws)
         # per-kernel shares of one decode step (separate, traced steps)
         dtr = {}
@@ -372,7 +399,9 @@ def run_ours(args, ws, rank, local):
                 dtr[name]["by_flops"] = {k: [v[0], v[1] / v[0]] for k, v in by.items()}
         cache_bytes = 2 * B * s.k * s.Hkv * Tmax * s.d * 2
         decode = {"value": ws * B * nd / (dms / 1e3), "unit": "tok/s", "steps": nd, "batch": B,
-                  "prefix": T, "ms_per_step": dms / nd, "peak_cache_bytes": cache_bytes,
+                  "prefix": T, "ms_per_step": dms / nd, "replay": "cuda_graph",
+                  "eager": {"value": ws * B * nd / (dms_eager / 1e3), "ms_per_step": dms_eager / nd},
+                  "peak_cache_bytes": cache_bytes,
                   "cache_bytes_L_channels": cache_bytes // s.k * s.L, "kernels": dtr}
     if wm.wm_check_flags(wsp) != 0:
         raise RuntimeError("device-side checks failed")

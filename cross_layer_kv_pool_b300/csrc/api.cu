@@ -433,6 +433,36 @@ void zero_partials(const Ctx& x) {
   if (n) cudaMemsetAsync(x.buf<char>(B_PARTIAL), 0, n, x.st);
 }
 
+// One decode step of B single-token rows whose tok/seq/pos rows and RoPE
+// table rows are in place: embed, layer stack, final norm + LM head, then the
+// pool appends every row's channels. pos_sum: sum of the rows' positions (or
+// B * Tmax when only the bound is known on the host).
+void decode_body(const Ctx& x, int B, double pos_sum, void* cache_k, void* cache_v, int Tmax,
+                 float* logits) {
+  const wm_config& c = *x.c;
+  const wm_weights* w = x.w;
+  zero_partials(x);
+  ++x.launches;
+  launch_embed(c.dtype, x.buf<int32_t>(B_TOK), B, w->embed, c.V, c.D, x.buf<void>(B_STASH),
+               (long long)c.L * c.D, x.flags(), x.st);
+  run_stack(x, B, 1, pos_sum, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
+  ++x.launches;
+  launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, B, c.D, w->final_norm,
+                 x.buf<void>(B_LASTX), c.eps, x.st);
+  GemmDesc lg;
+  lg.M = B; lg.N = c.V; lg.K = c.D;
+  lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
+  lg.B = w->lm_head; lg.ldb = c.D;
+  lg.epi = base_epi(x);
+  lg.epi.mode = EPI_STORE;
+  lg.epi.out_f32 = 1;
+  lg.epi.C = logits; lg.epi.ldc = c.V;
+  ++x.launches;
+  gemm(x, lg);
+  run_pool(x, B, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
+           x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+}
+
 wm_status finish(const Ctx& x) {
   if (x.c->trace) x.c->trace->launches += x.launches;
   const cudaError_t e = cudaGetLastError();
@@ -695,29 +725,31 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w, const int32_
   const wm_config& c = *cfg;
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), pos, pos + 1, c.d, c.rope_base, x.st);
-  zero_partials(x);
   ++x.launches;
   launch_decode_rows(tokens, B, pos, x.buf<int32_t>(B_TOK), x.buf<int32_t>(B_SEQ),
                      x.buf<int32_t>(B_POS), x.st);
+  decode_body(x, B, (double)B * pos, cache_k, cache_v, Tmax, logits);
+  return finish(x);
+}
+
+wm_status wm_decode_batch(const wm_config* cfg, const wm_weights* w, const int32_t* tokens,
+                          const int32_t* pos, int32_t B, void* cache_k, void* cache_v, int32_t Tmax,
+                          float* logits, void* ws, size_t ws_bytes, void* stream) {
+  wm_status s;
+  if ((s = check_config(cfg)) != WM_OK) return s;
+  if ((s = check_weights(w)) != WM_OK) return s;
+  if (!tokens || !pos || !cache_k || !cache_v || !logits || B < 1 || Tmax < 1)
+    return WM_ERR_INVALID_ARG;
+  if (!aligned16(cache_k) || !aligned16(cache_v) || !aligned16(logits)) return WM_ERR_INVALID_ARG;
+  if ((s = check_ws(*cfg, ws, ws_bytes, B, Tmax)) != WM_OK) return s;
+  Ctx x = make_ctx(cfg, w, ws, B, Tmax, stream);
+  const wm_config& c = *cfg;
   ++x.launches;
-  launch_embed(c.dtype, x.buf<int32_t>(B_TOK), B, w->embed, c.V, c.D, x.buf<void>(B_STASH),
-               (long long)c.L * c.D, x.flags(), x.st);
-  run_stack(x, B, 1, (double)B * pos, true, cache_k, cache_v, B, Tmax, w->static_coeff == nullptr);
-  ++x.launches;
-  launch_rmsnorm(c.dtype, x.buf<void>(B_HL), c.D, 0, 1, B, c.D, w->final_norm,
-                 x.buf<void>(B_LASTX), c.eps, x.st);
-  GemmDesc lg;
-  lg.M = B; lg.N = c.V; lg.K = c.D;
-  lg.A = x.buf<void>(B_LASTX); lg.lda = c.D;
-  lg.B = w->lm_head; lg.ldb = c.D;
-  lg.epi = base_epi(x);
-  lg.epi.mode = EPI_STORE;
-  lg.epi.out_f32 = 1;
-  lg.epi.C = logits; lg.epi.ldc = c.V;
-  ++x.launches;
-  gemm(x, lg);
-  run_pool(x, B, x.buf<void>(B_STASH), (long long)c.L * c.D, x.buf<float>(B_COEFF),
-           x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
+  launch_decode_rows_dev(tokens, pos, B, c.d, c.rope_base, x.buf<int32_t>(B_TOK),
+                         x.buf<int32_t>(B_SEQ), x.buf<int32_t>(B_POS), x.buf<float2>(B_ROPE), Tmax,
+                         x.st);
+  // the host knows only the bound on visible keys
+  decode_body(x, B, (double)B * Tmax, cache_k, cache_v, Tmax, logits);
   return finish(x);
 }
 

@@ -96,6 +96,42 @@ void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32
   launch_k(decode_rows_kernel, dim3((B + 255) / 256), dim3(256), 0, st, tokens, B, t, tok, seq, pos);
 }
 
+// Decode rows from device arrays: row b is sequence b at pos[b]; its RoPE
+// table row is written here too (rows of equal positions get equal values).
+__global__ void decode_rows_dev_kernel(const int32_t* __restrict__ tokens,
+                                       const int32_t* __restrict__ pos_in, int B, int d,
+                                       double base, int32_t* tok, int32_t* seq, int32_t* pos,
+                                       float2* tab, int Tmax) {
+  pdl_wait();
+  pdl_trigger();
+  const int half = d >> 1;
+  const long long n = (long long)B * half;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < n;
+       idx += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / half), t = (int)(idx % half);
+    const int ps = pos_in[r];
+    if (t == 0) {
+      tok[r] = tokens[r];
+      seq[r] = r;
+      pos[r] = ps;
+    }
+    if (ps < 0 || ps >= Tmax) continue;  // the consumers flag the position
+    const double theta = pow(base, -2.0 * (double)t / (double)d);
+    double sn, cs;
+    sincos((double)ps * theta, &sn, &cs);
+    tab[(long long)ps * half + t] = make_float2((float)cs, (float)sn);
+  }
+}
+
+void launch_decode_rows_dev(const int32_t* tokens, const int32_t* pos_in, int B, int d, float base,
+                            int32_t* tok, int32_t* seq, int32_t* pos, float2* tab, int Tmax,
+                            cudaStream_t st) {
+  const long long n = (long long)B * (d / 2);
+  const int blocks = (int)((n + 255) / 256 < 1184 ? (n + 255) / 256 : 1184);
+  launch_k(decode_rows_dev_kernel, dim3(blocks), dim3(256), 0, st, tokens, pos_in, B, d,
+           (double)base, tok, seq, pos, tab, Tmax);
+}
+
 // ---------------------------------------------------------------------------
 // h^0 = embed[token]; an out-of-range id writes zeros and sets a flag.
 // ---------------------------------------------------------------------------

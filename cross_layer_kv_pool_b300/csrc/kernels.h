@@ -25,6 +25,9 @@ void launch_rope_table(float2* tab, int p0, int p1, int d, float base, cudaStrea
 void launch_group_rows(const int32_t* tokens, int B, int T, int g, int q, int nq,
                        int32_t* tok, int32_t* seq, int32_t* pos, int32_t* rowmap, cudaStream_t st,
                        int pos0 = 0);
+void launch_decode_rows_dev(const int32_t* tokens, const int32_t* pos_in, int B, int d, float base,
+                            int32_t* tok, int32_t* seq, int32_t* pos, float2* tab, int Tmax,
+                            cudaStream_t st);
 void launch_decode_rows(const int32_t* tokens, int B, int t, int32_t* tok, int32_t* seq,
                         int32_t* pos, cudaStream_t st);
 void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V, int D,

@@ -26,7 +26,7 @@ LOGITS = {"none": 0, None: 0, "last": 1, "all": 2}
 WM_FLAG_SIMT_GEMM = 1
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
-            "wm_decode_step", "wm_check_flags", "wm_status_string", "wm_abi_version",
+            "wm_decode_step", "wm_decode_batch", "wm_check_flags", "wm_status_string", "wm_abi_version",
             "wm_pool_mix_static", "wm_feedforward_pass", "wm_pool_backward",
             "wm_pool_backward_workspace_size")
 
@@ -134,6 +134,8 @@ def lib():
                                        ctypes.POINTER(WMPoolGrads), vp, sz, vp]
         L.wm_decode_step.restype = ctypes.c_int
         L.wm_decode_step.argtypes = [cfgp, wp, vp, i32, i32, vp, vp, i32, vp, vp, sz, vp]
+        L.wm_decode_batch.restype = ctypes.c_int
+        L.wm_decode_batch.argtypes = [cfgp, wp, vp, vp, i32, vp, vp, i32, vp, vp, sz, vp]
         L.wm_pool_mix_static.restype = ctypes.c_int
         L.wm_pool_mix_static.argtypes = [cfgp, wp, vp, i32, vp, vp, vp, vp, i32, i32, vp, vp, vp]
         L.wm_check_flags.restype = ctypes.c_int
@@ -299,6 +301,18 @@ def wm_decode_step(m: Model, tokens, pos: int, cache_k, cache_v, logits, ws, str
                               int(pos), _ptr(cache_k), _ptr(cache_v), Tmax, _ptr(logits),
                               _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "wm_decode_step")
+
+
+def wm_decode_batch(m: Model, tokens, pos, cache_k, cache_v, logits, ws, stream=None):
+    """One decode step with per-sequence positions ``pos`` (int32 device [B]).
+    Nothing on the host depends on the values of ``tokens`` or ``pos``, so the
+    call can be captured once in a CUDA graph and replayed."""
+    B = tokens.shape[0]
+    Tmax = cache_k.shape[3]
+    st = lib().wm_decode_batch(ctypes.byref(m.cfg), ctypes.byref(m.wstruct), _ptr(tokens), _ptr(pos),
+                               B, _ptr(cache_k), _ptr(cache_v), Tmax, _ptr(logits), _ptr(ws),
+                               ws.numel(), _stream(stream))
+    _check(st, "wm_decode_batch")
 
 
 def wm_check_flags(ws, stream=None) -> int:

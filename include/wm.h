@@ -249,6 +249,19 @@ wm_status wm_decode_step(const wm_config* cfg, const wm_weights* w,
                          void* cache_k, void* cache_v, int32_t Tmax,
                          float* logits, void* ws, size_t ws_bytes, void* stream);
 
+/* wm_decode_step with per-sequence positions read on the device: sequence b
+ * of the batch appends its token tokens[b] at pos[b] (both int32 device
+ * arrays [B]), attends to its keys s < pos[b] and gets logits[b]. Sequences
+ * may sit at different positions. No host-side value depends on the device
+ * arrays, so the call can be recorded once into a CUDA graph and replayed,
+ * the caller updating tokens and pos in place between replays. A pos[b]
+ * outside [0, Tmax) sets the position check bit (see wm_check_flags) and
+ * that sequence's cache is left alone. */
+wm_status wm_decode_batch(const wm_config* cfg, const wm_weights* w,
+                          const int32_t* tokens, const int32_t* pos, int32_t B,
+                          void* cache_k, void* cache_v, int32_t Tmax,
+                          float* logits, void* ws, size_t ws_bytes, void* stream);
+
 /* Waits for ``stream``, copies the workspace flag word to *flags_out (host)
  * and clears it. Returns WM_ERR_DEVICE_BOUNDS if an index check failed and
  * WM_ERR_TIMEOUT if a bounded wait gave up since the last call. */

@@ -71,6 +71,10 @@ Readings where the pages are silent (each listed again in the design notes):
       router reads the sources of R inside 0..l (its other inputs unused)
       through rows l*L + 0..l of W_R (or static_coeff[b][l][0..l]); the
       channel is cached before layer l runs; layer l still attends to s < i.
+  R19 Decode with sequences at different positions (continuous batching):
+      the pages decode every sequence at the same step; a batch in which
+      sequence b sits at pos[b] is read as the per-sequence decode step at
+      t = pos[b] for each b, with no interaction between sequences.
 
 Parity pins for every function below live in tests/test_oracle_pins.py and
 tests/test_oracle_mutants.py (closed forms, special cases, brute force and an
@@ -376,6 +380,21 @@ def decode_step(cfg, W, tokens, t, cache_k, cache_v, static_coeff=None):
     B = len(tokens)
     seq = np.arange(B)
     pos = np.full(B, t, dtype=np.int64)
+    res, lg, _ = run_rows(cfg, W, tokens, seq, pos, cache_k, cache_v, True, static_coeff)
+    _write(cache_k, cache_v, seq, pos, res["K"], res["V"])
+    return lg
+
+
+def decode_batch(cfg, W, tokens, pos, cache_k, cache_v, static_coeff=None):
+    """A decode step in which sequence b sits at its own position pos[b]
+    (R19): it is decode_step with t = pos[b] for each sequence at once, as in
+    [PL 3 METHOD, "Execution schedules"] -- sequence b attends to its keys
+    s < pos[b], then its pooled channels are appended at pos[b]. Sequences do
+    not interact. Returns logits [B, V]."""
+    tokens = np.asarray(tokens, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    B = len(tokens)
+    seq = np.arange(B)
     res, lg, _ = run_rows(cfg, W, tokens, seq, pos, cache_k, cache_v, True, static_coeff)
     _write(cache_k, cache_v, seq, pos, res["K"], res["V"])
     return lg

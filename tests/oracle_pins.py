@@ -528,6 +528,28 @@ def check_last_logits_and_decode(O):
     _close(lg, lgar[:, 6], 1e-10, "decode")
 
 
+def check_decode_batch_ragged_positions(O):
+    """Sequences at different positions in one decode_batch call each get what
+    their own exact autoregressive evaluation gives at that position: logits
+    and the K/V appended there (a shared or swapped position fails)."""
+    c = _cfg()
+    W = _weights(c, seed=23)
+    B, T = 3, 6
+    tokens = _tokens(c, B, T, 7)
+    lgar, rk, rv = _ar(O, c, W, tokens)
+    pos = np.array([4, 0, 5])
+    ck, cv = O.new_cache(c, B, T)
+    for b in range(B):  # each sequence's exact prefix, alone
+        if pos[b]:
+            O.autoregressive(c, W, tokens[b:b + 1, :pos[b]], ck[b:b + 1], cv[b:b + 1])
+    lg = O.decode_batch(c, W, tokens[np.arange(B), pos], pos, ck, cv)
+    for b in range(B):
+        _close(lg[b], lgar[b, pos[b]], 1e-10, f"logits {b}")
+        _close(ck[b, :, :, pos[b]], rk[b, :, :, pos[b]], 1e-10, f"K {b}")
+        _close(cv[b, :, :, pos[b]], rv[b, :, :, pos[b]], 1e-10, f"V {b}")
+        assert not np.any(ck[b, :, :, pos[b] + 1:]), "nothing written past pos"
+
+
 def check_round_bf16(O):
     """Ties to even at the 2^-8 midpoints near 1; agreement with torch's own
     fp32 -> bf16 conversion on random values of many magnitudes."""
@@ -738,6 +760,7 @@ ALL_CHECKS = [
     check_bruteforce_T4,
     check_partial_pass_positions,
     check_last_logits_and_decode,
+    check_decode_batch_ragged_positions,
     check_feedback_free_one_hot_static,
     check_feedback_free_one_pass_is_autoregressive,
     check_feedback_free_router_reads_prefix,

@@ -115,6 +115,13 @@ def test_other_entry_points_validate(L):
                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
     assert L.wm_decode_step(ctypes.byref(c), ctypes.byref(w), vp, 1, 3, vp, vp, 64, None, vp,
                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
+    # batched decode: null positions, B = 0, null tokens
+    assert L.wm_decode_batch(ctypes.byref(c), ctypes.byref(w), vp, None, 1, vp, vp, 64, vp, vp,
+                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
+    assert L.wm_decode_batch(ctypes.byref(c), ctypes.byref(w), vp, vp, 0, vp, vp, 64, vp, vp,
+                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
+    assert L.wm_decode_batch(ctypes.byref(c), ctypes.byref(w), None, vp, 1, vp, vp, 64, vp, vp,
+                             1 << 40, None) == wm.WM_ERR_INVALID_ARG
     # attention: channel out of range
     assert L.wm_channel_attn(ctypes.byref(c), vp, 4, vp, vp, 2, vp, vp, 1, 64, vp, 0, vp, 1 << 40,
                              None) == wm.WM_ERR_INVALID_ARG

@@ -51,6 +51,9 @@ MUTANTS = [
     ("bwd_no_router_to_states", "pool_backward", "dn[:, R, :] += (daf @", "dn[:, R, :] -= 0 * (daf @"),
     ("bwd_mix_transposed", "pool_backward", 'dn = np.einsum("njl,njd->nld", a, dm)', 'dn = np.einsum("njl,njd->nld", a[:, ::-1], dm)'),
     ("bwd_branch_grads_overwrite", "pool_backward", 'g["dstates"] += dh', 'g["dstates"] = dh'),
+    ("batch_shared_position", "decode_batch", "pos = np.asarray(pos, dtype=np.int64)",
+     "pos = np.full(len(pos), int(np.max(pos)), dtype=np.int64)"),
+    ("batch_sequences_swapped", "decode_batch", "seq = np.arange(B)", "seq = np.arange(B)[::-1].copy()"),
     ("ff_router_rows_shifted", "feedback_free_channel", "[l * L: l * L + l + 1, : len(Rl) * D]",
      "[l * L + 1: l * L + l + 2, : len(Rl) * D]"),
     ("ff_router_all_rows_of_channel", "feedback_free_channel", "Rl = [s for s in router_sources(cfg) if s <= l]",
