@@ -159,15 +159,7 @@ void gemm(const Ctx& x, const GemmDesc& gd) {
   g.partial = x.buf<float>(B_PARTIAL);
   g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
   if (g.partial_elems <= 0) g.partial = nullptr;
-  // Few rows, two weight matrices and many column blocks (the SwiGLU
-  // projection of a decode step): the mma.sync engine streams both weight
-  // blocks past one activation load; measured faster there than the split-K
-  // tcgen05 path, which wins for the single-matrix decode products.
-  const bool skinny = g.M <= 64 && g.B2 != nullptr && (long long)((g.N + 15) / 16) * g.batch >= 96 &&
-                      g.N < 32768;
-  if (x.tc && skinny && gemm_skinny_supported(g)) {
-    x.launches += launch_gemm_skinny(g, x.st) - 1;  // the caller counted one launch
-  } else if (x.tc && gemm_tc_supported(g)) {
+  if (x.tc && gemm_tc_supported(g)) {
     int n = 0;
     const cudaError_t e = launch_gemm_tc(g, x.st, &n);
     x.launches += n - 1;

@@ -1058,26 +1058,6 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
 
 }  // namespace tc
 
-// Per-head epilogue over fp32 sums that another engine left in g.partial.
-int launch_finalize_head(const GemmDesc& g, cudaStream_t st) {
-  tc::Params p;
-  p.M = g.M; p.N = g.N; p.K = g.K; p.batch = g.batch;
-  p.m_tiles = p.n_tiles = p.num_kb = p.ksplit = p.kb_per = 1;
-  p.total_tiles = 0; p.vec_out = p.vec_res = p.vec_fin = 0; p.cluster_red = 0;
-  p.partial = g.partial;
-  p.epi = g.epi;
-  const long long work = 32LL * g.batch * g.M * (g.N / g.epi.d);
-  const unsigned blocks = (unsigned)((work + 255) / 256);
-  if (g.epi.mode == EPI_QNORM_ROPE) {
-    if (g.epi.d == 128) launch_k(tc::finalize_kernel<EPI_QNORM_ROPE, 128>, dim3(blocks), dim3(256), 0, st, p);
-    else launch_k(tc::finalize_kernel<EPI_QNORM_ROPE, 64>, dim3(blocks), dim3(256), 0, st, p);
-  } else {
-    if (g.epi.d == 128) launch_k(tc::finalize_kernel<EPI_KV, 128>, dim3(blocks), dim3(256), 0, st, p);
-    else launch_k(tc::finalize_kernel<EPI_KV, 64>, dim3(blocks), dim3(256), 0, st, p);
-  }
-  return 1;
-}
-
 bool gemm_tc_supported(const GemmDesc& g) {
   auto a16 = [](const void* p) { return ((uintptr_t)p & 15u) == 0; };
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batch <= 0) return false;

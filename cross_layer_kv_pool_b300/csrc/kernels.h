@@ -49,10 +49,6 @@ void launch_broadcast_coeff(const float* stat, int N, int n_per_row, float* coef
 void launch_gemm_simt(int dtype, const GemmDesc& g, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int* launches);
-int launch_finalize_head(const GemmDesc& g, cudaStream_t st);
-// Few-row engine (M <= 64): returns kernels launched.
-bool gemm_skinny_supported(const GemmDesc& g);
-int launch_gemm_skinny(const GemmDesc& g, cudaStream_t st);
 
 // ---- attn.cu ---------------------------------------------------------------
 struct AttnArgs {

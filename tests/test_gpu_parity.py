@@ -274,9 +274,9 @@ def test_decode_long_context_isolated(dtype, shape_kw):
 
 def test_decode_1p3b_widths_isolated():
     """Decode steps with the 1.3B model's widths (D 1792, 14 query heads of 128,
-    2 KV heads, F 4608), 8 layers and 8 channels: split-K tcgen05 products
-    with finalize epilogues, the few-row engine for the SwiGLU projection and
-    the split-key decode attention."""
+    2 KV heads, F 4608), 8 layers and 8 channels: tcgen05 products with K
+    split over a thread-block cluster (the SwiGLU projection included) and the
+    split-key decode attention."""
     s = synth.HALF_1P3B.replace(L=8, k=8, V=2000)
     m, Wn = model(s, seed=21, jitter=0.1)
     B, Tmax, start = 8, 300, 250
