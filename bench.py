@@ -59,7 +59,8 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k", type=int, default=None, help="override the channel count k")
-    ap.add_argument("--kernel", choices=["mixer", "attention", "pool_backward"], default=None,
+    ap.add_argument("--kernel", choices=["mixer", "attention", "pool_backward", "decode"],
+                    default=None,
                     help="time one kernel of the path alone (1.3B shapes)")
     ap.add_argument("--rows", type=int, default=8192, help="--kernel mixer: token rows")
     ap.add_argument("--batch", type=int, default=64, help="--kernel attention: sequences")
@@ -352,29 +353,42 @@ def run_ours(args, ws, rank, local):
         d1.record(stream)
         torch.cuda.synchronize()
         dms_eager = max_over_ranks(d0.elapsed_time(d1), ws)
-        # The same steps replayed from one CUDA graph of wm_decode_batch (positions
-        # on the device): per step a token copy, the replay and a position bump.
-        # The entries rewritten at T .. T + nd - 1 get the values they already hold.
-        tok_buf = cols[0].clone()
+        # The same steps replayed from one CUDA graph per step: the step's
+        # tokens gathered on the device, wm_decode_batch (positions on the
+        # device), then the position and step counters advanced, so that each
+        # step is a single graph launch. The entries rewritten at
+        # T .. T + nd - 1 get the values they already hold.
+        dec_all = dec_tok[:, :nd].t().contiguous()
+        tok_buf = torch.empty(B, dtype=torch.int32, device=dev)
         pos_buf = torch.full((B,), T, dtype=torch.int32, device=dev)
+        step_idx = torch.zeros(1, dtype=torch.long, device=dev)
+
+        def one_step():
+            torch.index_select(dec_all, 0, step_idx, out=tok_buf.view(1, B))
+            wm.wm_decode_batch(m, tok_buf, pos_buf, ck, cv, dlg, wsp)
+            pos_buf.add_(1)
+            step_idx.add_(1)
+
         side = torch.cuda.Stream()
         side.wait_stream(stream)
         with torch.cuda.stream(side):
-            wm.wm_decode_batch(m, tok_buf, pos_buf, ck, cv, dlg, wsp)
+            one_step()
         stream.wait_stream(side)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            wm.wm_decode_batch(m, tok_buf, pos_buf, ck, cv, dlg, wsp)
+            one_step()
         for _ in range(3):
+            pos_buf.fill_(T)
+            step_idx.zero_()
             graph.replay()
+        pos_buf.fill_(T)
+        step_idx.zero_()
         torch.cuda.synchronize()
         barrier(ws)
         d0.record(stream)
         for t in range(nd):
-            tok_buf.copy_(cols[t])
             graph.replay()
-            pos_buf += 1
         d1.record(stream)
         torch.cuda.synchronize()
         dms = max_over_ranks(d0.elapsed_time(d1), ws)
@@ -468,12 +482,24 @@ def run_ours(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def decode_step_bytes(s, B, pos):
+    """Bytes a decode step must move at least: every weight it multiplies by
+    (layer stack, LM head, router, channel projections; the B embedding rows),
+    the visible K and V entries of each layer's channel, and the new entries."""
+    Hd, kv = s.Hq * s.d, s.Hkv * s.d
+    layer = Hd * s.D + s.D * Hd + 2 * s.F * s.D + s.D * s.F + 2 * s.D + s.d
+    weights = s.L * layer + s.V * s.D + s.D + 2 * s.k * s.L * s.nR * s.D + 2 * s.k * kv * s.D
+    cache = s.L * B * 2 * kv * pos + 2 * B * s.k * kv
+    return 2 * (weights + B * s.D + cache)
+
+
 def run_kernel(args):
     """One kernel alone at 1.3B shapes, timed by the library's CUDA events on
     its stream (warm-up launches first; inputs above L2 size for the mixer)."""
     from cross_layer_kv_pool_b300 import wm
 
-    s = synth.HALF_1P3B.replace(V=1024)  # the pool and attention do not read the vocabulary
+    # the pool and attention do not read the vocabulary; a decode step does
+    s = synth.HALF_1P3B if args.kernel == "decode" else synth.HALF_1P3B.replace(V=1024)
     dev = torch.device("cuda", torch.cuda.current_device())
     m = wm.Model(s, synth.make_weights(s, seed=0, device=dev, gain_jitter=0.1))
     pk, pk_src = peaks()
@@ -515,6 +541,24 @@ def run_kernel(args):
         fp32_peak = 148 * 128 * 2 * 2.032e9 / 1e12  # FMA pipes at the maximum SM clock
         unit, peak, bound = "TFLOP/s", fp32_peak, "alu"
         desc = f"wm_pool_backward, {N} rows of the 1.3B pool, fp32 arithmetic"
+    elif args.kernel == "decode":
+        # one decode step of B sequences at position 2048 over a random prefix
+        B, T, Tmax = args.batch, 2048, 2304
+        ck, cv = m.new_cache(B, Tmax)
+        ck.copy_(synth.make_normal(tuple(ck.shape), 4, dev, 1.0, torch.bfloat16))
+        cv.copy_(synth.make_normal(tuple(cv.shape), 5, dev, 1.0, torch.bfloat16))
+        wsp = m.workspace(B, Tmax)
+        tok = synth.make_tokens(s, B, 1, seed=7, device=dev)[:, 0].contiguous()
+        pos = torch.full((B,), T, dtype=torch.int32, device=dev)
+        lg = torch.empty((B, s.V), dtype=torch.float32, device=dev)
+        kind = None
+
+        def call():
+            wm.wm_decode_batch(m, tok, pos, ck, cv, lg, wsp)
+        work = decode_step_bytes(s, B, T)
+        unit, peak, bound = "GB/s", pk["hbm_gbs"], "hbm"
+        desc = (f"wm_decode_batch, {B} sequences at position {T} of the 1.3B model "
+                "(weights and visible cache entries read once)")
     else:
         B, T, g, Tmax = args.batch, 2048, 16, 2048
         nq = T // g
@@ -539,10 +583,12 @@ def run_kernel(args):
     torch.cuda.synchronize()
     if kind is None:  # a whole entry point: events around the call on the current stream
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push("timed")
         e0.record()
         for _ in range(args.steps):
             call()
         e1.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / max(args.steps, 1)
     else:
