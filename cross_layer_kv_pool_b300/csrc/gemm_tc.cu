@@ -605,11 +605,12 @@ __device__ __forceinline__ void cluster_reduce(const Params& p, const float* red
     } else {
       for (int c = 4 * lane; c < BN && n0 + c < p.N; c += 128) {
         const uint32_t off = (uint32_t)(j * RS + c) * 4u;
-        float4 a[KS_MAX], b[DUAL ? KS_MAX : 1];
+        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 a[KS_MAX], b[KS_MAX];
 #pragma unroll
         for (int q = 0; q < KS_MAX; ++q) {
-          a[q] = q < ks ? ld_peer4(peer[q] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-          if constexpr (DUAL) b[q] = q < ks ? ld_peer4(peer[q] + off + BN * 4u) : make_float4(0.f, 0.f, 0.f, 0.f);
+          a[q] = q < ks ? ld_peer4(peer[q] + off) : z4;
+          b[q] = (DUAL && q < ks) ? ld_peer4(peer[q] + off + BN * 4u) : z4;
         }
         float4 g = a[0], u = b[0];
 #pragma unroll
@@ -725,8 +726,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      // Weight tiles of the first ring stages go out before the wait for the
-      // predecessor grid (its results are only read through A).
+      // Weight tiles of the first two ring stages go out before the wait for
+      // the predecessor grid (its results are only read through A). More
+      // measured slower on decode steps: A tiles issued after the wait queue
+      // behind the weight tiles still in flight.
+      constexpr int PRE_MAX = C::STAGES < 2 ? C::STAGES : 2;
       int pre = 0;
       if (p.b_const && blockIdx.x < p.total_tiles) {
         const long long ot = blockIdx.x / p.ksplit;
@@ -734,7 +738,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nt = (int)(ot % tiles_per_batch) % p.n_tiles;
         const int kb0 = (int)(blockIdx.x % p.ksplit) * p.kb_per;
         const int kb1 = min(p.num_kb, kb0 + p.kb_per);
-        for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+        for (int kb = kb0; kb < kb1 && pre < PRE_MAX; ++kb, ++pre) {
           uint8_t* sa = smem + pre * C::STAGE_BYTES;
           mbar_expect_tx(&full[pre], C::STAGE_BYTES);
           tma_load3(&tmB, &full[pre], sa + C::A_BYTES, kb * BK, nt * BN, bidx);

@@ -162,3 +162,34 @@ def test_decode_batch_out_of_range_position_flags():
     rl = O.decode_batch(ocfg(s), Wn, tok_h[ok], pos_h[ok], rk, rv)
     assert relerr(host(lg)[ok], rl) <= TOL["f32"]["logits"]
     assert np.array_equal(host(ck)[1], sk[1]) and np.array_equal(host(cv)[1], sv[1])
+
+
+def test_decode_batch_1p3b_widths_ragged():
+    """The 1.3B model's widths (8 layers, 8 channels), 8 sequences spread over
+    positions 1..299: cluster split-K products and the split-key attention
+    with sequences of different lengths, against the oracle."""
+    s = synth.HALF_1P3B.replace(L=8, k=8, V=2000)
+    m, Wn = model(s, seed=43, jitter=0.1)
+    B, Tmax = 8, 300
+    ck, cv = _random_cache(s, B, Tmax, 44)
+    pos_h = np.array([1, 17, 64, 129, 200, 255, 298, 299])
+    tok_h = np.random.default_rng(45).integers(0, s.V, size=B)
+    sk, sv = host(ck), host(cv)
+    ws = m.workspace(B, Tmax)
+    lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
+    wm.wm_decode_batch(m, _i32(tok_h), _i32(pos_h), ck, cv, lg, ws)
+    torch.cuda.synchronize()
+    assert wm.wm_check_flags(ws) == 0
+    oc = ocfg(s)
+    rk, rv = sk.copy(), sv.copy()
+    rl = O.decode_batch(oc, Wn, tok_h, pos_h, rk, rv)
+    pk, pv = sk.copy(), sv.copy()
+    pl = O.decode_batch(oc, perturbed(Wn, SPREAD_EPS), tok_h, pos_h, pk, pv)
+    rows = np.arange(B)
+    gk, gv = host(ck), host(cv)
+    got_kv = np.stack([gk[rows, :, :, pos_h], gv[rows, :, :, pos_h]])
+    ref_kv = np.stack([rk[rows, :, :, pos_h], rv[rows, :, :, pos_h]])
+    spread_kv = relerr(np.stack([pk[rows, :, :, pos_h], pv[rows, :, :, pos_h]]), ref_kv)
+    tol = TOL["bf16"]
+    assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl))
+    assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv)
