@@ -20,6 +20,12 @@ the C ABI (``wm_pool_mix`` on ``--rows`` token rows of the 1.3B pool, or
 one JSON line with its CUDA-event time and roofline fraction; the profiles
 under profiles/ capture these invocations.
 
+``--kernel decode`` times one decode step (``wm_decode_batch``, 64 sequences at
+position 2048) against the bytes it must move. ``--sweep convergence`` runs
+the fixed-point residual per pass of the prefill schedules g in {1, 4, 16, 64}
+on the full-cache small model. ``--workload half_small|full_small|tiny_fp32``
+runs the other configurations through the same step.
+
 Under torchrun each rank runs an independent replica on its own GPU (the
 path has no exchange step); rank 0 prints one JSON line.
 """
@@ -55,7 +61,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_1p3b",
-                    choices=["prefill_1p3b", "half_small", "full_small"])
+                    choices=["prefill_1p3b", "half_small", "full_small", "tiny_fp32"])
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--k", type=int, default=None, help="override the channel count k")
@@ -65,6 +71,9 @@ def parse():
     ap.add_argument("--rows", type=int, default=8192, help="--kernel mixer: token rows")
     ap.add_argument("--batch", type=int, default=64, help="--kernel attention: sequences")
     ap.add_argument("--group", type=int, default=15, help="--kernel attention: group index q")
+    ap.add_argument("--sweep", choices=["convergence"], default=None,
+                    help="fixed-point residual per pass for g in {1, 4, 16, 64} (full-small model)")
+    ap.add_argument("--passes", type=int, default=32, help="--sweep convergence: passes per g")
     ap.add_argument("--variant", choices=["feedback_free"], default=None,
                     help="time the feedback-free variant (k = L, one pass) at the workload's shape")
     ap.add_argument("--chunk", type=int, default=8,
@@ -473,7 +482,8 @@ def run_ours(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded tokens, N(0,0.02) weights)",
+        "vs_baseline": None, "dtype": "f32" if s.dtype == "f32" else "bf16",
+        "data": "synthetic (seeded tokens, N(0,0.02) weights)",
         "config": config_dict(args, wl), "e2e": e2e, "gpu_launches": gpu_launches,
         "roofline": roofline, "mixer": mixer, "attention": attention, "decode": decode,
         "cpu_baseline": cpu, "clocks": clk,
@@ -672,10 +682,61 @@ def run_variant(args):
         "cache_bytes": 2 * B * s.k * T * s.Hkv * s.d * 2}), flush=True)
 
 
+def run_convergence(args):
+    """Fixed-point convergence of the prefill schedules on the full-cache small
+    model (L=16, D=512, k=16, B=8, T=2048): for g in {1 (Jacobi), 4, 16, 64},
+    up to ``--passes`` whole passes from a zero cache, each followed by the
+    relative residual r_n = ||KV_n - KV_{n-1}||_F / ||KV_n||_F over the cache
+    and its CUDA-event time per sequence; then the passes (and milliseconds per
+    sequence) needed to reach r <= 1e-1, 3e-2 and 1e-2. Random weights: the
+    counts say how contractive this model is, not what a trained one needs."""
+    from cross_layer_kv_pool_b300 import wm
+
+    wl = synth.WORKLOADS["full_small"]
+    s, B, T = wl["shape"], wl["B"], wl["T"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    m = wm.Model(s, synth.make_weights(s, seed=0, device=dev))
+    tok = synth.make_tokens(s, B, T, seed=1, device=dev)
+    thresholds = (1e-1, 3e-2, 1e-2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    out = {}
+    for g in (1, 4, 16, 64):
+        ck, cv = m.new_cache(B, T)
+        wsp = m.workspace(wm.rows_for_pass(B, T, g), T)
+        pk, pv = ck.clone(), cv.clone()
+        r, ms = [], []
+        for n in range(args.passes):
+            torch.cuda.synchronize()
+            e0.record()
+            wm.wm_cyclic_pass(m, tok, g, ck, cv, wsp)
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1) / B)
+            num = (ck.float() - pk.float()).square().sum() + (cv.float() - pv.float()).square().sum()
+            den = ck.float().square().sum() + cv.float().square().sum()
+            r.append(float((num / den).sqrt()) if float(den) > 0 else 0.0)
+            pk.copy_(ck)
+            pv.copy_(cv)
+        if wm.wm_check_flags(wsp) != 0:
+            raise RuntimeError("device-side checks failed")
+        reach = {}
+        for thr in thresholds:
+            n = next((i + 1 for i, v in enumerate(r) if v <= thr), None)
+            reach[f"{thr:g}"] = None if n is None else {"passes": n, "ms_per_seq": sum(ms[:n])}
+        out[str(g)] = {"residual": r, "ms_per_seq_per_pass": statistics.mean(ms[1:] or ms),
+                       "reach": reach, "passes_for_exactness": -(-T // g)}
+        del ck, cv, pk, pv, wsp
+    print(json.dumps({"sweep": "convergence", "workload": "full_small (L=16, D=512, k=16, B=8, T=2048)",
+                      "data": "synthetic", "passes": args.passes, "schedules": out}), flush=True)
+
+
 def main():
     args = parse()
     if args.kernel:
         run_kernel(args)
+        return
+    if args.sweep == "convergence":
+        run_convergence(args)
         return
     if args.variant:
         run_variant(args)
