@@ -213,6 +213,25 @@ def cpu_sample(shape, rows: int, Wn, seed: int = 0):
     return time.perf_counter() - t0, rows, threads
 
 
+def cpu_decode_record(shape, pos: int, Tmax: int):
+    """The CPU oracle on one decode step of one sequence at ``pos`` (stack,
+    LM head and pool against a zero cache of Tmax positions)."""
+    import oracle.whitematter as O
+    from types import SimpleNamespace
+    import dataclasses
+    oc = SimpleNamespace(**dataclasses.asdict(shape))
+    oc.storage = "bf16"
+    Wn = oracle_weights(shape)
+    ck, cv = O.new_cache(oc, 1, Tmax)
+    tok = np.random.default_rng(0).integers(0, shape.V, size=1)
+    threads = torch.get_num_threads()
+    t0 = time.perf_counter()
+    O.decode_batch(oc, Wn, tok, np.array([pos]), ck, cv)
+    secs = time.perf_counter() - t0
+    return {"value": 1.0 / secs, "unit": "tok/s", "cores": threads, "kind": "oracle",
+            "sample": f"one decode step of one sequence at position {pos} (fp64 NumPy, {secs:.1f} s)"}
+
+
 def cpu_baseline_record(shape, passes: int, rows: int):
     secs, n, threads = cpu_sample(shape, rows, oracle_weights(shape))
     tok_s = n / secs / passes
@@ -426,6 +445,8 @@ def run_ours(args, ws, rank, local):
                   "eager": {"value": ws * B * nd / (dms_eager / 1e3), "ms_per_step": dms_eager / nd},
                   "peak_cache_bytes": cache_bytes,
                   "cache_bytes_L_channels": cache_bytes // s.k * s.L, "kernels": dtr}
+        if rank == 0 and not args.no_cpu_baseline:
+            decode["cpu_baseline"] = cpu_decode_record(s, T, Tmax)
     if wm.wm_check_flags(wsp) != 0:
         raise RuntimeError("device-side checks failed")
 
