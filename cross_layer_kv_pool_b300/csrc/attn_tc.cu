@@ -1,29 +1,34 @@
 // Strictly causal channel attention on tcgen05 tensor cores (bf16, prefill).
 //
-// A CTA owns one KV head and two tiles of up to 128 query rows (M) each: R
-// consecutive token rows of one sequence per tile times the G = Hq/Hkv query
-// heads that read this KV head, packed in (row, head) order. A Q tile is one
-// 3-D TMA box {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly
-// in that order. Keys and values stream in blocks of 128 positions of the
-// channel and serve both tiles.
+// A CTA owns one KV head and one tile of up to 128 query rows (M): R
+// consecutive token rows of one sequence times the G = Hq/Hkv query heads
+// that read this KV head, packed in (row, head) order. The Q tile is one 3-D
+// TMA box {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly in
+// that order. Keys and values stream in blocks of 128 positions of the channel.
 //
-//   warp 0       TMA: both Q tiles once, then K and V blocks into two-stage rings;
-//   warp 1       tcgen05.mma, per key block j and tile t:
-//                  S_t = Q_t K_j^T  (K-major smem operands, fp32 in TMEM),
-//                  O_t += P_t V_j   (P from TMEM, V an MN-major smem operand),
-//                issued as O_0, S_0(j+1), O_1, S_1(j+1) so that one tile's
-//                MMAs run while the other tile's softmax works;
-//   warps 4-11   one softmax warpgroup per tile, one thread per query row
-//                (TMEM lane): the row's 128 scores are read once; keys s >= pos
-//                are masked only in partly visible blocks; P = 2^(s*scale -
-//                base) goes back into TMEM as bf16 pairs over S's first
-//                columns. The base is raised lazily, only when a row maximum
-//                exceeds it by more than 8 (P stays below 2^8); then the
-//                thread rescales its row of O in TMEM. O is read once, at the
-//                end. The control warpgroup gives registers to the softmax
+//   warp 0       TMA: the Q tile once, then K and V blocks into two-stage rings;
+//   warp 1       tcgen05.mma, per key block j:
+//                  S(j) = Q K_j^T   (K-major smem operands, fp32 into one of
+//                                    two TMEM buffers),
+//                  O += P(j) V_j    (P from TMEM, V an MN-major smem operand);
+//                issued as O(j), S(j + 2), so that S(j + 1) is ready while
+//                the softmax still works on block j;
+//   warps 4-11   two softmax warpgroups, both one thread per query row (TMEM
+//                lane): warpgroup w takes keys 64w .. 64w + 63 of every block.
+//                The two threads of a row swap their maxima through shared
+//                memory (a 64-thread named barrier per lane quarter), then
+//                each writes P = 2^(s*scale - base) for its keys back into
+//                TMEM as bf16 pairs over the S buffer's first 64 columns and
+//                keeps its own part of the row sum. The base is raised lazily,
+//                only when a row maximum exceeds it by more than 8 (P stays
+//                below 2^8); then each thread rescales its half of the row's O
+//                in TMEM. O is read once, at the end, each thread its half.
+//                The control warpgroup gives registers to the softmax
 //                warpgroups (setmaxnreg).
 // Every wait is bounded: on timeout the CTA raises FLAG_TIMEOUT, stops issuing,
-// drains its copies and MMAs, frees TMEM and returns.
+// drains its copies and MMAs, frees TMEM and returns. The two warps that share
+// a lane quarter decide together whether to stop, so neither is left at a
+// named barrier.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -32,7 +37,8 @@
 namespace wm {
 namespace atc {
 
-constexpr int BQ = 128, BKEY = 128, NTHREADS = 384;  // 3 warpgroups: control, tile 0, tile 1
+constexpr int BQ = 128, BKEY = 128, NTHREADS = 384;  // 3 warpgroups: control, softmax x2
+constexpr int NST = 2;                                // K and V ring stages
 // Register split: 384 threads x 168 at launch = 64512; the control warpgroup
 // keeps 88, each softmax warpgroup takes 208: 128 x 88 + 256 x 208 = 64512
 // (per SM sub-partition, one control and two softmax warps: 32 x 504 <= 16384).
@@ -241,15 +247,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 
 template <int HD>
 struct Smem {
-  static constexpr int QB = BQ * HD * 2;     // one Q tile
+  static constexpr int QB = BQ * HD * 2;     // the Q tile
   static constexpr int KB = BKEY * HD * 2;   // one K (or V) block
-  static constexpr int OFF_Q = 0;                    // 2 tiles
-  static constexpr int OFF_K = OFF_Q + 2 * QB;       // 2 stages
-  static constexpr int OFF_V = OFF_K + 2 * KB;       // 2 stages
-  static constexpr int OFF_BAR = OFF_V + 2 * KB;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;          // NST stages
+  static constexpr int OFF_V = OFF_K + NST * KB;    // NST stages
+  static constexpr int OFF_X = OFF_V + NST * KB;    // max exchange [2][2][128], sums [2][128]
+  static constexpr int OFF_BAR = OFF_X + 6 * 128 * 4;
   static constexpr int BYTES = 1024 + OFF_BAR + 256;
-  // per tile t: S_t (128 fp32 columns; P_t, bf16 pairs, overwrites its first
-  // 64 after S_t is read) at t * 256, O_t (HD columns) at t * 256 + 128
+  // S buffers b = 0, 1 (128 fp32 columns each; P, bf16 pairs, overwrites the
+  // first 64 after S is read) at b * 128, O (HD columns) at 256
   static constexpr int TMEM_COLS = 512;
 };
 
@@ -263,6 +270,21 @@ __device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
       : "memory");
 }
 
+// Named barrier ``id`` over ``n`` threads; the AND of ``v`` over them.
+__device__ __forceinline__ void bar_pair(int id) {
+  asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+__device__ __forceinline__ bool bar_pair_and(int id, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
 template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -272,50 +294,58 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   using SM = Smem<HD>;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  float* xmax = (float*)(sm + SM::OFF_X);   // [block parity][warpgroup][row]
+  float* xsum = xmax + 4 * 128;             // [warpgroup][row]
   uint64_t* bar = (uint64_t*)(sm + SM::OFF_BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;    // [2]
-  uint64_t* k_empty = bar + 3;   // [2]
-  uint64_t* v_full = bar + 5;    // [2]
-  uint64_t* v_empty = bar + 7;   // [2]
-  uint64_t* s_full = bar + 9;    // [2] per tile: S_t of the current block is in TMEM
-  uint64_t* p_full = bar + 11;   // [2] per tile: P_t written (4 warps arrive)
-  uint64_t* pv_done = bar + 13;  // [2] per tile: O_t += P_t V_j complete
-  uint64_t* mma_done = bar + 15;
-  uint32_t* tmem_holder = (uint32_t*)(bar + 16);
+  uint64_t* k_full = bar + 1;          // [NST]
+  uint64_t* k_empty = k_full + NST;    // [NST]
+  uint64_t* v_full = k_empty + NST;    // [NST]
+  uint64_t* v_empty = v_full + NST;    // [NST]
+  uint64_t* s_full = v_empty + NST;    // [buffer]: S(j) is in TMEM
+  uint64_t* p_full = s_full + 2;       // [buffer]: P(j) written (8 warps arrive)
+  uint64_t* pv_done = p_full + 2;      // O += P(j) V_j complete
+  uint64_t* mma_done = pv_done + 1;
+  uint32_t* tmem_holder = (uint32_t*)(mma_done + 1);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
   int* s_meta = (int*)(tmem_holder + 2);  // [0] = number of key blocks, [1] = sequence
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hk = blockIdx.y;
-  // token rows of this CTA (two tiles of rpt rows each): late positions first
-  const int span = 2 * p.rpt;
-  const int tps = (p.nq + span - 1) / span;
+  // token rows of this CTA: late positions first
+  const int tps = (p.nq + p.rpt - 1) / p.rpt;
   const int b = blockIdx.x / tps, t = tps - 1 - blockIdx.x % tps;
-  const int r0 = b * p.nq + t * span;
-  const int rend = (b + 1) * p.nq;
+  const int r0 = b * p.nq + t * p.rpt;
+  const int nrows = max(0, min(p.rpt, (b + 1) * p.nq - r0));
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&pv_done[i], 1);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 8);
+    }
+    mbar_init(pv_done, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
-    // key blocks: enough for the largest visible position of the CTA
-    int maxp = 0;
-    for (int r = r0; r < min(r0 + span, rend); ++r) maxp = max(maxp, p.pos[r]);
-    maxp = min(maxp, p.Tmax);
-    s_meta[0] = (maxp + BKEY - 1) / BKEY;
     s_meta[1] = p.seq[r0];
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 2) {
+    // key blocks: enough for the largest visible position of the CTA (one
+    // load per lane, then a warp maximum)
+    int maxp = 0;
+    for (int r = r0 + lane; r < r0 + nrows; r += 32) maxp = max(maxp, p.pos[r]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+    maxp = min(maxp, p.Tmax);
+    if (lane == 0) s_meta[0] = (maxp + BKEY - 1) / BKEY;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -338,18 +368,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       // ---------------- TMA producer ----------------
       bool ok = true;
-      // each tile's box fills R*G rows of each 128-row operand chunk; rows
-      // past them feed only accumulator rows that are never read back
-      mbar_expect_tx(q_full, (uint32_t)(2 * (HD / 64) * p.G * p.rpt * 128));
-      for (int tt = 0; tt < 2; ++tt)
-        for (int c = 0; c < HD / 64; ++c)
-          tma3(&tmQ, q_full, sm + SM::OFF_Q + tt * SM::QB + c * BQ * 128, c * 64, hk * p.G,
-               r0 + tt * p.rpt);
+      // the box fills R*G rows of each 128-row operand chunk; rows past them
+      // feed only accumulator rows that are never read back
+      mbar_expect_tx(q_full, (uint32_t)((HD / 64) * p.G * p.rpt * 128));
+      for (int c = 0; c < HD / 64; ++c)
+        tma3(&tmQ, q_full, sm + SM::OFF_Q + c * BQ * 128, c * 64, hk * p.G, r0);
       const int zc = ((sq * p.k) + p.channel) * p.Hkv + hk;
       uint32_t used = 0, lastk = 0;
       for (int j = 0; j < nkb && ok; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
+        const int s = j % NST;
+        const uint32_t ph = (j / NST) & 1;
         if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
         mbar_expect_tx(&k_full[s], (uint32_t)SM::KB);
         for (int c = 0; c < HD / 64; ++c)
@@ -367,7 +395,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       volatile int no_abort = 0;
       mbar_wait(q_full, 0, &no_abort);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NST; ++s)
         if (used & (1u << s)) {
           mbar_wait(&k_full[s], (lastk >> s) & 1, &no_abort);
           mbar_wait(&v_full[s], (lastk >> s) & 1, &no_abort);
@@ -377,59 +405,44 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       // tcgen05.mma operations of this thread execute in issue order, so
-      // S_t(j + 1) (issued after O_t += P_t(j) V_j) cannot overwrite P_t(j)
-      // before the product has read it.
+      // S(j + 2) (issued after O += P(j) V_j, into the same buffer) cannot
+      // overwrite P(j) before the product has read it.
       bool ok = mbar_wait(q_full, 0, abort_flag);
       fence_after();
       const uint32_t sQ = su32(sm + SM::OFF_Q);
       constexpr uint32_t id_qk = idesc(BKEY, false);
       constexpr uint32_t id_pv = idesc(HD, true);
-      auto qk = [&](int tt, int j) {
-        const uint32_t sK = su32(sm + SM::OFF_K + (j & 1) * SM::KB);
-        const uint32_t q = sQ + tt * SM::QB;
+      auto qk = [&](int j) -> bool {
+        if (!mbar_wait(&k_full[j % NST], (j / NST) & 1, abort_flag)) return false;
+        fence_after();
+        const uint32_t sK = su32(sm + SM::OFF_K + (j % NST) * SM::KB);
 #pragma unroll
         for (int k16 = 0; k16 < HD / 16; ++k16) {
           const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
           const uint32_t offk = (k16 >> 2) * BKEY * 128 + (k16 & 3) * 32;
-          umma(tmem + tt * 256, sdesc(q + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
+          umma(tmem + (j & 1) * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
         }
-        commit(&s_full[tt]);
-      };
-      auto pv = [&](int tt, int j) -> bool {
-        if (!mbar_wait(&p_full[tt], j & 1, abort_flag)) return false;
-        fence_after();
-        const uint32_t sV = su32(sm + SM::OFF_V + (j & 1) * SM::KB);
-#pragma unroll
-        for (int k16 = 0; k16 < BKEY / 16; ++k16)
-          umma_ts(tmem + tt * 256 + 128, tmem + tt * 256 + k16 * 8,
-                  sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, (j > 0 || k16 > 0) ? 1u : 0u);
-        commit(&pv_done[tt]);
+        commit(&s_full[j & 1]);
+        commit(&k_empty[j % NST]);
         return true;
       };
-      if (ok && nkb > 0) {
-        ok = mbar_wait(&k_full[0], 0, abort_flag);
-        if (ok) {
-          fence_after();
-          qk(0, 0);
-          qk(1, 0);
-          commit(&k_empty[0]);
-        }
-      }
+      auto pv = [&](int j) -> bool {
+        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag)) return false;
+        fence_after();
+        const uint32_t sV = su32(sm + SM::OFF_V + (j % NST) * SM::KB);
+#pragma unroll
+        for (int k16 = 0; k16 < BKEY / 16; ++k16)
+          umma_ts(tmem + 256, tmem + (j & 1) * 128 + k16 * 8,
+                  sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, (j > 0 || k16 > 0) ? 1u : 0u);
+        commit(pv_done);
+        return true;
+      };
+      for (int j = 0; j < 2 && j < nkb && ok; ++j) ok = qk(j);
       for (int j = 0; j < nkb && ok; ++j) {
-        const bool next = j + 1 < nkb;
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
-        if (!pv(0, j)) { ok = false; break; }
-        if (next) {
-          if (!mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag)) { ok = false; break; }
-          fence_after();
-          qk(0, j + 1);
-        }
-        if (!pv(1, j)) { ok = false; break; }
-        commit(&v_empty[j & 1]);
-        if (next) {
-          qk(1, j + 1);
-          commit(&k_empty[(j + 1) & 1]);
-        }
+        if (!mbar_wait(&v_full[j % NST], (j / NST) & 1, abort_flag)) { ok = false; break; }
+        if (!pv(j)) { ok = false; break; }
+        commit(&v_empty[j % NST]);
+        if (j + 2 < nkb && !qk(j + 2)) { ok = false; break; }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -442,22 +455,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_SOFTMAX));
-    // ------------- softmax warps: tile tt, one thread per query row -------------
-    const int tt = (warp - 4) >> 2;
+    // ------------- softmax warps: keys 64wg .. 64wg + 63 of each block, one
+    // thread per query row
+    constexpr int HK = BKEY / 2;         // keys per thread and block
+    const int wg = (warp - 4) >> 2;
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+    const int pair = 1 + quarter;        // named barrier of the two warps of this quarter
     const int m = quarter * 32 + lane;   // query row of the tile = TMEM lane
-    const int rt0 = r0 + tt * p.rpt;
-    const int mrows = max(0, min(p.rpt, rend - rt0)) * p.G;
+    const int mrows = nrows * p.G;
     const bool valid = m < mrows;
-    const int r = rt0 + (valid ? m / p.G : 0);
+    const int r = r0 + (valid ? m / p.G : 0);
     const int h = hk * p.G + (valid ? m % p.G : 0);
     int ps = valid ? p.pos[r] : 0;
     if (valid && (ps < 0 || ps >= p.Tmax)) {
-      atomicOr(p.flags, FLAG_BAD_POS);
+      if (wg == 0) atomicOr(p.flags, FLAG_BAD_POS);
       ps = 0;
     }
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16) + tt * 256;
-    float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and row sum
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and this half's row sum
     bool ok = true;
     auto warp_wait = [&](uint64_t* bb, uint32_t parity) -> bool {
       int w = 1;
@@ -466,31 +481,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     const float sl2 = p.scale_log2;
     for (int j = 0; j < nkb && ok; ++j) {
-      if (!warp_wait(&s_full[tt], j & 1)) { ok = false; break; }
+      if (!bar_pair_and(pair, warp_wait(&s_full[j & 1], (j >> 1) & 1))) { ok = false; break; }
       fence_after();
-      // The row's 128 scores, one TMEM load wait.
-      const int nvis = min(max(ps - j * BKEY, 0), BKEY);
-      float sv[BKEY];
+      const uint32_t s_base = lane_base + (j & 1) * 128;
+      // This thread's HK scores, one TMEM load wait.
+      const int nvis = min(max(ps - j * BKEY - HK * wg, 0), HK);
+      float sv[HK];
       {
         uint32_t* ru = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
-        for (int c = 0; c < BKEY / 32; ++c) tmem_ld32_nw(lane_base + c * 32, ru + 32 * c);
+        for (int c = 0; c < HK / 32; ++c) tmem_ld32_nw(s_base + HK * wg + c * 32, ru + 32 * c);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
       }
-      if (!__all_sync(0xffffffffu, nvis == BKEY)) {
+      if (!__all_sync(0xffffffffu, nvis == HK)) {
 #pragma unroll
-        for (int i = 0; i < BKEY; ++i)
+        for (int i = 0; i < HK; ++i)
           if (i >= nvis) sv[i] = -INFINITY;
       }
       float mx;
       {
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < BKEY; i += 8)
+        for (int i = 0; i < HK; i += 8)
 #pragma unroll
           for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], sv[i + 2 * q], sv[i + 2 * q + 1]);
         mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;  // scaled log2 units
       }
+      // the row maximum over both halves (both threads then take the same
+      // decisions below); the slot alternates with the block parity
+      float* xm = xmax + (j & 1) * 256;
+      xm[wg * 128 + m] = mx;
+      bar_pair(pair);
+      mx = fmaxf(mx, xm[(wg ^ 1) * 128 + m]);
       float corr = 1.f;
       bool resc = false;
       if (mx > mrun + 8.f) {
@@ -503,28 +525,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mrun = mx;
       }
       const float base = mrun == -INFINITY ? 0.f : mrun;
-      if (__any_sync(0xffffffffu, resc)) {
-        // O_t holds the products of blocks < j once the previous one landed
-        if (!warp_wait(&pv_done[tt], (j - 1) & 1)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, resc)) {  // the partner warp holds the same rows
+        // O holds the products of blocks < j once the previous one landed
+        if (!bar_pair_and(pair, warp_wait(pv_done, (j - 1) & 1))) { ok = false; break; }
         fence_after();
         l *= corr;
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
+        for (int c = 0; c < HD / 64; ++c) {
           uint32_t ro[32];
-          tmem_ld32_nw(lane_base + 128 + c * 32, ro);
+          const uint32_t oa = lane_base + 256 + (HD / 2) * wg + c * 32;
+          tmem_ld32_nw(oa, ro);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
           for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * corr);
-          tmem_st32(lane_base + 128 + c * 32, ro);
+          tmem_st32(oa, ro);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      // P = 2^(s * scale - base) as bf16 pairs over S_t's first 64 columns (16
-      // at a time); row sum in two packed partial sums.
+      // P = 2^(s * scale - base) as bf16 pairs over the buffer's columns
+      // 32wg .. 32wg + 31 (16 at a time; the partner read its scores there
+      // before the barrier above); this half's row sum in two packed sums.
       const unsigned long long sc2 = f2pack(sl2, sl2), nb2 = f2pack(-base, -base);
       unsigned long long rs2[2] = {0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < BKEY / 32; ++c) {
+      for (int c = 0; c < HK / 32; ++c) {
         uint32_t pw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -536,7 +560,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
           pw[e] = *reinterpret_cast<uint32_t*>(&hh);
         }
-        tmem_st16(lane_base + 16 * c, pw);
+        tmem_st16(s_base + (HK / 2) * wg + 16 * c, pw);
       }
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       {
@@ -547,11 +571,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[tt]);
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
     }
     const bool have_o = ok && nkb > 0;
     if (have_o) {
-      if (!warp_wait(&pv_done[tt], (nkb - 1) & 1)) ok = false;
+      if (!bar_pair_and(pair, warp_wait(pv_done, (nkb - 1) & 1))) ok = false;
       else fence_after();
     }
     if (!ok) {
@@ -560,13 +584,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         atomicOr(p.flags, FLAG_TIMEOUT);
       }
     } else {
-      // O / l, 32 dims at a time (the TMEM loads are warp-collective)
+      // the row sum over both halves, then O / l, this thread's HD/2 dims
+      xsum[wg * 128 + m] = l;
+      bar_pair(pair);
+      l += xsum[(wg ^ 1) * 128 + m];
       const float inv = (valid && ps > 0 && l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD;
+      __nv_bfloat16* dst = (__nv_bfloat16*)p.out + ((long long)r * p.Hq + h) * HD + (HD / 2) * wg;
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
+      for (int c = 0; c < HD / 64; ++c) {
         float o[32];
-        if (have_o) tmem_ld32(lane_base + 128 + c * 32, o);
+        if (have_o) tmem_ld32(lane_base + 256 + (HD / 2) * wg + c * 32, o);
         else
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -624,10 +651,9 @@ template <int HD>
 cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
   using SM = Smem<HD>;
   const int G = a.Hq / a.Hkv;
-  // rows per tile: a full 128-row tile, or half of a short sequence's rows so
-  // that both tiles of the CTA have work
+  // rows per tile: a full 128-row tile, or a short sequence's rows
   int rpt = BQ / G;
-  if (2 * rpt > nq) rpt = (nq + 1) / 2;
+  if (rpt > nq) rpt = nq;
   CUtensorMap mq, mk, mv;
   // q as [N][Hq][HD]: box {64 dims, G heads, rpt rows}
   if (!map3(&mq, a.q, HD, a.Hq, a.N, (cuuint64_t)HD * 2, (cuuint64_t)a.Hq * HD * 2, 64, G, rpt))
@@ -646,7 +672,7 @@ cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
   p.k = a.k; p.channel = a.channel; p.B = a.B;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
   const int B = a.N / nq;
-  const int tiles = B * ((nq + 2 * rpt - 1) / (2 * rpt));
+  const int tiles = B * ((nq + rpt - 1) / rpt);
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES);
   if (e != cudaSuccess) return e;
