@@ -51,8 +51,35 @@ struct Params {
   void* out;          // [N][Hq][HD] bf16
   uint32_t* flags;
   int N, Hq, Hkv, G, rpt, nq, Tmax, k, channel, B;
+  int nseq, tps, tiles;  // sequences of the call, tiles per sequence, all tiles (x KV heads)
   float scale_log2;   // log2(e) / sqrt(d)
 };
+
+// Tile ``idx`` of the persistent schedule: tiles with the latest positions
+// (the most keys) first, then sequence, then KV head.
+struct Tile {
+  int b, hk, r0, nrows, sq, nkb;
+  bool seq_ok;
+};
+// Warp-collective (every lane gets the same result).
+__device__ __forceinline__ Tile tile_of(const Params& p, int idx, int lane) {
+  Tile tl;
+  const int per_t = p.nseq * p.Hkv;
+  const int t = p.tps - 1 - idx / per_t, rem = idx % per_t;
+  tl.b = rem / p.Hkv;
+  tl.hk = rem % p.Hkv;
+  tl.r0 = tl.b * p.nq + t * p.rpt;
+  tl.nrows = max(0, min(p.rpt, (tl.b + 1) * p.nq - tl.r0));
+  int maxp = 0;
+  for (int r = tl.r0 + lane; r < tl.r0 + tl.nrows; r += 32) maxp = max(maxp, p.pos[r]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
+  maxp = min(maxp, p.Tmax);
+  tl.sq = p.seq[tl.r0];
+  tl.seq_ok = tl.sq >= 0 && tl.sq < p.B;
+  tl.nkb = tl.seq_ok ? (maxp + BKEY - 1) / BKEY : 0;  // an invalid sequence reads no keys
+  return tl;
+}
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -247,10 +274,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 
 template <int HD>
 struct Smem {
-  static constexpr int QB = BQ * HD * 2;     // the Q tile
+  static constexpr int QB = BQ * HD * 2;     // one Q tile
   static constexpr int KB = BKEY * HD * 2;   // one K (or V) block
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + QB;          // NST stages
+  static constexpr int OFF_Q = 0;                   // 2 tiles (the next one loads early)
+  static constexpr int OFF_K = OFF_Q + 2 * QB;      // NST stages
   static constexpr int OFF_V = OFF_K + NST * KB;    // NST stages
   static constexpr int OFF_X = OFF_V + NST * KB;    // max exchange [2][2][128], sums [2][128]
   static constexpr int OFF_BAR = OFF_X + 6 * 128 * 4;
@@ -270,7 +297,7 @@ __device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b,
       : "memory");
 }
 
-// Named barrier ``id`` over ``n`` threads; the AND of ``v`` over them.
+// Named barrier ``id`` over the 64 threads of two warps; the AND of ``v``.
 __device__ __forceinline__ void bar_pair(int id) {
   asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
 }
@@ -285,6 +312,10 @@ __device__ __forceinline__ bool bar_pair_and(int id, bool v) {
   return r != 0;
 }
 
+// Persistent: CTA c takes tiles c, c + gridDim.x, ... The key blocks of all
+// its tiles form one sequence (counter gb) that drives the K/V ring and the
+// S/P buffers, so the next tile's Q, first K/V blocks and first two S
+// products proceed while the softmax warps finish the current tile.
 template <int HD>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -297,55 +328,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   float* xmax = (float*)(sm + SM::OFF_X);   // [block parity][warpgroup][row]
   float* xsum = xmax + 4 * 128;             // [warpgroup][row]
   uint64_t* bar = (uint64_t*)(sm + SM::OFF_BAR);
-  uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;          // [NST]
+  uint64_t* q_full = bar + 0;          // [Q buffer]
+  uint64_t* q_empty = bar + 2;         // [Q buffer]: the tile's S products are done
+  uint64_t* k_full = bar + 4;          // [NST]
   uint64_t* k_empty = k_full + NST;    // [NST]
   uint64_t* v_full = k_empty + NST;    // [NST]
   uint64_t* v_empty = v_full + NST;    // [NST]
-  uint64_t* s_full = v_empty + NST;    // [buffer]: S(j) is in TMEM
-  uint64_t* p_full = s_full + 2;       // [buffer]: P(j) written (8 warps arrive)
-  uint64_t* pv_done = p_full + 2;      // O += P(j) V_j complete
-  uint64_t* mma_done = pv_done + 1;
+  uint64_t* s_full = v_empty + NST;    // [buffer]: S of block gb is in TMEM
+  uint64_t* p_full = s_full + 2;       // [buffer]: P of block gb written (8 warps arrive)
+  uint64_t* pv_done = p_full + 2;      // O += P V of block gb complete
+  uint64_t* o_free = pv_done + 1;      // the softmax warps have read the tile's O (8 arrive)
+  uint64_t* mma_done = o_free + 1;
   uint32_t* tmem_holder = (uint32_t*)(mma_done + 1);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
-  int* s_meta = (int*)(tmem_holder + 2);  // [0] = number of key blocks, [1] = sequence
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int hk = blockIdx.y;
-  // token rows of this CTA: late positions first
-  const int tps = (p.nq + p.rpt - 1) / p.rpt;
-  const int b = blockIdx.x / tps, t = tps - 1 - blockIdx.x % tps;
-  const int r0 = b * p.nq + t * p.rpt;
-  const int nrows = max(0, min(p.rpt, (b + 1) * p.nq - r0));
-
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 8);
+    }
     for (int i = 0; i < NST; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
-    }
     mbar_init(pv_done, 1);
+    mbar_init(o_free, 8);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
-    s_meta[1] = p.seq[r0];
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (warp == 2) {
-    // key blocks: enough for the largest visible position of the CTA (one
-    // load per lane, then a warp maximum)
-    int maxp = 0;
-    for (int r = r0 + lane; r < r0 + nrows; r += 32) maxp = max(maxp, p.pos[r]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) maxp = max(maxp, __shfl_xor_sync(0xffffffffu, maxp, o));
-    maxp = min(maxp, p.Tmax);
-    if (lane == 0) s_meta[0] = (maxp + BKEY - 1) / BKEY;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -358,43 +374,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
-  const int sq = s_meta[1];
-  const bool seq_ok = sq >= 0 && sq < p.B;
-  const int nkb = seq_ok ? s_meta[0] : 0;  // an invalid sequence reads no keys
-  if (!seq_ok && threadIdx.x == 0) atomicOr(p.flags, FLAG_BAD_SEQ);
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
   if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      bool ok = true;
-      // the box fills R*G rows of each 128-row operand chunk; rows past them
-      // feed only accumulator rows that are never read back
-      mbar_expect_tx(q_full, (uint32_t)((HD / 64) * p.G * p.rpt * 128));
-      for (int c = 0; c < HD / 64; ++c)
-        tma3(&tmQ, q_full, sm + SM::OFF_Q + c * BQ * 128, c * 64, hk * p.G, r0);
-      const int zc = ((sq * p.k) + p.channel) * p.Hkv + hk;
-      uint32_t used = 0, lastk = 0;
-      for (int j = 0; j < nkb && ok; ++j) {
-        const int s = j % NST;
-        const uint32_t ph = (j / NST) & 1;
-        if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-        mbar_expect_tx(&k_full[s], (uint32_t)SM::KB);
-        for (int c = 0; c < HD / 64; ++c)
-          tma3(&tmK, &k_full[s], sm + SM::OFF_K + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
-        if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-        mbar_expect_tx(&v_full[s], (uint32_t)SM::KB);
-        for (int c = 0; c < HD / 64; ++c)
-          tma3(&tmV, &v_full[s], sm + SM::OFF_V + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
-        used |= 1u << s;
-        lastk = (lastk & ~(1u << s)) | (ph << s);
+    // ---------------- TMA producer (lane 0; the warp computes tile metadata) ----------------
+    bool ok = true;
+    int gb = 0, it = 0;
+    uint32_t used = 0, lastk = 0;
+    for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
+      const Tile tl = tile_of(p, idx, lane);
+      if (lane == 0) {
+        if (!tl.seq_ok) atomicOr(p.flags, FLAG_BAD_SEQ);
+        const int qb = it & 1;
+        if (!mbar_wait(&q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag)) ok = false;
+        if (ok) {
+          // the box fills R*G rows of each 128-row operand chunk; rows past
+          // them feed only accumulator rows that are never read back
+          mbar_expect_tx(&q_full[qb], (uint32_t)((HD / 64) * p.G * p.rpt * 128));
+          for (int c = 0; c < HD / 64; ++c)
+            tma3(&tmQ, &q_full[qb], sm + SM::OFF_Q + qb * SM::QB + c * BQ * 128, c * 64,
+                 tl.hk * p.G, tl.r0);
+        }
+        const int zc = ((tl.sq * p.k) + p.channel) * p.Hkv + tl.hk;
+        for (int j = 0; j < tl.nkb && ok; ++j, ++gb) {
+          const int s = gb % NST;
+          const uint32_t ph = (gb / NST) & 1;
+          if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(&k_full[s], (uint32_t)SM::KB);
+          for (int c = 0; c < HD / 64; ++c)
+            tma3(&tmK, &k_full[s], sm + SM::OFF_K + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
+          if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(&v_full[s], (uint32_t)SM::KB);
+          for (int c = 0; c < HD / 64; ++c)
+            tma3(&tmV, &v_full[s], sm + SM::OFF_V + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
+          used |= 1u << s;
+          lastk = (lastk & ~(1u << s)) | (ph << s);
+        }
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
         atomicOr(p.flags, FLAG_TIMEOUT);
       }
+      // Drain: every issued copy has landed before the CTA may exit.
       volatile int no_abort = 0;
-      mbar_wait(q_full, 0, &no_abort);
+      for (int q = 0; q < 2 && q < it; ++q) mbar_wait(&q_full[(it - 1 - q) & 1], ((it - 1 - q) >> 1) & 1, &no_abort);
       for (int s = 0; s < NST; ++s)
         if (used & (1u << s)) {
           mbar_wait(&k_full[s], (lastk >> s) & 1, &no_abort);
@@ -402,48 +428,72 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      // tcgen05.mma operations of this thread execute in issue order, so
-      // S(j + 2) (issued after O += P(j) V_j, into the same buffer) cannot
-      // overwrite P(j) before the product has read it.
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      fence_after();
-      const uint32_t sQ = su32(sm + SM::OFF_Q);
-      constexpr uint32_t id_qk = idesc(BKEY, false);
-      constexpr uint32_t id_pv = idesc(HD, true);
-      auto qk = [&](int j) -> bool {
-        if (!mbar_wait(&k_full[j % NST], (j / NST) & 1, abort_flag)) return false;
+    // ---------------- MMA issuer (lane 0) ----------------
+    // tcgen05.mma operations of this thread execute in issue order, so
+    // S(gb + 2) (issued after O += P(gb) V, into the same buffer) cannot
+    // overwrite P(gb) before the product has read it.
+    bool ok = true;
+    int gb = 0, it = 0, o_waited = 0;
+    constexpr uint32_t id_qk = idesc(BKEY, false);
+    constexpr uint32_t id_pv = idesc(HD, true);
+    for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
+      const Tile tl = tile_of(p, idx, lane);
+      if (lane == 0) {
+        const int qb = it & 1;
+        const uint32_t sQ = su32(sm + SM::OFF_Q + qb * SM::QB);
+        if (!mbar_wait(&q_full[qb], (it >> 1) & 1, abort_flag)) ok = false;
         fence_after();
-        const uint32_t sK = su32(sm + SM::OFF_K + (j % NST) * SM::KB);
+        const int g0 = gb;  // first block of this tile
+        auto qk = [&](int j) -> bool {
+          const int g = g0 + j;
+          if (!mbar_wait(&k_full[g % NST], (g / NST) & 1, abort_flag)) return false;
+          fence_after();
+          const uint32_t sK = su32(sm + SM::OFF_K + (g % NST) * SM::KB);
 #pragma unroll
-        for (int k16 = 0; k16 < HD / 16; ++k16) {
-          const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
-          const uint32_t offk = (k16 >> 2) * BKEY * 128 + (k16 & 3) * 32;
-          umma(tmem + (j & 1) * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
+          for (int k16 = 0; k16 < HD / 16; ++k16) {
+            const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
+            const uint32_t offk = (k16 >> 2) * BKEY * 128 + (k16 & 3) * 32;
+            umma(tmem + (g & 1) * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
+          }
+          commit(&s_full[g & 1]);
+          commit(&k_empty[g % NST]);
+          return true;
+        };
+        auto pv = [&](int j) -> bool {
+          const int g = g0 + j;
+          if (!mbar_wait(&p_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
+          fence_after();
+          const uint32_t sV = su32(sm + SM::OFF_V + (g % NST) * SM::KB);
+#pragma unroll
+          for (int k16 = 0; k16 < BKEY / 16; ++k16)
+            umma_ts(tmem + 256, tmem + (g & 1) * 128 + k16 * 8,
+                    sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, (j > 0 || k16 > 0) ? 1u : 0u);
+          commit(pv_done);
+          return true;
+        };
+        for (int j = 0; j < 2 && j < tl.nkb && ok; ++j) ok = qk(j);
+        if (ok && tl.nkb > 0) {
+          // the first product of this tile overwrites O: every earlier tile's O
+          // must have been read back
+          while (o_waited < it && ok) {
+            if (!mbar_wait(o_free, o_waited & 1, abort_flag)) ok = false;
+            ++o_waited;
+          }
+          fence_after();
         }
-        commit(&s_full[j & 1]);
-        commit(&k_empty[j % NST]);
-        return true;
-      };
-      auto pv = [&](int j) -> bool {
-        if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag)) return false;
-        fence_after();
-        const uint32_t sV = su32(sm + SM::OFF_V + (j % NST) * SM::KB);
-#pragma unroll
-        for (int k16 = 0; k16 < BKEY / 16; ++k16)
-          umma_ts(tmem + 256, tmem + (j & 1) * 128 + k16 * 8,
-                  sdesc(sV + k16 * 16 * 128, BKEY * 128), id_pv, (j > 0 || k16 > 0) ? 1u : 0u);
-        commit(pv_done);
-        return true;
-      };
-      for (int j = 0; j < 2 && j < nkb && ok; ++j) ok = qk(j);
-      for (int j = 0; j < nkb && ok; ++j) {
-        if (!mbar_wait(&v_full[j % NST], (j / NST) & 1, abort_flag)) { ok = false; break; }
-        if (!pv(j)) { ok = false; break; }
-        commit(&v_empty[j % NST]);
-        if (j + 2 < nkb && !qk(j + 2)) { ok = false; break; }
+        for (int j = 0; j < tl.nkb && ok; ++j) {
+          const int g = g0 + j;
+          if (!mbar_wait(&v_full[g % NST], (g / NST) & 1, abort_flag)) { ok = false; break; }
+          if (!pv(j)) { ok = false; break; }
+          commit(&v_empty[g % NST]);
+          if (j + 2 < tl.nkb && !qk(j + 2)) { ok = false; break; }
+        }
+        if (ok) commit(&q_empty[qb]);  // this tile's S products are issued and in order before
+        gb = g0 + tl.nkb;
       }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) {
       if (!ok) {
         *abort_flag = 1;
         atomicOr(p.flags, FLAG_TIMEOUT);
@@ -462,128 +512,126 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
     const int pair = 1 + quarter;        // named barrier of the two warps of this quarter
     const int m = quarter * 32 + lane;   // query row of the tile = TMEM lane
-    const int mrows = nrows * p.G;
-    const bool valid = m < mrows;
-    const int r = r0 + (valid ? m / p.G : 0);
-    const int h = hk * p.G + (valid ? m % p.G : 0);
-    int ps = valid ? p.pos[r] : 0;
-    if (valid && (ps < 0 || ps >= p.Tmax)) {
-      if (wg == 0) atomicOr(p.flags, FLAG_BAD_POS);
-      ps = 0;
-    }
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and this half's row sum
+    const float sl2 = p.scale_log2;
     bool ok = true;
+    int gb = 0;
     auto warp_wait = [&](uint64_t* bb, uint32_t parity) -> bool {
       int w = 1;
       if (lane == 0) w = mbar_wait(bb, parity, abort_flag) ? 1 : 0;
       return __shfl_sync(0xffffffffu, w, 0) != 0;
     };
-    const float sl2 = p.scale_log2;
-    for (int j = 0; j < nkb && ok; ++j) {
-      if (!bar_pair_and(pair, warp_wait(&s_full[j & 1], (j >> 1) & 1))) { ok = false; break; }
-      fence_after();
-      const uint32_t s_base = lane_base + (j & 1) * 128;
-      // This thread's HK scores, one TMEM load wait.
-      const int nvis = min(max(ps - j * BKEY - HK * wg, 0), HK);
-      float sv[HK];
-      {
-        uint32_t* ru = reinterpret_cast<uint32_t*>(sv);
-#pragma unroll
-        for (int c = 0; c < HK / 32; ++c) tmem_ld32_nw(s_base + HK * wg + c * 32, ru + 32 * c);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x) {
+      const Tile tl = tile_of(p, idx, lane);
+      const int mrows = tl.nrows * p.G;
+      const bool valid = m < mrows;
+      const int r = tl.r0 + (valid ? m / p.G : 0);
+      const int h = tl.hk * p.G + (valid ? m % p.G : 0);
+      int ps = valid ? p.pos[r] : 0;
+      if (valid && (ps < 0 || ps >= p.Tmax)) {
+        if (wg == 0) atomicOr(p.flags, FLAG_BAD_POS);
+        ps = 0;
       }
-      if (!__all_sync(0xffffffffu, nvis == HK)) {
-#pragma unroll
-        for (int i = 0; i < HK; ++i)
-          if (i >= nvis) sv[i] = -INFINITY;
-      }
-      float mx;
-      {
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int i = 0; i < HK; i += 8)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], sv[i + 2 * q], sv[i + 2 * q + 1]);
-        mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;  // scaled log2 units
-      }
-      // the row maximum over both halves (both threads then take the same
-      // decisions below); the slot alternates with the block parity
-      float* xm = xmax + (j & 1) * 256;
-      xm[wg * 128 + m] = mx;
-      bar_pair(pair);
-      mx = fmaxf(mx, xm[(wg ^ 1) * 128 + m]);
-      float corr = 1.f;
-      bool resc = false;
-      if (mx > mrun + 8.f) {
-        // O and l hold blocks < j taken against the old base (nothing if the
-        // row had no visible key yet)
-        if (j > 0 && mrun != -INFINITY) {
-          resc = true;
-          corr = ex2(mrun - mx);
-        }
-        mrun = mx;
-      }
-      const float base = mrun == -INFINITY ? 0.f : mrun;
-      if (__any_sync(0xffffffffu, resc)) {  // the partner warp holds the same rows
-        // O holds the products of blocks < j once the previous one landed
-        if (!bar_pair_and(pair, warp_wait(pv_done, (j - 1) & 1))) { ok = false; break; }
+      float mrun = -INFINITY, l = 0.f;  // exponent base (log2 units) and this half's row sum
+      for (int j = 0; j < tl.nkb && ok; ++j, ++gb) {
+        if (!bar_pair_and(pair, warp_wait(&s_full[gb & 1], (gb >> 1) & 1))) { ok = false; break; }
         fence_after();
-        l *= corr;
+        const uint32_t s_base = lane_base + (gb & 1) * 128;
+        // This thread's HK scores, one TMEM load wait.
+        const int nvis = min(max(ps - j * BKEY - HK * wg, 0), HK);
+        float sv[HK];
+        {
+          uint32_t* ru = reinterpret_cast<uint32_t*>(sv);
 #pragma unroll
-        for (int c = 0; c < HD / 64; ++c) {
-          uint32_t ro[32];
-          const uint32_t oa = lane_base + 256 + (HD / 2) * wg + c * 32;
-          tmem_ld32_nw(oa, ro);
+          for (int c = 0; c < HK / 32; ++c) tmem_ld32_nw(s_base + HK * wg + c * 32, ru + 32 * c);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        }
+        if (!__all_sync(0xffffffffu, nvis == HK)) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * corr);
-          tmem_st32(oa, ro);
+          for (int i = 0; i < HK; ++i)
+            if (i >= nvis) sv[i] = -INFINITY;
+        }
+        float mx;
+        {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int i = 0; i < HK; i += 8)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m4[q] = fmax3(m4[q], sv[i + 2 * q], sv[i + 2 * q + 1]);
+          mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3])) * sl2;  // scaled log2 units
+        }
+        // the row maximum over both halves (both threads then take the same
+        // decisions below); the slot alternates with the block parity
+        float* xm = xmax + (gb & 1) * 256;
+        xm[wg * 128 + m] = mx;
+        bar_pair(pair);
+        mx = fmaxf(mx, xm[(wg ^ 1) * 128 + m]);
+        float corr = 1.f;
+        bool resc = false;
+        if (mx > mrun + 8.f) {
+          // O and l hold blocks < j taken against the old base (nothing if the
+          // row had no visible key yet)
+          if (j > 0 && mrun != -INFINITY) {
+            resc = true;
+            corr = ex2(mrun - mx);
+          }
+          mrun = mx;
+        }
+        const float base = mrun == -INFINITY ? 0.f : mrun;
+        if (__any_sync(0xffffffffu, resc)) {  // the partner warp holds the same rows
+          // O holds the products of blocks < j once the previous one landed
+          if (!bar_pair_and(pair, warp_wait(pv_done, (gb - 1) & 1))) { ok = false; break; }
+          fence_after();
+          l *= corr;
+#pragma unroll
+          for (int c = 0; c < HD / 64; ++c) {
+            uint32_t ro[32];
+            const uint32_t oa = lane_base + 256 + (HD / 2) * wg + c * 32;
+            tmem_ld32_nw(oa, ro);
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * corr);
+            tmem_st32(oa, ro);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        // P = 2^(s * scale - base) as bf16 pairs over the buffer's columns
+        // 32wg .. 32wg + 31 (16 at a time; the partner read its scores there
+        // before the barrier above); this half's row sum in two packed sums.
+        const unsigned long long sc2 = f2pack(sl2, sl2), nb2 = f2pack(-base, -base);
+        unsigned long long rs2[2] = {0ull, 0ull};
+#pragma unroll
+        for (int c = 0; c < HK / 32; ++c) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int i = 32 * c + 2 * e;
+            float x0, x1;
+            f2unpack(ffma2(f2pack(sv[i], sv[i + 1]), sc2, nb2), x0, x1);
+            const float e0 = ex2(x0), e1 = ex2(x1);
+            rs2[e & 1] = fadd2(rs2[e & 1], f2pack(e0, e1));
+            __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
+            pw[e] = *reinterpret_cast<uint32_t*>(&hh);
+          }
+          tmem_st16(s_base + (HK / 2) * wg + 16 * c, pw);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      }
-      // P = 2^(s * scale - base) as bf16 pairs over the buffer's columns
-      // 32wg .. 32wg + 31 (16 at a time; the partner read its scores there
-      // before the barrier above); this half's row sum in two packed sums.
-      const unsigned long long sc2 = f2pack(sl2, sl2), nb2 = f2pack(-base, -base);
-      unsigned long long rs2[2] = {0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < HK / 32; ++c) {
-        uint32_t pw[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i = 32 * c + 2 * e;
-          float x0, x1;
-          f2unpack(ffma2(f2pack(sv[i], sv[i + 1]), sc2, nb2), x0, x1);
-          const float e0 = ex2(x0), e1 = ex2(x1);
-          rs2[e & 1] = fadd2(rs2[e & 1], f2pack(e0, e1));
-          __nv_bfloat162 hh = __floats2bfloat162_rn(e0, e1);
-          pw[e] = *reinterpret_cast<uint32_t*>(&hh);
+        {
+          float a0, a1, b0, b1;
+          f2unpack(rs2[0], a0, a1);
+          f2unpack(rs2[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
         }
-        tmem_st16(s_base + (HK / 2) * wg + 16 * c, pw);
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[gb & 1]);
       }
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      {
-        float a0, a1, b0, b1;
-        f2unpack(rs2[0], a0, a1);
-        f2unpack(rs2[1], b0, b1);
-        l += (a0 + a1) + (b0 + b1);
+      if (!ok) break;
+      const bool have_o = tl.nkb > 0;
+      if (have_o) {
+        if (!bar_pair_and(pair, warp_wait(pv_done, (gb - 1) & 1))) { ok = false; break; }
+        fence_after();
       }
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
-    }
-    const bool have_o = ok && nkb > 0;
-    if (have_o) {
-      if (!bar_pair_and(pair, warp_wait(pv_done, (nkb - 1) & 1))) ok = false;
-      else fence_after();
-    }
-    if (!ok) {
-      if (lane == 0) {
-        *abort_flag = 1;
-        atomicOr(p.flags, FLAG_TIMEOUT);
-      }
-    } else {
       // the row sum over both halves, then O / l, this thread's HD/2 dims
       xsum[wg * 128 + m] = l;
       bar_pair(pair);
@@ -609,6 +657,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
+      // O (and the sums slot) may be reused by the next tile
+      fence_before();
+      bar_pair(pair);
+      if (lane == 0) mbar_arrive(o_free);
+    }
+    if (!ok && lane == 0) {
+      *abort_flag = 1;
+      atomicOr(p.flags, FLAG_TIMEOUT);
     }
   }
   fence_before();
@@ -671,12 +727,16 @@ cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
   p.N = a.N; p.Hq = a.Hq; p.Hkv = a.Hkv; p.G = G; p.rpt = rpt; p.nq = nq; p.Tmax = a.Tmax;
   p.k = a.k; p.channel = a.channel; p.B = a.B;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-  const int B = a.N / nq;
-  const int tiles = B * ((nq + rpt - 1) / rpt);
+  p.nseq = a.N / nq;
+  p.tps = (nq + rpt - 1) / rpt;
+  p.tiles = p.nseq * p.tps * a.Hkv;
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<HD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SM::BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(tiles, a.Hkv);
+  int sms = 148, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  dim3 grid((unsigned)(p.tiles < sms ? p.tiles : sms));
   launch_k(attn_tc_kernel<HD>, dim3(grid), dim3(NTHREADS), SM::BYTES, st, mq, mk, mv, p);
   return cudaGetLastError();
 }
