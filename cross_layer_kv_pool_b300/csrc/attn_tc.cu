@@ -6,7 +6,8 @@
 // TMA box {64 dims, G heads, R rows} per 64-dim chunk, which lands exactly in
 // that order. Keys and values stream in blocks of 128 positions of the channel.
 //
-//   warp 0       TMA: the Q tile once, then K and V blocks into two-stage rings;
+//   warps 0, 3   TMA: the Q tile and K blocks (three-stage ring), V blocks
+//                (two-stage ring), from separate threads so K runs ahead;
 //   warp 1       tcgen05.mma, per key block j:
 //                  S(j) = Q K_j^T   (K-major smem operands, fp32 into one of
 //                                    two TMEM buffers),
@@ -38,7 +39,7 @@ namespace wm {
 namespace atc {
 
 constexpr int BQ = 128, BKEY = 128, NTHREADS = 384;  // 3 warpgroups: control, softmax x2
-constexpr int NST = 2;                                // K and V ring stages
+constexpr int NSK = 3, NSV = 2;                       // K and V ring stages
 // Register split: 384 threads x 168 at launch = 64512; the control warpgroup
 // keeps 88, each softmax warpgroup takes 208: 128 x 88 + 256 x 208 = 64512
 // (per SM sub-partition, one control and two softmax warps: 32 x 504 <= 16384).
@@ -276,10 +277,10 @@ template <int HD>
 struct Smem {
   static constexpr int QB = BQ * HD * 2;     // one Q tile
   static constexpr int KB = BKEY * HD * 2;   // one K (or V) block
-  static constexpr int OFF_Q = 0;                   // 2 tiles (the next one loads early)
-  static constexpr int OFF_K = OFF_Q + 2 * QB;      // NST stages
-  static constexpr int OFF_V = OFF_K + NST * KB;    // NST stages
-  static constexpr int OFF_X = OFF_V + NST * KB;    // max exchange [2][2][128], sums [2][128]
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + QB;          // NSK stages
+  static constexpr int OFF_V = OFF_K + NSK * KB;    // NSV stages
+  static constexpr int OFF_X = OFF_V + NSV * KB;    // max exchange [2][2][128], sums [2][128]
   static constexpr int OFF_BAR = OFF_X + 6 * 128 * 4;
   static constexpr int BYTES = 1024 + OFF_BAR + 256;
   // S buffers b = 0, 1 (128 fp32 columns each; P, bf16 pairs, overwrites the
@@ -328,13 +329,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   float* xmax = (float*)(sm + SM::OFF_X);   // [block parity][warpgroup][row]
   float* xsum = xmax + 4 * 128;             // [warpgroup][row]
   uint64_t* bar = (uint64_t*)(sm + SM::OFF_BAR);
-  uint64_t* q_full = bar + 0;          // [Q buffer]
-  uint64_t* q_empty = bar + 2;         // [Q buffer]: the tile's S products are done
-  uint64_t* k_full = bar + 4;          // [NST]
-  uint64_t* k_empty = k_full + NST;    // [NST]
-  uint64_t* v_full = k_empty + NST;    // [NST]
-  uint64_t* v_empty = v_full + NST;    // [NST]
-  uint64_t* s_full = v_empty + NST;    // [buffer]: S of block gb is in TMEM
+  uint64_t* q_full = bar + 0;
+  uint64_t* q_empty = bar + 1;         // the tile's S products are done
+  uint64_t* k_full = bar + 2;          // [NSK]
+  uint64_t* k_empty = k_full + NSK;    // [NSK]
+  uint64_t* v_full = k_empty + NSK;    // [NSV]
+  uint64_t* v_empty = v_full + NSV;    // [NSV]
+  uint64_t* s_full = v_empty + NSV;    // [buffer]: S of block gb is in TMEM
   uint64_t* p_full = s_full + 2;       // [buffer]: P of block gb written (8 warps arrive)
   uint64_t* pv_done = p_full + 2;      // O += P V of block gb complete
   uint64_t* o_free = pv_done + 1;      // the softmax warps have read the tile's O (8 arrive)
@@ -344,15 +345,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1);
-      mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 8);
     }
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < NSK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
@@ -376,37 +379,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t tmem = *tmem_holder;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
-  if (warp == 0) {
-    // ---------------- TMA producer (lane 0; the warp computes tile metadata) ----------------
+  if (warp == 0 || warp == 3) {
+    // ---------------- TMA producers (lane 0; the warp computes tile metadata):
+    // warp 0 the Q tiles and K blocks, warp 3 the V blocks, so that K runs
+    // ahead of V by its deeper ring
+    const bool kq = warp == 0;
+    const int ns = kq ? NSK : NSV;
+    uint64_t* full = kq ? k_full : v_full;
+    uint64_t* empty = kq ? k_empty : v_empty;
+    const CUtensorMap* map = kq ? &tmK : &tmV;
+    uint8_t* ring = sm + (kq ? SM::OFF_K : SM::OFF_V);
     bool ok = true;
     int gb = 0, it = 0;
     uint32_t used = 0, lastk = 0;
     for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
       const Tile tl = tile_of(p, idx, lane);
       if (lane == 0) {
-        if (!tl.seq_ok) atomicOr(p.flags, FLAG_BAD_SEQ);
-        const int qb = it & 1;
-        if (!mbar_wait(&q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag)) ok = false;
-        if (ok) {
-          // the box fills R*G rows of each 128-row operand chunk; rows past
-          // them feed only accumulator rows that are never read back
-          mbar_expect_tx(&q_full[qb], (uint32_t)((HD / 64) * p.G * p.rpt * 128));
-          for (int c = 0; c < HD / 64; ++c)
-            tma3(&tmQ, &q_full[qb], sm + SM::OFF_Q + qb * SM::QB + c * BQ * 128, c * 64,
-                 tl.hk * p.G, tl.r0);
+        if (kq) {
+          if (!tl.seq_ok) atomicOr(p.flags, FLAG_BAD_SEQ);
+          // one Q buffer: the previous tile's S products have read it
+          if (!mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) ok = false;
+          if (ok) {
+            // the box fills R*G rows of each 128-row operand chunk; rows past
+            // them feed only accumulator rows that are never read back
+            mbar_expect_tx(q_full, (uint32_t)((HD / 64) * p.G * p.rpt * 128));
+            for (int c = 0; c < HD / 64; ++c)
+              tma3(&tmQ, q_full, sm + SM::OFF_Q + c * BQ * 128, c * 64, tl.hk * p.G, tl.r0);
+          }
         }
         const int zc = ((tl.sq * p.k) + p.channel) * p.Hkv + tl.hk;
         for (int j = 0; j < tl.nkb && ok; ++j, ++gb) {
-          const int s = gb % NST;
-          const uint32_t ph = (gb / NST) & 1;
-          if (!mbar_wait(&k_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-          mbar_expect_tx(&k_full[s], (uint32_t)SM::KB);
+          const int s = gb % ns;
+          const uint32_t ph = (gb / ns) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(&full[s], (uint32_t)SM::KB);
           for (int c = 0; c < HD / 64; ++c)
-            tma3(&tmK, &k_full[s], sm + SM::OFF_K + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
-          if (!mbar_wait(&v_empty[s], ph ^ 1, abort_flag)) { ok = false; break; }
-          mbar_expect_tx(&v_full[s], (uint32_t)SM::KB);
-          for (int c = 0; c < HD / 64; ++c)
-            tma3(&tmV, &v_full[s], sm + SM::OFF_V + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
+            tma3(map, &full[s], ring + s * SM::KB + c * BKEY * 128, c * 64, j * BKEY, zc);
           used |= 1u << s;
           lastk = (lastk & ~(1u << s)) | (ph << s);
         }
@@ -420,12 +428,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // Drain: every issued copy has landed before the CTA may exit.
       volatile int no_abort = 0;
-      for (int q = 0; q < 2 && q < it; ++q) mbar_wait(&q_full[(it - 1 - q) & 1], ((it - 1 - q) >> 1) & 1, &no_abort);
-      for (int s = 0; s < NST; ++s)
-        if (used & (1u << s)) {
-          mbar_wait(&k_full[s], (lastk >> s) & 1, &no_abort);
-          mbar_wait(&v_full[s], (lastk >> s) & 1, &no_abort);
-        }
+      if (kq && it > 0) mbar_wait(q_full, (it - 1) & 1, &no_abort);
+      for (int s = 0; s < ns; ++s)
+        if (used & (1u << s)) mbar_wait(&full[s], (lastk >> s) & 1, &no_abort);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer (lane 0) ----------------
@@ -439,16 +444,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
       const Tile tl = tile_of(p, idx, lane);
       if (lane == 0) {
-        const int qb = it & 1;
-        const uint32_t sQ = su32(sm + SM::OFF_Q + qb * SM::QB);
-        if (!mbar_wait(&q_full[qb], (it >> 1) & 1, abort_flag)) ok = false;
+        const uint32_t sQ = su32(sm + SM::OFF_Q);
+        if (!mbar_wait(q_full, it & 1, abort_flag)) ok = false;
         fence_after();
         const int g0 = gb;  // first block of this tile
         auto qk = [&](int j) -> bool {
           const int g = g0 + j;
-          if (!mbar_wait(&k_full[g % NST], (g / NST) & 1, abort_flag)) return false;
+          if (!mbar_wait(&k_full[g % NSK], (g / NSK) & 1, abort_flag)) return false;
           fence_after();
-          const uint32_t sK = su32(sm + SM::OFF_K + (g % NST) * SM::KB);
+          const uint32_t sK = su32(sm + SM::OFF_K + (g % NSK) * SM::KB);
 #pragma unroll
           for (int k16 = 0; k16 < HD / 16; ++k16) {
             const uint32_t off = (k16 >> 2) * BQ * 128 + (k16 & 3) * 32;
@@ -456,14 +460,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             umma(tmem + (g & 1) * 128, sdesc(sQ + off, 16), sdesc(sK + offk, 16), id_qk, k16 > 0);
           }
           commit(&s_full[g & 1]);
-          commit(&k_empty[g % NST]);
+          commit(&k_empty[g % NSK]);
           return true;
         };
         auto pv = [&](int j) -> bool {
           const int g = g0 + j;
           if (!mbar_wait(&p_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
           fence_after();
-          const uint32_t sV = su32(sm + SM::OFF_V + (g % NST) * SM::KB);
+          const uint32_t sV = su32(sm + SM::OFF_V + (g % NSV) * SM::KB);
 #pragma unroll
           for (int k16 = 0; k16 < BKEY / 16; ++k16)
             umma_ts(tmem + 256, tmem + (g & 1) * 128 + k16 * 8,
@@ -483,12 +487,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int j = 0; j < tl.nkb && ok; ++j) {
           const int g = g0 + j;
-          if (!mbar_wait(&v_full[g % NST], (g / NST) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&v_full[g % NSV], (g / NSV) & 1, abort_flag)) { ok = false; break; }
           if (!pv(j)) { ok = false; break; }
-          commit(&v_empty[g % NST]);
+          commit(&v_empty[g % NSV]);
           if (j + 2 < tl.nkb && !qk(j + 2)) { ok = false; break; }
         }
-        if (ok) commit(&q_empty[qb]);  // this tile's S products are issued and in order before
+        if (ok) commit(q_empty);  // this tile's S products are issued and in order before
         gb = g0 + tl.nkb;
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
