@@ -56,8 +56,13 @@ struct Params {
   float scale_log2;   // log2(e) / sqrt(d)
 };
 
-// Tile ``idx`` of the persistent schedule: tiles with the latest positions
-// (the most keys) first, then sequence, then KV head.
+// Tile ``idx`` of the persistent schedule. The tiles of one (sequence, KV
+// head) are consecutive, so the CTAs working at the same time share that
+// sequence's K/V blocks through L2 (a position-major order re-read the whole
+// channel from DRAM once per tile row). Within a sequence the order is
+// t = tps-1, tps-2, ... for the first half and 0, 1, ... for the second, so a
+// CTA whose tiles lie half a sequence apart (148 CTAs, 8 tiles per sequence)
+// alternates heavy and light tiles.
 struct Tile {
   int b, hk, r0, nrows, sq, nkb;
   bool seq_ok;
@@ -65,10 +70,10 @@ struct Tile {
 // Warp-collective (every lane gets the same result).
 __device__ __forceinline__ Tile tile_of(const Params& p, int idx, int lane) {
   Tile tl;
-  const int per_t = p.nseq * p.Hkv;
-  const int t = p.tps - 1 - idx / per_t, rem = idx % per_t;
-  tl.b = rem / p.Hkv;
-  tl.hk = rem % p.Hkv;
+  const int pr = idx / p.tps, i = idx % p.tps, half = (p.tps + 1) / 2;
+  const int t = i < half ? p.tps - 1 - i : i - half;
+  tl.b = pr / p.Hkv;
+  tl.hk = pr % p.Hkv;
   tl.r0 = tl.b * p.nq + t * p.rpt;
   tl.nrows = max(0, min(p.rpt, (tl.b + 1) * p.nq - tl.r0));
   int maxp = 0;
