@@ -82,7 +82,7 @@ wm_status check_config(const wm_config* c) {
   if (c->dtype != WM_F32 && c->dtype != WM_BF16) return WM_ERR_INVALID_ARG;
   if (c->d != 64 && c->d != 128) return WM_ERR_UNSUPPORTED;
   if (count_nR(*c) < 1) return WM_ERR_INVALID_ARG;
-  if (c->flags & ~(uint32_t)WM_FLAG_SIMT_GEMM) return WM_ERR_INVALID_ARG;
+  if (c->flags & ~(uint32_t)(WM_FLAG_SIMT_GEMM | WM_FLAG_NO_CLUSTER)) return WM_ERR_INVALID_ARG;
   return WM_OK;
 }
 
@@ -156,6 +156,7 @@ void gemm(const Ctx& x, const GemmDesc& gd) {
   const int tr = trace_begin(x, WM_TRACE_GEMM);
   GemmDesc g = gd;
   g.b_const = true;  // every product of the model multiplies by a weight matrix
+  g.no_cluster = (x.c->flags & WM_FLAG_NO_CLUSTER) != 0;
   g.partial = x.buf<float>(B_PARTIAL);
   g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
   if (g.partial_elems <= 0) g.partial = nullptr;

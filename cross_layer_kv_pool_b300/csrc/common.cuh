@@ -145,6 +145,7 @@ struct GemmDesc {
   // B (and B2) are weights that no kernel writes: the tensor-core engine may
   // request them before its predecessor in the stream has finished.
   bool b_const = false;
+  bool no_cluster = false;       // split K through global atomics, never a cluster
   Epi epi;
   // Zero-filled fp32 scratch for split-K (nullable): when a GEMM has too few
   // output tiles to occupy the GPU, K is split across CTAs that add their

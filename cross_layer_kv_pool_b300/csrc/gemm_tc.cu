@@ -988,7 +988,7 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   // Few output tiles (decode-sized M): split K over a cluster of up to 8
   // CTAs that sum their slices through distributed shared memory; the
   // largest split whose clusters are all resident at once (one wave).
-  if (g.M <= BM && out_tiles * 2 <= sms && p.num_kb >= 4) {
+  if (!g.no_cluster && g.M <= BM && out_tiles * 2 <= sms && p.num_kb >= 4) {
     long long ks0 = sms / out_tiles;
     if (ks0 > 8) ks0 = 8;
     if (ks0 > p.num_kb / 2) ks0 = p.num_kb / 2;

@@ -24,6 +24,7 @@ WM_OK, WM_ERR_INVALID_ARG, WM_ERR_UNSUPPORTED, WM_ERR_WORKSPACE, WM_ERR_CUDA, \
 WM_F32, WM_BF16 = 0, 1
 LOGITS = {"none": 0, None: 0, "last": 1, "all": 2}
 WM_FLAG_SIMT_GEMM = 1
+WM_FLAG_NO_CLUSTER = 2
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
             "wm_decode_step", "wm_decode_batch", "wm_check_flags", "wm_status_string", "wm_abi_version",

@@ -61,6 +61,10 @@ typedef enum {
 
 /* Engine flags (wm_config.flags). */
 #define WM_FLAG_SIMT_GEMM 1u  /* run every contraction on CUDA cores (debug aid) */
+#define WM_FLAG_NO_CLUSTER 2u /* few-row products split K with fp32 atomics and a
+                                 finalize kernel instead of a thread-block
+                                 cluster (the path taken where a cluster does
+                                 not fit; a test aid elsewhere) */
 
 /* Optional measurement hook (wm_config.trace, nullable). While entries
  * remain, an entry point records begin[i] / end[i] (caller-created

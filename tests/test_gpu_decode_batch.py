@@ -193,3 +193,27 @@ def test_decode_batch_1p3b_widths_ragged():
     tol = TOL["bf16"]
     assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl))
     assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv)
+
+
+def test_decode_batch_split_k_fallback_matches_cluster():
+    """The few-row products' other split-K path (global fp32 atomics and a
+    finalize kernel, taken where a cluster does not fit) gives what the
+    cluster path gives, at the 1.3B widths."""
+    s = synth.HALF_1P3B.replace(L=4, k=4, V=2000)
+    out = []
+    for flags in (0, wm.WM_FLAG_NO_CLUSTER):
+        W = synth.make_weights(s, seed=46, device="cuda", gain_jitter=0.1)
+        m = wm.Model(s, W, flags=flags)
+        B, Tmax = 8, 96
+        ck, cv = _random_cache(s, B, Tmax, 47)
+        pos_h = np.array([3, 10, 20, 33, 47, 60, 80, 95])
+        tok_h = np.random.default_rng(48).integers(0, s.V, size=B)
+        ws = m.workspace(B, Tmax)
+        lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
+        wm.wm_decode_batch(m, _i32(tok_h), _i32(pos_h), ck, cv, lg, ws)
+        torch.cuda.synchronize()
+        assert wm.wm_check_flags(ws) == 0
+        rows = np.arange(B)
+        out.append((host(lg), host(ck)[rows, :, :, pos_h], host(cv)[rows, :, :, pos_h]))
+    for a, b in zip(out[0], out[1]):
+        assert relerr(b, a) <= 1e-2
