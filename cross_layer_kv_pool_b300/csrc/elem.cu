@@ -164,10 +164,65 @@ void launch_embed(int dtype, const int32_t* tok, int N, const void* embed, int V
 }
 
 // ---------------------------------------------------------------------------
-// Layer-input RMSNorm with the pool's emissions (one block per (row, layer)).
+// Layer-input RMSNorm with the pool's emissions: one warp per (row, layer),
+// eight rows per block. The row is read twice (the second time from L1).
 // ---------------------------------------------------------------------------
+constexpr int NORM_ROWS = 8;             // rows per 256-thread block
+constexpr int NORM_WARP_MIN_ROWS = 1024;  // fewer rows: a block per row
+
 template <typename S>
-__global__ void norm_emit_kernel(const S* __restrict__ X, long long ldx_row, long long ldx_l,
+__global__ void __launch_bounds__(32 * NORM_ROWS) norm_emit_kernel(
+    const S* __restrict__ X, long long ldx_row, long long ldx_l, int l0, int D, int L,
+    const S* __restrict__ gain_in, S* __restrict__ xn, float* __restrict__ inv_out,
+    const S* __restrict__ src_norm, S* __restrict__ rin, int N, int nR, int p, int p_off,
+    float eps) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int VN = VecT<S>::N;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * NORM_ROWS + (threadIdx.x >> 5), l = l0 + blockIdx.y;
+  if (r >= N) return;  // warp-uniform
+  const S* x = X + (long long)r * ldx_row + (long long)l * ldx_l;
+  float ss = 0.f;
+#pragma unroll 4
+  for (int c = lane * VN; c < D; c += 32 * VN) {
+    float v[VN];
+    ld_vec(x + c, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) ss += v[i] * v[i];
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)D + eps);
+  if (lane == 0) inv_out[(long long)r * L + l] = inv;
+  const bool in_R = rin != nullptr && (l % p) == p_off;
+  const int ridx = (l - p_off) / p;
+  if (xn == nullptr && !in_R) return;
+  const long long rin_b = (long long)N * nR * D;
+  for (int c = lane * VN; c < D; c += 32 * VN) {
+    float v[VN], o[VN], gv[VN];
+    ld_vec(x + c, v);
+    if (xn) {
+      ld_vec(gain_in + (long long)l * D + c, gv);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) o[i] = v[i] * inv * gv[i];
+      st_vec(xn + (long long)r * D + c, o);
+    }
+    if (in_R) {
+#pragma unroll
+      for (int beta = 0; beta < 2; ++beta) {
+        ld_vec(src_norm + ((long long)beta * L + l) * D + c, gv);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) o[i] = v[i] * inv * gv[i];
+        st_vec(rin + beta * rin_b + (long long)r * nR * D + (long long)ridx * D + c, o);
+      }
+    }
+  }
+}
+
+// Few rows (a decode step): one 256-thread block per (row, layer), more loads
+// in flight per row than a warp has.
+template <typename S>
+__global__ void norm_emit_block_kernel(const S* __restrict__ X, long long ldx_row, long long ldx_l,
                                  int l0, int D, int L, const S* __restrict__ gain_in,
                                  S* __restrict__ xn, float* __restrict__ inv_out,
                                  const S* __restrict__ src_norm, S* __restrict__ rin, int N,
@@ -218,14 +273,52 @@ void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx
                       const void* src_norm, void* rin, int nR, int p, int p_off, float eps,
                       cudaStream_t st) {
   if (N <= 0 || nl <= 0) return;
-  dim3 grid(N, nl);
-  WM_DISPATCH_S(dtype, launch_k(norm_emit_kernel<S>, dim3(grid), dim3(256), 0, st, 
-                           (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in, (S*)xn, inv,
-                           (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
+  if (N < NORM_WARP_MIN_ROWS) {
+    WM_DISPATCH_S(dtype, launch_k(norm_emit_block_kernel<S>, dim3(N, nl), dim3(256), 0, st,
+                                  (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in,
+                                  (S*)xn, inv, (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
+    return;
+  }
+  dim3 grid((N + NORM_ROWS - 1) / NORM_ROWS, nl);
+  WM_DISPATCH_S(dtype, launch_k(norm_emit_kernel<S>, dim3(grid), dim3(32 * NORM_ROWS), 0, st,
+                                (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in, (S*)xn,
+                                inv, (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
+}
+
+// y = RMSNorm(x; gain): one warp per row, eight rows per block.
+template <typename S>
+__global__ void __launch_bounds__(32 * NORM_ROWS) rmsnorm_kernel(
+    const S* __restrict__ X, long long ldx, int row0, int rstride, int D,
+    const S* __restrict__ gain, S* __restrict__ y, float eps, int N) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int VN = VecT<S>::N;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * NORM_ROWS + (threadIdx.x >> 5);
+  if (r >= N) return;  // warp-uniform
+  const S* x = X + (long long)(row0 + (long long)r * rstride) * ldx;
+  float ss = 0.f;
+#pragma unroll 4
+  for (int c = lane * VN; c < D; c += 32 * VN) {
+    float v[VN];
+    ld_vec(x + c, v);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) ss += v[i] * v[i];
+  }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)D + eps);
+  for (int c = lane * VN; c < D; c += 32 * VN) {
+    float v[VN], gv[VN];
+    ld_vec(x + c, v);
+    ld_vec(gain + c, gv);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) v[i] = v[i] * inv * gv[i];
+    st_vec(y + (long long)r * D + c, v);
+  }
 }
 
 template <typename S>
-__global__ void rmsnorm_kernel(const S* __restrict__ X, long long ldx, int row0, int rstride,
+__global__ void rmsnorm_block_kernel(const S* __restrict__ X, long long ldx, int row0, int rstride,
                                int D, const S* __restrict__ gain, S* __restrict__ y, float eps) {
   pdl_wait();
   pdl_trigger();
@@ -255,8 +348,14 @@ __global__ void rmsnorm_kernel(const S* __restrict__ X, long long ldx, int row0,
 void launch_rmsnorm(int dtype, const void* X, long long ldx, int row0, int rstride, int N, int D,
                     const void* gain, void* y, float eps, cudaStream_t st) {
   if (N <= 0) return;
-  WM_DISPATCH_S(dtype, launch_k(rmsnorm_kernel<S>, dim3(N), dim3(256), 0, st, (const S*)X, ldx, row0, rstride, D,
-                                                           (const S*)gain, (S*)y, eps));
+  if (N < NORM_WARP_MIN_ROWS) {
+    WM_DISPATCH_S(dtype, launch_k(rmsnorm_block_kernel<S>, dim3(N), dim3(256), 0, st,
+                                  (const S*)X, ldx, row0, rstride, D, (const S*)gain, (S*)y, eps));
+    return;
+  }
+  WM_DISPATCH_S(dtype, launch_k(rmsnorm_kernel<S>, dim3((N + NORM_ROWS - 1) / NORM_ROWS),
+                                dim3(32 * NORM_ROWS), 0, st, (const S*)X, ldx, row0, rstride, D,
+                                (const S*)gain, (S*)y, eps, N));
 }
 
 __global__ void broadcast_coeff_kernel(const float* __restrict__ stat, long long total, int n_per_row,

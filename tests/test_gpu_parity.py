@@ -393,7 +393,20 @@ def test_multi_tile_groups_isolated(dtype):
     assert within(w["cache_norm"], tol["cache_step_norm"], w["spread_cache_norm"]), w
 
 
-@pytest.mark.parametrize("N", [300, 1000])
+def test_large_groups_fp32_isolated():
+    """Groups of 1,024 rows (the row norms switch to one warp per row from
+    there), one pass, every group against the oracle from the GPU snapshot."""
+    s = small_shape("f32", L=2, k=2)
+    m, Wn = model(s, seed=6, jitter=0.1)
+    B, T, g = 16, 128, 2
+    tokens = np.random.default_rng(7).integers(0, s.V, size=(B, T))
+    w = isolated_passes(m, Wn, tokens, g, 1, logits_mode="last")
+    tol = TOL["f32"]
+    assert w["checked"] == 2
+    assert w["logits"] <= tol["logits"] and w["cache"] <= tol["cache"], w
+
+
+@pytest.mark.parametrize("N", [300, 1000, 1500])
 def test_pool_mix_multi_tile_bf16(N):
     s = synth.HALF_SMALL.replace(V=1000)
     m, Wn = model(s, seed=9, jitter=0.2)
