@@ -31,12 +31,10 @@ def _cfg(**kw):
     return c
 
 
-def _weights(c, seed=0, std=0.3, jitter=0.2):
-    """Seeded fp64 weights for the pins (numpy; larger std than the workloads
-    so that every term visibly moves the result)."""
-    rng = np.random.default_rng(seed)
+def _shapes(c):
+    """The tensors the oracle is run with, and their shapes."""
     L, D, k, d = c.L, c.D, c.k, c.d
-    shapes = {
+    return {
         "embed": (c.V, D), "lm_head": (c.V, D), "final_norm": (D,),
         "in_norm": (L, D), "post_norm": (L, D), "q_norm": (L, d),
         "Wq": (L, c.Hq * d, D), "Wo": (L, D, c.Hq * d),
@@ -45,6 +43,13 @@ def _weights(c, seed=0, std=0.3, jitter=0.2):
         "chan_norm": (2, k, D), "Wk": (k, c.Hkv * d, D), "Wv": (k, c.Hkv * d, D),
         "k_norm": (k, d),
     }
+
+
+def _weights(c, seed=0, std=0.3, jitter=0.2):
+    """Seeded fp64 weights for the pins (numpy; larger std than the workloads
+    so that every term visibly moves the result)."""
+    rng = np.random.default_rng(seed)
+    shapes = _shapes(c)
     gains = {"final_norm", "in_norm", "post_norm", "q_norm", "src_norm", "chan_norm", "k_norm"}
     W = {}
     for n, s in shapes.items():
@@ -739,6 +744,88 @@ def check_pool_backward_finite_differences(O):
     _fd_check(O, c, W, states, pos, static, 54)
 
 
+def _golden(name):
+    """Entries "name value unit" of a fixture under tests/golden/."""
+    import os
+    out = {}
+    with open(os.path.join(os.path.dirname(__file__), "golden", name)) as f:
+        for line in f:
+            line = line.split("#", 1)[0].split()
+            if line:
+                out[line[0]] = float(line[1]) * {"B": 1e9, "M": 1e6}[line[2]]
+    return out
+
+
+def _vanilla_count(c, embeddings=True, tied=True):
+    """Parameters of a vanilla Qwen3-style Transformer of the same widths,
+    written out afresh: per layer its own K/V projections and K-norm gain, no
+    pool."""
+    L, D, d = c.L, c.D, c.d
+    per_layer = (2 * D                      # input and post-attention norms
+                 + D * c.Hq * d + D * c.Hkv * d * 2 + c.Hq * d * D   # Q, K, V, O
+                 + 2 * d                    # q-norm and k-norm gains
+                 + 3 * D * c.F)             # gate, up, down
+    n = L * per_layer + D                   # + final norm
+    if embeddings:
+        n += c.V * D * (1 if tied else 2)
+    return n
+
+
+def check_parameter_counts_match_pages(O):
+    """The pool's parameterisation against the totals the pages print
+    (tests/golden/param_counts.txt). At D = 1792, L = 28, the printed vanilla
+    and half-cache (k = 14) totals are met together by Qwen3 widths Hq 14,
+    d 128, F 3D = 5376 with the embedding tied to the LM head and Hkv 7, and
+    the difference between them fixes the pool: a router per branch from the
+    every-p-th sources (|R| D inputs) to k L weights, per-channel K/V
+    projections and K-norm gains, source and channel norm gains, and no
+    per-layer K/V (a router over all L sources, a single router, or one
+    projection shared by the channels each misses by 10M or more). At D = 512,
+    L = 16 the full-cache minus vanilla difference is the router alone.
+    The oracle is then run on weights of exactly these shapes, and each tensor
+    (each router branch, each channel's projections) must move its output."""
+    g = _golden("param_counts.txt")
+    c = _cfg(L=28, D=1792, k=14, p=2, Hq=14, Hkv=7, d=128, F=5376, V=151936)
+    wm = sum(int(np.prod(s)) for n, s in _shapes(c).items() if n != "lm_head")  # tied
+    van = _vanilla_count(c)
+    assert abs(van - g["vanilla_d1792_l28_total"]) <= 0.5e6, van
+    assert abs(wm - g["whitematter_d1792_l28_k14_total"]) <= 0.5e6, wm
+    cs = _cfg(L=16, D=512, k=16, p=2, Hq=8, Hkv=8, d=64, F=1536, V=151936)
+    wm_s = sum(int(np.prod(s)) for n, s in _shapes(cs).items() if n not in ("embed", "lm_head"))
+    diff = wm_s - _vanilla_count(cs, embeddings=False)
+    printed = g["whitematter_d512_l16_k16_nonembed"] - g["vanilla_d512_l16_nonembed"]
+    assert abs(diff - printed) <= 0.1e6, (diff, printed)
+
+    # every tensor counted above is one the oracle's forward consumes
+    t = _cfg(L=4, D=16, k=4, p=2, Hq=4, Hkv=2, d=8, F=24, V=32)
+    W = _weights(t, seed=7)
+    B, Tc = 2, 6
+    ck0 = np.random.default_rng(8).standard_normal((B, t.k, t.Hkv, Tc, t.d))
+    cv0 = np.random.default_rng(9).standard_normal((B, t.k, t.Hkv, Tc, t.d))
+    toks = np.array([3, 17, 29])
+    seq = np.array([0, 1, 1])
+    pos = np.array([2, 4, 5])
+
+    def out(Wx):
+        res, lg, _ = O.run_rows(t, Wx, toks, seq, pos, ck0.copy(), cv0.copy(), want_logits=True)
+        return np.concatenate([res["K"].ravel(), res["V"].ravel(), lg.ravel()])
+
+    ref = out(W)
+    parts = []
+    for n, a in W.items():
+        if n in ("Wr", "src_norm", "chan_norm"):
+            parts += [(n, (b,)) for b in range(2)]
+        elif n in ("Wk", "Wv", "k_norm"):
+            parts += [(n, (j,)) for j in range(t.k)]
+        else:
+            parts.append((n, ()))
+    for n, idx in parts:
+        Wp = dict(W)
+        Wp[n] = W[n].copy()
+        Wp[n][idx] = Wp[n][idx] + 0.25 * np.random.default_rng(10).standard_normal(Wp[n][idx].shape)
+        assert np.max(np.abs(out(Wp) - ref)) > 1e-6, f"{n}{list(idx)} does not reach the output"
+
+
 ALL_CHECKS = [
     check_round_bf16,
     check_bf16_storage_mode,
@@ -765,4 +852,5 @@ ALL_CHECKS = [
     check_feedback_free_one_pass_is_autoregressive,
     check_feedback_free_router_reads_prefix,
     check_pool_backward_finite_differences,
+    check_parameter_counts_match_pages,
 ]

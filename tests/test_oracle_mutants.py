@@ -73,6 +73,10 @@ MUTANTS = [
             cache_v[seq[r], l, :, pos[r], :] = V[r]"""),
     ("ff_no_prefix_states", "feedback_free_pass", "states[:, : l + 1], pos, l, static_coeff)",
      "states[:, : max(l, 1)], pos, max(l - 1, 0), static_coeff)"),
+    ("pool_router_one_branch", "pool", '(x @ _f64(W["Wr"][beta]).T).reshape(N, k, L)',
+     '(x @ _f64(W["Wr"][0]).T).reshape(N, k, L)'),
+    ("pool_channels_share_wk", "pool", '(stored[:, 0, j] @ _f64(W["Wk"][j]).T)',
+     '(stored[:, 0, j] @ _f64(W["Wk"][0]).T)'),
     ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
      'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
     ("states_are_outputs", "run_rows", "        states[:, l] = h\n        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)",
