@@ -52,6 +52,14 @@ from cross_layer_kv_pool_b300 import synth  # noqa: E402
 
 METRIC = "prefill tok/s (3 cyclic passes, g=16) at 1.3B k=14"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+# DRAM bytes (read + written) per tcgen05 GEMM launch of the prefill step, from
+# one ncu capture of the step's launch list (dram__bytes_read.sum +
+# dram__bytes_write.sum over the 337 GEMM launches of its first three groups:
+# 82 gate/up at 102.1 MB, 82 O and 82 down at 99.8 MB, 82 Q at 35.9 MB, 3
+# router at 896.1 MB, 6 K/V projections at 469.9 MB), launch-weighted.
+GEMM_DRAM_BYTES_PER_LAUNCH = (82 * 102.1 + 164 * 99.8 + 82 * 35.9 + 3 * 896.1 + 6 * 469.9) / 337 * 1e6
+GEMM_DRAM_SOURCE = ("ncu launch list of the timed prefill step (first 600 launches), "
+                    "launch-weighted mean over its 337 GEMM launches")
 
 
 def parse():
@@ -478,7 +486,8 @@ def run_ours(args, ws, rank, local):
         roofline = {"kernel": "gemm_tc_kernel (tcgen05 GEMM engine, all stack/router/projection/"
                               "LM-head contractions)",
                     "bound": "tensor", "achieved": gemm["achieved"], "peak": tc_peak,
-                    "unit": "TFLOP/s", "frac": gemm["achieved"] / tc_peak, "traffic": None,
+                    "unit": "TFLOP/s", "frac": gemm["achieved"] / tc_peak,
+                    "traffic": GEMM_DRAM_BYTES_PER_LAUNCH, "traffic_source": GEMM_DRAM_SOURCE,
                     "peak_source": f"{pk_kind} bf16_tflops_sustained",
                     "launches_timed": gemm["launches"], "avg_launch_ms": gemm["avg_ms"],
                     "flops_per_launch": gemm["work_per_launch"], "by_flops_per_launch": gemm_shapes}
