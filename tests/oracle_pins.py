@@ -744,6 +744,30 @@ def check_pool_backward_finite_differences(O):
     _fd_check(O, c, W, states, pos, static, 54)
 
 
+def check_kv_residual(O):
+    """The fixed-point residual ||KV_n - KV_(n-1)|| / ||KV_n||: zero between a
+    cache and itself, one from a zero cache, a / (1 + a) for a cache scaled by
+    1 + a, and zero between two passes once the fixed point is reached (a pass
+    with g = T is exact token-by-token evaluation, so a second one moves
+    nothing)."""
+    rng = np.random.default_rng(21)
+    k = rng.standard_normal((2, 3, 2, 5, 4))
+    v = rng.standard_normal(k.shape)
+    assert O.kv_residual(k, v, k, v) == 0.0
+    _close(O.kv_residual(0.0 * k, 0.0 * v, k, v), 1.0, what="from zero")
+    _close(O.kv_residual(k, v, 1.5 * k, 1.5 * v), 0.5 / 1.5, what="scaled")
+    _close(O.kv_residual(k, v, k, 2.0 * v),
+           math.sqrt(np.sum(v * v) / (np.sum(k * k) + 4.0 * np.sum(v * v))), what="one branch")
+    c = _cfg()
+    W = _weights(c, seed=22)
+    tokens = _tokens(c, 2, 5, 23)
+    ck, cv = O.new_cache(c, 2, 5)
+    O.cyclic_pass(c, W, tokens, 5, ck, cv)
+    pk, pv = ck.copy(), cv.copy()
+    O.cyclic_pass(c, W, tokens, 5, ck, cv)
+    assert O.kv_residual(pk, pv, ck, cv) <= 1e-14
+
+
 def _golden(name):
     """Entries "name value unit" of a fixture under tests/golden/."""
     import os
@@ -853,4 +877,5 @@ ALL_CHECKS = [
     check_feedback_free_router_reads_prefix,
     check_pool_backward_finite_differences,
     check_parameter_counts_match_pages,
+    check_kv_residual,
 ]

@@ -77,6 +77,9 @@ MUTANTS = [
      '(x @ _f64(W["Wr"][0]).T).reshape(N, k, L)'),
     ("pool_channels_share_wk", "pool", '(stored[:, 0, j] @ _f64(W["Wk"][j]).T)',
      '(stored[:, 0, j] @ _f64(W["Wk"][0]).T)'),
+    ("residual_key_branch_only", "kv_residual",
+     "num = np.sum((_f64(cur_k) - _f64(prev_k)) ** 2) + np.sum((_f64(cur_v) - _f64(prev_v)) ** 2)",
+     "num = np.sum((_f64(cur_k) - _f64(prev_k)) ** 2)"),
     ("pool_shared_src_norm", "pool", 'n = rmsnorm(states, W["src_norm"][beta], cfg.eps)',
      'n = rmsnorm(states, W["src_norm"][0], cfg.eps)'),
     ("states_are_outputs", "run_rows", "        states[:, l] = h\n        h = consumer_layer(cfg, W, l, h, seq, pos, cache_k, cache_v)",
