@@ -52,14 +52,11 @@ from cross_layer_kv_pool_b300 import synth  # noqa: E402
 
 METRIC = "prefill tok/s (3 cyclic passes, g=16) at 1.3B k=14"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
-# DRAM bytes (read + written) per tcgen05 GEMM launch of the prefill step, from
-# one ncu capture of the step's launch list (dram__bytes_read.sum +
-# dram__bytes_write.sum over the 337 GEMM launches of its first three groups:
-# 82 gate/up at 102.1 MB, 82 O and 82 down at 99.8 MB, 82 Q at 35.9 MB, 3
-# router at 896.1 MB, 6 K/V projections at 469.9 MB), launch-weighted.
-GEMM_DRAM_BYTES_PER_LAUNCH = (82 * 102.1 + 164 * 99.8 + 82 * 35.9 + 3 * 896.1 + 6 * 469.9) / 337 * 1e6
-GEMM_DRAM_SOURCE = ("ncu launch list of the timed prefill step (first 600 launches), "
-                    "launch-weighted mean over its 337 GEMM launches")
+# DRAM bytes (read + written) per tcgen05 GEMM launch of the prefill step:
+# None until a capture of the current kernels exists (the roofline's
+# ``traffic`` is then reported as null).
+GEMM_DRAM_BYTES_PER_LAUNCH = None
+GEMM_DRAM_SOURCE = "not captured for the current kernels"
 
 
 def parse():
@@ -72,6 +69,8 @@ def parse():
                     choices=["prefill_1p3b", "half_small", "full_small", "tiny_fp32"])
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="skip the tiny / half-small / full-small prefill lines")
     ap.add_argument("--k", type=int, default=None, help="override the channel count k")
     ap.add_argument("--kernel", choices=["mixer", "attention", "pool_backward", "decode"],
                     default=None,
@@ -212,7 +211,12 @@ def cpu_sample(shape, rows: int, Wn, seed: int = 0):
     oc.storage = "bf16"
     T, g = 2048, 16
     q = g - 1
-    pos = np.arange(q, T, g)[:rows]
+    # rows spread over the sequence (first and last of the group, then the
+    # middle), so that the sample's attention sees ~T/2 keys on average
+    allp = np.arange(q, T, g)
+    pick = np.unique(np.linspace(0, len(allp) - 1, rows).round().astype(int))
+    pos = allp[pick]
+    rows = len(pos)
     toks = np.random.default_rng(seed).integers(0, shape.V, size=rows)
     ck, cv = O.new_cache(oc, 1, T)
     threads = torch.get_num_threads()
@@ -244,7 +248,7 @@ def cpu_baseline_record(shape, passes: int, rows: int):
     secs, n, threads = cpu_sample(shape, rows, oracle_weights(shape))
     tok_s = n / secs / passes
     return {"value": tok_s, "unit": "tok/s", "cores": threads, "kind": "oracle",
-            "sample": (f"{n} token rows of one cyclic group (positions 15, 31, ... of a "
+            "sample": (f"{n} token rows of one cyclic group (positions 15 and 2047 of a "
                        f"2048-token sequence) through the {shape.L}-layer stack and the pool, "
                        f"fp64 NumPy, {secs:.1f} s; tok/s = rows / time / {passes} passes")}
 
@@ -505,6 +509,29 @@ def run_ours(args, ws, rank, local):
                      "flops": "causal only (4*Hq*d per visible key)",
                      "launches_timed": attn["launches"], "avg_launch_ms": attn["avg_ms"]}
 
+    # cache writes of the K/V projections (their epilogue scatters the new
+    # channel entries): bytes written per launch over the launch's time
+    cache_write = None
+    kv_flops = 2.0 * wm.rows_for_pass(B, T, g) * s.Hkv * s.d * s.D * s.k
+    kv = [(ms_, w_) for ms_, w_ in tracers[0].results() if abs(w_ - kv_flops) < 0.5]
+    if kv:
+        kv_ms = statistics.mean(r[0] for r in kv)
+        kv_bytes = wm.rows_for_pass(B, T, g) * s.k * s.Hkv * s.d * 2
+        hbm = pk.get("hbm_gbs", 6400.0)
+        cache_write = {"kernel": "gemm_tc_kernel EPI_KV (K or V projection + K-norm + RoPE + "
+                                 "cache scatter)",
+                       "launches_timed": len(kv), "avg_launch_ms": kv_ms,
+                       "bytes_written_per_launch": kv_bytes,
+                       "achieved": kv_bytes / (kv_ms * 1e-3) / 1e9, "unit": "GB/s",
+                       "frac_of_hbm": kv_bytes / (kv_ms * 1e-3) / 1e9 / hbm,
+                       "note": "the launch is a tensor-core product; the cache write is its "
+                               "output stream, not its bound",
+                       "tflops": kv_flops / (kv_ms * 1e-3) / 1e12}
+
+    others = None
+    if args.workload == "prefill_1p3b" and not args.no_other_configs:
+        others = other_configs(args, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline_record(s, passes, rows=2)
@@ -516,10 +543,58 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded tokens, N(0,0.02) weights)",
         "config": config_dict(args, wl), "e2e": e2e, "gpu_launches": gpu_launches,
         "roofline": roofline, "mixer": mixer, "attention": attention, "decode": decode,
-        "cpu_baseline": cpu, "clocks": clk,
+        "cache_write": cache_write, "configs": others, "cpu_baseline": cpu, "clocks": clk,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def other_configs(args, dev):
+    """Prefill tok/s of the other workloads through the same step (CUDA events
+    around ``steps`` whole steps after ``warmup``): the tiny fp32 model (3
+    cyclic passes g = 4, and 64 Jacobi passes), the half-cache and the
+    full-cache small models (3 cyclic passes g = 16, B = 8, T = 2048)."""
+    from cross_layer_kv_pool_b300 import wm
+    out = {}
+    for name, sched in (("tiny_fp32", ((4, 3), (1, 64))), ("half_small", ((16, 3),)),
+                        ("full_small", ((16, 3),))):
+        wl = synth.WORKLOADS[name]
+        s, B, T = wl["shape"], wl["B"], wl["T"]
+        m = wm.Model(s, synth.make_weights(s, seed=0, device=dev))
+        tok = synth.make_tokens(s, B, T, seed=1, device=dev)
+        ck, cv = m.new_cache(B, T)
+        lg = torch.empty((B, s.V), dtype=torch.float32, device=dev)
+        res = {}
+        for g, passes in sched:
+            wsp = m.workspace(wm.rows_for_pass(B, T, g), T)
+
+            def step():
+                ck.zero_()
+                cv.zero_()
+                for n in range(passes):
+                    last = n == passes - 1
+                    wm.wm_cyclic_pass(m, tok, g, ck, cv, wsp, logits=lg if last else None,
+                                      logits_mode="last" if last else "none")
+            for _ in range(2):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(3):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            if wm.wm_check_flags(wsp) != 0:
+                raise RuntimeError(f"device-side checks failed ({name})")
+            ms = e0.elapsed_time(e1) / 3
+            res["jacobi" if g == 1 else "cyclic"] = {
+                "g": g, "passes": passes, "ms_per_step": ms, "tok_s": B * T / (ms / 1e3)}
+            del wsp
+        out[name] = {"L": s.L, "D": s.D, "k": s.k, "B": B, "T": T, "dtype": s.dtype,
+                     "tok_s": res["cyclic"]["tok_s"], **res}
+        del m, ck, cv
+        torch.cuda.empty_cache()
+    return out
 
 
 def decode_step_bytes(s, B, pos):

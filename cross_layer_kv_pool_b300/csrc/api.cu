@@ -82,7 +82,8 @@ wm_status check_config(const wm_config* c) {
   if (c->dtype != WM_F32 && c->dtype != WM_BF16) return WM_ERR_INVALID_ARG;
   if (c->d != 64 && c->d != 128) return WM_ERR_UNSUPPORTED;
   if (count_nR(*c) < 1) return WM_ERR_INVALID_ARG;
-  if (c->flags & ~(uint32_t)(WM_FLAG_SIMT_GEMM | WM_FLAG_NO_CLUSTER)) return WM_ERR_INVALID_ARG;
+  if (c->flags & ~(uint32_t)(WM_FLAG_SIMT_GEMM | WM_FLAG_NO_CLUSTER | WM_FLAG_WAIT_PROBE))
+    return WM_ERR_INVALID_ARG;
   return WM_OK;
 }
 
@@ -157,6 +158,7 @@ void gemm(const Ctx& x, const GemmDesc& gd) {
   GemmDesc g = gd;
   g.b_const = true;  // every product of the model multiplies by a weight matrix
   g.no_cluster = (x.c->flags & WM_FLAG_NO_CLUSTER) != 0;
+  g.wait_probe = (x.c->flags & WM_FLAG_WAIT_PROBE) != 0;
   g.partial = x.buf<float>(B_PARTIAL);
   g.partial_elems = (long long)(x.lay.off[B_PARTIAL + 1] - x.lay.off[B_PARTIAL]) / 4;
   if (g.partial_elems <= 0) g.partial = nullptr;
@@ -456,11 +458,24 @@ void decode_body(const Ctx& x, int B, double pos_sum, void* cache_k, void* cache
            x.buf<void>(B_MIXED), cache_k, cache_v, B, Tmax);
 }
 
+// The caller's per-row sequence and position arrays into the workspace.
+cudaError_t copy_rows(const Ctx& x, const int32_t* seq, const int32_t* pos, int N) {
+  cudaError_t e = cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4,
+                                  cudaMemcpyDeviceToDevice, x.st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  return e;
+}
+
 wm_status finish(const Ctx& x) {
   if (x.c->trace) x.c->trace->launches += x.launches;
   const cudaError_t e = cudaGetLastError();
   return (e == cudaSuccess && x.err == cudaSuccess) ? WM_OK : WM_ERR_CUDA;
 }
+
+// Device address of the allocation-free pool call's flag word (the first 256
+// bytes of its scratch array), defined with that array at the end of the file.
+void* pool_static_flags();
 
 }  // namespace
 
@@ -501,8 +516,7 @@ wm_status wm_pool_mix(const wm_config* cfg, const wm_weights* w, const void* sta
   if ((s = check_ws(*cfg, ws, ws_bytes, N, Tmax)) != WM_OK) return s;
   Ctx x = make_ctx(cfg, w, ws, N, Tmax, stream);
   const wm_config& c = *cfg;
-  cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
-  cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  if (copy_rows(x, seq, pos, N) != cudaSuccess) return WM_ERR_CUDA;
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
   zero_partials(x);
@@ -747,7 +761,14 @@ wm_status wm_decode_batch(const wm_config* cfg, const wm_weights* w, const int32
 }
 
 wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream) {
-  if (!ws || ws_bytes < 256 || ((uintptr_t)ws & 255u) || !flags_out) return WM_ERR_INVALID_ARG;
+  if (!flags_out) return WM_ERR_INVALID_ARG;
+  if (!ws && ws_bytes == 0) {
+    // the flag word of the allocation-free pool call (wm_pool_mix_static)
+    ws = pool_static_flags();
+    if (!ws) return WM_ERR_CUDA;
+    ws_bytes = 256;
+  }
+  if (!ws || ws_bytes < 256 || ((uintptr_t)ws & 255u)) return WM_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint32_t f = 0;
   if (cudaMemcpyAsync(&f, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return WM_ERR_CUDA;
@@ -793,6 +814,8 @@ void* pool_scratch_address() {
   }
   return addr[dev];
 }
+
+void* pool_static_flags() { return pool_scratch_address(); }
 
 // Compact layout: only the buffers the pool touches.
 Layout pool_static_layout(const wm_config& c, long long N, long long Tmax) {
@@ -842,8 +865,7 @@ extern "C" wm_status wm_pool_mix_static(const wm_config* cfg, const wm_weights* 
   const wm_config& c = *cfg;
   // the previous call's flag bits must not leak into this one
   if (cudaMemsetAsync(x.flags(), 0, 256, x.st) != cudaSuccess) return WM_ERR_CUDA;
-  cudaMemcpyAsync(x.buf<int32_t>(B_SEQ), seq, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
-  cudaMemcpyAsync(x.buf<int32_t>(B_POS), pos, (size_t)N * 4, cudaMemcpyDeviceToDevice, x.st);
+  if (copy_rows(x, seq, pos, N) != cudaSuccess) return WM_ERR_CUDA;
   ++x.launches;
   launch_rope_table(x.buf<float2>(B_ROPE), 0, Tmax, c.d, c.rope_base, x.st);
   ++x.launches;

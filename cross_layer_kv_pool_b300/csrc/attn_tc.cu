@@ -367,7 +367,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(pv_done, 1);
     mbar_init(o_free, 8);
     mbar_init(mma_done, 1);
-    *abort_flag = 0;
+    // A bounded wait of an earlier kernel of this call gave up: every role
+    // stops before issuing anything, so one timeout costs one wait limit per
+    // call rather than one per launch.
+    *abort_flag = (*(volatile const uint32_t*)p.flags & FLAG_TIMEOUT) ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -382,6 +385,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_holder;
+  // read by every thread here, before any role can have timed out, so that
+  // the two warps of a lane quarter agree
+  const bool entry_ok = *abort_flag == 0;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
   if (warp == 0 || warp == 3) {
@@ -394,7 +400,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* empty = kq ? k_empty : v_empty;
     const CUtensorMap* map = kq ? &tmK : &tmV;
     uint8_t* ring = sm + (kq ? SM::OFF_K : SM::OFF_V);
-    bool ok = true;
+    bool ok = entry_ok;
     int gb = 0, it = 0;
     uint32_t used = 0, lastk = 0;
     for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // tcgen05.mma operations of this thread execute in issue order, so
     // S(gb + 2) (issued after O += P(gb) V, into the same buffer) cannot
     // overwrite P(gb) before the product has read it.
-    bool ok = true;
+    bool ok = entry_ok;
     int gb = 0, it = 0, o_waited = 0;
     constexpr uint32_t id_qk = idesc(BKEY, false);
     constexpr uint32_t id_pv = idesc(HD, true);
@@ -523,7 +529,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int m = quarter * 32 + lane;   // query row of the tile = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = p.scale_log2;
-    bool ok = true;
+    bool ok = entry_ok;
     int gb = 0;
     auto warp_wait = [&](uint64_t* bb, uint32_t parity) -> bool {
       int w = 1;

@@ -146,6 +146,7 @@ struct GemmDesc {
   // request them before its predecessor in the stream has finished.
   bool b_const = false;
   bool no_cluster = false;       // split K through global atomics, never a cluster
+  bool wait_probe = false;       // test aid (WM_FLAG_WAIT_PROBE): see gemm_tc.cu
   Epi epi;
   // Zero-filled fp32 scratch for split-K (nullable): when a GEMM has too few
   // output tiles to occupy the GPU, K is split across CTAs that add their

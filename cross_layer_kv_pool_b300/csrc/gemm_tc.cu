@@ -23,6 +23,7 @@ namespace tc {
 
 constexpr int BM = 128, BK = 64, NTHREADS = 192;
 constexpr unsigned long long WAIT_NS = 4000000000ull;  // 4 s bound on any wait
+constexpr unsigned long long PROBE_NS = 2000000ull;    // 2 ms: the wait_probe barrier
 
 struct Params {
   int M, N, K, batch;
@@ -33,6 +34,7 @@ struct Params {
   float* partial;         // split-K accumulation target [batch][M][N] (x2 when DUAL)
   int cluster_red;        // split-K over a thread-block cluster, reduced in shared memory
   int b_const;            // B tiles may be requested before the predecessor grid ends
+  int wait_probe;         // test aid: the MMA issuer first waits on a barrier nothing completes
   Epi epi;
 };
 
@@ -69,13 +71,14 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait; false on timeout or when another role already gave up.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          unsigned long long limit_ns = WAIT_NS) {
   if (mbar_try(b, parity)) return true;
   const unsigned long long t0 = gtimer();
   while (true) {
     if (mbar_try(b, parity)) return true;
     if (*abort_flag) return false;
-    if (gtimer() - t0 > WAIT_NS) return false;
+    if (gtimer() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ void tma_load3(const CUtensorMap* map, uint64_t* bar, void* dst, int c0,
@@ -687,7 +690,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* tfull = empty + C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* mma_done = tempty + 2;
-  uint32_t* tmem_holder = (uint32_t*)(mma_done + 1);
+  uint64_t* probe = mma_done + 1;  // wait_probe: a barrier that nothing completes
+  uint32_t* tmem_holder = (uint32_t*)(probe + 1);
   volatile int* abort_flag = (volatile int*)(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -701,6 +705,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(&tempty[a], 4);
     }
     mbar_init(mma_done, 1);
+    mbar_init(probe, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -757,6 +762,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int nt = rem % p.n_tiles, mt = rem / p.n_tiles;  // column tiles fastest
         const int kb0 = ks * p.kb_per, kb1 = min(p.num_kb, kb0 + p.kb_per);
         for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+          // Another role gave up (or the call had already timed out): stop,
+          // once the stages whose B tiles went out early have their A tiles
+          // too (their byte counts are posted in full).
+          if (issued >= pre && *abort_flag) {
+            ok = false;
+            break;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag)) {
             ok = false;
             break;
@@ -792,6 +804,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int stage = 0, it = 0;
       uint32_t phase = 0;
       bool ok = true;
+      // A bounded wait of an earlier kernel of this call gave up: issue
+      // nothing, so that one timeout costs one wait limit per call rather
+      // than one per launch.
+      if (*(volatile uint32_t*)p.epi.flags & FLAG_TIMEOUT) {
+        ok = false;
+        *abort_flag = 1;
+      } else if (p.wait_probe) {
+        // test aid: a wait that runs out (nothing arrives at ``probe``)
+        if (!mbar_wait(probe, 0, abort_flag, PROBE_NS)) ok = false;
+      }
       for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
@@ -1025,6 +1047,7 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   p.vec_res = ((uintptr_t)g.epi.R % 16 == 0) && ((g.epi.ldr * 2) % 16 == 0);
   p.vec_fin = fin_vectorisable(g);
   p.b_const = g.b_const ? 1 : 0;
+  p.wait_probe = g.wait_probe ? 1 : 0;
   if (p.cluster_red) {
     // one CTA per (output tile, K slice); a cluster holds one tile's slices
     cudaLaunchConfig_t lc = {};

@@ -125,6 +125,12 @@ __global__ void __launch_bounds__(NT, 1) mix_stream_kernel(const MixArgs a, uint
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  {  // an earlier kernel of this call timed out: leave before issuing anything
+    __shared__ int stop;
+    if (tid == 0) stop = (*(volatile const uint32_t*)flags & FLAG_TIMEOUT) != 0;
+    __syncthreads();
+    if (stop) return;
+  }
   // Chunk q of this block: row blockIdx.x + (q / nc) * gridDim.x, layers of chunk q % nc.
   auto issue = [&](int q) {
     const long long r = blockIdx.x + (long long)(q / nc) * gridDim.x;

@@ -169,6 +169,9 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
   // everything above touched only weights and shared memory
   pdl_wait();
   pdl_trigger();
+  // A bounded wait of an earlier kernel of this call gave up: nothing has
+  // been issued yet, so the CTA leaves at once (one wait limit per call).
+  if (*(volatile const uint32_t*)flags & FLAG_TIMEOUT) return;
 
   bool ok = true;
   if (warp == g.nwc) {

@@ -25,6 +25,7 @@ WM_F32, WM_BF16 = 0, 1
 LOGITS = {"none": 0, None: 0, "last": 1, "all": 2}
 WM_FLAG_SIMT_GEMM = 1
 WM_FLAG_NO_CLUSTER = 2
+WM_FLAG_WAIT_PROBE = 4
 
 EXPORTED = ("wm_workspace_size", "wm_pool_mix", "wm_channel_attn", "wm_cyclic_pass",
             "wm_decode_step", "wm_decode_batch", "wm_check_flags", "wm_status_string", "wm_abi_version",
@@ -322,6 +323,15 @@ def wm_check_flags(ws, stream=None) -> int:
     st = lib().wm_check_flags(_ptr(ws), ws.numel(), ctypes.byref(f), _stream(stream))
     if st not in (WM_OK,):
         raise WMError(st, f"wm_check_flags (flags=0x{f.value:x})")
+    return f.value
+
+
+def wm_check_static_flags(stream=None) -> int:
+    """wm_check_flags on the flag word of wm_pool_mix_static's internal scratch."""
+    f = ctypes.c_uint32(0)
+    st = lib().wm_check_flags(None, 0, ctypes.byref(f), _stream(stream))
+    if st not in (WM_OK,):
+        raise WMError(st, f"wm_check_flags (static scratch, flags=0x{f.value:x})")
     return f.value
 
 

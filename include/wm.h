@@ -23,6 +23,11 @@
  *    Device-side checks (token ids, sequence indices, positions out of range)
  *    skip the offending access and set bits in the workspace's flag word, read
  *    (and cleared) by wm_check_flags after the work.
+ *  - Every device-side wait is bounded (4 s). A wait that gives up sets the
+ *    timeout bit of the flag word; each later kernel of the same call that
+ *    holds bounded waits reads that bit at entry and returns without work, so
+ *    one timeout costs at most one wait limit per kernel in flight, not one
+ *    per launch. Results of a call that timed out are unspecified.
  *  - Cache layout: cache_k and cache_v are [B][k][Hkv][Tmax][d] each. Keys are
  *    stored after K-norm and RoPE, values raw ([PL 3 METHOD, "Cross-layer KV
  *    pool"]: stored keys are rotated and K-normalised, values stay raw; the
@@ -65,6 +70,16 @@ typedef enum {
                                  finalize kernel instead of a thread-block
                                  cluster (the path taken where a cluster does
                                  not fit; a test aid elsewhere) */
+#define WM_FLAG_WAIT_PROBE 4u /* test aid for the timeout path: before its first
+                                 product, each CTA of the tensor-core GEMM
+                                 engine waits on a barrier that nothing
+                                 completes, with a 2 ms limit. The wait runs
+                                 out, the kernel raises the timeout bit, drains
+                                 its copies and returns; every later kernel of
+                                 the call that holds bounded waits finds the
+                                 bit at entry and returns at once. The call's
+                                 results are then unspecified and
+                                 wm_check_flags reports WM_ERR_TIMEOUT. */
 
 /* Optional measurement hook (wm_config.trace, nullable). While entries
  * remain, an entry point records begin[i] / end[i] (caller-created
@@ -268,7 +283,9 @@ wm_status wm_decode_batch(const wm_config* cfg, const wm_weights* w,
 
 /* Waits for ``stream``, copies the workspace flag word to *flags_out (host)
  * and clears it. Returns WM_ERR_DEVICE_BOUNDS if an index check failed and
- * WM_ERR_TIMEOUT if a bounded wait gave up since the last call. */
+ * WM_ERR_TIMEOUT if a bounded wait gave up since the last call.
+ * ws = NULL with ws_bytes = 0 selects the flag word that wm_pool_mix_static
+ * keeps in its internal scratch (on the current device). */
 wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* stream);
 
 /* wm_pool_mix without a workspace, for callers that cannot allocate device
@@ -280,9 +297,12 @@ wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* s
  *
  * Scratch: one device array of WM_POOL_STATIC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
- * Rows beyond what fits (RoPE table of Tmax positions, then per row about
- * 4*nR*D + 4*k*D + 8*k*L + 4*L + 8 bytes in bf16 storage) return
- * WM_ERR_WORKSPACE before anything is launched. The call itself allocates
+ * It holds a 256-byte flag word, the RoPE table (4*d*Tmax bytes) and, per
+ * row, 8 + 2*e*nR*D + 4*L + 8*k*L + 2*e*k*D + 64*k bytes, where e is the
+ * storage element size (2 for bf16, 4 for fp32); each of those seven
+ * per-row buffers is rounded up to a multiple of 256 bytes (at most 7*255
+ * more in all). Calls whose rows do not fit return WM_ERR_WORKSPACE before
+ * anything is launched. The call itself allocates
  * nothing: no cudaMalloc, cudaFree or allocating library routine.
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
@@ -290,8 +310,9 @@ wm_status wm_check_flags(void* ws, size_t ws_bytes, uint32_t* flags_out, void* s
  * previous call's contents there; the call clears what must start at zero
  * (its flag word) itself. Calls that overlap on the GPU - on different
  * streams, or from different host threads - race on the array and must be
- * serialised by the caller. Device-side index checks of this call are not
- * reported (its flag word is internal). */
+ * serialised by the caller. Device-side checks of this call (index bounds,
+ * bounded waits) set bits in its internal flag word, which the call clears
+ * at its start; read it with wm_check_flags(NULL, 0, &flags, stream). */
 #define WM_POOL_STATIC_SCRATCH_BYTES (32u << 20)
 wm_status wm_pool_mix_static(const wm_config* cfg, const wm_weights* w,
                              const void* states, int32_t N,

@@ -26,6 +26,21 @@ TOL = {"f32": dict(logits=1e-4, cache=1e-4, mixed=1e-4, coeff=1e-4, attn=1e-4,
                     cache_step=1e-1, cache_step_norm=3e-2)}
 
 
+def record(test: str, **vals):
+    """Print the measured errors of one parity check and, when the
+    environment variable WM_PARITY_LOG names a file, append them to it as one
+    JSON line (the record of what each bf16 comparison achieved)."""
+    import json
+    import os
+    line = json.dumps({"test": test, **{k: (float(v) if isinstance(v, (float, np.floating)) else v)
+                                        for k, v in vals.items()}})
+    print("parity", line)
+    path = os.environ.get("WM_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
+
+
 def normerr(a, b) -> float:
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
@@ -88,13 +103,17 @@ SPREAD_EPS = 1e-5     # relative size of fp32-vs-fp64 differences in long reduct
 SPREAD_FACTOR = 2.5   # the GPU may move at most this many times the oracle's own spread
 
 
-def within(err, base, spread):
-    """err <= max(base tolerance, SPREAD_FACTOR x measured oracle spread)."""
+def within(err, base, spread, what=""):
+    """err <= max(base tolerance, SPREAD_FACTOR x measured oracle spread).
+    Records the error, the spread and whether the fixed bound alone held."""
+    import os
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    record(test, what=what, err=err, base=base, spread=spread, fixed_ok=bool(err <= base))
     return err <= max(base, SPREAD_FACTOR * spread)
 
 
 def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", check=None,
-                    spread=False):
+                    spread=False, static=None, oc=None):
     """Run ``passes`` cyclic passes on the GPU one group at a time. Before each
     checked group (``check(n, q)``), copy the GPU cache to the host, run the
     oracle's same group from that snapshot, and compare what the group wrote
@@ -105,7 +124,7 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
     any bf16-level difference along the sequence (see the design notes)."""
     import oracle.whitematter as O
     s = m.shape
-    oc = ocfg(s)
+    oc = oc or ocfg(s)
     B, T = tokens_h.shape
     Tmax = Tmax or T
     tok = torch.tensor(tokens_h, dtype=torch.int32, device="cuda")
@@ -130,12 +149,12 @@ def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", c
                 continue
             torch.cuda.synchronize()
             rl = O.cyclic_pass(oc, Wn, tokens_h, g, sk, sv, q_begin=q, q_end=q + 1,
-                               logits=None if mode == "none" else mode)
+                               logits=None if mode == "none" else mode, static_coeff=static)
             P = np.arange(q, T, g)
             gk, gv = host(ck), host(cv)
             if spread:
                 pl = O.cyclic_pass(oc, Wp, tokens_h, g, pk, pv, q_begin=q, q_end=q + 1,
-                                   logits=None if mode == "none" else mode)
+                                   logits=None if mode == "none" else mode, static_coeff=static)
                 worst["spread_cache"] = max(worst["spread_cache"],
                                             relerr(pk[:, :, :, P], sk[:, :, :, P]),
                                             relerr(pv[:, :, :, P], sv[:, :, :, P]))

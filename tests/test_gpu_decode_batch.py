@@ -62,8 +62,8 @@ def test_decode_batch_ragged_positions(dtype, shape_kw):
         pk, pv = sk.copy(), sv.copy()
         pl = O.decode_batch(oc, perturbed(Wn, SPREAD_EPS), tok_h, pos_h, pk, pv)
         spread_kv = relerr(np.stack([pk[rows, :, :, pos_h], pv[rows, :, :, pos_h]]), ref_kv)
-        assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl))
-        assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv)
+        assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl), "logits")
+        assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv, "cache")
     # nothing but the rows' own positions changed
     mask = np.ones(Tmax, dtype=bool)
     for b in range(B):
@@ -191,8 +191,8 @@ def test_decode_batch_1p3b_widths_ragged():
     ref_kv = np.stack([rk[rows, :, :, pos_h], rv[rows, :, :, pos_h]])
     spread_kv = relerr(np.stack([pk[rows, :, :, pos_h], pv[rows, :, :, pos_h]]), ref_kv)
     tol = TOL["bf16"]
-    assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl))
-    assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv)
+    assert within(relerr(host(lg), rl), tol["logits"], relerr(pl, rl), "logits")
+    assert within(relerr(got_kv, ref_kv), tol["cache"], spread_kv, "cache")
 
 
 def test_decode_batch_split_k_fallback_matches_cluster():

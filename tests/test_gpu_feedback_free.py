@@ -113,5 +113,5 @@ def test_feedback_free_bf16_vs_oracle(shape_kw):
     rlg, rck, rcv = _oracle(s, Wn, tokens)
     plg, pck, pcv = _oracle(s, perturbed(Wn, SPREAD_EPS), tokens)
     spread_c = max(relerr(pck, rck), relerr(pcv, rcv))
-    assert within(relerr(lg, rlg), TOL["bf16"]["logits"], relerr(plg, rlg))
-    assert within(max(relerr(ck, rck), relerr(cv, rcv)), TOL["bf16"]["cache"], spread_c)
+    assert within(relerr(lg, rlg), TOL["bf16"]["logits"], relerr(plg, rlg), "logits")
+    assert within(max(relerr(ck, rck), relerr(cv, rcv)), TOL["bf16"]["cache"], spread_c, "cache")

@@ -97,11 +97,11 @@ def test_full_prefill_group_sampled_rows():
     ref = np.stack([res["K"], res["V"]])
     per = np.stack([rp["K"], rp["V"]])
     tol = TOL["bf16"]
-    assert within(relerr(got, ref), tol["cache_step"], relerr(per, ref)), (relerr(got, ref), relerr(per, ref))
-    assert within(normerr(got, ref), tol["cache_step_norm"], normerr(per, ref)), \
+    assert within(relerr(got, ref), tol["cache_step"], relerr(per, ref), "cache"), (relerr(got, ref), relerr(per, ref))
+    assert within(normerr(got, ref), tol["cache_step_norm"], normerr(per, ref), "cache_norm"), \
         (normerr(got, ref), normerr(per, ref))
     last = pos == T - 1
     got_l = host(lg)[np.array(seqs)[last]][:, vocab]
-    assert within(relerr(got_l, lo[last]), tol["logits"], relerr(lp[last], lo[last])), \
+    assert within(relerr(got_l, lo[last]), tol["logits"], relerr(lp[last], lo[last]), "logits"), \
         (relerr(got_l, lo[last]), relerr(lp[last], lo[last]))
 

@@ -7,7 +7,7 @@ import torch
 import oracle.whitematter as O
 from cross_layer_kv_pool_b300 import synth, wm
 from tests.gpu_util import (TOL, ensure_lib, host, isolated_decode, isolated_passes, model, ocfg,
-                            relerr, small_shape, within)
+                            record, relerr, small_shape, within)
 
 pytestmark = pytest.mark.gpu
 
@@ -91,6 +91,8 @@ def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax, rps):
         ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
                         for r in range(N)])
         err = relerr(host(out).reshape(N, Hq, d), ref)
+        record(f"attention_vs_oracle[{dtype},d={d},Hq={Hq},Hkv={Hkv},Tmax={Tmax},rps={rps}]",
+               channel=c, attn=err)
         assert err <= TOL[dtype]["attn"], err
 
 
@@ -124,6 +126,7 @@ def test_attention_group_rows_vs_oracle(dtype, d, Hq, Hkv, Tmax, g):
     ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
                     for r in rows])
     err = relerr(host(out).reshape(N, Hq, d)[rows], ref)
+    record(f"attention_group_rows[{dtype},d={d},Tmax={Tmax},g={g}]", attn=err)
     assert err <= TOL[dtype]["attn"], err
 
 
@@ -153,6 +156,10 @@ def test_pool_mix_vs_oracle(dtype, shape_kw):
     assert wm.wm_check_flags(ws) == 0
     ref = O.pool(ocfg(s), Wn, host(states), pos_h)
     tol = TOL[dtype]
+    record(f"pool_mix_vs_oracle[{dtype},{shape_kw}]", coeff=relerr(host(coeff), ref["coeff"]),
+           mixed=relerr(host(mixed).transpose(2, 0, 1, 3), ref["mixed"]),
+           K=relerr(host(ck)[seq_h, :, :, pos_h, :], ref["K"]),
+           V=relerr(host(cv)[seq_h, :, :, pos_h, :], ref["V"]))
     assert relerr(host(coeff), ref["coeff"]) <= tol["coeff"]
     assert relerr(host(mixed).transpose(2, 0, 1, 3), ref["mixed"]) <= tol["mixed"]
     K, Vv = host(ck), host(cv)
@@ -248,8 +255,8 @@ def test_decode_steps_isolated(dtype, shape_kw):
     tokens = np.random.default_rng(3).integers(0, s.V, size=(B, T))
     w = isolated_decode(m, Wn, tokens, Tmax=T + 5, spread=dtype == "bf16")
     tol = TOL[dtype]
-    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
-    assert within(w["cache"], tol["cache"], w["spread_cache"]), w
+    assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), w
+    assert within(w["cache"], tol["cache"], w["spread_cache"], "cache"), w
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -268,8 +275,8 @@ def test_decode_long_context_isolated(dtype, shape_kw):
         w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start,
                             spread=dtype == "bf16")
         tol = TOL[dtype]
-        assert within(w["logits"], tol["logits"], w["spread_logits"]), (start, w)
-        assert within(w["cache"], tol["cache"], w["spread_cache"]), (start, w)
+        assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), (start, w)
+        assert within(w["cache"], tol["cache"], w["spread_cache"], "cache"), (start, w)
 
 
 def test_decode_1p3b_widths_isolated():
@@ -285,8 +292,8 @@ def test_decode_1p3b_widths_isolated():
     tokens = np.random.default_rng(5).integers(0, s.V, size=(B, 3))
     w = isolated_decode(m, Wn, tokens, Tmax, start_cache=(ck, cv), start_pos=start, spread=True)
     tol = TOL["bf16"]
-    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
-    assert within(w["cache"], tol["cache"], w["spread_cache"]), w
+    assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), w
+    assert within(w["cache"], tol["cache"], w["spread_cache"], "cache"), w
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -328,8 +335,8 @@ def test_uneven_groups_isolated(dtype, mode):
     w = isolated_passes(m, Wn, tokens, g, 3, Tmax=T + 3, logits_mode=mode, spread=dtype == "bf16")
     tol = TOL[dtype]
     assert w["checked"] == 18
-    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
-    assert within(w["cache"], tol["cache"], w["spread_cache"]), w
+    assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), w
+    assert within(w["cache"], tol["cache"], w["spread_cache"], "cache"), w
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -357,6 +364,7 @@ def test_identity_router_full_cache(dtype):
             w = isolated_passes(m, Wn, tokens, 4, 4, logits_mode="all")
         finally:
             Om.cyclic_pass = orig
+        record("identity_router_bf16", **w)
         assert w["logits"] <= 2e-2 and w["cache"] <= 2e-2, w
 
 
@@ -370,9 +378,9 @@ def test_half_small_bf16_isolated_groups():
     w = isolated_passes(m, Wn, tokens, g, 3, logits_mode="last", spread=True)
     tol = TOL["bf16"]
     assert w["checked"] == 48
-    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
-    assert within(w["cache"], tol["cache_step"], w["spread_cache"]), w
-    assert within(w["cache_norm"], tol["cache_step_norm"], w["spread_cache_norm"]), w
+    assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), w
+    assert within(w["cache"], tol["cache_step"], w["spread_cache"], "cache"), w
+    assert within(w["cache_norm"], tol["cache_step_norm"], w["spread_cache_norm"], "cache_norm"), w
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -388,9 +396,9 @@ def test_multi_tile_groups_isolated(dtype):
                         spread=dtype == "bf16")
     tol = TOL[dtype]
     assert w["checked"] == 3
-    assert within(w["logits"], tol["logits"], w["spread_logits"]), w
-    assert within(w["cache"], tol["cache_step"], w["spread_cache"]), w
-    assert within(w["cache_norm"], tol["cache_step_norm"], w["spread_cache_norm"]), w
+    assert within(w["logits"], tol["logits"], w["spread_logits"], "logits"), w
+    assert within(w["cache"], tol["cache_step"], w["spread_cache"], "cache"), w
+    assert within(w["cache_norm"], tol["cache_step_norm"], w["spread_cache_norm"], "cache_norm"), w
 
 
 def test_large_groups_fp32_isolated():
@@ -424,6 +432,10 @@ def test_pool_mix_multi_tile_bf16(N):
     wm.wm_pool_mix(m, states, seq, pos, ck, cv, ws, coeff_out=coeff, mixed_out=mixed)
     torch.cuda.synchronize()
     ref = O.pool(ocfg(s), Wn, host(states), pos_h)
+    record(f"pool_mix_multi_tile_bf16[N={N}]", coeff=relerr(host(coeff), ref["coeff"]),
+           mixed=relerr(host(mixed).transpose(2, 0, 1, 3), ref["mixed"]),
+           K=relerr(host(ck)[seq_h, :, :, pos_h, :], ref["K"]),
+           V=relerr(host(cv)[seq_h, :, :, pos_h, :], ref["V"]))
     assert relerr(host(coeff), ref["coeff"]) <= 2e-2
     assert relerr(host(mixed).transpose(2, 0, 1, 3), ref["mixed"]) <= 1e-2
     K = host(ck)
