@@ -100,6 +100,10 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
 // Tensor-core mixer (bf16, deferred norm); returns P, or 0 if the shape is
 // outside its envelope (k > 16, L > 64, 2kL > 1024, misaligned operands).
 int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
+// tcgen05 mixer with the layer operand in tensor memory (bf16, deferred
+// norm); returns P, or 0 outside its envelope (k > 16, L > 32, D not a
+// multiple of 128 or more than 8 slices of 256 columns, misaligned operands).
+int launch_mix_tmem(const MixArgs& a, cudaStream_t st, uint32_t* flags);
 
 // ---------------------------------------------------------------------------
 // Backward pass of the pool (pool_bwd.cu)

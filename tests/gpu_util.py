@@ -100,16 +100,38 @@ def perturbed(Wn, eps, seed=12345):
 
 
 SPREAD_EPS = 1e-5     # relative size of fp32-vs-fp64 differences in long reductions
-SPREAD_FACTOR = 2.5   # the GPU may move at most this many times the oracle's own spread
+SPREAD_FACTOR = 2.5   # a widened check allows this many times the oracle's own spread
+
+# Whole-step bf16 comparisons for which the fixed bound is not attainable: the
+# oracle against itself, with its weights perturbed by SPREAD_EPS, already
+# moves the quantity by about the bound or more (random-weight models amplify
+# single bf16 rounding flips through the signed mixing and the depth of the
+# stack). Only these (test, quantity) pairs may use max(bound, SPREAD_FACTOR x
+# spread); every other comparison is held to its fixed bound. The recorded
+# numbers (max-element error / oracle spread, B300) that justify each entry:
+WIDENED = {
+    ("test_full_prefill_group_sampled_rows", "logits"): "3.70e-2 / 3.84e-2",
+    ("test_full_prefill_group_sampled_rows", "cache_norm"): "3.71e-2 / 3.58e-2 (norm)",
+    ("test_multi_tile_groups_isolated", "logits"): "2.57e-2 / 2.69e-2",
+    ("test_decode_batch_1p3b_widths_ragged", "cache"): "2.73e-2 / 4.75e-2",
+    ("test_decode_1p3b_widths_isolated", "cache"): "3.29e-2 / 4.13e-2",
+    ("test_decode_long_context_isolated", "cache"): "2.17e-2 / 4.55e-2",
+    ("test_uneven_groups_isolated", "cache"): "2.02e-2 / 3.23e-2",
+    ("test_cyclic_pass_rank_bf16_isolated", "logits"): "2.00e-2 / (spread first recorded here)",
+}
 
 
 def within(err, base, spread, what=""):
-    """err <= max(base tolerance, SPREAD_FACTOR x measured oracle spread).
+    """The fixed bound ``base``, or, for the (test, quantity) pairs listed in
+    WIDENED only, max(base, SPREAD_FACTOR x the oracle's measured spread).
     Records the error, the spread and whether the fixed bound alone held."""
     import os
     test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
-    record(test, what=what, err=err, base=base, spread=spread, fixed_ok=bool(err <= base))
-    return err <= max(base, SPREAD_FACTOR * spread)
+    name = test.split("::")[-1].split("[")[0]
+    widened = (name, what) in WIDENED
+    record(test, what=what, err=err, base=base, spread=spread, fixed_ok=bool(err <= base),
+           widened=widened)
+    return err <= (max(base, SPREAD_FACTOR * spread) if widened else base)
 
 
 def isolated_passes(m, Wn, tokens_h, g, passes, Tmax=None, logits_mode="last", check=None,
