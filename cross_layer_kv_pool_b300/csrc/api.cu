@@ -12,7 +12,7 @@ namespace {
 
 enum Buf {
   B_FLAGS, B_ROPE, B_TOK, B_SEQ, B_POS, B_ROWMAP, B_STASH, B_HMID, B_HL, B_XN, B_Q, B_O,
-  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_CHSS, B_LASTX, B_PARTIAL, B_CNT, B_ATTNP, B_END,
+  B_ACT, B_RIN, B_INV, B_COEFF, B_MIXED, B_CHSS, B_ATILE, B_LASTX, B_PARTIAL, B_CNT, B_ATTNP, B_END,
   NBUF
 };
 
@@ -46,6 +46,7 @@ Layout make_layout(const wm_config& c, long long N, long long Tmax) {
   sz[B_COEFF] = (size_t)N * 2 * c.k * c.L * 4;
   sz[B_MIXED] = (size_t)N * 2 * c.k * c.D * es;
   sz[B_CHSS] = (size_t)N * 2 * c.k * 8 * 4;  // deferred channel-norm partial sums
+  sz[B_ATILE] = c.dtype == WM_BF16 ? (size_t)N * MIX_ATILE_BYTES : 0;  // mixer coefficient tiles
   {  // split-K partial sums for GEMMs of at most 128 rows
     const long long rows = N < 128 ? N : 128;
     long long w = 2LL * c.F;
@@ -171,6 +172,11 @@ void gemm(const Ctx& x, const GemmDesc& gd) {
     launch_gemm_simt(x.c->dtype, g, x.st);
   }
   trace_end(x, tr, 2.0 * g.M * g.N * (double)g.K * g.batch * (g.B2 ? 2 : 1));
+}
+
+// The mixer's coefficient-tile scratch, or null where the layout has none.
+void* mix_atile(const Ctx& x) {
+  return x.lay.off[B_ATILE + 1] > x.lay.off[B_ATILE] ? x.buf<void>(B_ATILE) : nullptr;
 }
 
 Epi base_epi(const Ctx& x) {
@@ -306,6 +312,7 @@ int run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* c
   m.stash = states; m.ld_row = ld_row; m.inv = x.buf<float>(B_INV); m.coeff = coeff;
   m.src_norm = w.src_norm; m.chan_norm = w.chan_norm; m.mixed = mixed;
   m.chan_ss = x.buf<float>(B_CHSS);
+  m.atile = mix_atile(x);
   m.N = N; m.L = c.L; m.D = c.D; m.k = c.k; m.eps = c.eps;
   m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
   const int tr = trace_begin(x, WM_TRACE_MIX);
@@ -391,6 +398,7 @@ void run_pool_channel(const Ctx& x, int N, int l, void* cache_k, void* cache_v, 
   m.stash = x.buf<void>(B_STASH); m.ld_row = (long long)c.L * c.D; m.inv = x.buf<float>(B_INV);
   m.coeff = coeff; m.src_norm = w.src_norm; m.chan_norm = x.wp(w.chan_norm, (long long)l * c.D);
   m.mixed = x.buf<void>(B_MIXED); m.chan_ss = x.buf<float>(B_CHSS);
+  m.atile = mix_atile(x);
   m.N = N; m.L = Ls; m.D = c.D; m.k = 1; m.eps = c.eps;
   m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
   const int tr = trace_begin(x, WM_TRACE_MIX);
@@ -837,6 +845,8 @@ Layout pool_static_layout(const wm_config& c, long long N, long long Tmax) {
   put(B_COEFF, (size_t)N * 2 * c.k * c.L * 4);
   put(B_MIXED, (size_t)N * 2 * c.k * c.D * es);
   put(B_CHSS, (size_t)N * 2 * c.k * 8 * 4);
+  put(B_ATILE, c.dtype == WM_BF16 ? (size_t)N * MIX_ATILE_BYTES : 0);
+  lay.off[B_ATILE + 1] = o;  // marks the end of the tile scratch
   lay.total = o;
   return lay;
 }

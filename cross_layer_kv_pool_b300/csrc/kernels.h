@@ -76,6 +76,10 @@ bool attention_tc_supported(const AttnArgs& a, int nq);
 cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st);
 
 // ---- pool.cu ---------------------------------------------------------------
+// Bytes per row of the tensor-core mixer's coefficient tiles: [2 branches]
+// [hi, lo][16 channels][40] bf16 (32 layers + 8 of padding per row).
+constexpr long long MIX_ATILE_BYTES = 2 * 2 * 16 * 40 * 2;
+
 struct MixArgs {
   const void* stash;      // [N][L][D] source states
   long long ld_row;       // elements between rows (L*D for a stash)
@@ -85,6 +89,9 @@ struct MixArgs {
   const void* chan_norm;  // [2][k][D]
   void* mixed;            // [2][k][N][D]
   float* chan_ss;         // [N][2][k][8] slice sums of squares (deferred-norm output)
+  // scratch of the tensor-core mixer (nullable: that mixer is then not used):
+  // per row the hi/lo bf16 coefficient tile, MIX_ATILE_BYTES bytes
+  void* atile;
   int N, L, D, k;         // rows, source layers mixed (the first L of each row), width, channels
   int inv_ld;             // floats between rows of inv (>= L)
   int sn_layers;          // layers per branch in src_norm (>= L)
@@ -97,13 +104,10 @@ struct MixArgs {
 // rsqrt(sum / D + eps) (applied by the projection epilogue, or in place by
 // launch_mix_normalize).
 int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags);
-// Tensor-core mixer (bf16, deferred norm); returns P, or 0 if the shape is
-// outside its envelope (k > 16, L > 64, 2kL > 1024, misaligned operands).
+// Tensor-core mixer (bf16 mma.sync, deferred norm); returns P, or 0 if the
+// shape is outside its envelope (k > 16, L > 32, no slicing of D into at
+// most 8 slices of at most 448 columns, misaligned operands).
 int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
-// tcgen05 mixer with the layer operand in tensor memory (bf16, deferred
-// norm); returns P, or 0 outside its envelope (k > 16, L > 32, D not a
-// multiple of 128 or more than 8 slices of 256 columns, misaligned operands).
-int launch_mix_tmem(const MixArgs& a, cudaStream_t st, uint32_t* flags);
 
 // ---------------------------------------------------------------------------
 // Backward pass of the pool (pool_bwd.cu)

@@ -357,8 +357,7 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
   const bool stream_ok = dtype == WM_BF16 && !simt && a.D % (8 * MIX_C) == 0 &&
                          ((uintptr_t)a.stash % 16 == 0) && (a.ld_row % 8 == 0);
   if (dtype == WM_BF16 && !simt) {
-    int parts = launch_mix_tmem(a, st, flags);
-    if (!parts) parts = launch_mix_tc(a, st, flags);
+    const int parts = launch_mix_tc(a, st, flags);
     if (parts) return parts;
   }
   if (stream_ok) {

@@ -1,4 +1,4 @@
-// Pool mixer on the tensor cores (bf16 storage).
+// Pool mixer on the tensor cores (bf16 storage), mma.sync.
 //
 // Per token and branch b the mix is a small dense contraction
 //   M^b [k x D] = A^b [k x L] . X^b [L x D],
@@ -6,82 +6,110 @@
 // followed by the channel RMSNorm of each row of M^b ("WhiteMatter: All-to-All
 // Cross-Layer Connections via KV Mixing", 3 METHOD, "Cross-layer KV pool").
 // At 1.3B widths it is 2kL*D = 1.4M MAC per token against 204 kB of HBM
-// traffic, 13.8 flop/B: streaming at the HBM rate needs ~90 TFLOP/s, more than
-// the fp32 FMA pipes deliver, so the contraction runs on bf16 mma.sync.
-// A is split into hi + lo bf16 halves (~16 significant bits); X, the product
-// of a stored bf16 state and its bf16 gain, is split exactly into hi + lo;
-// three MMAs (hi.hi, hi.lo, lo.hi) keep the mix near fp32 accuracy.
+// traffic. The fp32 FMA pipes (35 TFMA/s measured) would need more time than
+// HBM does; bf16 mma.sync (287 TMAC/s measured) needs about 60% of it even
+// with three products per tile: A is split into hi + lo bf16 halves (~16
+// significant bits) and X, the product of a stored bf16 state and its bf16
+// gain, is split exactly into hi + lo; X_hi.A_hi + X_lo.A_hi + X_hi.A_lo keep
+// the mix near fp32 accuracy. (The contraction is too narrow for tcgen05:
+// with N = k <= 16 channels one M128 N16 K16 instruction costs ~100 cycles.)
 //
-// Layout of the work: D is cut into CS column slices of W <= 448 columns; a
-// CTA owns one slice for a subset of the rows (rows rg, rg + nrg, ...). Its
-// slice of both branches' source-norm gains stays resident in shared memory.
-// One producer warp streams the states through a ring of 16-layer chunks
-// (bulk TMA copies, one per layer, into padded rows so ldmatrix.trans is
-// conflict-free). Each compute warp owns 32 columns (four n8 tiles) of both
-// branches; the 16 x 8 accumulator tiles hold all k <= 16 channels. The
-// compute warps also build each row's hi/lo bf16 A tile together, one row
-// ahead (each its share, from coefficients prefetched a row earlier). Warps
-// synchronise only through mbarriers, so they drift by up to a row and one
-// warp's epilogue overlaps another's MMAs. Outputs go through a
-// double-buffered shared tile that a storer warp writes out with one bulk copy
-// per (branch, channel) row segment (full-line writes instead of 16-byte
-// pieces of eight rows per warp store).
-//
-// The channel RMSNorm's factor needs sums of squares over all D columns, which
-// no single CTA sees. The kernel therefore writes u = tau (.) m (the gained,
-// not yet normalised channel) and, per row, branch, channel and slice, the
+// Work layout. D is cut into CS column slices of W = 32 * nwc columns; a CTA
+// owns one slice for the rows rg, rg + nrg, ... Warp roles:
+//   compute warps (nwc): each owns 32 columns (four n8 tiles) of both
+//     branches; its source-norm gains live in registers in the B-fragment
+//     layout for the whole kernel. Per row: ldmatrix the coefficient tile
+//     (A, hi and lo) and the states (B, transposed), split gain x state into
+//     hi + lo, 24 mma.sync per K16 step; then the epilogue: u = tau (.) m
+//     (bf16) into a staging tile by stmatrix, and the sums of squares of m;
+//   feeder warp: lane 0 brings each row into a ring of NS stages: the
+//     states with ONE four-dimensional TMA box {64 columns, LP layers, W/64
+//     column blocks, 1 row} under the 128-byte swizzle (consecutive layers in
+//     consecutive 128-byte rows: conflict-free for ldmatrix.trans; the layers
+//     past L of the K padding arrive zero-filled), and the row's hi/lo
+//     coefficient tile with one bulk copy. The tiles are built beforehand by
+//     mix_atile_kernel: a feeder that computed them itself, sharing its
+//     sub-partition's issue slots with busy compute warps, took ~2.3 us per
+//     row for ~300 instructions;
+//   storer warp: sends each row's staging tile out with ONE four-dimensional
+//     TMA store {64 columns, 2k channel planes, W/64 blocks, 1 row} and sums
+//     the compute warps' partial sums of squares into the slice's value.
+// (Per-layer and per-channel bulk copies cost ~0.1 us each to issue: 28 of
+// each per row limited an earlier version to ~3.5 us per row.)
+// The channel RMSNorm factor needs sums over all D columns, which no CTA sees:
+// the kernel writes u = tau (.) m and, per row, branch, channel and slice, the
 // slice's sum of squares of m; the consumer of the channels (the K/V
-// projection, which is linear in its input) applies rsqrt(sum / D + eps) to
-// its output rows. launch_mix_normalize produces c itself where a caller
-// asks for it.
-#include <mutex>
+// projection, linear in its input) applies rsqrt(sum / D + eps) to its output
+// rows. launch_mix_normalize produces c itself where a caller asks for it.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "kernels.h"
 
 namespace wm {
 namespace {
 
-constexpr int NTW = 4;        // n8 tiles per compute warp (32 columns)
-constexpr int MAXV = 4;       // tile entries per compute thread per row (2kL <= 4 * 32 * warps)
-constexpr int MAX_WARPS = 14; // + producer + storer = 16 warps, 4 per SM sub-partition (128 registers)
-constexpr int RS = 4;         // rows in the coefficient-tile ring (>= 4, see the row loop)
+constexpr int NTW = 4;      // n8 tiles per compute warp (32 columns)
+constexpr int MAX_CW = 14;  // compute warps (+ feeder + storer = 16 warps: 128 registers)
+constexpr int NS = 4;       // stages (rows in flight): the row's states and coefficient tile
 
 struct MixGeo {
   int CS;    // column slices
   int W;     // columns per CTA
-  int LP;    // L rounded up to a multiple of 16 (MMA K)
-  int SROW;  // padded row stride (elements) of staged states and gains
-  int AST;   // padded row stride (elements) of the coefficient tiles
-  int nstg;  // 16-layer chunks in the state ring
   int nwc;   // compute warps (W / 32)
-  int OST;   // padded row stride (elements) of the output tiles
-  unsigned off_stage, off_atile, off_ss, off_out, off_bar, smem;
+  int LP;    // L rounded up to 16 or 32 (MMA K)
+  int AST;   // padded row stride (elements) of the coefficient tiles
+  int NB;    // 64-column blocks per CTA (W / 64)
+  unsigned state_bytes, stage_bytes, out_bytes;
+  unsigned off_stage, off_out, off_red, off_bar, smem;
 };
+
+constexpr unsigned long long WAIT_NS = 4000000000ull;  // 4 s bound on any wait
 
 __device__ __forceinline__ uint32_t su32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
-
-// Bounded phase wait: false after ~4 s (the caller records a timeout flag).
-__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity) {
-  unsigned long long t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    if (it == 0) t0 = t;
-    else if (t - t0 > 4000000000ull) return false;
+__device__ __forceinline__ unsigned long long gtimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false on timeout or when another warp already gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try(b, parity)) return true;
+  const unsigned long long t0 = gtimer();
+  while (true) {
+    if (mbar_try(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (gtimer() - t0 > WAIT_NS) return false;
   }
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+// One lane waits, the warp learns the outcome; then every lane observes the
+// completed phase itself (an acquire of its own, so that what the producer
+// or the TMA wrote is visible to each lane's reads).
+__device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait(b, parity, abort_flag) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) mbar_try(b, parity);
+  return ok != 0;
 }
 
 __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t (&r)[4]) {
@@ -93,6 +121,12 @@ __device__ __forceinline__ void ldsm4t(uint32_t addr, uint32_t (&r)[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                : "r"(addr));
+}
+__device__ __forceinline__ void stsm4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                      uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
 }
 // x*y of two bf16 pairs as an exact hi + lo pair of bf16 pairs: the product
 // of two 8-bit significands has at most 16 bits, hi holds it rounded to 8
@@ -110,161 +144,158 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// The first product of an accumulator: D = A.B (no zeroing pass).
+__device__ __forceinline__ void mma16816_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  const float z = 0.f;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 
-__global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
-    mix_tc_kernel(const MixArgs a, const MixGeo g, uint32_t* flags) {
-  extern __shared__ __align__(128) uint8_t sm[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rank = blockIdx.x % g.CS;            // column slice
-  const long long rg = blockIdx.x / g.CS;        // first row
-  const long long nrg = gridDim.x / g.CS;        // row stride
-  const int L = a.L, D = a.D, K = a.k, W = g.W, SROW = g.SROW, AST = g.AST, LP = g.LP;
-  const int c0 = rank * W;
-  const int nks = LP / 16;
-  const int atile_elems = 2 * 2 * 16 * AST;
-  __nv_bfloat16* gains = reinterpret_cast<__nv_bfloat16*>(sm);                // [2][LP][SROW]
-  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(sm + g.off_stage);  // [nstg][16][SROW]
-  __nv_bfloat16* atile = reinterpret_cast<__nv_bfloat16*>(sm + g.off_atile);  // [RS][2][2][16][AST]
-  float* red = reinterpret_cast<float*>(sm + g.off_ss);                       // [RS][nwc][32]
-  uint32_t* sscnt = reinterpret_cast<uint32_t*>(red + RS * g.nwc * 32);       // [RS]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + g.off_bar);               // [nstg]
-  uint64_t* empty = full + g.nstg;                                            // [nstg]
-  uint64_t* afull = empty + g.nstg;                                           // [RS]
-  uint64_t* ofull = afull + RS;                                               // [2]
-  uint64_t* oempty = ofull + 2;                                               // [2]
-  __nv_bfloat16* otile = reinterpret_cast<__nv_bfloat16*>(sm + g.off_out);    // [2][2][k][OST]
-  const int otile_elems = 2 * K * g.OST;
-  const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm;
+// Address of 16-byte chunk ``c16`` of 128-byte row ``row`` of a tile stored
+// with the 128-byte swizzle (the layout TMA writes and reads).
+__device__ __forceinline__ uint32_t swz128(uint32_t base, int row, int c16) {
+  return base + (uint32_t)row * 128u + (uint32_t)((c16 ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ void tma_load4(const CUtensorMap* map, uint64_t* bar, uint32_t dst, int c0,
+                                          int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(map), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store4(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                           int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(map),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
 
-  // Resident gains of this slice (rows l >= L zero); zeroed ring, tiles and sums.
-  {
-    const int w8 = W / 8, per_b = LP * w8;
-    for (int i = tid; i < 2 * per_b; i += blockDim.x) {
-      const int be = i / per_b, rem = i - be * per_b, l = rem / w8, c8 = (rem - l * w8) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (l < L) v = *reinterpret_cast<const uint4*>(sn + ((size_t)be * a.sn_layers + l) * D + c0 + c8);
-      *reinterpret_cast<uint4*>(gains + ((size_t)be * LP + l) * SROW + c8) = v;
-    }
-    for (unsigned o = g.off_stage + 16u * tid; o < g.off_bar; o += 16u * blockDim.x)
-      *reinterpret_cast<uint4*>(sm + o) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (tid == 0) {
-    for (int i = 0; i < g.nstg; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full[i])) : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&empty[i])), "r"(g.nwc)
-                   : "memory");
-    }
-    for (int i = 0; i < RS; ++i)
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&afull[i])), "r"(g.nwc)
-                   : "memory");
-    for (int i = 0; i < 2; ++i) {
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&ofull[i])), "r"(g.nwc)
-                   : "memory");
-      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&oempty[i])) : "memory");
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  __syncthreads();
-  // everything above touched only weights and shared memory
+// The mixer's per-row coefficient tiles: A^b_{j,l} = a^b_{j,l} inv_l split
+// into bf16 hi + lo (hi = bf16(A), lo = bf16(A - hi)), laid out as the
+// mixer's ldmatrix reads them, [2 b][2 hi/lo][16 j][40] (j >= k, l >= L and
+// the 8 padding columns zero). One block of 128 threads per row; each thread
+// writes pairs of entries.
+__global__ void __launch_bounds__(128) mix_atile_kernel(const MixArgs a) {
   pdl_wait();
   pdl_trigger();
-  // A bounded wait of an earlier kernel of this call gave up: nothing has
-  // been issued yet, so the CTA leaves at once (one wait limit per call).
-  if (*(volatile const uint32_t*)flags & FLAG_TIMEOUT) return;
+  const long long row = blockIdx.x;
+  const int L = a.L, K = a.k;
+  const float* cf = a.coeff + row * 2 * K * L;
+  const float* iv = a.inv + row * a.inv_ld;
+  uint32_t* out = reinterpret_cast<uint32_t*>((uint8_t*)a.atile + row * MIX_ATILE_BYTES);
+  // 2 * 2 * 16 rows of 20 pairs
+  for (int p = threadIdx.x; p < 2 * 2 * 16 * 20; p += blockDim.x) {
+    const int rr = p / 20, l0 = (p - rr * 20) * 2;
+    const int be = rr >> 5, hl = (rr >> 4) & 1, j = rr & 15;
+    float v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int l = l0 + e;
+      float x = 0.f;
+      if (j < K && l < L) {
+        const float A = cf[(be * K + j) * L + l] * iv[l];
+        const float hi = __bfloat162float(__float2bfloat16_rn(A));
+        x = hl ? A - hi : hi;
+      }
+      v[e] = x;
+    }
+    out[p] = pack_bf16(v[0], v[1]);
+  }
+}
+
+__global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
+    mix_tc_kernel(const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmU,
+                  const MixArgs a, const MixGeo g, uint32_t* flags) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwc = g.nwc, W_FEED = nwc, W_STORE = nwc + 1;
+  const int slice = (int)(blockIdx.x % g.CS);
+  const long long rg = blockIdx.x / g.CS, nrg = gridDim.x / g.CS;
+  const int L = a.L, D = a.D, K = a.k, AST = g.AST, LP = g.LP, NB = g.NB;
+  const int c0 = slice * g.W;
+  const int nks = LP / 16;
+  const long long nrows = rg < a.N ? (a.N - 1 - rg) / nrg + 1 : 0;  // rows of this CTA
+  // stage s: the states, [NB blocks][LP layers] rows of 128 B (64 columns),
+  // swizzled, then the row's coefficient tile [2 be][2 hi/lo][16 j][AST]
+  const uint32_t stage0 = su32(sm + g.off_stage);
+  // staging tile ob: [NB blocks][2k channel planes] rows of 128 B, swizzled,
+  // then one spare 128-byte row that takes the padding channels k..15
+  const uint32_t out0 = su32(sm + g.off_out);
+  float* red = reinterpret_cast<float*>(sm + g.off_red);                      // [2][nwc][32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + g.off_bar);               // [NS]
+  uint64_t* empty = full + NS;                                                // [NS]
+  uint64_t* ofull = empty + NS;                                               // [2]
+  uint64_t* oempty = ofull + 2;                                               // [2]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(oempty + 2);
+  volatile int* stop = abort_flag + 1;
+
+  if (tid == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nwc);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ofull[i], nwc);
+      mbar_init(&oempty[i], 1);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmS) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmU) : "memory");
+  }
+  // everything above touched only shared memory
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) *stop = (*(volatile const uint32_t*)flags & FLAG_TIMEOUT) != 0;
+  __syncthreads();
+  // an earlier kernel of this call timed out: leave before issuing anything
+  if (*stop) return;
 
   bool ok = true;
-  if (warp == g.nwc) {
-    // ------------- producer: lane 0 streams the state chunks
-    if (lane == 0) {
-      const __nv_bfloat16* src = (const __nv_bfloat16*)a.stash;
-      int q = 0;
-      for (;; ++q) {
-        const long long row = rg + (long long)(q / nks) * nrg;
-        if (row >= a.N) break;
-        const int ks = q % nks, st = q % g.nstg;
-        if (q >= g.nstg) ok = tc_wait(su32(&empty[st]), (uint32_t)((q / g.nstg - 1) & 1));
-        if (!ok) break;
-        const int l0 = ks * 16, lc = min(16, L - l0);
-        const uint32_t b = su32(&full[st]);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b),
-                     "r"((uint32_t)(lc * W * 2))
-                     : "memory");
-        const __nv_bfloat16* s0 = src + row * a.ld_row + (long long)l0 * D + c0;
-        __nv_bfloat16* d0 = stage + (size_t)st * 16 * SROW;
-        for (int l = 0; l < lc; ++l)
-          asm volatile(
-              "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-              "[%3];" ::"r"(su32(d0 + (size_t)l * SROW)),
-              "l"(s0 + (long long)l * D), "r"((uint32_t)(W * 2)), "r"(b)
-              : "memory");
-      }
-      // copies still in flight land before the CTA may exit
-      for (int p = max(0, q - g.nstg); p < q; ++p)
-        tc_wait(su32(&full[p % g.nstg]), (uint32_t)((p / g.nstg) & 1));
-    }
-    __syncwarp();
-  } else if (warp == g.nwc + 1) {
-    // ------------- storer: the row's output tile leaves by bulk copies, one per
-    // (branch, channel) row segment of W columns
-    __nv_bfloat16* out = (__nv_bfloat16*)a.mixed;
-    long long it = 0;
-    for (long long row = rg; row < a.N; row += nrg, ++it) {
-      const int os = (int)(it & 1);
-      if (ok) ok = tc_wait(su32(&ofull[os]), (uint32_t)((it >> 1) & 1));
-      const __nv_bfloat16* ot = otile + (size_t)os * otile_elems;
-      for (int idx = lane; idx < 2 * K; idx += 32)
-        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                         out + ((size_t)idx * a.N + row) * D + c0),
-                     "r"(su32(ot + (size_t)idx * g.OST)), "r"((uint32_t)(W * 2))
-                     : "memory");
-      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&oempty[os]));
-    }
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  } else {
-    // ------------- compute warps
+  if (warp < nwc) {
+    // ---------------- compute warps ----------------
     const int gq = lane >> 2, tq = lane & 3;
-    const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm;
     const int wcol = warp * NTW * 8;  // first column of this warp within the slice
-    // This warp's share of each row's coefficient tile: entries idx = tid + NC * i
-    // (i < MAXV) of the row's 2kL values; tile offset (hi half) and source layer fixed.
-    const int NC = g.nwc * 32, ncoef = 2 * K * L;
-    uint32_t pk[MAXV];
+    const __nv_bfloat16* sn = (const __nv_bfloat16*)a.src_norm;
+    const __nv_bfloat16* cn = (const __nv_bfloat16*)a.chan_norm;
+    // Source-norm gains in the B-fragment layout of ldmatrix.trans below:
+    // gf[be][ks][np][i]: i = 0, 1 -> n-tile 2np (layers 2tq.., 2tq+8..),
+    // i = 2, 3 -> n-tile 2np + 1; layers >= L are zero.
+    uint32_t gf[2][2][2][4];
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int idx = tid + NC * i;
-      const int be = idx / (K * L), j = (idx / L) % K, l = idx % L;
-      pk[i] = idx < ncoef ? ((uint32_t)(((be * 2) * 16 + j) * AST + l) | ((uint32_t)l << 16))
-                          : 0xffffffffu;
-    }
-    float pc[MAXV], pi[MAXV];
-    auto fetch = [&](long long row) {
+    for (int be = 0; be < 2; ++be)
 #pragma unroll
-      for (int i = 0; i < MAXV; ++i) {
-        const bool v = row < a.N && pk[i] != 0xffffffffu;
-        pc[i] = v ? a.coeff[row * ncoef + tid + NC * i] : 0.f;
-        pi[i] = v ? a.inv[row * a.inv_ld + (pk[i] >> 16)] : 0.f;
-      }
-    };
-    auto convert = [&](long long it_dst) {  // prefetched values -> tile of iteration it_dst
-      __nv_bfloat16* at = atile + (size_t)(it_dst % RS) * atile_elems;
+      for (int ks = 0; ks < 2; ++ks)
 #pragma unroll
-      for (int i = 0; i < MAXV; ++i) {
-        if (pk[i] != 0xffffffffu) {
-          const float v = pc[i] * pi[i];
-          const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-          const uint32_t o = pk[i] & 0xffffu;
-          at[o] = hi;
-          at[o + 16 * AST] = lo;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&afull[it_dst % RS]));
-    };
+        for (int np = 0; np < 2; ++np)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int nt = 2 * np + (i >> 1);
+            const int l0 = ks * 16 + 2 * tq + (i & 1) * 8;
+            const size_t col = (size_t)c0 + wcol + nt * 8 + gq;
+            const size_t rowb = (size_t)be * a.sn_layers;
+            const uint32_t x0 = l0 < L ? __bfloat16_as_ushort(sn[(rowb + l0) * D + col]) : 0u;
+            const uint32_t x1 = l0 + 1 < L ? __bfloat16_as_ushort(sn[(rowb + l0 + 1) * D + col]) : 0u;
+            gf[be][ks][np][i] = x0 | (x1 << 16);
+          }
     // channel-norm gains of this thread's outputs: [branch][n-tile][row half]
     uint32_t tau[2][NTW][2];
 #pragma unroll
@@ -275,139 +306,190 @@ __global__ void __launch_bounds__((MAX_WARPS + 2) * 32, 1)
         for (int h = 0; h < 2; ++h) {
           const int j = gq + 8 * h;
           tau[be][nt][h] =
-              j < K ? *reinterpret_cast<const uint32_t*>(cn + ((size_t)be * a.cn_channels + j) * D + c0 + wcol +
-                                                         nt * 8 + 2 * tq)
+              j < K ? *reinterpret_cast<const uint32_t*>(cn + ((size_t)be * a.cn_channels + j) * D + c0 +
+                                                         wcol + nt * 8 + 2 * tq)
                     : 0u;
         }
-    float acc[2][NTW][4];
-#pragma unroll
-    for (int be = 0; be < 2; ++be)
-#pragma unroll
-      for (int nt = 0; nt < NTW; ++nt) acc[be][nt][0] = acc[be][nt][1] = acc[be][nt][2] = acc[be][nt][3] = 0.f;
-    const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix.trans source row (layer)
-    const int lc8 = (lane >> 4) * 8;                     // and column offset
-    // Tiles run one row ahead of use: a warp converts row it + 1's share at the
-    // start of row it, then waits for row it's tile (all warps' shares). A warp
-    // at row it has seen row it - 1's tile complete, so every warp has started
-    // row it - 2 and finished row it - 3: the slot written at row it (last used
-    // by row it + 1 - RS) is free for RS >= 4.
-    fetch(rg);
-    convert(0);
-    fetch(rg + nrg);
-    int q = 0;
-    long long it = 0;
-    for (long long row = rg; row < a.N; row += nrg, ++it) {
-      const int slot = (int)(it % RS);
-      if (row + nrg < a.N) {
-        convert(it + 1);
-        fetch(row + 2 * nrg);
+    // ldmatrix.trans rows: lane -> layer lr of the K16 step, 8-column chunk
+    const int lr = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int blk = wcol >> 6;                       // 64-column block of this warp
+    const int cchunk = ((wcol & 63) >> 3) + (lane >> 4);  // chunk of n-tile pair 0
+    for (long long r = 0; r < nrows && ok; ++r) {
+      const int s = (int)(r % NS), ob = (int)(r & 1);
+      if (!warp_wait(&full[s], (uint32_t)((r / NS) & 1), abort_flag, lane)) {
+        ok = false;
+        break;
       }
-      if (ok) ok = tc_wait(su32(&afull[slot]), (uint32_t)((it / RS) & 1));
-      const __nv_bfloat16* at = atile + (size_t)slot * atile_elems;
-      for (int ks = 0; ks < nks; ++ks, ++q) {
-        const int st = q % g.nstg;
-        if (ok) ok = tc_wait(su32(&full[st]), (uint32_t)((q / g.nstg) & 1));
-        uint32_t A[2][2][4];
+      const uint32_t st = stage0 + (uint32_t)s * g.stage_bytes;
+      const __nv_bfloat16* at =
+          reinterpret_cast<const __nv_bfloat16*>(sm + g.off_stage + (size_t)s * g.stage_bytes + g.state_bytes);
+      float acc[2][NTW][4];
 #pragma unroll
-        for (int be = 0; be < 2; ++be)
+      for (int ks = 0; ks < 2; ++ks) {
+        if (ks < nks) {
+          uint32_t A[2][2][4];
 #pragma unroll
-          for (int hl = 0; hl < 2; ++hl)
-            ldsm4(su32(at + ((size_t)(be * 2 + hl) * 16 + (lane & 15)) * AST + ks * 16 + (lane >> 4) * 8),
-                  A[be][hl]);
-        const __nv_bfloat16* sb = stage + (size_t)st * 16 * SROW + (size_t)lr * SROW + wcol + lc8;
-        const __nv_bfloat16* gk0 = gains + (size_t)(ks * 16 + lr) * SROW + wcol + lc8;
-        const __nv_bfloat16* gv0 = gk0 + (size_t)LP * SROW;
+          for (int be = 0; be < 2; ++be)
 #pragma unroll
-        for (int np = 0; np < NTW / 2; ++np) {
-          uint32_t h[4], gk[4], gv[4], xk[2][4], xv[2][4];
-          ldsm4t(su32(sb + np * 16), h);
-          ldsm4t(su32(gk0 + np * 16), gk);
-          ldsm4t(su32(gv0 + np * 16), gv);
+            for (int hl = 0; hl < 2; ++hl)
+              ldsm4(su32(at + ((size_t)(be * 2 + hl) * 16 + (lane & 15)) * AST + ks * 16 + (lane >> 4) * 8),
+                    A[be][hl]);
+          const int row = blk * LP + ks * 16 + lr;  // 128-byte row of (block, layer)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            bmul2_split(h[i], gk[i], xk[0][i], xk[1][i]);
-            bmul2_split(h[i], gv[i], xv[0][i], xv[1][i]);
-          }
-          // A_hi X_hi + A_hi X_lo + A_lo X_hi (A_lo X_lo is below 2^-16 relative)
+          for (int np = 0; np < NTW / 2; ++np) {
+            uint32_t h[4];
+            ldsm4t(swz128(st, row, cchunk + 2 * np), h);
+            uint32_t xk[2][4], xv[2][4];
 #pragma unroll
-          for (int t = 0; t < 3; ++t) {
-            const int ha = t == 2 ? 1 : 0, hx = t == 1 ? 1 : 0;
-            mma16816(acc[0][2 * np], A[0][ha], xk[hx][0], xk[hx][1]);
-            mma16816(acc[0][2 * np + 1], A[0][ha], xk[hx][2], xk[hx][3]);
-            mma16816(acc[1][2 * np], A[1][ha], xv[hx][0], xv[hx][1]);
-            mma16816(acc[1][2 * np + 1], A[1][ha], xv[hx][2], xv[hx][3]);
+            for (int i = 0; i < 4; ++i) {
+              bmul2_split(h[i], gf[0][ks][np][i], xk[0][i], xk[1][i]);
+              bmul2_split(h[i], gf[1][ks][np][i], xv[0][i], xv[1][i]);
+            }
+            // A_hi X_hi (+) A_hi X_lo (+) A_lo X_hi; A_lo X_lo is below 2^-16 relative
+            if (ks == 0) {
+              mma16816_first(acc[0][2 * np], A[0][0], xk[0][0], xk[0][1]);
+              mma16816_first(acc[0][2 * np + 1], A[0][0], xk[0][2], xk[0][3]);
+              mma16816_first(acc[1][2 * np], A[1][0], xv[0][0], xv[0][1]);
+              mma16816_first(acc[1][2 * np + 1], A[1][0], xv[0][2], xv[0][3]);
+            } else {
+              mma16816(acc[0][2 * np], A[0][0], xk[0][0], xk[0][1]);
+              mma16816(acc[0][2 * np + 1], A[0][0], xk[0][2], xk[0][3]);
+              mma16816(acc[1][2 * np], A[1][0], xv[0][0], xv[0][1]);
+              mma16816(acc[1][2 * np + 1], A[1][0], xv[0][2], xv[0][3]);
+            }
+            mma16816(acc[0][2 * np], A[0][0], xk[1][0], xk[1][1]);
+            mma16816(acc[0][2 * np + 1], A[0][0], xk[1][2], xk[1][3]);
+            mma16816(acc[1][2 * np], A[1][0], xv[1][0], xv[1][1]);
+            mma16816(acc[1][2 * np + 1], A[1][0], xv[1][2], xv[1][3]);
+            mma16816(acc[0][2 * np], A[0][1], xk[0][0], xk[0][1]);
+            mma16816(acc[0][2 * np + 1], A[0][1], xk[0][2], xk[0][3]);
+            mma16816(acc[1][2 * np], A[1][1], xv[0][0], xv[0][1]);
+            mma16816(acc[1][2 * np + 1], A[1][1], xv[0][2], xv[0][3]);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(su32(&empty[st]));
       }
-      // this warp's sums of squares per (branch, channel) into its entry of the row's slot
-      float* rw = red + ((size_t)slot * g.nwc + warp) * 32;
+      // the row's states and coefficient tile are consumed
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      // sums of squares of m per (branch, channel) over this warp's columns
+      float ss[2][2];
 #pragma unroll
       for (int be = 0; be < 2; ++be)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          float s = 0.f;
+          float v = 0.f;
 #pragma unroll
           for (int nt = 0; nt < NTW; ++nt)
-            s += acc[be][nt][2 * h] * acc[be][nt][2 * h] + acc[be][nt][2 * h + 1] * acc[be][nt][2 * h + 1];
-          s += __shfl_xor_sync(0xffffffffu, s, 1);
-          s += __shfl_xor_sync(0xffffffffu, s, 2);
-          if (tq == 0) rw[be * 16 + gq + 8 * h] = s;
+            v = fmaf(acc[be][nt][2 * h], acc[be][nt][2 * h], fmaf(acc[be][nt][2 * h + 1], acc[be][nt][2 * h + 1], v));
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          ss[be][h] = v;
         }
-      // u = tau (.) m into the row's output tile (free once the storer has read
-      // the tile of row it - 2)
-      const int os = (int)(it & 1);
-      if (it >= 2 && ok) ok = tc_wait(su32(&oempty[os]), (uint32_t)(((it >> 1) - 1) & 1));
-      __nv_bfloat16* ot = otile + (size_t)os * otile_elems + wcol + 2 * tq;
-#pragma unroll
-      for (int be = 0; be < 2; ++be)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int j = gq + 8 * h;
-          if (j < K) {
-            __nv_bfloat16* orow = ot + (size_t)(be * K + j) * g.OST;
-#pragma unroll
-            for (int nt = 0; nt < NTW; ++nt) {
-              // bf16 -> fp32 is a 16-bit shift of the pair's halves
-              const float tx = __uint_as_float(tau[be][nt][h] << 16);
-              const float ty = __uint_as_float(tau[be][nt][h] & 0xffff0000u);
-              const __nv_bfloat162 o =
-                  __floats2bfloat162_rn(acc[be][nt][2 * h] * tx, acc[be][nt][2 * h + 1] * ty);
-              *reinterpret_cast<__nv_bfloat162*>(orow + nt * 8) = o;
-            }
-          }
-        }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(su32(&ofull[os]));
-      // The last warp of the row adds the warps' sums and publishes the slice's
-      // (the slot is reused at row it + RS, which no warp reaches before all
-      // have left row it).
-      __syncwarp();
-      uint32_t last = 0;
-      if (lane == 0) {
-        __threadfence_block();
-        last = atomicAdd(&sscnt[slot], 1u) == (uint32_t)(g.nwc - 1);
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence_block();
-        const float* rs = red + (size_t)slot * g.nwc * 32 + lane;
-        float v = 0.f;
-        for (int w = 0; w < g.nwc; ++w) v += rs[w * 32];
-        const int be = lane >> 4, j = lane & 15;
-        if (j < K) a.chan_ss[(((size_t)row * 2 + be) * K + j) * g.CS + rank] = v;
-        if (lane == 0) atomicExch(&sscnt[slot], 0u);
-      }
+      // u = tau (.) m as bf16 pairs, the m16n8 fragments being stmatrix's
+      uint32_t pk[2][NTW][2];
 #pragma unroll
       for (int be = 0; be < 2; ++be)
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt)
-          acc[be][nt][0] = acc[be][nt][1] = acc[be][nt][2] = acc[be][nt][3] = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            // bf16 -> fp32 is a 16-bit shift of the pair's halves
+            const float tx = __uint_as_float(tau[be][nt][h] << 16);
+            const float ty = __uint_as_float(tau[be][nt][h] & 0xffff0000u);
+            pk[be][nt][h] = pack_bf16(acc[be][nt][2 * h] * tx, acc[be][nt][2 * h + 1] * ty);
+          }
+      // staging tile ob is free once the storer has read row r - 2's
+      if (r >= 2 && !warp_wait(&oempty[ob], (uint32_t)(((r >> 1) - 1) & 1), abort_flag, lane)) {
+        ok = false;
+        break;
+      }
+      {
+        // matrix i of an x4 store: n-tile 2q + (i >> 1), channel rows 8 * (i & 1)..;
+        // lane 8i + x gives the address of row x of matrix i: channel plane
+        // be * k + j, block blk, chunk of the n-tile (channels >= k go to the
+        // spare row)
+        const uint32_t ot = out0 + (uint32_t)ob * g.out_bytes;
+        const int i = lane >> 3, x = lane & 7;
+        const int j = (i & 1) * 8 + x;
+#pragma unroll
+        for (int be = 0; be < 2; ++be)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int nt = 2 * q + (i >> 1);
+            const int c16 = ((wcol & 63) >> 3) + nt;
+            const uint32_t addr = j < K ? swz128(ot, blk * 2 * K + be * K + j, c16)
+                                        : ot + (uint32_t)(2 * K * NB) * 128u + (uint32_t)(c16 << 4);
+            stsm4(addr, pk[be][2 * q][0], pk[be][2 * q][1], pk[be][2 * q + 1][0], pk[be][2 * q + 1][1]);
+          }
+      }
+      if (tq == 0) {
+        float* rw = red + ((size_t)ob * nwc + warp) * 32;
+#pragma unroll
+        for (int be = 0; be < 2; ++be)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) rw[be * 16 + gq + 8 * h] = ss[be][h];
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofull[ob]);
     }
+  } else if (warp == W_FEED) {
+    // ---------------- feeder: lane 0 issues each row's two copies ----------------
+    const uint8_t* tiles = (const uint8_t*)a.atile;
+    long long issued = 0;
+    if (lane == 0) {
+      for (long long r = 0; r < nrows; ++r) {
+        const int s = (int)(r % NS);
+        const long long row = rg + r * nrg;
+        if (r >= NS && !mbar_wait(&empty[s], (uint32_t)(((r / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        const uint32_t st = stage0 + (uint32_t)s * g.stage_bytes;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(&full[s])),
+                     "r"(g.state_bytes + (uint32_t)MIX_ATILE_BYTES)
+                     : "memory");
+        // states: one box {64, LP, NB, 1}; layers >= L arrive as zeros
+        tma_load4(&tmS, &full[s], st, 0, 0, c0 / 64, (int)row);
+        bulk_load(st + g.state_bytes, tiles + row * MIX_ATILE_BYTES, (uint32_t)MIX_ATILE_BYTES, &full[s]);
+        issued = r + 1;
+      }
+      // copies still in flight land before the CTA may exit
+      volatile int no_abort = 0;
+      for (long long r = issued - NS > 0 ? issued - NS : 0; r < issued; ++r)
+        mbar_wait(&full[r % NS], (uint32_t)((r / NS) & 1), &no_abort);
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  } else if (warp == W_STORE) {
+    // ---------------- storer: staging tile -> u, sums of squares -> chan_ss ----------------
+    for (long long r = 0; r < nrows && ok; ++r) {
+      const int ob = (int)(r & 1);
+      const long long row = rg + r * nrg;
+      if (!warp_wait(&ofull[ob], (uint32_t)((r >> 1) & 1), abort_flag, lane)) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) tma_store4(&tmU, out0 + (uint32_t)ob * g.out_bytes, 0, 0, c0 / 64, (int)row);
+      if (lane < 2 * K) {
+        const int be = lane >= K ? 1 : 0, j = lane - be * K;
+        float v = 0.f;
+        const float* rs = red + (size_t)ob * nwc * 32 + be * 16 + j;
+        for (int w = 0; w < nwc; ++w) v += rs[w * 32];
+        a.chan_ss[(((size_t)row * 2 + be) * K + j) * g.CS + slice] = v;
+      }
+      if (lane == 0) {
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&oempty[ob]);
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
-  if (!ok) atomicOr(flags, FLAG_TIMEOUT);
+  if (!ok && lane == 0) {
+    *abort_flag = 1;
+    atomicOr(flags, FLAG_TIMEOUT);
+  }
 }
 
 // c = s * u in place: one block per (branch, channel, row) of the deferred-norm output.
@@ -431,79 +513,93 @@ __global__ void __launch_bounds__(256) mix_normalize_kernel(void* mixed, const f
 
 // Geometry for a slice count CS, or false if it does not fit.
 bool mix_geo(const MixArgs& a, int CS, MixGeo& g) {
-  if (a.D % (32 * CS)) return false;
+  if (a.D % (64 * CS)) return false;
   g.CS = CS;
   g.W = a.D / CS;
-  if (g.W > 32 * MAX_WARPS) return false;
+  if (g.W > 32 * MAX_CW) return false;
   g.nwc = g.W / 32;
-  if (2 * a.k * a.L > MAXV * 32 * g.nwc) return false;
-  g.LP = (a.L + 15) / 16 * 16;
-  g.SROW = g.W % 64 == 0 ? g.W + 8 : g.W + 40;  // row stride = 16 B mod 128 B
-  g.AST = g.LP + 8;
-  g.OST = g.SROW;
-  const unsigned gains = 2u * g.LP * g.SROW * 2, stage = 16u * g.SROW * 2;
-  const unsigned atile = (unsigned)RS * 2 * 2 * 16 * g.AST * 2, ss = RS * (g.nwc * 32 + 1) * 4 + 12;
-  const unsigned otile = 2u * 2 * a.k * g.OST * 2;
-  const unsigned fixed = gains + atile + ss + otile + (RS + 4) * 8 + 160;
-  const unsigned budget = 227u * 1024;
-  if (fixed >= budget) return false;
-  int nstg = (int)((budget - fixed) / (stage + 16));
-  if (nstg > 8) nstg = 8;
-  const int nks = g.LP / 16;
-  if (nstg < 2 * nks && nstg < 4) return false;
-  g.nstg = nstg;
-  g.off_stage = gains;
-  g.off_atile = g.off_stage + (unsigned)nstg * stage;
-  g.off_ss = g.off_atile + atile;
-  g.off_out = g.off_ss + (ss + 15) / 16 * 16;
-  g.off_bar = g.off_out + otile;
-  g.smem = g.off_bar + (2u * nstg + RS + 4) * 8;
-  return g.smem <= budget;
+  g.NB = g.W / 64;
+  g.LP = a.L <= 16 ? 16 : 32;
+  g.AST = 40;
+  g.state_bytes = (unsigned)g.LP * g.W * 2;                                // multiple of 1024
+  g.stage_bytes = (g.state_bytes + (unsigned)MIX_ATILE_BYTES + 1023u) / 1024u * 1024u;
+  g.out_bytes = ((unsigned)(2 * a.k * g.NB + 1) * 128u + 1023u) / 1024u * 1024u;
+  const unsigned redb = 2u * g.nwc * 32 * 4;
+  const unsigned bars = (2 * NS + 4) * 8 + 16;
+  g.off_stage = 0;
+  g.off_out = g.off_stage + NS * g.stage_bytes;
+  g.off_red = g.off_out + 2 * g.out_bytes;
+  g.off_bar = (g.off_red + redb + 7) / 8 * 8;
+  g.smem = g.off_bar + bars + 1024;  // + alignment of the base to 1024 bytes
+  return g.smem <= 227u * 1024;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
 }
 
 }  // namespace
 
 int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags) {
-  if (a.N <= 0 || a.k < 1 || a.k > 16 || a.L < 1 || a.L > 64) return 0;
-  if (!a.chan_ss || (uintptr_t)a.stash % 16 || a.ld_row % 8 || (uintptr_t)a.src_norm % 16 ||
-      (uintptr_t)a.chan_norm % 4 || (uintptr_t)a.mixed % 16)
+  if (a.N <= 0 || a.k < 1 || a.k > 16 || a.L < 1 || a.L > 32 || !a.atile) return 0;
+  if ((uintptr_t)a.atile % 16) return 0;
+  if (!a.chan_ss || (uintptr_t)a.stash % 16 || a.ld_row % 8 || (uintptr_t)a.src_norm % 4 ||
+      (uintptr_t)a.chan_norm % 4 || (uintptr_t)a.mixed % 16 || a.D % 64)
     return 0;
   MixGeo g{};
   bool found = false;
   for (int cs = 1; cs <= 8 && !found; ++cs) found = mix_geo(a, cs, g);
   if (!found) return 0;
-  if (cudaFuncSetAttribute(mix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem) !=
-      cudaSuccess)
-    return 0;
-  // persistent grid: every resident CTA (cached per shared-memory size and device)
-  static std::mutex mu;
-  static int cached_smem = -1, cached_dev = -1, cached_nwc = -1, cached_blocks = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int blocks = 0;
+  auto enc = encode_fn();
+  if (!enc) return 0;
+  // states [N][L][D] (row stride ld_row) as {64 columns, L, D/64 blocks, N}
+  CUtensorMap ms, mu;
   {
-    std::lock_guard<std::mutex> lock(mu);
-    if (cached_smem != (int)g.smem || cached_dev != dev || cached_nwc != g.nwc) {
-      int per_sm = 0, sms = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, mix_tc_kernel,
-                                                        (g.nwc + 2) * 32, g.smem) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-          per_sm < 1) {
-        cudaGetLastError();
-        return 0;
-      }
-      cached_blocks = per_sm * sms;
-      cached_smem = (int)g.smem;
-      cached_dev = dev;
-      cached_nwc = g.nwc;
-    }
-    blocks = cached_blocks;
+    cuuint64_t dims[4] = {64, (cuuint64_t)a.L, (cuuint64_t)(a.D / 64), (cuuint64_t)a.N};
+    cuuint64_t strides[3] = {(cuuint64_t)a.D * 2, 128, (cuuint64_t)a.ld_row * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)g.LP, (cuuint32_t)g.NB, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&ms, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.stash), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return 0;
   }
-  long long nrg = blocks / g.CS;
+  // u [2k][N][D] as {64 columns, 2k planes, D/64 blocks, N}
+  {
+    cuuint64_t dims[4] = {64, (cuuint64_t)(2 * a.k), (cuuint64_t)(a.D / 64), (cuuint64_t)a.N};
+    cuuint64_t strides[3] = {(cuuint64_t)a.N * a.D * 2, 128, (cuuint64_t)a.D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)(2 * a.k), (cuuint32_t)g.NB, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (enc(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.mixed, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return 0;
+  }
+  if (cudaFuncSetAttribute(mix_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long nrg = sms / g.CS;
   if (nrg < 1) nrg = 1;
   if (nrg > a.N) nrg = a.N;
-  launch_k(mix_tc_kernel, dim3((unsigned)(nrg * g.CS)), dim3((g.nwc + 2) * 32), g.smem, st, a, g, flags);
-  return cudaGetLastError() == cudaSuccess ? g.CS : 0;
+  if (launch_k(mix_atile_kernel, dim3((unsigned)a.N), dim3(128), 0, st, a) != cudaSuccess) return 0;
+  if (launch_k(mix_tc_kernel, dim3((unsigned)(nrg * g.CS)), dim3((g.nwc + 2) * 32), g.smem, st, ms, mu, a,
+               g, flags) != cudaSuccess)
+    return 0;
+  return g.CS;
 }
 
 void launch_mix_normalize(const MixArgs& a, int parts, cudaStream_t st) {
