@@ -100,15 +100,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, volatile
     if (gtimer() - t0 > WAIT_NS) return false;
   }
 }
-// One lane waits, the warp learns the outcome; then every lane observes the
-// completed phase itself (an acquire of its own, so that what the producer
-// or the TMA wrote is visible to each lane's reads).
+// One lane waits (acquiring the completed phase), the warp learns the
+// outcome; __syncwarp then orders the other lanes' reads after that acquire.
 __device__ __forceinline__ bool warp_wait(uint64_t* b, uint32_t parity, volatile int* abort_flag,
                                           int lane) {
   int ok = 1;
   if (lane == 0) ok = mbar_wait(b, parity, abort_flag) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (ok) mbar_try(b, parity);
+  __syncwarp();
   return ok != 0;
 }
 
