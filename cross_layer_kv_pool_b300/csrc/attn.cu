@@ -628,7 +628,7 @@ int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, i
   // prefill groups (several rows per sequence) run on tcgen05; single-row
   // sequences (decode) and unstructured row lists run on mma.sync
   if (dtype == WM_BF16 && !simt && nq >= 8 && attention_tc_supported(a, nq)) {
-    launch_attention_tc(a, nq, st);
+    launch_attention_pair(a, nq, st);
     return 1;
   }
   if (dtype == WM_BF16 && !simt && G <= AQ) {

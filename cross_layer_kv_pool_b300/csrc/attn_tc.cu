@@ -401,21 +401,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const CUtensorMap* map = kq ? &tmK : &tmV;
     uint8_t* ring = sm + (kq ? SM::OFF_K : SM::OFF_V);
     bool ok = entry_ok;
-    int gb = 0, it = 0;
+    int gb = 0, nqi = 0;  // K or V blocks issued, Q tiles issued
     uint32_t used = 0, lastk = 0;
-    for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x, ++it) {
+    for (int idx = blockIdx.x; idx < p.tiles && ok; idx += gridDim.x) {
       const Tile tl = tile_of(p, idx, lane);
       if (lane == 0) {
         if (kq) {
           if (!tl.seq_ok) atomicOr(p.flags, FLAG_BAD_SEQ);
           // one Q buffer: the previous tile's S products have read it
-          if (!mbar_wait(q_empty, (it & 1) ^ 1, abort_flag)) ok = false;
+          if (!mbar_wait(q_empty, (nqi & 1) ^ 1, abort_flag)) ok = false;
           if (ok) {
             // the box fills R*G rows of each 128-row operand chunk; rows past
             // them feed only accumulator rows that are never read back
             mbar_expect_tx(q_full, (uint32_t)((HD / 64) * p.G * p.rpt * 128));
             for (int c = 0; c < HD / 64; ++c)
               tma3(&tmQ, q_full, sm + SM::OFF_Q + c * BQ * 128, c * 64, tl.hk * p.G, tl.r0);
+            ++nqi;
           }
         }
         const int zc = ((tl.sq * p.k) + p.channel) * p.Hkv + tl.hk;
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       // Drain: every issued copy has landed before the CTA may exit.
       volatile int no_abort = 0;
-      if (kq && it > 0) mbar_wait(q_full, (it - 1) & 1, &no_abort);
+      if (kq && nqi > 0) mbar_wait(q_full, (nqi - 1) & 1, &no_abort);
       for (int s = 0; s < ns; ++s)
         if (used & (1u << s)) mbar_wait(&full[s], (lastk >> s) & 1, &no_abort);
     }

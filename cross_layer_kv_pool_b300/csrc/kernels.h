@@ -74,6 +74,27 @@ int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, i
                      float* part, long long part_elems);
 bool attention_tc_supported(const AttnArgs& a, int nq);
 cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st);
+// The same calls on the paired-tile kernel (two query tiles of one sequence
+// and KV head per CTA, sharing every K and V block).
+cudaError_t launch_attention_pair(const AttnArgs& a, int nq, cudaStream_t st);
+
+// ---- sgemm.cu --------------------------------------------------------------
+// C[b] = op(A[b]) op(B[b]) + beta C[b] for b < batch, fp32, row-major: op(A)
+// is M x K (A stored K x M when ta), op(B) K x N (B stored N x K when tb);
+// sa, sb, sc are the strides between batch entries (0 broadcasts).
+struct SgemmArgs {
+  bool ta, tb;
+  int M, N, K;
+  const float* A;
+  long long lda, sa;
+  const float* B;
+  long long ldb, sb;
+  float beta;
+  float* C;
+  long long ldc, sc;
+  int batch;
+};
+cudaError_t sgemm_rm(const SgemmArgs& g, cudaStream_t st);
 
 // ---- pool.cu ---------------------------------------------------------------
 // Bytes per row of the tensor-core mixer's coefficient tiles: [2 branches]

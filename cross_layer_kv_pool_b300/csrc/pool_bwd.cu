@@ -10,13 +10,9 @@
 //   dW_R += da^T x,  dn_R += da W_R                     (router)
 //   per-source norm backward                           -> dh,     d sigma
 // Everything is fp32 (weights converted once per call). The norm, RoPE and
-// scatter steps are this file's kernels; the products, all plain GEMMs, are
-// cuBLAS fp32 GEMMs (strided-batched over channels or rows). Gains and weight
-// gradients accumulate (+=); dstates is overwritten.
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// scatter steps are this file's kernels; the products, all plain GEMMs, run
+// on the fp32 strided-batched GEMM of sgemm.cu (batched over channels or
+// rows). Gains and weight gradients accumulate (+=); dstates is overwritten.
 #include "kernels.h"
 
 namespace wm {
@@ -247,30 +243,11 @@ __global__ void broadcast_rows(const float* __restrict__ src, int n, int N, floa
   if (i < (long long)N * n) dst[i] = src[i % n];
 }
 
-// ---------------------------------------------------------------------------
-// cuBLAS (column-major) for row-major operands: C[M x N] = op(A) op(B) + beta C,
-// strided-batched. A row-major [R x C] matrix with leading dimension ld is the
-// column-major [C x R] matrix with the same ld, so C^T = op(B)^T op(A)^T.
-// ---------------------------------------------------------------------------
-cublasHandle_t handle_for_device() {
-  static std::mutex mu;
-  static cublasHandle_t h[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!h[dev] && cublasCreate(&h[dev]) != CUBLAS_STATUS_SUCCESS) h[dev] = nullptr;
-  if (h[dev]) cublasSetMathMode(h[dev], CUBLAS_PEDANTIC_MATH);
-  return h[dev];
-}
-
-bool gemm_rm(cublasHandle_t hd, bool ta, bool tb, int M, int N, int K, const float* A, long long lda,
-             long long sa, const float* B, long long ldb, long long sb, float beta, float* C,
-             long long ldc, long long sc, int batch) {
-  const float one = 1.f;
-  return cublasSgemmStridedBatched(hd, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N,
-                                   N, M, K, &one, B, (int)ldb, sb, A, (int)lda, sa, &beta, C,
-                                   (int)ldc, sc, batch) == CUBLAS_STATUS_SUCCESS;
+bool gemm_rm(bool ta, bool tb, int M, int N, int K, const float* A, long long lda, long long sa,
+             const float* B, long long ldb, long long sb, float beta, float* C, long long ldc,
+             long long sc, int batch, cudaStream_t st) {
+  SgemmArgs g{ta, tb, M, N, K, A, lda, sa, B, ldb, sb, beta, C, ldc, sc, batch};
+  return sgemm_rm(g, st) == cudaSuccess;
 }
 
 }  // namespace
@@ -321,8 +298,6 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
         *dc = buf(PoolBwdLayout::DC), *dn = buf(PoolBwdLayout::DN), *dx = buf(PoolBwdLayout::DX),
         *wr = buf(PoolBwdLayout::WR), *wp = buf(PoolBwdLayout::WP), *gains = buf(PoolBwdLayout::G),
         *a_keep = buf(PoolBwdLayout::AK);
-  cublasHandle_t hd = handle_for_device();
-  if (!hd || cublasSetStream(hd, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorUnknown;
   const wm_weights& W = *q.w;
   const long long WRn = (long long)k * L * nR * D, WPn = (long long)k * w * D;
   float* tau32 = gains;  // [2][k][D]
@@ -345,8 +320,8 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       WM_DISPATCH_S(c.dtype, {
         to_f32<S><<<(unsigned)((WRn + 255) / 256), 256, 0, st>>>((const S*)wrs, WRn, wr);
       });
-      ok = ok && gemm_rm(hd, false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
-                         k * L, 0, 1);
+      ok = ok && gemm_rm(false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
+                         k * L, 0, 1, st);
     }
     bwd_mix_fwd<<<N, 256, 0, st>>>(a_keep, n, N, L, D, k, tau32 + (size_t)be * k * D, c.eps, m, rj, cc);
     // projections: kt (keys only), dY, weight gradients and dc
@@ -355,8 +330,8 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       to_f32<S><<<(unsigned)((WPn + 255) / 256), 256, 0, st>>>((const S*)wps, WPn, wp);
     });
     if (be == 0) {
-      ok = ok && gemm_rm(hd, false, true, N, w, D, cc, D, (long long)N * D, wp, D, (long long)w * D,
-                         0.f, kt, w, (long long)N * w, k);
+      ok = ok && gemm_rm(false, true, N, w, D, cc, D, (long long)N * D, wp, D, (long long)w * D,
+                         0.f, kt, w, (long long)N * w, k, st);
       const int rows = 64;
       dim3 grid((N + rows - 1) / rows, k);
       WM_DISPATCH_S(c.dtype, {
@@ -371,10 +346,10 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     }
     float* dW = be == 0 ? q.g.dWk : q.g.dWv;
     // dW_j += dY_j^T c_j  ([w x N] [N x D]);  dc_j = dY_j W_j  ([N x w] [w x D])
-    ok = ok && gemm_rm(hd, true, false, w, D, N, dY, w, (long long)N * w, cc, D, (long long)N * D, 1.f,
-                       dW, D, (long long)w * D, k);
-    ok = ok && gemm_rm(hd, false, false, N, D, w, dY, w, (long long)N * w, wp, D, (long long)w * D, 0.f,
-                       dc, D, (long long)N * D, k);
+    ok = ok && gemm_rm(true, false, w, D, N, dY, w, (long long)N * w, cc, D, (long long)N * D, 1.f,
+                       dW, D, (long long)w * D, k, st);
+    ok = ok && gemm_rm(false, false, N, D, w, dY, w, (long long)N * w, wp, D, (long long)w * D, 0.f,
+                       dc, D, (long long)N * D, k, st);
     {  // channel norm backward, in place: dc -> dm
       const int rows = 32;
       dim3 grid((N + rows - 1) / rows, k);
@@ -382,18 +357,18 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
                                     rows, dc, q.g.dchan_norm + (size_t)be * k * D);
     }
     // mix backward per row r: da_r [k x L] = dm_r [k x D] n_r^T; dn_r [L x D] = a_r^T dm_r
-    ok = ok && gemm_rm(hd, false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
-                       L, (long long)k * L, N);
-    ok = ok && gemm_rm(hd, true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
-                       0.f, dn, D, (long long)L * D, N);
+    ok = ok && gemm_rm(false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
+                       L, (long long)k * L, N, st);
+    ok = ok && gemm_rm(true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
+                       0.f, dn, D, (long long)L * D, N, st);
     if (!W.static_coeff && q.g.dWr) {
       // router: dW_R += da^T x ([kL x N] [N x nR D]);  dx = da W_R ([N x kL] [kL x nR D])
-      ok = ok && gemm_rm(hd, true, false, k * L, nR * D, N, a, k * L, 0, x, nR * D, 0, 1.f,
-                         q.g.dWr + (size_t)be * WRn, nR * D, 0, 1);
+      ok = ok && gemm_rm(true, false, k * L, nR * D, N, a, k * L, 0, x, nR * D, 0, 1.f,
+                         q.g.dWr + (size_t)be * WRn, nR * D, 0, 1, st);
     }
     if (!W.static_coeff) {
-      ok = ok && gemm_rm(hd, false, false, N, nR * D, k * L, a, k * L, 0, wr, nR * D, 0, 0.f, dx, nR * D,
-                         0, 1);
+      ok = ok && gemm_rm(false, false, N, nR * D, k * L, a, k * L, 0, wr, nR * D, 0, 0.f, dx, nR * D,
+                         0, 1, st);
       bwd_scatter_dx<<<(unsigned)(((long long)N * nR * D + 255) / 256), 256, 0, st>>>(
           dx, N, L, D, c.p, c.p_offset, nR, dn);
     }

@@ -249,10 +249,10 @@ size_t wm_pool_backward_workspace_size(const wm_config* cfg, int32_t max_rows);
  * fp32 and write dstates [N][L][D] (fp32, overwritten: the gradient of the
  * pool's outputs with respect to every layer state of each row) and add the
  * parameter gradients to ``grads``. With static_coeff set the router is not
- * used and dWr is left alone. Plain products run as cuBLAS fp32 GEMMs, the
- * rest in this library's kernels. Errors: WM_ERR_INVALID_ARG (null or
+ * used and dWr is left alone. Every step, the plain fp32 products included,
+ * runs in this library's kernels. Errors: WM_ERR_INVALID_ARG (null or
  * misaligned pointers, N < 1, k * L > 1024, D > 8192), WM_ERR_WORKSPACE,
- * WM_ERR_CUDA (a failed launch or cuBLAS call). */
+ * WM_ERR_CUDA (a failed launch). */
 wm_status wm_pool_backward(const wm_config* cfg, const wm_weights* w,
                            const void* states, int32_t N, const int32_t* pos,
                            const void* dK, const void* dV, float* dstates,

@@ -130,6 +130,54 @@ def test_attention_group_rows_vs_oracle(dtype, d, Hq, Hkv, Tmax, g):
     assert err <= TOL[dtype]["attn"], err
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,Tmax,nq", [(128, 14, 2, 900, 61), (64, 8, 2, 520, 37),
+                                              (128, 2, 2, 300, 300), (64, 16, 1, 260, 9)])
+def test_attention_tile_pairs_all_rows(d, Hq, Hkv, Tmax, nq):
+    """Every row of structured calls on the tensor-core path (two query tiles
+    per CTA sharing each key block): positions in any order within a
+    sequence, a first tile whose rows all sit at position 0 (no visible key)
+    beside a second that sees keys, a ragged last tile, and a sequence id
+    out of range (its rows read no key and come out zero, with the flag)."""
+    s = small_shape("bf16", d=d, Hq=Hq, Hkv=Hkv, k=2)
+    cfg = wm.make_config(s)
+    B = 3
+    G = Hq // Hkv
+    ck = synth.make_normal((B, s.k, Hkv, Tmax, d), 31, "cuda", 2.0, s.torch_dtype)
+    cv = synth.make_normal((B, s.k, Hkv, Tmax, d), 32, "cuda", 1.0, s.torch_dtype)
+    rng = np.random.default_rng(nq)
+    nseq = 4
+    seq_h = np.repeat(np.array([0, 2, 1, B]), nq)        # the last sequence id is invalid
+    pos_h = rng.integers(0, Tmax, size=nseq * nq)
+    cap = 128 // G
+    tiles = -(-nq // cap)
+    tiles += tiles & 1
+    rpt = -(-nq // tiles)
+    pos_h[nq:nq + min(rpt, nq)] = 0                       # sequence 1: its first tile sees nothing
+    pos_h[0] = Tmax - 1
+    N = nseq * nq
+    seq = torch.tensor(seq_h, dtype=torch.int32, device="cuda")
+    pos = torch.tensor(pos_h, dtype=torch.int32, device="cuda")
+    qt = synth.make_normal((N, Hq, d), 33, "cuda", 1.0, s.torch_dtype)
+    out = torch.full((N, Hq * d), float("nan"), dtype=s.torch_dtype, device="cuda")
+    ws = torch.zeros(wm.workspace_size(cfg, N, Tmax), dtype=torch.uint8, device="cuda")
+    c = 1
+    wm.wm_channel_attn(cfg, qt, seq, pos, c, ck, cv, out, ws, rows_per_seq=nq)
+    torch.cuda.synchronize()
+    with pytest.raises(wm.WMError) as e:
+        wm.wm_check_flags(ws)
+    assert e.value.status == wm.WM_ERR_DEVICE_BOUNDS
+    got = host(out).reshape(N, Hq, d)
+    K, Vv, Q = host(ck), host(cv), host(qt)
+    ok_rows = np.arange(3 * nq)
+    ref = np.stack([O.channel_attention(Q[r], K[seq_h[r], c], Vv[seq_h[r], c], pos_h[r], Hq, Hkv)
+                    for r in ok_rows])
+    err = relerr(got[ok_rows], ref)
+    record(f"attention_tile_pairs[d={d},Hq={Hq},Hkv={Hkv},Tmax={Tmax},nq={nq}]", attn=err)
+    assert err <= TOL["bf16"]["attn"], err
+    assert np.all(got[:3 * nq][pos_h[:3 * nq] == 0] == 0)
+    assert np.all(got[3 * nq:] == 0)
+
+
 # ---------------------------------------------------------------------------
 # Pool
 # ---------------------------------------------------------------------------
