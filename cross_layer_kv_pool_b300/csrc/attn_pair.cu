@@ -502,6 +502,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     constexpr uint32_t id_qk = idesc(BKEY, false);
     constexpr uint32_t id_pv = idesc(HD, true);
     const uint32_t sQ = su32(sm + SM::OFF_Q + x * SM::QB);
+    bool lead_ok = entry_ok;  // the leader's waits have all succeeded
+    bool issued = false;      // the leader has issued products (drain at exit)
+    int cs = 0, gk = 0;       // S_X phases consumed; the pair's first block in the CTA's sequence
     // S_X = Q_X K^T of the block in K stage ``ks`` (leader only)
     auto issue_qk = [&](int ks) {
       const uint32_t sK = su32(sm + SM::OFF_K + ks * SM::KB);
@@ -514,9 +517,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       commit(&s_full[x]);
       commit(&k_empty[x * NSK + ks]);
     };
-    bool lead_ok = entry_ok;  // the leader's waits have all succeeded
-    bool issued = false;      // the leader has issued products (drain at exit)
-    int cs = 0, gk = 0;       // S_X phases consumed; the pair's first block in the CTA's sequence
     for (int it = 0;; ++it) {
       // ---- the pair: the leader's warp takes its number and issues S_X(0)
       int idx = 0;
@@ -833,6 +833,17 @@ cudaError_t run(const AttnArgs& a, int nq, cudaStream_t st) {
 }
 
 }  // namespace apr
+
+// The tensor-core path takes structured calls (rows = sequences of nq
+// consecutive rows) whose G heads fit a 128-row tile.
+bool attention_tc_supported(const AttnArgs& a, int nq) {
+  if (nq <= 0 || a.N % nq) return false;
+  const int G = a.Hq / a.Hkv;
+  if (G > apr::BQ || (a.d != 64 && a.d != 128)) return false;
+  if (((uintptr_t)a.q | (uintptr_t)a.cache_k | (uintptr_t)a.cache_v | (uintptr_t)a.out) & 15u)
+    return false;
+  return apr::encode_fn() != nullptr;
+}
 
 cudaError_t launch_attention_pair(const AttnArgs& a, int nq, cudaStream_t st) {
   return a.d == 128 ? apr::run<128>(a, nq, st) : apr::run<64>(a, nq, st);

@@ -72,10 +72,9 @@ struct AttnArgs {
 // decode engine's key splits (part_elems floats), nullable.
 int launch_attention(int dtype, const AttnArgs& a, bool simt, cudaStream_t st, int nq, int kv_len,
                      float* part, long long part_elems);
+// Prefill attention on tcgen05 (attn_pair.cu): two query tiles of one
+// sequence and KV head per CTA, sharing every K and V block.
 bool attention_tc_supported(const AttnArgs& a, int nq);
-cudaError_t launch_attention_tc(const AttnArgs& a, int nq, cudaStream_t st);
-// The same calls on the paired-tile kernel (two query tiles of one sequence
-// and KV head per CTA, sharing every K and V block).
 cudaError_t launch_attention_pair(const AttnArgs& a, int nq, cudaStream_t st);
 
 // ---- sgemm.cu --------------------------------------------------------------
