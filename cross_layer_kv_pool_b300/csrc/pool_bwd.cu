@@ -80,6 +80,76 @@ __global__ void __launch_bounds__(256) bwd_mix_fwd(const float* __restrict__ a,
   }
 }
 
+// The same for k <= KMAX, one block per row reading each n element once: a
+// thread holds the k mixed values of its column in registers.
+template <int KMAX>
+__global__ void __launch_bounds__(256) bwd_mix_fwd_k(const float* __restrict__ a,
+                                                     const float* __restrict__ n, int N, int L,
+                                                     int D, int k, const float* __restrict__ tau,
+                                                     float eps, float* __restrict__ m,
+                                                     float* __restrict__ rj, float* __restrict__ c) {
+  __shared__ float coef[1024];
+  __shared__ float red[KMAX][8];
+  __shared__ float rr[KMAX];
+  const long long r = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < k * L; i += blockDim.x) coef[i] = a[r * k * L + i];
+  __syncthreads();
+  const float* nr = n + r * L * D;
+  float ss[KMAX];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) ss[j] = 0.f;
+  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    float acc[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) acc[j] = 0.f;
+    // eight source rows per step: their loads are in flight together
+    int l = 0;
+    for (; l + 8 <= L; l += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = nr[(size_t)(l + u) * D + t];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) acc[j] = fmaf(coef[j * L + l + u], v[u], acc[j]);
+    }
+    for (; l < L; ++l) {
+      const float v = nr[(size_t)l * D + t];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) acc[j] = fmaf(coef[j * L + l], v, acc[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) {
+        m[((size_t)j * N + r) * D + t] = acc[j];
+        ss[j] = fmaf(acc[j], acc[j], ss[j]);
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    const float v = warp_sum(ss[j]);
+    if (lane == 0) red[j][warp] = v;
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    float t = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[threadIdx.x][w];
+    rr[threadIdx.x] = sqrtf(t / (float)D + eps);
+    rj[r * k + threadIdx.x] = rr[threadIdx.x];
+  }
+  __syncthreads();
+  for (int j = 0; j < k; ++j) {
+    const float inv = 1.f / rr[j];
+    for (int t = threadIdx.x; t < D; t += blockDim.x) {
+      const size_t i = ((size_t)j * N + r) * D + t;
+      c[i] = m[i] * inv * tau[(size_t)j * D + t];
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Backward steps
 // ---------------------------------------------------------------------------
@@ -136,46 +206,41 @@ __global__ void bwd_copy_dv(const S* __restrict__ dV, int N, int k, int w, float
 }
 
 // RMSNorm backward over rows of D (y = w * x / rr), in place on dx:
-// dx = g / rr - x * sum(g * x) / (D rr^3) with g = w * dy; w-gradient summed over
-// the block's rows and added once. One block per (gain row, chunk of rows);
-// row q of the chunk is x + (q * xstride), its gain index is blockIdx.y.
-__global__ void __launch_bounds__(256) bwd_rms(const float* __restrict__ x, long long xstride_gain,
-                                               long long xstride_row, const float* __restrict__ rr,
-                                               long long rr_stride_gain, long long rr_stride_row,
-                                               const float* __restrict__ w, int D, int rows_total,
-                                               int rows, float* __restrict__ dxy,
-                                               float* __restrict__ dw) {
-  __shared__ float red[32];
-  constexpr int U = 32;  // columns per thread: D <= 32 * 256
+// dx = g / rr - x * sum(g * x) / (D rr^3) with g = w * dy; the w-gradient
+// sum(x / rr * dy) over the rows is added to dw. One warp per row (8 rows in
+// flight per block), the w-gradient gathered in shared memory (dynamic, D
+// floats) and added once per block; block (chunk, gain gi) takes rows
+// chunk * rows .. + rows, row q of gain gi at x + gi * xstride_gain + q *
+// xstride_row.
+__global__ void __launch_bounds__(256) bwd_rms_w(const float* __restrict__ x, long long xstride_gain,
+                                                 long long xstride_row, const float* __restrict__ rr,
+                                                 long long rr_stride_gain, long long rr_stride_row,
+                                                 const float* __restrict__ w, int D, int rows_total,
+                                                 int rows, float* __restrict__ dxy,
+                                                 float* __restrict__ dw) {
+  extern __shared__ float acc[];
   const int gi = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* wg = w + (size_t)gi * D;
-  float acc[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) acc[u] = 0.f;
-  const int r0 = blockIdx.x * rows;
-  for (int q = r0; q < r0 + rows && q < rows_total; ++q) {
+  for (int t = threadIdx.x; t < D; t += blockDim.x) acc[t] = 0.f;
+  __syncthreads();
+  const int r0 = blockIdx.x * rows, r1 = min(r0 + rows, rows_total);
+  for (int q = r0 + warp; q < r1; q += (int)(blockDim.x >> 5)) {
     const float* xr = x + gi * xstride_gain + q * xstride_row;
     float* dr = dxy + gi * xstride_gain + q * xstride_row;
     const float rv = rr[gi * rr_stride_gain + q * rr_stride_row];
     float s = 0.f;
-    for (int t = threadIdx.x; t < D; t += blockDim.x) s += wg[t] * dr[t] * xr[t];
-    s = block_sum(s, red);
-    const float c3 = s / ((float)D * rv * rv * rv);
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = threadIdx.x + u * blockDim.x;
-      if (t < D) {
-        const float dy = dr[t];
-        acc[u] += xr[t] / rv * dy;
-        dr[t] = wg[t] * dy / rv - xr[t] * c3;
-      }
+    for (int t = lane; t < D; t += 32) s = fmaf(wg[t] * dr[t], xr[t], s);
+    s = warp_sum(s);
+    const float c3 = s / ((float)D * rv * rv * rv), iv = 1.f / rv;
+    for (int t = lane; t < D; t += 32) {
+      const float dy = dr[t], xv = xr[t];
+      atomicAdd(&acc[t], xv * iv * dy);
+      dr[t] = wg[t] * dy * iv - xv * c3;
     }
   }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int t = threadIdx.x + u * blockDim.x;
-    if (t < D) atomicAdd(&dw[(size_t)gi * D + t], acc[u]);
-  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < D; t += blockDim.x) atomicAdd(&dw[(size_t)gi * D + t], acc[t]);
 }
 
 // dn[r][R_i] += dx[r][i]
@@ -191,45 +256,40 @@ __global__ void bwd_scatter_dx(const float* __restrict__ dx, int N, int L, int D
 }
 
 // Source norm backward: dh = sigma*dn*inv - h*sum(sigma*dn*h)*inv^3/D, added to
-// dstates; d sigma_l accumulated. One block per (layer, chunk of rows).
+// dstates (written on the first branch); d sigma_l accumulated. One warp per
+// row (8 rows in flight per block), d sigma gathered in shared memory
+// (dynamic, D floats) and added once per block; block (chunk, l) takes rows
+// chunk * rows .. + rows of layer l.
 template <typename S>
-__global__ void __launch_bounds__(256) bwd_src_norm(const S* __restrict__ states, int N, int L,
-                                                    int D, const float* __restrict__ inv,
-                                                    const S* __restrict__ sigma,
-                                                    const float* __restrict__ dn, int rows,
-                                                    bool first, float* __restrict__ dstates,
-                                                    float* __restrict__ dsigma) {
-  __shared__ float red[32];
-  constexpr int U = 32;  // columns per thread: D <= 32 * 256
+__global__ void __launch_bounds__(256) bwd_src_norm_w(const S* __restrict__ states, int N, int L,
+                                                      int D, const float* __restrict__ inv,
+                                                      const S* __restrict__ sigma,
+                                                      const float* __restrict__ dn, int rows,
+                                                      bool first, float* __restrict__ dstates,
+                                                      float* __restrict__ dsigma) {
+  extern __shared__ float acc[];
   const int l = blockIdx.y;
-  float acc[U];
-#pragma unroll
-  for (int u = 0; u < U; ++u) acc[u] = 0.f;
-  const int r0 = blockIdx.x * rows;
-  for (int r = r0; r < r0 + rows && r < N; ++r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const S* sg = sigma + (size_t)l * D;
+  for (int t = threadIdx.x; t < D; t += blockDim.x) acc[t] = 0.f;
+  __syncthreads();
+  const int r0 = blockIdx.x * rows, r1 = min(r0 + rows, N);
+  for (int r = r0 + warp; r < r1; r += (int)(blockDim.x >> 5)) {
     const size_t base = ((size_t)r * L + l) * D;
     const float iv = inv[(size_t)r * L + l];
     float s = 0.f;
-    for (int t = threadIdx.x; t < D; t += blockDim.x)
-      s += to_f(sigma[(size_t)l * D + t]) * dn[base + t] * to_f(states[base + t]);
-    s = block_sum(s, red);
+    for (int t = lane; t < D; t += 32) s = fmaf(to_f(sg[t]) * dn[base + t], to_f(states[base + t]), s);
+    s = warp_sum(s);
     const float c3 = s * iv * iv * iv / (float)D;
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = threadIdx.x + u * blockDim.x;
-      if (t < D) {
-        const float h = to_f(states[base + t]), g = dn[base + t];
-        acc[u] += h * iv * g;
-        const float dh = to_f(sigma[(size_t)l * D + t]) * g * iv - h * c3;
-        dstates[base + t] = first ? dh : dstates[base + t] + dh;
-      }
+    for (int t = lane; t < D; t += 32) {
+      const float h = to_f(states[base + t]), g = dn[base + t];
+      atomicAdd(&acc[t], h * iv * g);
+      const float dh = to_f(sg[t]) * g * iv - h * c3;
+      dstates[base + t] = first ? dh : dstates[base + t] + dh;
     }
   }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const int t = threadIdx.x + u * blockDim.x;
-    if (t < D) atomicAdd(&dsigma[(size_t)l * D + t], acc[u]);
-  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < D; t += blockDim.x) atomicAdd(&dsigma[(size_t)l * D + t], acc[t]);
 }
 
 template <typename S>
@@ -323,7 +383,10 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       ok = ok && gemm_rm(false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
                          k * L, 0, 1, st);
     }
-    bwd_mix_fwd<<<N, 256, 0, st>>>(a_keep, n, N, L, D, k, tau32 + (size_t)be * k * D, c.eps, m, rj, cc);
+    if (k <= 16)
+      bwd_mix_fwd_k<16><<<N, 256, 0, st>>>(a_keep, n, N, L, D, k, tau32 + (size_t)be * k * D, c.eps, m, rj, cc);
+    else
+      bwd_mix_fwd<<<N, 256, 0, st>>>(a_keep, n, N, L, D, k, tau32 + (size_t)be * k * D, c.eps, m, rj, cc);
     // projections: kt (keys only), dY, weight gradients and dc
     const char* wps = static_cast<const char*>(be == 0 ? W.Wk : W.Wv);
     WM_DISPATCH_S(c.dtype, {
@@ -351,10 +414,11 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     ok = ok && gemm_rm(false, false, N, D, w, dY, w, (long long)N * w, wp, D, (long long)w * D, 0.f,
                        dc, D, (long long)N * D, k, st);
     {  // channel norm backward, in place: dc -> dm
-      const int rows = 32;
+      const int rows = 64;
       dim3 grid((N + rows - 1) / rows, k);
-      bwd_rms<<<grid, 256, 0, st>>>(m, (long long)N * D, D, rj, 1, k, tau32 + (size_t)be * k * D, D, N,
-                                    rows, dc, q.g.dchan_norm + (size_t)be * k * D);
+      bwd_rms_w<<<grid, 256, (size_t)D * 4, st>>>(m, (long long)N * D, D, rj, 1, k,
+                                                  tau32 + (size_t)be * k * D, D, N, rows, dc,
+                                                  q.g.dchan_norm + (size_t)be * k * D);
     }
     // mix backward per row r: da_r [k x L] = dm_r [k x D] n_r^T; dn_r [L x D] = a_r^T dm_r
     ok = ok && gemm_rm(false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
@@ -373,11 +437,13 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
           dx, N, L, D, c.p, c.p_offset, nR, dn);
     }
     {  // source norm backward into dstates
-      const int rows = 32;
+      const int rows = 64;
       dim3 grid((N + rows - 1) / rows, L);
       WM_DISPATCH_S(c.dtype, {
-        bwd_src_norm<S><<<grid, 256, 0, st>>>((const S*)q.states, N, L, D, inv, (const S*)sig, dn, rows,
-                                              be == 0, q.dstates, q.g.dsrc_norm + (size_t)be * L * D);
+        bwd_src_norm_w<S><<<grid, 256, (size_t)D * 4, st>>>((const S*)q.states, N, L, D, inv,
+                                                            (const S*)sig, dn, rows, be == 0,
+                                                            q.dstates,
+                                                            q.g.dsrc_norm + (size_t)be * L * D);
       });
     }
   }
