@@ -52,6 +52,7 @@ namespace {
 constexpr int NTW = 4;      // n8 tiles per compute warp (32 columns)
 constexpr int MAX_CW = 14;  // compute warps (+ feeder + storer = 16 warps: 128 registers)
 constexpr int NS = 4;       // stages (rows in flight): the row's states and coefficient tile
+constexpr int NOB = 2;      // output staging tiles (rows being stored)
 
 struct MixGeo {
   int CS;    // column slices
@@ -238,12 +239,12 @@ __global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
   // staging tile ob: [NB blocks][2k channel planes] rows of 128 B, swizzled,
   // then one spare 128-byte row that takes the padding channels k..15
   const uint32_t out0 = su32(sm + g.off_out);
-  float* red = reinterpret_cast<float*>(sm + g.off_red);                      // [2][nwc][32]
+  float* red = reinterpret_cast<float*>(sm + g.off_red);                      // [NOB][nwc][32]
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + g.off_bar);               // [NS]
   uint64_t* empty = full + NS;                                                // [NS]
-  uint64_t* ofull = empty + NS;                                               // [2]
-  uint64_t* oempty = ofull + 2;                                               // [2]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(oempty + 2);
+  uint64_t* ofull = empty + NS;                                               // [NOB]
+  uint64_t* oempty = ofull + NOB;                                             // [NOB]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(oempty + NOB);
   volatile int* stop = abort_flag + 1;
 
   if (tid == 0) {
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], nwc);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NOB; ++i) {
       mbar_init(&ofull[i], nwc);
       mbar_init(&oempty[i], 1);
     }
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
     const int blk = wcol >> 6;                       // 64-column block of this warp
     const int cchunk = ((wcol & 63) >> 3) + (lane >> 4);  // chunk of n-tile pair 0
     for (long long r = 0; r < nrows && ok; ++r) {
-      const int s = (int)(r % NS), ob = (int)(r & 1);
+      const int s = (int)(r % NS), ob = (int)(r % NOB);
       if (!warp_wait(&full[s], (uint32_t)((r / NS) & 1), abort_flag, lane)) {
         ok = false;
         break;
@@ -397,8 +398,8 @@ __global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
             const float ty = __uint_as_float(tau[be][nt][h] & 0xffff0000u);
             pk[be][nt][h] = pack_bf16(acc[be][nt][2 * h] * tx, acc[be][nt][2 * h + 1] * ty);
           }
-      // staging tile ob is free once the storer has read row r - 2's
-      if (r >= 2 && !warp_wait(&oempty[ob], (uint32_t)(((r >> 1) - 1) & 1), abort_flag, lane)) {
+      // staging tile ob is free once the storer has read row r - NOB's
+      if (r >= NOB && !warp_wait(&oempty[ob], (uint32_t)(((r / NOB) - 1) & 1), abort_flag, lane)) {
         ok = false;
         break;
       }
@@ -462,9 +463,9 @@ __global__ void __launch_bounds__((MAX_CW + 2) * 32, 1)
   } else if (warp == W_STORE) {
     // ---------------- storer: staging tile -> u, sums of squares -> chan_ss ----------------
     for (long long r = 0; r < nrows && ok; ++r) {
-      const int ob = (int)(r & 1);
+      const int ob = (int)(r % NOB);
       const long long row = rg + r * nrg;
-      if (!warp_wait(&ofull[ob], (uint32_t)((r >> 1) & 1), abort_flag, lane)) {
+      if (!warp_wait(&ofull[ob], (uint32_t)((r / NOB) & 1), abort_flag, lane)) {
         ok = false;
         break;
       }
@@ -523,11 +524,11 @@ bool mix_geo(const MixArgs& a, int CS, MixGeo& g) {
   g.state_bytes = (unsigned)g.LP * g.W * 2;                                // multiple of 1024
   g.stage_bytes = (g.state_bytes + (unsigned)MIX_ATILE_BYTES + 1023u) / 1024u * 1024u;
   g.out_bytes = ((unsigned)(2 * a.k * g.NB + 1) * 128u + 1023u) / 1024u * 1024u;
-  const unsigned redb = 2u * g.nwc * 32 * 4;
-  const unsigned bars = (2 * NS + 4) * 8 + 16;
+  const unsigned redb = (unsigned)NOB * g.nwc * 32 * 4;
+  const unsigned bars = (2 * NS + 2 * NOB) * 8 + 16;
   g.off_stage = 0;
   g.off_out = g.off_stage + NS * g.stage_bytes;
-  g.off_red = g.off_out + 2 * g.out_bytes;
+  g.off_red = g.off_out + NOB * g.out_bytes;
   g.off_bar = (g.off_red + redb + 7) / 8 * 8;
   g.smem = g.off_bar + bars + 1024;  // + alignment of the base to 1024 bytes
   return g.smem <= 227u * 1024;
