@@ -76,6 +76,9 @@ def parse():
                     default=None,
                     help="time one kernel of the path alone (1.3B shapes)")
     ap.add_argument("--rows", type=int, default=8192, help="--kernel mixer: token rows")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="sequences of the prefill workload (default: the workload's own; "
+                         "a smaller count gives the small case a profiler captures)")
     ap.add_argument("--batch", type=int, default=64, help="--kernel attention: sequences")
     ap.add_argument("--group", type=int, default=15, help="--kernel attention: group index q")
     ap.add_argument("--sweep", choices=["convergence"], default=None,
@@ -92,6 +95,8 @@ def workload(args):
     wl = dict(synth.WORKLOADS[args.workload])
     if args.k is not None:
         wl["shape"] = wl["shape"].replace(k=args.k)
+    if getattr(args, "seqs", None):
+        wl["B"] = args.seqs
     return wl
 
 
