@@ -486,9 +486,10 @@ def check_prefix_exactness(O):
 
 
 def check_bruteforce_T4(O):
-    """Brute force on 4-token inputs: every g in 1..4 and pass count 1..4."""
+    """Brute force on 4-token inputs: every g in 1..4 and pass count 1..4, for
+    100 seeded weight and token draws."""
     c = _cfg(L=3, D=8, k=2, Hq=2, Hkv=1, d=8, F=12, V=16)
-    for seed in range(4):
+    for seed in range(100):
         W = _weights(c, seed=100 + seed)
         tokens = _tokens(c, 1, 4, 10 + seed)
         lgar, kar, _ = _ar(O, c, W, tokens)
