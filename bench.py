@@ -662,9 +662,12 @@ def run_kernel(args):
         per_branch = (2.0 * N * kL * nRD + 2.0 * N * kL * s.D + 4.0 * N * w * s.D * s.k
                       + 4.0 * N * kL * s.D + 4.0 * N * kL * nRD)
         work = 2 * per_branch + 2.0 * N * w * s.D * s.k
-        fp32_peak = 148 * 128 * 2 * 2.032e9 / 1e12  # FMA pipes at the maximum SM clock
-        unit, peak, bound = "TFLOP/s", fp32_peak, "alu"
-        desc = f"wm_pool_backward, {N} rows of the 1.3B pool, fp32 arithmetic"
+        # the products run on the tensor cores as bf16 hi/lo splits, three
+        # bf16 products per fp32-accurate one: their ceiling is a third of
+        # the measured bf16 peak, in fp32-equivalent FLOP/s
+        unit, peak, bound = "TFLOP/s", pk["bf16_tflops"] / 3.0, "tensor"
+        desc = (f"wm_pool_backward, {N} rows of the 1.3B pool, fp32-accurate products "
+                "(bf16 hi/lo splits on the tensor cores); peak = measured bf16 burst / 3")
     elif args.kernel == "decode":
         # one decode step of B sequences at position 2048 over a random prefix
         B, T, Tmax = args.batch, 2048, 2304

@@ -133,7 +133,11 @@ int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
 // Backward pass of the pool (pool_bwd.cu)
 // ---------------------------------------------------------------------------
 struct PoolBwdLayout {
-  enum { INV, N_, X, A, M, RJ, C, KT, DY, DC, DN, DX, WR, WP, G, AK, NB };
+  // FLAGS first: the flag word sits where wm_check_flags reads it. SX .. TMPW
+  // hold the router products' bf16 hi/lo operands, SC .. TMPP the channel
+  // projections' (see pool_bwd.cu).
+  enum { FLAGS, INV, N_, X, A, M, RJ, C, KT, DY, DC, DN, DX, WR, WP, G, AK,
+         SX, SW, SWT, SDA, SDAT, SXT, TMPW, SC, SWP, SDY, SWPT, SDYT, SCT, TMPP, NB };
   size_t off[NB];
   size_t total;
 };

@@ -10,9 +10,15 @@
 //   dW_R += da^T x,  dn_R += da W_R                     (router)
 //   per-source norm backward                           -> dh,     d sigma
 // Everything is fp32 (weights converted once per call). The norm, RoPE and
-// scatter steps are this file's kernels; the products, all plain GEMMs, run
-// on the fp32 strided-batched GEMM of sgemm.cu (batched over channels or
-// rows). Gains and weight gradients accumulate (+=); dstates is overwritten.
+// scatter steps are this file's kernels. The router's three products (a =
+// x W_R^T, dx = da W_R, dW_R += da^T x; two thirds of the work) run on the
+// tcgen05 GEMM engine with bf16 operands split exactly-to-16-bits: each fp32
+// operand v = hi + lo (hi = bf16(v), lo = bf16(v - hi)), the left operand laid
+// out along K as [hi | hi | lo] and the right one as [hi | lo | hi], so one
+// product over 3K sums hi.hi + hi.lo + lo.hi in fp32 (the dropped lo.lo is
+// below 2^-16 relative). The other products run on the fp32 GEMM of sgemm.cu
+// (batched over channels or rows). Gains and weight gradients accumulate
+// (+=); dstates is overwritten.
 #include "kernels.h"
 
 namespace wm {
@@ -292,6 +298,70 @@ __global__ void __launch_bounds__(256) bwd_src_norm_w(const S* __restrict__ stat
   for (int t = threadIdx.x; t < D; t += blockDim.x) atomicAdd(&dsigma[(size_t)l * D + t], acc[t]);
 }
 
+// Leading dimension (elements) of a split operand of K columns: 3K, rounded
+// up to 8 so that rows start on 16-byte boundaries.
+inline long long ld3(long long K) { return (3 * K + 7) / 8 * 8; }
+
+__device__ __forceinline__ void split_hl(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// dst[r][j * C + c], j = 0, 1, 2: the split of src[r][c], left operand
+// (right = false: hi, hi, lo) or right operand (right = true: hi, lo, hi).
+__global__ void __launch_bounds__(256) split3_rows(const float* __restrict__ src, long long lds,
+                                                   int R, int C, __nv_bfloat16* __restrict__ dst,
+                                                   long long ldd, bool right) {
+  const long long n = (long long)R * C;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / C;
+    const int c = (int)(i - r * C);
+    __nv_bfloat16 hi, lo;
+    split_hl(src[r * lds + c], hi, lo);
+    __nv_bfloat16* d = dst + r * ldd + c;
+    d[0] = hi;
+    d[C] = right ? lo : hi;
+    d[2 * C] = right ? hi : lo;
+  }
+}
+
+// The same for the transpose: dst[c][j * R + r] from src[r][c] (32 x 32 tiles
+// through shared memory, reads and writes coalesced).
+// blockIdx.z selects a batch entry (src + z * sbs, dst + z * dbs).
+__global__ void __launch_bounds__(256) split3_t(const float* __restrict__ src, long long lds, int R,
+                                                int C, __nv_bfloat16* __restrict__ dst,
+                                                long long ldd, bool right, long long sbs = 0,
+                                                long long dbs = 0) {
+  __shared__ float tile[32][33];
+  src += blockIdx.z * sbs;
+  dst += blockIdx.z * dbs;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32
+  for (int y = ty; y < 32; y += 8) {
+    const int r = r0 + y, c = c0 + tx;
+    tile[y][tx] = (r < R && c < C) ? src[(long long)r * lds + c] : 0.f;
+  }
+  __syncthreads();
+  for (int y = ty; y < 32; y += 8) {
+    const int c = c0 + y, r = r0 + tx;
+    if (c < C && r < R) {
+      __nv_bfloat16 hi, lo;
+      split_hl(tile[tx][y], hi, lo);
+      __nv_bfloat16* d = dst + (long long)c * ldd + r;
+      d[0] = hi;
+      d[R] = right ? lo : hi;
+      d[2 * R] = right ? hi : lo;
+    }
+  }
+}
+
+__global__ void add_f32(float* __restrict__ dst, const float* __restrict__ src, long long n) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] += src[i];
+}
+
 template <typename S>
 __global__ void to_f32(const S* __restrict__ src, long long n, float* __restrict__ dst) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -310,6 +380,39 @@ bool gemm_rm(bool ta, bool tb, int M, int N, int K, const float* A, long long ld
   return sgemm_rm(g, st) == cudaSuccess;
 }
 
+// C[M][N] (fp32, ldc) = A B^T on the tensor cores for split operands A [M][3K]
+// and B [N][3K] (bf16, leading dimensions lda, ldb). False if the engine
+// does not take the shape (the caller then uses the fp32 GEMM).
+bool gemm_split_tc(int M, int N, int K, const __nv_bfloat16* A, long long lda,
+                   const __nv_bfloat16* B, long long ldb, float* C, long long ldc, uint32_t* flags,
+                   cudaStream_t st, int batch = 1, long long abs = 0, long long bbs = 0,
+                   long long cbs = 0) {
+  GemmDesc g;
+  g.M = M;
+  g.N = N;
+  g.K = 3 * K;
+  g.batch = batch;
+  g.A = A;
+  g.lda = lda;
+  g.a_bstride = abs;
+  g.B = B;
+  g.ldb = ldb;
+  g.b_bstride = bbs;
+  g.epi.mode = EPI_STORE;
+  g.epi.out_f32 = 1;
+  g.epi.C = C;
+  g.epi.ldc = ldc;
+  g.epi.c_bstride = cbs;
+  g.epi.flags = flags;
+  if (!gemm_tc_supported(g)) return false;
+  return launch_gemm_tc(g, st, nullptr) == cudaSuccess;
+}
+
+inline unsigned blocks_for(long long n) {
+  long long b = (n + 255) / 256;
+  return (unsigned)(b > 148 * 32 ? 148 * 32 : (b < 1 ? 1 : b));
+}
+
 }  // namespace
 
 // Workspace for N rows: fp32 buffers (see run_pool_backward), 256-byte aligned.
@@ -318,7 +421,10 @@ PoolBwdLayout pool_bwd_layout(const wm_config& c, long long N) {
   const long long L = c.L, D = c.D, k = c.k, w = (long long)c.Hkv * c.d;
   long long nR = 0;
   for (int l = 0; l < c.L; ++l) nR += (l % c.p) == c.p_offset;
+  const long long kL = k * L, nRD = nR * D;
+  auto bf = [](long long elems) { return (elems + 1) / 2; };  // bf16 elements in floats
   const long long sz[PoolBwdLayout::NB] = {
+      64,             // flag word (256 bytes)
       N * L,          // inv
       N * L * D,      // n (one branch)
       N * nR * D,     // x (router input)
@@ -335,6 +441,20 @@ PoolBwdLayout pool_bwd_layout(const wm_config& c, long long N) {
       k * w * D,      // W_K or W_V (fp32)
       2 * k * D,      // channel-norm gains (fp32)
       N * k * L,      // a (kept for the mix backward)
+      bf(N * ld3(nRD)),    // x split (left operand of a = x W_R^T)
+      bf(kL * ld3(nRD)),   // W_R split (right operand)
+      bf(nRD * ld3(kL)),   // W_R^T split (right operand of dx = da W_R)
+      bf(N * ld3(kL)),     // da split (left operand)
+      bf(kL * ld3(N)),     // da^T split (left operand of dW_R = da^T x)
+      bf(nRD * ld3(N)),    // x^T split (right operand)
+      kL * nRD,            // dW_R of this call (fp32), then added
+      bf(k * N * ld3(D)),  // c split, per channel (left operand of kt = c W^T)
+      bf(k * w * ld3(D)),  // W split, per channel (right operand)
+      bf(k * N * ld3(w)),  // dY split (left operand of dc = dY W)
+      bf(k * D * ld3(w)),  // W^T split (right operand)
+      bf(k * w * ld3(N)),  // dY^T split (left operand of dW = dY^T c)
+      bf(k * D * ld3(N)),  // c^T split (right operand)
+      k * w * D,           // dW of this call (fp32), then added
   };
   size_t o = 0;
   for (int i = 0; i < PoolBwdLayout::NB; ++i) {
@@ -357,7 +477,20 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
         *cc = buf(PoolBwdLayout::C), *kt = buf(PoolBwdLayout::KT), *dY = buf(PoolBwdLayout::DY),
         *dc = buf(PoolBwdLayout::DC), *dn = buf(PoolBwdLayout::DN), *dx = buf(PoolBwdLayout::DX),
         *wr = buf(PoolBwdLayout::WR), *wp = buf(PoolBwdLayout::WP), *gains = buf(PoolBwdLayout::G),
-        *a_keep = buf(PoolBwdLayout::AK);
+        *a_keep = buf(PoolBwdLayout::AK), *tmpw = buf(PoolBwdLayout::TMPW);
+  auto bbuf = [&](int b) {
+    return reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(q.ws) + lay.off[b]);
+  };
+  __nv_bfloat16 *sx = bbuf(PoolBwdLayout::SX), *sw = bbuf(PoolBwdLayout::SW),
+                *swt = bbuf(PoolBwdLayout::SWT), *sda = bbuf(PoolBwdLayout::SDA),
+                *sdat = bbuf(PoolBwdLayout::SDAT), *sxt = bbuf(PoolBwdLayout::SXT);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(q.ws);  // FLAGS is the first buffer
+  const long long kL = (long long)k * L, nRD = (long long)nR * D;
+  __nv_bfloat16 *sc = bbuf(PoolBwdLayout::SC), *swp = bbuf(PoolBwdLayout::SWP),
+                *sdy = bbuf(PoolBwdLayout::SDY), *swpt = bbuf(PoolBwdLayout::SWPT),
+                *sdyt = bbuf(PoolBwdLayout::SDYT), *sct = bbuf(PoolBwdLayout::SCT);
+  float* tmpp = buf(PoolBwdLayout::TMPP);
+  const long long kN = (long long)k * N;
   const wm_weights& W = *q.w;
   const long long WRn = (long long)k * L * nR * D, WPn = (long long)k * w * D;
   float* tau32 = gains;  // [2][k][D]
@@ -380,8 +513,12 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       WM_DISPATCH_S(c.dtype, {
         to_f32<S><<<(unsigned)((WRn + 255) / 256), 256, 0, st>>>((const S*)wrs, WRn, wr);
       });
-      ok = ok && gemm_rm(false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
-                         k * L, 0, 1, st);
+      // a = x W_R^T on the tensor cores (split operands), else in fp32
+      split3_rows<<<blocks_for((long long)N * nRD), 256, 0, st>>>(x, nRD, N, (int)nRD, sx, ld3(nRD), false);
+      split3_rows<<<blocks_for(kL * nRD), 256, 0, st>>>(wr, nRD, (int)kL, (int)nRD, sw, ld3(nRD), true);
+      if (!gemm_split_tc(N, (int)kL, (int)nRD, sx, ld3(nRD), sw, ld3(nRD), a_keep, kL, flags, st))
+        ok = ok && gemm_rm(false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
+                           k * L, 0, 1, st);
     }
     if (k <= 16)
       bwd_mix_fwd_k<16><<<N, 256, 0, st>>>(a_keep, n, N, L, D, k, tau32 + (size_t)be * k * D, c.eps, m, rj, cc);
@@ -393,8 +530,14 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       to_f32<S><<<(unsigned)((WPn + 255) / 256), 256, 0, st>>>((const S*)wps, WPn, wp);
     });
     if (be == 0) {
-      ok = ok && gemm_rm(false, true, N, w, D, cc, D, (long long)N * D, wp, D, (long long)w * D,
-                         0.f, kt, w, (long long)N * w, k, st);
+      // kt = c W_K^T per channel on split operands (rows of all channels at once)
+      split3_rows<<<blocks_for(kN * D), 256, 0, st>>>(cc, D, (int)kN, D, sc, ld3(D), false);
+      split3_rows<<<blocks_for((long long)k * w * D), 256, 0, st>>>(wp, D, (int)(k * w), D, swp, ld3(D),
+                                                                   true);
+      if (!gemm_split_tc(N, w, D, sc, ld3(D), swp, ld3(D), kt, w, flags, st, k, N * ld3(D),
+                         w * ld3(D), (long long)N * w))
+        ok = ok && gemm_rm(false, true, N, w, D, cc, D, (long long)N * D, wp, D, (long long)w * D,
+                           0.f, kt, w, (long long)N * w, k, st);
       const int rows = 64;
       dim3 grid((N + rows - 1) / rows, k);
       WM_DISPATCH_S(c.dtype, {
@@ -409,10 +552,25 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     }
     float* dW = be == 0 ? q.g.dWk : q.g.dWv;
     // dW_j += dY_j^T c_j  ([w x N] [N x D]);  dc_j = dY_j W_j  ([N x w] [w x D])
-    ok = ok && gemm_rm(true, false, w, D, N, dY, w, (long long)N * w, cc, D, (long long)N * D, 1.f,
-                       dW, D, (long long)w * D, k, st);
-    ok = ok && gemm_rm(false, false, N, D, w, dY, w, (long long)N * w, wp, D, (long long)w * D, 0.f,
-                       dc, D, (long long)N * D, k, st);
+    {
+      split3_rows<<<blocks_for(kN * w), 256, 0, st>>>(dY, w, (int)kN, w, sdy, ld3(w), false);
+      dim3 gw((unsigned)((D + 31) / 32), (unsigned)((w + 31) / 32), (unsigned)k);
+      split3_t<<<gw, 256, 0, st>>>(wp, D, w, D, swpt, ld3(w), true, (long long)w * D, D * ld3(w));
+      dim3 gy((unsigned)((w + 31) / 32), (unsigned)((N + 31) / 32), (unsigned)k);
+      split3_t<<<gy, 256, 0, st>>>(dY, w, N, w, sdyt, ld3(N), false, (long long)N * w, w * ld3(N));
+      dim3 gc((unsigned)((D + 31) / 32), (unsigned)((N + 31) / 32), (unsigned)k);
+      split3_t<<<gc, 256, 0, st>>>(cc, D, N, D, sct, ld3(N), true, (long long)N * D, D * ld3(N));
+    }
+    if (gemm_split_tc(w, D, N, sdyt, ld3(N), sct, ld3(N), tmpp, D, flags, st, k, w * ld3(N),
+                      D * ld3(N), (long long)w * D))
+      add_f32<<<blocks_for((long long)k * w * D), 256, 0, st>>>(dW, tmpp, (long long)k * w * D);
+    else
+      ok = ok && gemm_rm(true, false, w, D, N, dY, w, (long long)N * w, cc, D, (long long)N * D, 1.f,
+                         dW, D, (long long)w * D, k, st);
+    if (!gemm_split_tc(N, D, w, sdy, ld3(w), swpt, ld3(w), dc, D, flags, st, k, N * ld3(w),
+                       D * ld3(w), (long long)N * D))
+      ok = ok && gemm_rm(false, false, N, D, w, dY, w, (long long)N * w, wp, D, (long long)w * D, 0.f,
+                         dc, D, (long long)N * D, k, st);
     {  // channel norm backward, in place: dc -> dm
       const int rows = 64;
       dim3 grid((N + rows - 1) / rows, k);
@@ -425,14 +583,30 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
                        L, (long long)k * L, N, st);
     ok = ok && gemm_rm(true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
                        0.f, dn, D, (long long)L * D, N, st);
-    if (!W.static_coeff && q.g.dWr) {
-      // router: dW_R += da^T x ([kL x N] [N x nR D]);  dx = da W_R ([N x kL] [kL x nR D])
-      ok = ok && gemm_rm(true, false, k * L, nR * D, N, a, k * L, 0, x, nR * D, 0, 1.f,
-                         q.g.dWr + (size_t)be * WRn, nR * D, 0, 1, st);
-    }
     if (!W.static_coeff) {
-      ok = ok && gemm_rm(false, false, N, nR * D, k * L, a, k * L, 0, wr, nR * D, 0, 0.f, dx, nR * D,
-                         0, 1, st);
+      // router: dW_R += da^T x ([kL x N] [N x nR D]);  dx = da W_R ([N x kL] [kL x nR D]),
+      // on the tensor cores with split operands (transposed where the
+      // engine's K-major layout needs it), else in fp32
+      split3_rows<<<blocks_for((long long)N * kL), 256, 0, st>>>(a, kL, N, (int)kL, sda, ld3(kL), false);
+      {
+        dim3 g1((unsigned)((nRD + 31) / 32), (unsigned)((kL + 31) / 32));
+        split3_t<<<g1, 256, 0, st>>>(wr, nRD, (int)kL, (int)nRD, swt, ld3(kL), true);
+      }
+      if (!gemm_split_tc(N, (int)nRD, (int)kL, sda, ld3(kL), swt, ld3(kL), dx, nRD, flags, st))
+        ok = ok && gemm_rm(false, false, N, nR * D, k * L, a, k * L, 0, wr, nR * D, 0, 0.f, dx,
+                           nR * D, 0, 1, st);
+      if (q.g.dWr) {
+        dim3 g2((unsigned)((kL + 31) / 32), (unsigned)((N + 31) / 32));
+        split3_t<<<g2, 256, 0, st>>>(a, kL, N, (int)kL, sdat, ld3(N), false);
+        dim3 g3((unsigned)((nRD + 31) / 32), (unsigned)((N + 31) / 32));
+        split3_t<<<g3, 256, 0, st>>>(x, nRD, N, (int)nRD, sxt, ld3(N), true);
+        float* dwr = q.g.dWr + (size_t)be * WRn;
+        if (gemm_split_tc((int)kL, (int)nRD, N, sdat, ld3(N), sxt, ld3(N), tmpw, nRD, flags, st))
+          add_f32<<<blocks_for(kL * nRD), 256, 0, st>>>(dwr, tmpw, kL * nRD);
+        else
+          ok = ok && gemm_rm(true, false, k * L, nR * D, N, a, k * L, 0, x, nR * D, 0, 1.f, dwr,
+                             nR * D, 0, 1, st);
+      }
       bwd_scatter_dx<<<(unsigned)(((long long)N * nR * D + 255) / 256), 256, 0, st>>>(
           dx, N, L, D, c.p, c.p_offset, nR, dn);
     }
