@@ -249,8 +249,12 @@ size_t wm_pool_backward_workspace_size(const wm_config* cfg, int32_t max_rows);
  * fp32 and write dstates [N][L][D] (fp32, overwritten: the gradient of the
  * pool's outputs with respect to every layer state of each row) and add the
  * parameter gradients to ``grads``. With static_coeff set the router is not
- * used and dWr is left alone. Every step, the plain fp32 products included,
- * runs in this library's kernels. Errors: WM_ERR_INVALID_ARG (null or
+ * used and dWr is left alone. Every step runs in this library's kernels; the
+ * router and channel-projection products run on the tensor cores with exact
+ * bf16 hi/lo operand splits (three bf16 products per fp32 one, summed in
+ * fp32: within ~1e-5 of fp32 products). The workspace begins with a flag word
+ * (wm_check_flags reads and clears it): a bounded wait of those products that
+ * gives up sets its timeout bit. Errors: WM_ERR_INVALID_ARG (null or
  * misaligned pointers, N < 1, k * L > 1024, D > 8192), WM_ERR_WORKSPACE,
  * WM_ERR_CUDA (a failed launch). */
 wm_status wm_pool_backward(const wm_config* cfg, const wm_weights* w,
