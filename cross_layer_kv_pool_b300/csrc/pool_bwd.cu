@@ -105,33 +105,47 @@ __global__ void __launch_bounds__(256) bwd_mix_fwd_k(const float* __restrict__ a
   float ss[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) ss[j] = 0.f;
-  for (int t = threadIdx.x; t < D; t += blockDim.x) {
-    float acc[KMAX];
+  // four consecutive columns per thread (D is a multiple of 64): 16-byte
+  // loads of the row's L states, four states' loads in flight at a time
+  for (int t = 4 * threadIdx.x; t < D; t += 4 * blockDim.x) {
+    float4 acc[KMAX];
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) acc[j] = 0.f;
-    // eight source rows per step: their loads are in flight together
+    for (int j = 0; j < KMAX; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
     int l = 0;
-    for (; l + 8 <= L; l += 8) {
-      float v[8];
+    for (; l + 4 <= L; l += 4) {
+      float4 v[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = nr[(size_t)(l + u) * D + t];
+      for (int u = 0; u < 4; ++u) v[u] = *reinterpret_cast<const float4*>(nr + (size_t)(l + u) * D + t);
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
-          if (j < k) acc[j] = fmaf(coef[j * L + l + u], v[u], acc[j]);
+          if (j < k) {
+            const float a = coef[j * L + l + u];
+            acc[j].x = fmaf(a, v[u].x, acc[j].x);
+            acc[j].y = fmaf(a, v[u].y, acc[j].y);
+            acc[j].z = fmaf(a, v[u].z, acc[j].z);
+            acc[j].w = fmaf(a, v[u].w, acc[j].w);
+          }
     }
     for (; l < L; ++l) {
-      const float v = nr[(size_t)l * D + t];
+      const float4 v = *reinterpret_cast<const float4*>(nr + (size_t)l * D + t);
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
-        if (j < k) acc[j] = fmaf(coef[j * L + l], v, acc[j]);
+        if (j < k) {
+          const float a = coef[j * L + l];
+          acc[j].x = fmaf(a, v.x, acc[j].x);
+          acc[j].y = fmaf(a, v.y, acc[j].y);
+          acc[j].z = fmaf(a, v.z, acc[j].z);
+          acc[j].w = fmaf(a, v.w, acc[j].w);
+        }
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j)
       if (j < k) {
-        m[((size_t)j * N + r) * D + t] = acc[j];
-        ss[j] = fmaf(acc[j], acc[j], ss[j]);
+        *reinterpret_cast<float4*>(m + ((size_t)j * N + r) * D + t) = acc[j];
+        ss[j] = fmaf(acc[j].x, acc[j].x, fmaf(acc[j].y, acc[j].y,
+                fmaf(acc[j].z, acc[j].z, fmaf(acc[j].w, acc[j].w, ss[j]))));
       }
   }
 #pragma unroll
@@ -149,9 +163,12 @@ __global__ void __launch_bounds__(256) bwd_mix_fwd_k(const float* __restrict__ a
   __syncthreads();
   for (int j = 0; j < k; ++j) {
     const float inv = 1.f / rr[j];
-    for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    for (int t = 4 * threadIdx.x; t < D; t += 4 * blockDim.x) {
       const size_t i = ((size_t)j * N + r) * D + t;
-      c[i] = m[i] * inv * tau[(size_t)j * D + t];
+      const float4 mv = *reinterpret_cast<const float4*>(m + i);
+      const float4 tv = *reinterpret_cast<const float4*>(tau + (size_t)j * D + t);
+      *reinterpret_cast<float4*>(c + i) =
+          make_float4(mv.x * inv * tv.x, mv.y * inv * tv.y, mv.z * inv * tv.z, mv.w * inv * tv.w);
     }
   }
 }
@@ -236,13 +253,28 @@ __global__ void __launch_bounds__(256) bwd_rms_w(const float* __restrict__ x, lo
     float* dr = dxy + gi * xstride_gain + q * xstride_row;
     const float rv = rr[gi * rr_stride_gain + q * rr_stride_row];
     float s = 0.f;
-    for (int t = lane; t < D; t += 32) s = fmaf(wg[t] * dr[t], xr[t], s);
+    // lane l takes columns 4l + 128i (D is a multiple of 64): 16-byte accesses
+#pragma unroll 4
+    for (int t = 4 * lane; t < D; t += 128) {
+      const float4 w = *reinterpret_cast<const float4*>(wg + t);
+      const float4 dy = *reinterpret_cast<const float4*>(dr + t);
+      const float4 xv = *reinterpret_cast<const float4*>(xr + t);
+      s = fmaf(w.x * dy.x, xv.x, fmaf(w.y * dy.y, xv.y, fmaf(w.z * dy.z, xv.z, fmaf(w.w * dy.w, xv.w, s))));
+    }
     s = warp_sum(s);
     const float c3 = s / ((float)D * rv * rv * rv), iv = 1.f / rv;
-    for (int t = lane; t < D; t += 32) {
-      const float dy = dr[t], xv = xr[t];
-      atomicAdd(&acc[t], xv * iv * dy);
-      dr[t] = wg[t] * dy * iv - xv * c3;
+#pragma unroll 4
+    for (int t = 4 * lane; t < D; t += 128) {
+      const float4 w = *reinterpret_cast<const float4*>(wg + t);
+      const float4 dy = *reinterpret_cast<const float4*>(dr + t);
+      const float4 xv = *reinterpret_cast<const float4*>(xr + t);
+      atomicAdd(&acc[t], xv.x * iv * dy.x);
+      atomicAdd(&acc[t + 1], xv.y * iv * dy.y);
+      atomicAdd(&acc[t + 2], xv.z * iv * dy.z);
+      atomicAdd(&acc[t + 3], xv.w * iv * dy.w);
+      *reinterpret_cast<float4*>(dr + t) =
+          make_float4(w.x * dy.x * iv - xv.x * c3, w.y * dy.y * iv - xv.y * c3,
+                      w.z * dy.z * iv - xv.z * c3, w.w * dy.w * iv - xv.w * c3);
     }
   }
   __syncthreads();
@@ -266,6 +298,20 @@ __global__ void bwd_scatter_dx(const float* __restrict__ dx, int N, int L, int D
 // row (8 rows in flight per block), d sigma gathered in shared memory
 // (dynamic, D floats) and added once per block; block (chunk, l) takes rows
 // chunk * rows .. + rows of layer l.
+// Four consecutive storage-type values as fp32 (16- or 8-byte aligned).
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+// The same with scalar loads (operands whose alignment the caller does not fix).
+template <typename S>
+__device__ __forceinline__ float4 ld4s(const S* p) {
+  return make_float4(to_f(p[0]), to_f(p[1]), to_f(p[2]), to_f(p[3]));
+}
+
 template <typename S>
 __global__ void __launch_bounds__(256) bwd_src_norm_w(const S* __restrict__ states, int N, int L,
                                                       int D, const float* __restrict__ inv,
@@ -280,18 +326,36 @@ __global__ void __launch_bounds__(256) bwd_src_norm_w(const S* __restrict__ stat
   for (int t = threadIdx.x; t < D; t += blockDim.x) acc[t] = 0.f;
   __syncthreads();
   const int r0 = blockIdx.x * rows, r1 = min(r0 + rows, N);
+  // lane l takes columns 4l + 128i (D is a multiple of 64): 16-byte loads
   for (int r = r0 + warp; r < r1; r += (int)(blockDim.x >> 5)) {
     const size_t base = ((size_t)r * L + l) * D;
     const float iv = inv[(size_t)r * L + l];
     float s = 0.f;
-    for (int t = lane; t < D; t += 32) s = fmaf(to_f(sg[t]) * dn[base + t], to_f(states[base + t]), s);
+#pragma unroll 4
+    for (int t = 4 * lane; t < D; t += 128) {
+      const float4 w = ld4s(sg + t), g = ld4(dn + base + t), h = ld4(states + base + t);
+      s = fmaf(w.x * g.x, h.x, s);
+      s = fmaf(w.y * g.y, h.y, s);
+      s = fmaf(w.z * g.z, h.z, s);
+      s = fmaf(w.w * g.w, h.w, s);
+    }
     s = warp_sum(s);
     const float c3 = s * iv * iv * iv / (float)D;
-    for (int t = lane; t < D; t += 32) {
-      const float h = to_f(states[base + t]), g = dn[base + t];
-      atomicAdd(&acc[t], h * iv * g);
-      const float dh = to_f(sg[t]) * g * iv - h * c3;
-      dstates[base + t] = first ? dh : dstates[base + t] + dh;
+#pragma unroll 4
+    for (int t = 4 * lane; t < D; t += 128) {
+      const float4 w = ld4s(sg + t), g = ld4(dn + base + t), h = ld4(states + base + t);
+      atomicAdd(&acc[t], h.x * iv * g.x);
+      atomicAdd(&acc[t + 1], h.y * iv * g.y);
+      atomicAdd(&acc[t + 2], h.z * iv * g.z);
+      atomicAdd(&acc[t + 3], h.w * iv * g.w);
+      float4 dh = make_float4(w.x * g.x * iv - h.x * c3, w.y * g.y * iv - h.y * c3,
+                              w.z * g.z * iv - h.z * c3, w.w * g.w * iv - h.w * c3);
+      float4* o = reinterpret_cast<float4*>(dstates + base + t);
+      if (!first) {
+        const float4 prev = *o;
+        dh.x += prev.x; dh.y += prev.y; dh.z += prev.z; dh.w += prev.w;
+      }
+      *o = dh;
     }
   }
   __syncthreads();
