@@ -317,7 +317,11 @@ int run_pool(const Ctx& x, int N, const void* states, long long ld_row, float* c
   m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
   const int tr = trace_begin(x, WM_TRACE_MIX);
   ++x.launches;
-  const int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  if (parts < 0) {
+    if (x.err == cudaSuccess) x.err = cudaErrorLaunchFailure;
+    parts = 0;
+  }
   trace_end(x, tr, (double)N * ((double)c.L * c.D * x.es + 2.0 * c.k * c.L * 4 + c.L * 4.0 +
                                  2.0 * c.k * c.D * x.es));
   for (int branch = 0; branch < 2; ++branch) {
@@ -403,7 +407,11 @@ void run_pool_channel(const Ctx& x, int N, int l, void* cache_k, void* cache_v, 
   m.inv_ld = c.L; m.sn_layers = c.L; m.cn_channels = c.k;
   const int tr = trace_begin(x, WM_TRACE_MIX);
   ++x.launches;
-  const int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  int parts = launch_mix(c.dtype, m, !x.tc, x.st, x.flags());
+  if (parts < 0) {
+    if (x.err == cudaSuccess) x.err = cudaErrorLaunchFailure;
+    parts = 0;
+  }
   trace_end(x, tr, (double)N * ((double)Ls * c.D * x.es + 2.0 * Ls * 4 + Ls * 4.0 + 2.0 * c.D * x.es));
   for (int branch = 0; branch < 2; ++branch) {
     GemmDesc g;

@@ -122,11 +122,12 @@ struct MixArgs {
 // if it holds u = tau (.) m with the norm deferred: chan_ss then holds P
 // partial sums of squares per (row, branch, channel) and the norm factor is
 // rsqrt(sum / D + eps) (applied by the projection epilogue, or in place by
-// launch_mix_normalize).
+// launch_mix_normalize); -1 if a launch failed.
 int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t* flags);
-// Tensor-core mixer (bf16 mma.sync, deferred norm); returns P, or 0 if the
+// Tensor-core mixer (bf16 mma.sync, deferred norm); returns P, 0 if the
 // shape is outside its envelope (k > 16, L > 32, no slicing of D into at
-// most 8 slices of at most 448 columns, misaligned operands).
+// most 8 slices of at most 448 columns, misaligned operands), or -1 if a
+// launch failed.
 int launch_mix_tc(const MixArgs& a, cudaStream_t st, uint32_t* flags);
 
 // ---------------------------------------------------------------------------

@@ -358,7 +358,7 @@ int launch_mix(int dtype, const MixArgs& a, bool simt, cudaStream_t st, uint32_t
                          ((uintptr_t)a.stash % 16 == 0) && (a.ld_row % 8 == 0);
   if (dtype == WM_BF16 && !simt) {
     const int parts = launch_mix_tc(a, st, flags);
-    if (parts) return parts;
+    if (parts) return parts;  // P > 0, or -1: its launch failed
   }
   if (stream_ok) {
     bool done = false;
