@@ -146,9 +146,6 @@ struct GemmDesc {
   // request them before its predecessor in the stream has finished.
   bool b_const = false;
   bool no_cluster = false;       // split K through global atomics, never a cluster
-  // split K over a cluster even with several row tiles (set internally for
-  // the rows that a large product leaves after its whole waves of tiles)
-  bool force_cluster = false;
   bool wait_probe = false;       // test aid (WM_FLAG_WAIT_PROBE): see gemm_tc.cu
   Epi epi;
   // Zero-filled fp32 scratch for split-K (nullable): when a GEMM has too few

@@ -981,28 +981,6 @@ int num_sms() {
   return n > 0 ? n : 148;
 }
 
-// K slices per cluster for ``out_tiles`` output tiles of ``num_kb`` K blocks:
-// the largest split (<= 8, slices of >= 2 blocks, equal slices) whose clusters
-// are all resident at once, or 0.
-template <int BN, bool DUAL, int MODE, int HD>
-int cluster_split(long long out_tiles, int num_kb, int& kb_per_out) {
-  const int sms = num_sms();
-  if (num_kb < 4 || out_tiles * 2 > sms) return 0;
-  long long ks0 = sms / out_tiles;
-  if (ks0 > 8) ks0 = 8;
-  if (ks0 > num_kb / 2) ks0 = num_kb / 2;
-  for (int ks = (int)ks0; ks >= 2; --ks) {
-    const int kb_per = (num_kb + ks - 1) / ks;
-    const int kse = (num_kb + kb_per - 1) / kb_per;
-    if (kse != ks) continue;
-    if (max_clusters<BN, DUAL, MODE, HD>(ks) >= out_tiles) {
-      kb_per_out = kb_per;
-      return ks;
-    }
-  }
-  return 0;
-}
-
 template <int BN, bool DUAL, int MODE, int HD>
 cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   using C = Cfg<BN, DUAL>;
@@ -1029,17 +1007,23 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   auto kern = gemm_tc_kernel<BN, DUAL, MODE, HD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  // Few output tiles (decode-sized M, or the rows a large product leaves
-  // after its whole waves): split K over a cluster of up to 8 CTAs that sum
-  // their slices through distributed shared memory; the largest split whose
-  // clusters are all resident at once (one wave).
-  if (!g.no_cluster && (g.M <= BM || g.force_cluster)) {
-    int kb_per = 0;
-    const int ks = cluster_split<BN, DUAL, MODE, HD>(out_tiles, p.num_kb, kb_per);
-    if (ks >= 2) {
-      p.ksplit = ks;
-      p.kb_per = kb_per;
-      p.cluster_red = 1;
+  // Few output tiles (decode-sized M): split K over a cluster of up to 8
+  // CTAs that sum their slices through distributed shared memory; the
+  // largest split whose clusters are all resident at once (one wave).
+  if (!g.no_cluster && g.M <= BM && out_tiles * 2 <= sms && p.num_kb >= 4) {
+    long long ks0 = sms / out_tiles;
+    if (ks0 > 8) ks0 = 8;
+    if (ks0 > p.num_kb / 2) ks0 = p.num_kb / 2;
+    for (int ks = (int)ks0; ks >= 2; --ks) {
+      const int kb_per = (p.num_kb + ks - 1) / ks;
+      const int kse = (p.num_kb + kb_per - 1) / kb_per;
+      if (kse != ks) continue;
+      if (max_clusters<BN, DUAL, MODE, HD>(ks) >= out_tiles) {
+        p.ksplit = ks;
+        p.kb_per = kb_per;
+        p.cluster_red = 1;
+        break;
+      }
     }
   }
   const long long need = (long long)g.batch * g.M * g.N * (DUAL ? 2 : 1);
@@ -1099,45 +1083,6 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   return cudaGetLastError();
 }
 
-// A large product whose output tiles end in a partial wave (e.g. 448 tiles
-// of 128 x 256 on 148 SMs: three waves and four tiles) runs as two launches:
-// the leading tile rows that fill whole waves, then the remaining rows with K
-// split over clusters, so that their tiles take one short wave instead of a
-// full-length one. Single products with a row-local epilogue only (rows are
-// offset for the second launch).
-template <int BN, bool DUAL, int MODE, int HD>
-cudaError_t run_waves(const GemmDesc& g, cudaStream_t st, int* launches) {
-  if (g.batch == 1 && !DUAL && !g.no_cluster && !g.force_cluster &&
-      (MODE == EPI_STORE || MODE == EPI_RESID || MODE == EPI_QNORM_ROPE)) {
-    const int sms = num_sms();
-    const long long m_tiles = (g.M + BM - 1) / BM, n_tiles = (g.N + BN - 1) / BN;
-    const long long tiles = m_tiles * n_tiles, waves = tiles / sms;
-    const long long rows0 = waves * sms / n_tiles;  // tile rows in the whole waves
-    if (waves >= 1 && tiles % sms && rows0 >= 1 && rows0 < m_tiles) {
-      int kb_per = 0;
-      const int num_kb = (g.K + BK - 1) / BK;
-      if (cluster_split<BN, DUAL, MODE, HD>((m_tiles - rows0) * n_tiles, num_kb, kb_per) >= 2) {
-        const long long m0 = rows0 * BM;
-        GemmDesc head = g, tail = g;
-        head.M = (int)m0;
-        tail.M = g.M - (int)m0;
-        tail.force_cluster = true;
-        tail.A = static_cast<const char*>(g.A) + m0 * g.lda * 2;
-        if (g.epi.rowmap) tail.epi.rowmap = g.epi.rowmap + m0;
-        else if (g.epi.C)
-          tail.epi.C = static_cast<char*>(g.epi.C) + m0 * g.epi.ldc * (g.epi.out_f32 ? 4 : 2);
-        if (g.epi.R) tail.epi.R = static_cast<const char*>(g.epi.R) + m0 * g.epi.ldr * 2;
-        if (g.epi.pos) tail.epi.pos = g.epi.pos + m0;
-        if (g.epi.seq) tail.epi.seq = g.epi.seq + m0;
-        const cudaError_t e = run<BN, DUAL, MODE, HD>(head, st, launches);
-        if (e != cudaSuccess) return e;
-        return run<BN, DUAL, MODE, HD>(tail, st, launches);
-      }
-    }
-  }
-  return run<BN, DUAL, MODE, HD>(g, st, launches);
-}
-
 }  // namespace tc
 
 bool gemm_tc_supported(const GemmDesc& g) {
@@ -1186,17 +1131,17 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int* launches) {
       const int bn = pick_bn(g, kPlain, 3);
       if (g.epi.mode == EPI_STORE) {
         switch (bn) {
-          case 256: return tc::run_waves<256, false, EPI_STORE, 0>(g, st, launches);
-          case 224: return tc::run_waves<224, false, EPI_STORE, 0>(g, st, launches);
-          case 128: return tc::run_waves<128, false, EPI_STORE, 0>(g, st, launches);
-          default: return tc::run_waves<112, false, EPI_STORE, 0>(g, st, launches);
+          case 256: return tc::run<256, false, EPI_STORE, 0>(g, st, launches);
+          case 224: return tc::run<224, false, EPI_STORE, 0>(g, st, launches);
+          case 128: return tc::run<128, false, EPI_STORE, 0>(g, st, launches);
+          default: return tc::run<112, false, EPI_STORE, 0>(g, st, launches);
         }
       }
       switch (bn) {
-        case 256: return tc::run_waves<256, false, EPI_RESID, 0>(g, st, launches);
-        case 224: return tc::run_waves<224, false, EPI_RESID, 0>(g, st, launches);
-        case 128: return tc::run_waves<128, false, EPI_RESID, 0>(g, st, launches);
-        default: return tc::run_waves<112, false, EPI_RESID, 0>(g, st, launches);
+        case 256: return tc::run<256, false, EPI_RESID, 0>(g, st, launches);
+        case 224: return tc::run<224, false, EPI_RESID, 0>(g, st, launches);
+        case 128: return tc::run<128, false, EPI_RESID, 0>(g, st, launches);
+        default: return tc::run<112, false, EPI_RESID, 0>(g, st, launches);
       }
     }
     case EPI_QNORM_ROPE:
@@ -1205,10 +1150,10 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int* launches) {
       const bool wide = g.N % 256 == 0 && pick_bn(g, kHeads, 2) == 256;
       if (g.epi.mode == EPI_QNORM_ROPE) {
         if (g.epi.d == 128)
-          return wide ? tc::run_waves<256, false, EPI_QNORM_ROPE, 128>(g, st, launches)
-                      : tc::run_waves<128, false, EPI_QNORM_ROPE, 128>(g, st, launches);
-        return wide ? tc::run_waves<256, false, EPI_QNORM_ROPE, 64>(g, st, launches)
-                    : tc::run_waves<128, false, EPI_QNORM_ROPE, 64>(g, st, launches);
+          return wide ? tc::run<256, false, EPI_QNORM_ROPE, 128>(g, st, launches)
+                      : tc::run<128, false, EPI_QNORM_ROPE, 128>(g, st, launches);
+        return wide ? tc::run<256, false, EPI_QNORM_ROPE, 64>(g, st, launches)
+                    : tc::run<128, false, EPI_QNORM_ROPE, 64>(g, st, launches);
       }
       if (g.epi.d == 128)
         return wide ? tc::run<256, false, EPI_KV, 128>(g, st, launches)
