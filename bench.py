@@ -52,15 +52,16 @@ from cross_layer_kv_pool_b300 import synth  # noqa: E402
 
 METRIC = "prefill tok/s (3 cyclic passes, g=16) at 1.3B k=14"
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
-# DRAM bytes (read + written) per tcgen05 GEMM launch of the prefill step,
-# launch-weighted over the 335 gemm_tc_kernel launches among the first 600
-# launches of the timed step (ncu --metrics gpu__time_duration.sum,
-# dram__bytes_read.sum,dram__bytes_write.sum --nvtx --nvtx-include "timed/"
-# -c 600, one pass). Set to None when the GEMM kernel changes, until it is
-# captured again.
-GEMM_DRAM_BYTES_PER_LAUNCH = 98.49e6
-GEMM_DRAM_SOURCE = ("ncu launch list of the prefill step: 335 gemm_tc_kernel launches of the "
-                    "first 600 timed launches, launch-weighted mean of dram bytes read + written")
+# DRAM bytes (read + written) per tcgen05 GEMM launch of the prefill step.
+# None: the GEMM kernel gained its entry check of the flag word (control path
+# only) after the last counter capture (98.5 MB per launch, launch-weighted
+# over the 335 gemm_tc_kernel launches among the first 600 of the timed step),
+# and a capture of the full-size step with DRAM counters holds more device
+# memory than such captures may; set it again from a capture of the current
+# kernel.
+GEMM_DRAM_BYTES_PER_LAUNCH = None
+GEMM_DRAM_SOURCE = ("null: the kernel changed (entry flag check) after the last DRAM counter "
+                    "capture of the full-size step, which is not repeated at that size")
 
 
 def parse():
