@@ -219,6 +219,65 @@ __global__ void __launch_bounds__(32 * NORM_ROWS) norm_emit_kernel(
   }
 }
 
+// The same with the row held in registers: lane t loads vectors t, t + 32, ...
+// (NV of them, all issued before the first is used) and writes the outputs
+// from them, so the row is read once with every load in flight. The sums run
+// in the same order as the loop above (bit-identical results).
+template <typename S, int NV>
+__global__ void __launch_bounds__(32 * NORM_ROWS) norm_emit_regs_kernel(
+    const S* __restrict__ X, long long ldx_row, long long ldx_l, int l0, int D, int L,
+    const S* __restrict__ gain_in, S* __restrict__ xn, float* __restrict__ inv_out,
+    const S* __restrict__ src_norm, S* __restrict__ rin, int N, int nR, int p, int p_off,
+    float eps) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int VN = VecT<S>::N;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * NORM_ROWS + (threadIdx.x >> 5), l = l0 + blockIdx.y;
+  if (r >= N) return;  // warp-uniform
+  const S* x = X + (long long)r * ldx_row + (long long)l * ldx_l;
+  float v[NV][VN];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c < D) ld_vec(x + c, v[k]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if ((lane + 32 * k) * VN < D) {
+#pragma unroll
+      for (int i = 0; i < VN; ++i) ss += v[k][i] * v[k][i];
+    }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)D + eps);
+  if (lane == 0) inv_out[(long long)r * L + l] = inv;
+  const bool in_R = rin != nullptr && (l % p) == p_off;
+  const int ridx = (l - p_off) / p;
+  const long long rin_b = (long long)N * nR * D;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c >= D) continue;
+    float o[VN], gv[VN];
+    if (xn) {
+      ld_vec(gain_in + (long long)l * D + c, gv);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) o[i] = v[k][i] * inv * gv[i];
+      st_vec(xn + (long long)r * D + c, o);
+    }
+    if (in_R) {
+#pragma unroll
+      for (int beta = 0; beta < 2; ++beta) {
+        ld_vec(src_norm + ((long long)beta * L + l) * D + c, gv);
+#pragma unroll
+        for (int i = 0; i < VN; ++i) o[i] = v[k][i] * inv * gv[i];
+        st_vec(rin + beta * rin_b + (long long)r * nR * D + (long long)ridx * D + c, o);
+      }
+    }
+  }
+}
+
 // Few rows (a decode step): one 256-thread block per (row, layer), more loads
 // in flight per row than a warp has.
 template <typename S>
@@ -280,6 +339,24 @@ void launch_norm_emit(int dtype, const void* X, long long ldx_row, long long ldx
     return;
   }
   dim3 grid((N + NORM_ROWS - 1) / NORM_ROWS, nl);
+  // rows of up to 8 vectors per lane stay in registers
+  const int nv = (D + 32 * (dtype == WM_BF16 ? 8 : 4) - 1) / (32 * (dtype == WM_BF16 ? 8 : 4));
+#define WM_EMIT_REGS(NV_)                                                                           \
+  WM_DISPATCH_S(dtype, launch_k(norm_emit_regs_kernel<S, NV_>, dim3(grid), dim3(32 * NORM_ROWS), 0, \
+                                st, (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in,      \
+                                (S*)xn, inv, (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps))
+  switch (nv) {
+    case 1: WM_EMIT_REGS(1); return;
+    case 2: WM_EMIT_REGS(2); return;
+    case 3: WM_EMIT_REGS(3); return;
+    case 4: WM_EMIT_REGS(4); return;
+    case 5: WM_EMIT_REGS(5); return;
+    case 6: WM_EMIT_REGS(6); return;
+    case 7: WM_EMIT_REGS(7); return;
+    case 8: WM_EMIT_REGS(8); return;
+    default: break;
+  }
+#undef WM_EMIT_REGS
   WM_DISPATCH_S(dtype, launch_k(norm_emit_kernel<S>, dim3(grid), dim3(32 * NORM_ROWS), 0, st,
                                 (const S*)X, ldx_row, ldx_l, l0, D, L, (const S*)gain_in, (S*)xn,
                                 inv, (const S*)src_norm, (S*)rin, N, nR, p, p_off, eps));
@@ -314,6 +391,45 @@ __global__ void __launch_bounds__(32 * NORM_ROWS) rmsnorm_kernel(
 #pragma unroll
     for (int i = 0; i < VN; ++i) v[i] = v[i] * inv * gv[i];
     st_vec(y + (long long)r * D + c, v);
+  }
+}
+
+// The same with the row held in registers (as norm_emit_regs_kernel).
+template <typename S, int NV>
+__global__ void __launch_bounds__(32 * NORM_ROWS) rmsnorm_regs_kernel(
+    const S* __restrict__ X, long long ldx, int row0, int rstride, int D,
+    const S* __restrict__ gain, S* __restrict__ y, float eps, int N) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int VN = VecT<S>::N;
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * NORM_ROWS + (threadIdx.x >> 5);
+  if (r >= N) return;  // warp-uniform
+  const S* x = X + (long long)(row0 + (long long)r * rstride) * ldx;
+  float v[NV][VN];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c < D) ld_vec(x + c, v[k]);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if ((lane + 32 * k) * VN < D) {
+#pragma unroll
+      for (int i = 0; i < VN; ++i) ss += v[k][i] * v[k][i];
+    }
+  ss = warp_sum(ss);
+  const float inv = rsqrtf(ss / (float)D + eps);
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c >= D) continue;
+    float gv[VN], o[VN];
+    ld_vec(gain + c, gv);
+#pragma unroll
+    for (int i = 0; i < VN; ++i) o[i] = v[k][i] * inv * gv[i];
+    st_vec(y + (long long)r * D + c, o);
   }
 }
 
@@ -353,9 +469,25 @@ void launch_rmsnorm(int dtype, const void* X, long long ldx, int row0, int rstri
                                   (const S*)X, ldx, row0, rstride, D, (const S*)gain, (S*)y, eps));
     return;
   }
-  WM_DISPATCH_S(dtype, launch_k(rmsnorm_kernel<S>, dim3((N + NORM_ROWS - 1) / NORM_ROWS),
-                                dim3(32 * NORM_ROWS), 0, st, (const S*)X, ldx, row0, rstride, D,
-                                (const S*)gain, (S*)y, eps, N));
+  const dim3 grid((N + NORM_ROWS - 1) / NORM_ROWS);
+  const int nv = (D + 32 * (dtype == WM_BF16 ? 8 : 4) - 1) / (32 * (dtype == WM_BF16 ? 8 : 4));
+#define WM_RMS_REGS(NV_)                                                                         \
+  WM_DISPATCH_S(dtype, launch_k(rmsnorm_regs_kernel<S, NV_>, grid, dim3(32 * NORM_ROWS), 0, st, \
+                                (const S*)X, ldx, row0, rstride, D, (const S*)gain, (S*)y, eps, N))
+  switch (nv) {
+    case 1: WM_RMS_REGS(1); return;
+    case 2: WM_RMS_REGS(2); return;
+    case 3: WM_RMS_REGS(3); return;
+    case 4: WM_RMS_REGS(4); return;
+    case 5: WM_RMS_REGS(5); return;
+    case 6: WM_RMS_REGS(6); return;
+    case 7: WM_RMS_REGS(7); return;
+    case 8: WM_RMS_REGS(8); return;
+    default: break;
+  }
+#undef WM_RMS_REGS
+  WM_DISPATCH_S(dtype, launch_k(rmsnorm_kernel<S>, grid, dim3(32 * NORM_ROWS), 0, st, (const S*)X, ldx,
+                                row0, rstride, D, (const S*)gain, (S*)y, eps, N));
 }
 
 __global__ void broadcast_coeff_kernel(const float* __restrict__ stat, long long total, int n_per_row,
