@@ -58,6 +58,63 @@ __global__ void __launch_bounds__(256) bwd_src_norm_fwd(const S* __restrict__ st
   }
 }
 
+// The same, one warp per (row, layer) with the state held in registers: lane
+// t loads 16-byte vectors t, t + 32, ... (NV of them, all in flight), sums
+// their squares, and writes n (and x) as 16-byte stores from the registers.
+template <typename S, int NV>
+__global__ void __launch_bounds__(256) bwd_src_norm_fwd_w(const S* __restrict__ states, long long NL,
+                                                          int L, int D, const S* __restrict__ sigma,
+                                                          float eps, int p, int p_offset, int nR,
+                                                          float* __restrict__ inv,
+                                                          float* __restrict__ n,
+                                                          float* __restrict__ x) {
+  constexpr int VN = 16 / sizeof(S);
+  const int lane = threadIdx.x & 31;
+  const long long rl = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // row * L + l
+  if (rl >= NL) return;  // warp-uniform
+  const int l = (int)(rl % L);
+  const long long r = rl / L;
+  const S* h = states + rl * D;
+  float v[NV][VN];
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c < D) {
+      const uint4 u = *reinterpret_cast<const uint4*>(h + c);
+      const S* e = reinterpret_cast<const S*>(&u);
+#pragma unroll
+      for (int i = 0; i < VN; ++i) v[k][i] = to_f(e[i]);
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NV; ++k)
+    if ((lane + 32 * k) * VN < D) {
+#pragma unroll
+      for (int i = 0; i < VN; ++i) ss += v[k][i] * v[k][i];
+    }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float iv = rsqrtf(ss / (float)D + eps);
+  if (lane == 0) inv[rl] = iv;
+  const bool src = (l % p) == p_offset;
+  float* xr = x + (r * nR + l / p) * D;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const int c = (lane + 32 * k) * VN;
+    if (c >= D) continue;
+    const uint4 u = *reinterpret_cast<const uint4*>(sigma + (size_t)l * D + c);
+    const S* g = reinterpret_cast<const S*>(&u);
+#pragma unroll
+    for (int i = 0; i < VN; i += 4) {
+      const float4 o = make_float4(v[k][i] * iv * to_f(g[i]), v[k][i + 1] * iv * to_f(g[i + 1]),
+                                   v[k][i + 2] * iv * to_f(g[i + 2]), v[k][i + 3] * iv * to_f(g[i + 3]));
+      *reinterpret_cast<float4*>(n + rl * D + c + i) = o;
+      if (src) *reinterpret_cast<float4*>(xr + c + i) = o;
+    }
+  }
+}
+
 // m[j][r] = sum_l a[r][j][l] n[r][l]; rj[r][j] = rms(m); c[j][r] = m / rj * tau_j.
 __global__ void __launch_bounds__(256) bwd_mix_fwd(const float* __restrict__ a,
                                                    const float* __restrict__ n, int N, int L, int D,
@@ -282,6 +339,19 @@ __global__ void __launch_bounds__(256) bwd_rms_w(const float* __restrict__ x, lo
 }
 
 // dn[r][R_i] += dx[r][i]
+// The same four columns at a time (D % 4 == 0, 16-byte aligned rows).
+__global__ void bwd_scatter_dx4(const float4* __restrict__ dx, int N, int L, int D4, int p,
+                                int p_offset, int nR, float4* __restrict__ dn) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)N * nR * D4) return;
+  const int t = (int)(i % D4);
+  const long long ri = i / D4;
+  const int s = (int)(ri % nR);
+  const long long r = ri / nR;
+  float4* d = dn + (r * L + p_offset + (long long)s * p) * D4 + t;
+  const float4 a = dx[i], b = *d;
+  *d = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
 __global__ void bwd_scatter_dx(const float* __restrict__ dx, int N, int L, int D, int p,
                                int p_offset, int nR, float* __restrict__ dn) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -564,10 +634,36 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
   bool ok = true;
   for (int be = 0; be < 2 && ok; ++be) {
     const char* sig = static_cast<const char*>(W.src_norm) + (size_t)be * L * D * (c.dtype == WM_F32 ? 4 : 2);
+// the warp source-norm recompute for NV vectors per lane (used inside the
+// storage-type dispatch below, where S is defined)
+#define WM_SNF(NV_)                                                                                    \
+  bwd_src_norm_fwd_w<S, NV_><<<gw, 256, 0, st>>>((const S*)q.states, NL, L, D, (const S*)sig, c.eps, \
+                                                 c.p, c.p_offset, nR, inv, n, x)
     WM_DISPATCH_S(c.dtype, {
-      bwd_src_norm_fwd<S><<<(unsigned)((long long)N * L), 256, 0, st>>>(
-          (const S*)q.states, L, D, (const S*)sig, c.eps, c.p, c.p_offset, nR, inv, n, x);
+      constexpr int VN = 16 / sizeof(S);
+      const int nv = (D + 32 * VN - 1) / (32 * VN);
+      const long long NL = (long long)N * L;
+      const bool vec = D % VN == 0 && ((uintptr_t)q.states % 16 == 0) && ((uintptr_t)sig % 16 == 0) &&
+                       D % 4 == 0 && nv <= 8;
+      const unsigned gw = (unsigned)((NL + 7) / 8);
+      if (vec) {
+        switch (nv) {
+          case 1: WM_SNF(1); break;
+          case 2: WM_SNF(2); break;
+          case 3: WM_SNF(3); break;
+          case 4: WM_SNF(4); break;
+          case 5: WM_SNF(5); break;
+          case 6: WM_SNF(6); break;
+          case 7: WM_SNF(7); break;
+          default: WM_SNF(8); break;
+        }
+      } else {
+        bwd_src_norm_fwd<S><<<(unsigned)NL, 256, 0, st>>>(
+            (const S*)q.states, L, D, (const S*)sig, c.eps, c.p, c.p_offset, nR, inv, n, x);
+      }
+
     });
+#undef WM_SNF
     // coefficients: the router (x W_R^T) or the constants
     if (W.static_coeff) {
       broadcast_rows<<<(unsigned)(((long long)N * k * L + 255) / 256), 256, 0, st>>>(
@@ -671,8 +767,13 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
           ok = ok && gemm_rm(true, false, k * L, nR * D, N, a, k * L, 0, x, nR * D, 0, 1.f, dwr,
                              nR * D, 0, 1, st);
       }
-      bwd_scatter_dx<<<(unsigned)(((long long)N * nR * D + 255) / 256), 256, 0, st>>>(
-          dx, N, L, D, c.p, c.p_offset, nR, dn);
+      if (D % 4 == 0 && (uintptr_t)dx % 16 == 0 && (uintptr_t)dn % 16 == 0)
+        bwd_scatter_dx4<<<(unsigned)(((long long)N * nR * (D / 4) + 255) / 256), 256, 0, st>>>(
+            reinterpret_cast<const float4*>(dx), N, L, D / 4, c.p, c.p_offset, nR,
+            reinterpret_cast<float4*>(dn));
+      else
+        bwd_scatter_dx<<<(unsigned)(((long long)N * nR * D + 255) / 256), 256, 0, st>>>(
+            dx, N, L, D, c.p, c.p_offset, nR, dn);
     }
     {  // source norm backward into dstates
       const int rows = 64;
