@@ -460,6 +460,46 @@ __global__ void __launch_bounds__(256) split3_rows(const float* __restrict__ src
   }
 }
 
+// The same four columns at a time: one 16-byte load, three 8-byte stores per
+// thread (C, lds and ldd multiples of 4, src 16- and dst 8-byte aligned).
+__global__ void __launch_bounds__(256) split3_rows4(const float* __restrict__ src, long long lds,
+                                                    int R, int C4, __nv_bfloat16* __restrict__ dst,
+                                                    long long ldd, bool right) {
+  const long long n = (long long)R * C4;
+  const int C = 4 * C4;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long r = i / C4;
+    const int c = 4 * (int)(i - r * C4);
+    const float4 v = *reinterpret_cast<const float4*>(src + r * lds + c);
+    __nv_bfloat16 hi[4], lo[4];
+    split_hl(v.x, hi[0], lo[0]);
+    split_hl(v.y, hi[1], lo[1]);
+    split_hl(v.z, hi[2], lo[2]);
+    split_hl(v.w, hi[3], lo[3]);
+    const uint2 h2 = *reinterpret_cast<const uint2*>(hi), l2 = *reinterpret_cast<const uint2*>(lo);
+    uint2* d = reinterpret_cast<uint2*>(dst + r * ldd + c);
+    d[0] = h2;
+    *reinterpret_cast<uint2*>(dst + r * ldd + C + c) = right ? l2 : h2;
+    *reinterpret_cast<uint2*>(dst + r * ldd + 2 * C + c) = right ? h2 : l2;
+  }
+}
+// split3_rows, vectorised where the shapes allow
+void launch_split3_rows(const float* src, long long lds, int R, int C, __nv_bfloat16* dst,
+                        long long ldd, bool right, cudaStream_t st) {
+  if (R <= 0 || C <= 0) return;
+  const long long n = (long long)R * C;
+  long long b = (n + 255) / 256;
+  if (C % 4 == 0 && lds % 4 == 0 && ldd % 4 == 0 && (uintptr_t)src % 16 == 0 && (uintptr_t)dst % 8 == 0) {
+    b = (n / 4 + 255) / 256;
+    split3_rows4<<<(unsigned)(b < 65536LL * 16 ? b : 65536LL * 16), 256, 0, st>>>(src, lds, R, C / 4, dst,
+                                                                             ldd, right);
+  } else {
+    split3_rows<<<(unsigned)(b < 65536LL * 16 ? b : 65536LL * 16), 256, 0, st>>>(src, lds, R, C, dst, ldd,
+                                                                             right);
+  }
+}
+
 // The same for the transpose: dst[c][j * R + r] from src[r][c] (32 x 32 tiles
 // through shared memory, reads and writes coalesced).
 // blockIdx.z selects a batch entry (src + z * sbs, dst + z * dbs).
@@ -487,6 +527,50 @@ __global__ void __launch_bounds__(256) split3_t(const float* __restrict__ src, l
       d[R] = right ? lo : hi;
       d[2 * R] = right ? hi : lo;
     }
+  }
+}
+
+// split3_t with two source rows per lane (64 x 32 tiles), so each warp
+// writes 128 contiguous bytes per destination row (R, ldd and dbs even, dst
+// 4-byte aligned).
+__global__ void __launch_bounds__(256) split3_t2(const float* __restrict__ src, long long lds, int R,
+                                                 int C, __nv_bfloat16* __restrict__ dst,
+                                                 long long ldd, bool right, long long sbs,
+                                                 long long dbs) {
+  __shared__ float tile[64][33];
+  src += blockIdx.z * sbs;
+  dst += blockIdx.z * dbs;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int y = ty; y < 64; y += 8) {
+    const int r = r0 + y, c = c0 + tx;
+    tile[y][tx] = (r < R && c < C) ? src[(long long)r * lds + c] : 0.f;
+  }
+  __syncthreads();
+  const int r = r0 + 2 * tx;
+  for (int y = ty; y < 32; y += 8) {
+    const int c = c0 + y;
+    if (c < C && r < R) {  // R even: r + 1 < R too
+      __nv_bfloat162 hi, lo;
+      split_hl(tile[2 * tx][y], hi.x, lo.x);
+      split_hl(tile[2 * tx + 1][y], hi.y, lo.y);
+      __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(dst + (long long)c * ldd + r);
+      d[0] = hi;
+      d[R / 2] = right ? lo : hi;
+      d[R] = right ? hi : lo;
+    }
+  }
+}
+// split3_t over a batch of blockIdx.z entries, vectorised where the shapes allow
+void launch_split3_t(const float* src, long long lds, int R, int C, __nv_bfloat16* dst, long long ldd,
+                     bool right, int batch, long long sbs, long long dbs, cudaStream_t st) {
+  if (R <= 0 || C <= 0 || batch <= 0) return;
+  if (R % 2 == 0 && ldd % 2 == 0 && dbs % 2 == 0 && (uintptr_t)dst % 4 == 0) {
+    dim3 g((unsigned)((C + 31) / 32), (unsigned)((R + 63) / 64), (unsigned)batch);
+    split3_t2<<<g, 256, 0, st>>>(src, lds, R, C, dst, ldd, right, sbs, dbs);
+  } else {
+    dim3 g((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)batch);
+    split3_t<<<g, 256, 0, st>>>(src, lds, R, C, dst, ldd, right, sbs, dbs);
   }
 }
 
@@ -674,8 +758,8 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
         to_f32<S><<<(unsigned)((WRn + 255) / 256), 256, 0, st>>>((const S*)wrs, WRn, wr);
       });
       // a = x W_R^T on the tensor cores (split operands), else in fp32
-      split3_rows<<<blocks_for((long long)N * nRD), 256, 0, st>>>(x, nRD, N, (int)nRD, sx, ld3(nRD), false);
-      split3_rows<<<blocks_for(kL * nRD), 256, 0, st>>>(wr, nRD, (int)kL, (int)nRD, sw, ld3(nRD), true);
+      launch_split3_rows(x, nRD, N, (int)nRD, sx, ld3(nRD), false, st);
+      launch_split3_rows(wr, nRD, (int)kL, (int)nRD, sw, ld3(nRD), true, st);
       if (!gemm_split_tc(N, (int)kL, (int)nRD, sx, ld3(nRD), sw, ld3(nRD), a_keep, kL, flags, st))
         ok = ok && gemm_rm(false, true, N, k * L, nR * D, x, nR * D, 0, wr, nR * D, 0, 0.f, a_keep,
                            k * L, 0, 1, st);
@@ -691,9 +775,8 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     });
     if (be == 0) {
       // kt = c W_K^T per channel on split operands (rows of all channels at once)
-      split3_rows<<<blocks_for(kN * D), 256, 0, st>>>(cc, D, (int)kN, D, sc, ld3(D), false);
-      split3_rows<<<blocks_for((long long)k * w * D), 256, 0, st>>>(wp, D, (int)(k * w), D, swp, ld3(D),
-                                                                   true);
+      launch_split3_rows(cc, D, (int)kN, D, sc, ld3(D), false, st);
+      launch_split3_rows(wp, D, (int)(k * w), D, swp, ld3(D), true, st);
       if (!gemm_split_tc(N, w, D, sc, ld3(D), swp, ld3(D), kt, w, flags, st, k, N * ld3(D),
                          w * ld3(D), (long long)N * w))
         ok = ok && gemm_rm(false, true, N, w, D, cc, D, (long long)N * D, wp, D, (long long)w * D,
@@ -713,13 +796,10 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     float* dW = be == 0 ? q.g.dWk : q.g.dWv;
     // dW_j += dY_j^T c_j  ([w x N] [N x D]);  dc_j = dY_j W_j  ([N x w] [w x D])
     {
-      split3_rows<<<blocks_for(kN * w), 256, 0, st>>>(dY, w, (int)kN, w, sdy, ld3(w), false);
-      dim3 gw((unsigned)((D + 31) / 32), (unsigned)((w + 31) / 32), (unsigned)k);
-      split3_t<<<gw, 256, 0, st>>>(wp, D, w, D, swpt, ld3(w), true, (long long)w * D, D * ld3(w));
-      dim3 gy((unsigned)((w + 31) / 32), (unsigned)((N + 31) / 32), (unsigned)k);
-      split3_t<<<gy, 256, 0, st>>>(dY, w, N, w, sdyt, ld3(N), false, (long long)N * w, w * ld3(N));
-      dim3 gc((unsigned)((D + 31) / 32), (unsigned)((N + 31) / 32), (unsigned)k);
-      split3_t<<<gc, 256, 0, st>>>(cc, D, N, D, sct, ld3(N), true, (long long)N * D, D * ld3(N));
+      launch_split3_rows(dY, w, (int)kN, w, sdy, ld3(w), false, st);
+      launch_split3_t(wp, D, w, D, swpt, ld3(w), true, k, (long long)w * D, D * ld3(w), st);
+      launch_split3_t(dY, w, N, w, sdyt, ld3(N), false, k, (long long)N * w, w * ld3(N), st);
+      launch_split3_t(cc, D, N, D, sct, ld3(N), true, k, (long long)N * D, D * ld3(N), st);
     }
     if (gemm_split_tc(w, D, N, sdyt, ld3(N), sct, ld3(N), tmpp, D, flags, st, k, w * ld3(N),
                       D * ld3(N), (long long)w * D))
@@ -747,19 +827,14 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
       // router: dW_R += da^T x ([kL x N] [N x nR D]);  dx = da W_R ([N x kL] [kL x nR D]),
       // on the tensor cores with split operands (transposed where the
       // engine's K-major layout needs it), else in fp32
-      split3_rows<<<blocks_for((long long)N * kL), 256, 0, st>>>(a, kL, N, (int)kL, sda, ld3(kL), false);
-      {
-        dim3 g1((unsigned)((nRD + 31) / 32), (unsigned)((kL + 31) / 32));
-        split3_t<<<g1, 256, 0, st>>>(wr, nRD, (int)kL, (int)nRD, swt, ld3(kL), true);
-      }
+      launch_split3_rows(a, kL, N, (int)kL, sda, ld3(kL), false, st);
+      launch_split3_t(wr, nRD, (int)kL, (int)nRD, swt, ld3(kL), true, 1, 0, 0, st);
       if (!gemm_split_tc(N, (int)nRD, (int)kL, sda, ld3(kL), swt, ld3(kL), dx, nRD, flags, st))
         ok = ok && gemm_rm(false, false, N, nR * D, k * L, a, k * L, 0, wr, nR * D, 0, 0.f, dx,
                            nR * D, 0, 1, st);
       if (q.g.dWr) {
-        dim3 g2((unsigned)((kL + 31) / 32), (unsigned)((N + 31) / 32));
-        split3_t<<<g2, 256, 0, st>>>(a, kL, N, (int)kL, sdat, ld3(N), false);
-        dim3 g3((unsigned)((nRD + 31) / 32), (unsigned)((N + 31) / 32));
-        split3_t<<<g3, 256, 0, st>>>(x, nRD, N, (int)nRD, sxt, ld3(N), true);
+        launch_split3_t(a, kL, N, (int)kL, sdat, ld3(N), false, 1, 0, 0, st);
+        launch_split3_t(x, nRD, N, (int)nRD, sxt, ld3(N), true, 1, 0, 0, st);
         float* dwr = q.g.dWr + (size_t)be * WRn;
         if (gemm_split_tc((int)kL, (int)nRD, N, sdat, ld3(N), sxt, ld3(N), tmpw, nRD, flags, st))
           add_f32<<<blocks_for(kL * nRD), 256, 0, st>>>(dwr, tmpw, kL * nRD);
