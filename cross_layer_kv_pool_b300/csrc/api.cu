@@ -202,6 +202,10 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
   const long long LD = (long long)c.L * c.D;
   const int Hd = c.Hq * c.d;
   char* stash = x.buf<char>(B_STASH);
+  // One row per sequence (decode): each product is a short weight stream, so
+  // it prefetches the next product's weights into L2 behind its own loads.
+  const bool pf = nq == 1;
+  const long long DHb = (long long)c.D * Hd * (long long)x.es, FDb = (long long)c.F * c.D * (long long)x.es;
   for (int l = 0; l < c.L; ++l) {
     const bool body = l < c.L - 1 || last_layer;
     char* h_in = stash + (long long)l * c.D * x.es;
@@ -222,6 +226,10 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
       g.epi.gain = x.wp(w.q_norm, (long long)l * c.d);
       g.epi.pos = x.buf<int>(B_POS);
       g.epi.Tmax = Tmax;
+      if (pf) {
+        g.pf[0] = x.wp(w.Wo, (long long)l * c.D * Hd);
+        g.pf_bytes[0] = DHb;
+      }
       ++x.launches;
       gemm(x, g);
     }
@@ -248,6 +256,11 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
       g.epi.mode = EPI_RESID;
       g.epi.R = h_in; g.epi.ldr = LD;
       g.epi.C = x.buf<void>(B_HMID); g.epi.ldc = c.D;
+      if (pf) {
+        g.pf[0] = x.wp(w.Wgate, (long long)l * c.F * c.D);
+        g.pf[1] = x.wp(w.Wup, (long long)l * c.F * c.D);
+        g.pf_bytes[0] = g.pf_bytes[1] = FDb;
+      }
       ++x.launches;
       gemm(x, g);
     }
@@ -263,6 +276,10 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
       g.epi = base_epi(x);
       g.epi.mode = EPI_SWIGLU;
       g.epi.C = x.buf<void>(B_ACT); g.epi.ldc = c.F;
+      if (pf) {
+        g.pf[0] = x.wp(w.Wdown, (long long)l * c.D * c.F);
+        g.pf_bytes[0] = FDb;
+      }
       ++x.launches;
       gemm(x, g);
     }
@@ -278,6 +295,10 @@ void run_stack(const Ctx& x, int N, int nq, double pos_sum, bool last_layer, voi
         g.epi.C = stash + (long long)(l + 1) * c.D * x.es; g.epi.ldc = LD;
       } else {
         g.epi.C = x.buf<void>(B_HL); g.epi.ldc = c.D;
+      }
+      if (pf && l + 1 < c.L && (l + 1 < c.L - 1 || last_layer)) {
+        g.pf[0] = x.wp(w.Wq, (long long)(l + 1) * Hd * c.D);
+        g.pf_bytes[0] = DHb;
       }
       ++x.launches;
       gemm(x, g);

@@ -365,11 +365,23 @@ __device__ __forceinline__ float merge_splits(const float* src, int nsplit, int 
   return L > 0.f ? acc / L : 0.f;
 }
 
+// 16-byte cp.async whose line is the first candidate for eviction from L2.
+__device__ __forceinline__ void cp_async16_ef(void* dst, const void* src, bool valid, uint64_t pol) {
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(smem_addr(dst)),
+               "l"(src), "r"(n), "l"(pol)
+               : "memory");
+}
+
 template <int HD>
 __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs a, int nsplit,
                                                                   float* part) {
   pdl_wait();
   pdl_trigger();
+  // The keys and values are read once per step: their lines go first when L2
+  // needs room (the weights that the next products prefetch stay).
+  uint64_t stream_pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream_pol));
   constexpr int LDS = HD + 8;
   extern __shared__ __align__(16) uint8_t sm[];
   __shared__ int last_split;
@@ -408,8 +420,8 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
       const int s = k0 + blk * DKEYS + rr;
       const bool v = s < k1;
       const long long off = (long long)(v ? s : 0) * HD + part8 * 8;
-      cp_async16(dK + rr * LDS + part8 * 8, Kg + off, v);
-      cp_async16(dV + rr * LDS + part8 * 8, Vg + off, v);
+      cp_async16_ef(dK + rr * LDS + part8 * 8, Kg + off, v, stream_pol);
+      cp_async16_ef(dV + rr * LDS + part8 * 8, Vg + off, v, stream_pol);
     }
     cp_async_commit();
   };

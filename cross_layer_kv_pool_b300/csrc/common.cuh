@@ -153,6 +153,13 @@ struct GemmDesc {
   // partial tiles here; a finalize kernel applies the epilogue and re-zeroes.
   float* partial = nullptr;
   long long partial_elems = 0;
+  // Optional L2 prefetch (tensor-core engine): byte ranges that a later
+  // product reads. Each CTA fetches its share into L2 once its own loads are
+  // issued, so the transfer overlaps this product's reduction and epilogue
+  // instead of opening the next product. Ranges must be 16-byte aligned with
+  // sizes multiples of 16; unused entries are null.
+  const void* pf[2] = {nullptr, nullptr};
+  long long pf_bytes[2] = {0, 0};
 };
 
 // Per-head epilogue on one row's d values (EPI_QNORM_ROPE and the key branch

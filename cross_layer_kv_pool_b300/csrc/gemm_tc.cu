@@ -35,6 +35,8 @@ struct Params {
   int cluster_red;        // split-K over a thread-block cluster, reduced in shared memory
   int b_const;            // B tiles may be requested before the predecessor grid ends
   int wait_probe;         // test aid: the MMA issuer first waits on a barrier nothing completes
+  const char* pf[2];      // L2 prefetch ranges for a later product (GemmDesc::pf)
+  long long pf_bytes[2];
   Epi epi;
 };
 
@@ -566,6 +568,29 @@ __global__ void __launch_bounds__(256) finalize_kernel(const Params p) {
   }
 }
 
+// This CTA's share of the L2 prefetch ranges: one contiguous, 4 KB-aligned
+// piece of each range, issued as bulk prefetches whose lines L2 keeps in
+// preference to normal and evict-first ones. Nothing waits for them.
+__device__ __forceinline__ void prefetch_share(const Params& p) {
+  if (!p.pf[0] && !p.pf[1]) return;
+  uint64_t keep;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+  const long long nb = gridDim.x;
+#pragma unroll 1
+  for (int r = 0; r < 2; ++r) {
+    const long long bytes = p.pf_bytes[r];
+    if (!p.pf[r]) continue;
+    const long long chunk = ((bytes + nb - 1) / nb + 4095) & ~4095LL;
+    const long long lo = (long long)blockIdx.x * chunk, hi = min(bytes, lo + chunk);
+    for (long long off = lo; off < hi; off += 65536) {
+      const uint32_t sz = (uint32_t)min(65536LL, hi - off);
+      asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p.pf[r] + off),
+                   "r"(sz), "l"(keep)
+                   : "memory");
+    }
+  }
+}
+
 // Split-K over a cluster: the CTAs of one output tile each hold their K
 // slice's accumulator rows in shared memory (``red``, RS floats per row);
 // CTA ``rank`` sums rows rank, rank + ks, ... over the cluster in a fixed
@@ -791,6 +816,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!ok) {
         *abort_flag = 1;
         atomicOr(p.epi.flags, FLAG_TIMEOUT);
+      } else {
+        prefetch_share(p);
       }
       // Drain: every issued copy has landed before the CTA may exit.
       volatile int no_abort = 0;
@@ -1059,6 +1086,11 @@ cudaError_t run(const GemmDesc& g, cudaStream_t st, int* launches) {
   p.vec_fin = fin_vectorisable(g);
   p.b_const = g.b_const ? 1 : 0;
   p.wait_probe = g.wait_probe ? 1 : 0;
+  for (int r = 0; r < 2; ++r) {
+    const bool use = g.pf[r] && g.pf_bytes[r] > 0 && (uintptr_t)g.pf[r] % 16 == 0 && g.pf_bytes[r] % 16 == 0;
+    p.pf[r] = use ? static_cast<const char*>(g.pf[r]) : nullptr;
+    p.pf_bytes[r] = use ? g.pf_bytes[r] : 0;
+  }
   if (p.cluster_red) {
     // one CTA per (output tile, K slice); a cluster holds one tile's slices
     cudaLaunchConfig_t lc = {};
