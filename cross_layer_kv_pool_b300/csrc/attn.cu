@@ -90,6 +90,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+// Transpose of an 8 x 8 bf16 matrix held one row pair per lane (the layout of
+// an m16n8 accumulator quarter packed to bf16x2).
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -373,7 +380,12 @@ __device__ __forceinline__ void cp_async16_ef(void* dst, const void* src, bool v
                : "memory");
 }
 
-template <int HD>
+// HT (G <= 8 query heads per KV head): the products are taken transposed,
+// S^T = K Q^T and O^T = V^T P^T, so keys and dimensions fill the 16 rows of
+// each MMA and the G heads its 8 columns; P^T reaches the second product's
+// operand layout through movmatrix. Without HT, the G heads are the rows of a
+// 16-row tile (rows >= G wasted).
+template <int HD, bool HT>
 __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs a, int nsplit,
                                                                   float* part) {
   pdl_wait();
@@ -426,10 +438,120 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
     cp_async_commit();
   };
   const float sl2 = 1.4426950408889634f / sqrtf((float)HD);
-  float o[HD / 8][4];
+  // HT: o[mt] holds O^T rows (dims) mt * 16 + lane / 4 (+ 8), heads 2 (lane % 4)
+  // (+ 1); m0, l0 / m1, l1 are those two heads' running max and sum.
+  // Otherwise o[dn] holds heads lane / 4 (+ 8), dims dn * 8 + 2 (lane % 4) (+ 1).
+  float o[HT ? HD / 16 : HD / 8][4];
 #pragma unroll
-  for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < (HT ? HD / 16 : HD / 8); ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  if constexpr (HT) {
+    // this warp's first blocks, then Q^T as B operands (head lane / 4), kept in registers
+    int blk = warp, buf = 0;
+#pragma unroll
+    for (int i = 0; i < DBUF - 1; ++i) {
+      if (blk + i * DWARPS < nblk) load_blk(blk + i * DWARPS, i);
+      else cp_async_commit();
+    }
+    cp_async_wait<DBUF - 2>();
+    __syncthreads();  // Q visible to every warp
+    uint32_t qf[HD / 16][2];
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ks += 2)
+      ldsm_x4(smem_addr(sQ + (lane & 7) * LDS + ks * 16 + (lane >> 3) * 8), qf[ks][0], qf[ks][1],
+              qf[ks + 1][0], qf[ks + 1][1]);
+
+  for (; blk < nblk; blk += DWARPS, buf = (buf + 1 == DBUF ? 0 : buf + 1)) {
+    const int ahead = blk + (DBUF - 1) * DWARPS;
+    if (ahead < nblk) load_blk(ahead, buf == 0 ? DBUF - 1 : buf - 1);
+    else cp_async_commit();
+    cp_async_wait<DBUF - 1>();
+    __syncwarp();
+    const __nv_bfloat16* Kb = myKV + (buf * 2 + 0) * DKEYS * LDS;
+    const __nv_bfloat16* Vb = myKV + (buf * 2 + 1) * DKEYS * LDS;
+    // S^T: keys mt * 16 + lane / 4 (+ 8), heads hA = 2 (lane % 4), hA + 1.
+    // The fragment loads and products are issued in this order (volatile
+    // asm keeps it): every K fragment first, then the products over four
+    // independent accumulators (even and odd k steps of both key tiles).
+    float st[DKEYS / 16][4], st2[DKEYS / 16][4];
+    {
+      uint32_t ka[DKEYS / 16][HD / 16][4];
+#pragma unroll
+      for (int mt = 0; mt < DKEYS / 16; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          ldsm_x4(smem_addr(Kb + (mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * LDS + ks * 16 +
+                            (lane >> 4) * 8),
+                  ka[mt][ks][0], ka[mt][ks][1], ka[mt][ks][2], ka[mt][ks][3]);
+#pragma unroll
+      for (int mt = 0; mt < DKEYS / 16; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st[mt][i] = st2[mt][i] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < HD / 16; ++ks)
+#pragma unroll
+        for (int mt = 0; mt < DKEYS / 16; ++mt)
+          mma_bf16((ks & 1) ? st2[mt] : st[mt], ka[mt][ks], qf[ks][0], qf[ks][1]);
+    }
+    // V^T fragments for O^T += V^T P^T, loaded before the softmax needs them
+    uint32_t va[HD / 16][DKEYS / 16][4];
+#pragma unroll
+    for (int j = 0; j < DKEYS / 16; ++j)
+#pragma unroll
+      for (int mt = 0; mt < HD / 16; ++mt)
+        ldsm_x4_t(smem_addr(Vb + (j * 16 + (lane & 7) + (lane >> 4) * 8) * LDS + mt * 16 +
+                            ((lane >> 3) & 1) * 8),
+                  va[mt][j][0], va[mt][j][1], va[mt][j][2], va[mt][j][3]);
+#pragma unroll
+    for (int mt = 0; mt < DKEYS / 16; ++mt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st[mt][i] += st2[mt][i];
+    float mx0 = m0, mx1 = m1;
+#pragma unroll
+    for (int mt = 0; mt < DKEYS / 16; ++mt)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int key = k0 + blk * DKEYS + mt * 16 + (lane >> 2) + hh * 8;
+        const bool vis = key < k1;
+        st[mt][2 * hh] = vis ? st[mt][2 * hh] * sl2 : -INFINITY;
+        st[mt][2 * hh + 1] = vis ? st[mt][2 * hh + 1] * sl2 : -INFINITY;
+        mx0 = fmaxf(mx0, st[mt][2 * hh]);
+        mx1 = fmaxf(mx1, st[mt][2 * hh + 1]);
+      }
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+    }
+    const float base0 = mx0 == -INFINITY ? 0.f : mx0, base1 = mx1 == -INFINITY ? 0.f : mx1;
+    const float corr0 = exp2f(m0 - base0), corr1 = exp2f(m1 - base1);
+    m0 = mx0;
+    m1 = mx1;
+    // P^T quarters (keys x heads) -> B operands (heads x keys) of O^T += V^T P^T
+    uint32_t pb[DKEYS / 16][2];
+#pragma unroll
+    for (int mt = 0; mt < DKEYS / 16; ++mt) {
+      const float e0 = exp2f(st[mt][0] - base0), e1 = exp2f(st[mt][1] - base1);
+      const float e2 = exp2f(st[mt][2] - base0), e3 = exp2f(st[mt][3] - base1);
+      l0 = l0 * (mt == 0 ? corr0 : 1.f) + e0 + e2;
+      l1 = l1 * (mt == 0 ? corr1 : 1.f) + e1 + e3;
+      __nv_bfloat162 p01 = __floats2bfloat162_rn(e0, e1), p23 = __floats2bfloat162_rn(e2, e3);
+      pb[mt][0] = movm_t(*reinterpret_cast<uint32_t*>(&p01));
+      pb[mt][1] = movm_t(*reinterpret_cast<uint32_t*>(&p23));
+    }
+#pragma unroll
+    for (int i = 0; i < HD / 16; ++i) {
+      o[i][0] *= corr0; o[i][1] *= corr1;
+      o[i][2] *= corr0; o[i][3] *= corr1;
+    }
+#pragma unroll
+    for (int j = 0; j < DKEYS / 16; ++j)
+#pragma unroll
+      for (int mt = 0; mt < HD / 16; ++mt) mma_bf16(o[mt], va[mt][j], pb[j][0], pb[j][1]);
+    __syncwarp();  // this buffer is refilled DBUF - 1 blocks later
+  }
+  } else {
+
   // this warp's blocks: warp, warp + DWARPS, ...; DBUF - 1 of them in flight
   int blk = warp, buf = 0;
 #pragma unroll
@@ -516,6 +638,33 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
     }
     __syncwarp();  // this buffer is refilled DBUF - 1 blocks later
   }
+  }
+  if constexpr (HT) {
+  cp_async_wait<0>();
+#pragma unroll
+  for (int x = 4; x < 32; x <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+  }
+  __syncthreads();  // all warps are done with their tiles: reuse shared memory
+  float* mine = sO + (size_t)warp * 16 * (HD + 2);
+  {
+    const int hA = 2 * (lane & 3), hB = hA + 1, dr = lane >> 2;
+#pragma unroll
+    for (int mt = 0; mt < HD / 16; ++mt) {
+      mine[hA * (HD + 2) + mt * 16 + dr] = o[mt][0];
+      mine[hB * (HD + 2) + mt * 16 + dr] = o[mt][1];
+      mine[hA * (HD + 2) + mt * 16 + dr + 8] = o[mt][2];
+      mine[hB * (HD + 2) + mt * 16 + dr + 8] = o[mt][3];
+    }
+    if (lane < 4) {
+      mine[hA * (HD + 2) + HD] = m0;
+      mine[hA * (HD + 2) + HD + 1] = l0;
+      mine[hB * (HD + 2) + HD] = m1;
+      mine[hB * (HD + 2) + HD + 1] = l1;
+    }
+  }
+  } else {
   cp_async_wait<0>();
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
@@ -538,6 +687,7 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
     mine[g0 * (HD + 2) + HD + 1] = l0;
     mine[g1 * (HD + 2) + HD] = m1;
     mine[g1 * (HD + 2) + HD + 1] = l1;
+  }
   }
   __syncthreads();
   // merge the warps: thread (head h, dims) for h < G
@@ -616,9 +766,14 @@ int launch_attn_decode(const AttnArgs& a, int kv_len, float* part, long long par
   const size_t smem_loop = (size_t)(16 + DWARPS * DBUF * 2 * DKEYS) * (HD + 8) * 2;
   const size_t smem_merge = (size_t)DWARPS * 16 * (HD + 2) * 4;
   const size_t smem = smem_loop > smem_merge ? smem_loop : smem_merge;
-  cudaFuncSetAttribute(attn_decode_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid((unsigned)ctas, nsplit);
-  launch_k(attn_decode_kernel<HD>, dim3(grid), dim3(32 * DWARPS), smem, st, aa, nsplit, part);
+  if (a.Hq / a.Hkv <= 8) {
+    cudaFuncSetAttribute(attn_decode_kernel<HD, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    launch_k(attn_decode_kernel<HD, true>, dim3(grid), dim3(32 * DWARPS), smem, st, aa, nsplit, part);
+  } else {
+    cudaFuncSetAttribute(attn_decode_kernel<HD, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    launch_k(attn_decode_kernel<HD, false>, dim3(grid), dim3(32 * DWARPS), smem, st, aa, nsplit, part);
+  }
   if (nsplit > 1 && !fused) {
     launch_k(attn_combine_kernel<HD>, dim3((unsigned)((long long)a.N * a.Hq)), dim3(HD), 0, st, a, nsplit, part);
     return 2;
