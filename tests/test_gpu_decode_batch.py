@@ -217,3 +217,27 @@ def test_decode_batch_split_k_fallback_matches_cluster():
         out.append((host(lg), host(ck)[rows, :, :, pos_h], host(cv)[rows, :, :, pos_h]))
     for a, b in zip(out[0], out[1]):
         assert relerr(b, a) <= 1e-2
+
+
+def test_decode_batch_cluster_path_is_repeatable():
+    """Without global atomics (the cluster split-K products, the one-wave
+    decode attention) a decode step is a fixed sequence of fixed-order sums:
+    two calls on the same inputs give bit-identical logits and cache rows."""
+    s = synth.HALF_1P3B.replace(L=4, k=4, V=2000)
+    W = synth.make_weights(s, seed=49, device="cuda", gain_jitter=0.1)
+    m = wm.Model(s, W)
+    B, Tmax = 8, 300
+    pos_h = np.array([3, 40, 77, 120, 161, 200, 250, 299])
+    tok_h = np.random.default_rng(50).integers(0, s.V, size=B)
+    rows = np.arange(B)
+    outs = []
+    for _ in range(2):
+        ck, cv = _random_cache(s, B, Tmax, 51)
+        ws = m.workspace(B, Tmax)
+        lg = torch.zeros((B, s.V), dtype=torch.float32, device="cuda")
+        wm.wm_decode_batch(m, _i32(tok_h), _i32(pos_h), ck, cv, lg, ws)
+        torch.cuda.synchronize()
+        assert wm.wm_check_flags(ws) == 0
+        outs.append((host(lg), host(ck)[rows, :, :, pos_h], host(cv)[rows, :, :, pos_h]))
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
