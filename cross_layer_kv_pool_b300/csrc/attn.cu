@@ -470,9 +470,10 @@ __global__ void __launch_bounds__(32 * DWARPS) attn_decode_kernel(const AttnArgs
     const __nv_bfloat16* Kb = myKV + (buf * 2 + 0) * DKEYS * LDS;
     const __nv_bfloat16* Vb = myKV + (buf * 2 + 1) * DKEYS * LDS;
     // S^T: keys mt * 16 + lane / 4 (+ 8), heads hA = 2 (lane % 4), hA + 1.
-    // The fragment loads and products are issued in this order (volatile
-    // asm keeps it): every K fragment first, then the products over four
-    // independent accumulators (even and odd k steps of both key tiles).
+    // Written in this order (the volatile asm statements keep it in the
+    // emitted code; the final schedule is the assembler's): every K
+    // fragment first, then the products over four independent accumulators
+    // (even and odd k steps of both key tiles).
     float st[DKEYS / 16][4], st2[DKEYS / 16][4];
     {
       uint32_t ka[DKEYS / 16][HD / 16][4];
