@@ -66,7 +66,8 @@ def test_attention_uniform_closed_form(dtype, d, Hq, Hkv, rps):
 @pytest.mark.parametrize("rps", [0, 1])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("d,Hq,Hkv,Tmax", [(64, 4, 2, 300), (128, 14, 2, 257), (64, 8, 8, 130),
-                                           (128, 14, 2, 2304), (64, 16, 2, 520), (128, 16, 1, 700)])
+                                           (128, 14, 2, 2304), (64, 16, 2, 520), (128, 16, 1, 700),
+                                           (64, 12, 4, 333), (64, 16, 1, 450), (128, 12, 1, 610)])
 def test_attention_vs_oracle(dtype, d, Hq, Hkv, Tmax, rps):
     """Random rows; rows_per_seq = 1 takes the decode engine (key splits)."""
     s = small_shape(dtype, d=d, Hq=Hq, Hkv=Hkv, k=2)
