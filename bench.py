@@ -462,9 +462,17 @@ def run_ours(args, ws, rank, local):
                     d_[1] += ms_
                 dtr[name]["by_flops"] = {k: [v[0], v[1] / v[0]] for k, v in by.items()}
         cache_bytes = 2 * B * s.k * s.Hkv * Tmax * s.d * 2
+        # bytes the steps must move, averaged over their positions T .. T + nd - 1
+        step_bytes = sum(decode_step_bytes(s, B, T + t) for t in range(nd)) / nd
+        hbm_peak = peaks()[0]["hbm_gbs"]
         decode = {"value": ws * B * nd / (dms / 1e3), "unit": "tok/s", "steps": nd, "batch": B,
                   "prefix": T, "ms_per_step": dms / nd, "replay": "cuda_graph",
                   "eager": {"value": ws * B * nd / (dms_eager / 1e3), "ms_per_step": dms_eager / nd},
+                  "hbm": {"bytes_per_step": step_bytes, "achieved": step_bytes / (dms / nd) / 1e6,
+                          "unit": "GB/s", "peak": hbm_peak,
+                          "frac": step_bytes / (dms / nd) / 1e6 / hbm_peak,
+                          "what": "weights once and the visible cache entries once per step, "
+                                  "averaged over the steps' positions; peak = measured HBM copy"},
                   "peak_cache_bytes": cache_bytes,
                   "cache_bytes_L_channels": cache_bytes // s.k * s.L, "kernels": dtr}
         if rank == 0 and not args.no_cpu_baseline:
