@@ -561,6 +561,91 @@ __global__ void __launch_bounds__(256) split3_t2(const float* __restrict__ src, 
     }
   }
 }
+// da_r = dm_r n_r^T for every row r, on the tensor cores: dm_r [k x D] (row j
+// of channel j at dm + j * ldj + r * D), n_r [L x D] (at n + r * L * D),
+// da_r [k x L] (at da + r * k * L); k <= 16, L <= 32, D % 16 == 0. One warp
+// per row: the m16n8k16 fragments are loaded straight from the fp32
+// operands (8-byte pairs along D) and split exactly into bf16 hi + lo, the
+// product taken as hi.hi + hi.lo + lo.hi with fp32 accumulation (lo.lo is
+// below 2^-16 of the product); rows j >= k and columns l >= L are zero.
+__device__ __forceinline__ void split_pair(float2 v, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(v.x - hf.x, v.y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__global__ void __launch_bounds__(256) bwd_da_tc(const float* __restrict__ dm, long long ldj,
+                                                 const float* __restrict__ n, int N, int L, int D,
+                                                 int k, float* __restrict__ da) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + warp;
+  if (r >= N) return;  // warp-uniform
+  const int g = lane >> 2, t = lane & 3;
+  // A rows g and g + 8 (channels), B columns nt * 8 + g (layers); absent
+  // ones read row 0 and are zeroed
+  const bool va0 = g < k, va1 = g + 8 < k;
+  const float* A0 = dm + (long long)(va0 ? g : 0) * ldj + r * D + 2 * t;
+  const float* A1 = dm + (long long)(va1 ? g + 8 : 0) * ldj + r * D + 2 * t;
+  const float* Bp[4];
+  bool vb[4];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) {
+    const int l = nt * 8 + g;
+    vb[nt] = l < L;
+    Bp[nt] = n + (r * L + (vb[nt] ? l : 0)) * D + 2 * t;
+  }
+  const float2 z = make_float2(0.f, 0.f);
+  float acc[4][4] = {};
+#pragma unroll 2
+  for (int k0 = 0; k0 < D; k0 += 16) {
+    const float2 a00 = va0 ? *reinterpret_cast<const float2*>(A0 + k0) : z;
+    const float2 a10 = va1 ? *reinterpret_cast<const float2*>(A1 + k0) : z;
+    const float2 a01 = va0 ? *reinterpret_cast<const float2*>(A0 + k0 + 8) : z;
+    const float2 a11 = va1 ? *reinterpret_cast<const float2*>(A1 + k0 + 8) : z;
+    float2 b0[4], b1[4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      b0[nt] = vb[nt] ? *reinterpret_cast<const float2*>(Bp[nt] + k0) : z;
+      b1[nt] = vb[nt] ? *reinterpret_cast<const float2*>(Bp[nt] + k0 + 8) : z;
+    }
+    uint32_t ah[4], al[4];
+    split_pair(a00, ah[0], al[0]);
+    split_pair(a10, ah[1], al[1]);
+    split_pair(a01, ah[2], al[2]);
+    split_pair(a11, ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_pair(b0[nt], bh0, bl0);
+      split_pair(b1[nt], bh1, bl1);
+      mma_16816(acc[nt], ah, bh0, bh1);
+      mma_16816(acc[nt], ah, bl0, bl1);
+      mma_16816(acc[nt], al, bh0, bh1);
+    }
+  }
+  float* out = da + r * k * L;
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = g + 8 * h;
+      if (j >= k) continue;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int l = nt * 8 + 2 * t + e;
+        if (l < L) out[j * L + l] = acc[nt][2 * h + e];
+      }
+    }
+}
+
 // split3_t over a batch of blockIdx.z entries, vectorised where the shapes allow
 void launch_split3_t(const float* src, long long lds, int R, int C, __nv_bfloat16* dst, long long ldd,
                      bool right, int batch, long long sbs, long long dbs, cudaStream_t st) {
@@ -819,8 +904,11 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
                                                   q.g.dchan_norm + (size_t)be * k * D);
     }
     // mix backward per row r: da_r [k x L] = dm_r [k x D] n_r^T; dn_r [L x D] = a_r^T dm_r
-    ok = ok && gemm_rm(false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
-                       L, (long long)k * L, N, st);
+    if (k <= 16 && L <= 32 && D % 16 == 0 && (uintptr_t)dc % 8 == 0 && (uintptr_t)n % 8 == 0)
+      bwd_da_tc<<<(unsigned)((N + 7) / 8), 256, 0, st>>>(dc, (long long)N * D, n, N, L, D, k, a);
+    else
+      ok = ok && gemm_rm(false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
+                         L, (long long)k * L, N, st);
     ok = ok && gemm_rm(true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
                        0.f, dn, D, (long long)L * D, N, st);
     if (!W.static_coeff) {
