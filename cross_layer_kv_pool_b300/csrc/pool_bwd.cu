@@ -646,6 +646,63 @@ __global__ void __launch_bounds__(256) bwd_da_tc(const float* __restrict__ dm, l
     }
 }
 
+// dn_r = a_r^T dm_r for every row r, on the tensor cores: a_r [k x L] (at
+// a + r * k * L), dm_r as in bwd_da_tc, dn_r [L x D] (at dn + r * L * D);
+// k <= 16, L <= 32, D % 8 == 0. One warp per row: a_r^T's two 16-row
+// fragments are split once; each 8-column step of D loads the four channel
+// rows a lane's B fragment needs (8 lanes read 8 consecutive columns of one
+// row), splits them and stores both 16-row output tiles with 8-byte stores.
+__global__ void __launch_bounds__(256) bwd_dn_tc(const float* __restrict__ a,
+                                                 const float* __restrict__ dm, long long ldj, int N,
+                                                 int L, int D, int k, float* __restrict__ dn) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long r = (long long)blockIdx.x * 8 + warp;
+  if (r >= N) return;  // warp-uniform
+  const int g = lane >> 2, t = lane & 3;
+  const float* ar = a + r * k * L;
+  auto av = [&](int l, int j) { return (l < L && j < k) ? ar[j * L + l] : 0.f; };
+  uint32_t ah[2][4], al[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int l0 = mt * 16 + g, l1 = l0 + 8;
+    split_pair(make_float2(av(l0, 2 * t), av(l0, 2 * t + 1)), ah[mt][0], al[mt][0]);
+    split_pair(make_float2(av(l1, 2 * t), av(l1, 2 * t + 1)), ah[mt][1], al[mt][1]);
+    split_pair(make_float2(av(l0, 2 * t + 8), av(l0, 2 * t + 9)), ah[mt][2], al[mt][2]);
+    split_pair(make_float2(av(l1, 2 * t + 8), av(l1, 2 * t + 9)), ah[mt][3], al[mt][3]);
+  }
+  // the B rows (channels) 2t, 2t + 1, 2t + 8, 2t + 9 at column g of each step
+  const float* Bj[4];
+  bool vj[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = 2 * t + (i & 1) + (i >> 1) * 8;
+    vj[i] = j < k;
+    Bj[i] = dm + (long long)(vj[i] ? j : 0) * ldj + r * D + g;
+  }
+  float* out = dn + r * L * D + 2 * t;
+  const bool w0 = g < L, w1 = g + 8 < L, w2 = g + 16 < L, w3 = g + 24 < L;
+#pragma unroll 4
+  for (int n0 = 0; n0 < D; n0 += 8) {
+    float b[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = vj[i] ? Bj[i][n0] : 0.f;
+    uint32_t bh0, bl0, bh1, bl1;
+    split_pair(make_float2(b[0], b[1]), bh0, bl0);
+    split_pair(make_float2(b[2], b[3]), bh1, bl1);
+    float c[2][4] = {};
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      mma_16816(c[mt], ah[mt], bh0, bh1);
+      mma_16816(c[mt], ah[mt], bl0, bl1);
+      mma_16816(c[mt], al[mt], bh0, bh1);
+    }
+    if (w0) *reinterpret_cast<float2*>(out + (long long)g * D + n0) = make_float2(c[0][0], c[0][1]);
+    if (w1) *reinterpret_cast<float2*>(out + (long long)(g + 8) * D + n0) = make_float2(c[0][2], c[0][3]);
+    if (w2) *reinterpret_cast<float2*>(out + (long long)(g + 16) * D + n0) = make_float2(c[1][0], c[1][1]);
+    if (w3) *reinterpret_cast<float2*>(out + (long long)(g + 24) * D + n0) = make_float2(c[1][2], c[1][3]);
+  }
+}
+
 // split3_t over a batch of blockIdx.z entries, vectorised where the shapes allow
 void launch_split3_t(const float* src, long long lds, int R, int C, __nv_bfloat16* dst, long long ldd,
                      bool right, int batch, long long sbs, long long dbs, cudaStream_t st) {
@@ -909,8 +966,11 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     else
       ok = ok && gemm_rm(false, true, k, L, D, dc, (long long)N * D, D, n, D, (long long)L * D, 0.f, a,
                          L, (long long)k * L, N, st);
-    ok = ok && gemm_rm(true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
-                       0.f, dn, D, (long long)L * D, N, st);
+    if (k <= 16 && L <= 32 && D % 8 == 0 && (uintptr_t)dn % 8 == 0)
+      bwd_dn_tc<<<(unsigned)((N + 7) / 8), 256, 0, st>>>(a_keep, dc, (long long)N * D, N, L, D, k, dn);
+    else
+      ok = ok && gemm_rm(true, false, L, D, k, a_keep, L, (long long)k * L, dc, (long long)N * D, D,
+                         0.f, dn, D, (long long)L * D, N, st);
     if (!W.static_coeff) {
       // router: dW_R += da^T x ([kL x N] [N x nR D]);  dx = da W_R ([N x kL] [kL x nR D]),
       // on the tensor cores with split operands (transposed where the
