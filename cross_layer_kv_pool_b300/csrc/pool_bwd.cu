@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(256) bwd_da_tc(const float* __restrict__ dm, l
   }
   const float2 z = make_float2(0.f, 0.f);
   float acc[4][4] = {};
-#pragma unroll 2
+#pragma unroll 1
   for (int k0 = 0; k0 < D; k0 += 16) {
     const float2 a00 = va0 ? *reinterpret_cast<const float2*>(A0 + k0) : z;
     const float2 a10 = va1 ? *reinterpret_cast<const float2*>(A1 + k0) : z;
@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(256) bwd_dn_tc(const float* __restrict__ a,
   }
   float* out = dn + r * L * D + 2 * t;
   const bool w0 = g < L, w1 = g + 8 < L, w2 = g + 16 < L, w3 = g + 24 < L;
-#pragma unroll 4
+#pragma unroll 2
   for (int n0 = 0; n0 < D; n0 += 8) {
     float b[4];
 #pragma unroll
