@@ -432,6 +432,98 @@ __global__ void __launch_bounds__(256) bwd_src_norm_w(const S* __restrict__ stat
   for (int t = threadIdx.x; t < D; t += blockDim.x) atomicAdd(&dsigma[(size_t)l * D + t], acc[t]);
 }
 
+// Four consecutive storage-type values kept raw in registers (bf16: two
+// registers), converted to fp32 where used.
+template <typename S> struct Raw4;
+template <> struct Raw4<float> {
+  using T = float4;
+  static __device__ __forceinline__ T load(const float* p) { return *reinterpret_cast<const float4*>(p); }
+  static __device__ __forceinline__ float4 f(const T& v) { return v; }
+};
+template <> struct Raw4<__nv_bfloat16> {
+  using T = uint2;
+  static __device__ __forceinline__ T load(const __nv_bfloat16* p) { return *reinterpret_cast<const uint2*>(p); }
+  static __device__ __forceinline__ float4 f(const T& u) {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+};
+
+// The same with each row held in registers (NV float4 columns a lane, D =
+// 128 NV): every load of a row is in flight before its sum, the layer's gains
+// sit in shared memory, and each warp sums d sigma over its rows in a shared
+// row of its own (plain read-add-write, no atomics), the warps' rows added
+// at the end. Dynamic shared memory: (2 + warps) D floats.
+template <typename S, int NV>
+__global__ void __launch_bounds__(256, 1) bwd_src_norm_wr(const S* __restrict__ states, int N, int L,
+                                                          int D, const float* __restrict__ inv,
+                                                          const S* __restrict__ sigma,
+                                                          const float* __restrict__ dn, int rows,
+                                                          bool first, float* __restrict__ dstates,
+                                                          float* __restrict__ dsigma) {
+  extern __shared__ float sm[];
+  const int nw = (int)(blockDim.x >> 5);
+  float* sgf = sm;                 // [D] the layer's gains in fp32
+  float* wacc = sm + D;            // [warps][D] each warp's d sigma
+  const int l = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = threadIdx.x; t < D; t += blockDim.x) sgf[t] = to_f(sigma[(size_t)l * D + t]);
+  for (int t = threadIdx.x; t < nw * D; t += blockDim.x) wacc[t] = 0.f;
+  __syncthreads();
+  float* ds = wacc + (size_t)warp * D + 4 * lane;
+  const int r0 = blockIdx.x * rows, r1 = min(r0 + rows, N);
+  for (int r = r0 + warp; r < r1; r += (int)(blockDim.x >> 5)) {
+    const size_t base = ((size_t)r * L + l) * D + 4 * lane;
+    const float iv = inv[(size_t)r * L + l];
+    float4 g[NV];
+    typename Raw4<S>::T hr[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      g[k] = ld4(dn + base + 128 * k);
+      hr[k] = Raw4<S>::load(states + base + 128 * k);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const float4 w = *reinterpret_cast<const float4*>(sgf + 4 * lane + 128 * k);
+      const float4 h = Raw4<S>::f(hr[k]);
+      s = fmaf(w.x * g[k].x, h.x, s);
+      s = fmaf(w.y * g[k].y, h.y, s);
+      s = fmaf(w.z * g[k].z, h.z, s);
+      s = fmaf(w.w * g[k].w, h.w, s);
+    }
+    s = warp_sum(s);
+    const float c3 = s * iv * iv * iv / (float)D;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const float4 w = *reinterpret_cast<const float4*>(sgf + 4 * lane + 128 * k);
+      const float4 h = Raw4<S>::f(hr[k]);
+      float4* dsk = reinterpret_cast<float4*>(ds + 128 * k);
+      float4 a4 = *dsk;
+      a4.x += h.x * iv * g[k].x;
+      a4.y += h.y * iv * g[k].y;
+      a4.z += h.z * iv * g[k].z;
+      a4.w += h.w * iv * g[k].w;
+      *dsk = a4;
+      float4 dh = make_float4(w.x * g[k].x * iv - h.x * c3, w.y * g[k].y * iv - h.y * c3,
+                              w.z * g[k].z * iv - h.z * c3, w.w * g[k].w * iv - h.w * c3);
+      float4* o = reinterpret_cast<float4*>(dstates + base + 128 * k);
+      if (!first) {
+        const float4 prev = *o;
+        dh.x += prev.x; dh.y += prev.y; dh.z += prev.z; dh.w += prev.w;
+      }
+      *o = dh;
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    float v = 0.f;
+    for (int w = 0; w < nw; ++w) v += wacc[(size_t)w * D + t];
+    atomicAdd(&dsigma[(size_t)l * D + t], v);
+  }
+}
+
 // Leading dimension (elements) of a split operand of K columns: 3K, rounded
 // up to 8 so that rows start on 16-byte boundaries.
 inline long long ld3(long long K) { return (3 * K + 7) / 8 * 8; }
@@ -1005,12 +1097,31 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     {  // source norm backward into dstates
       const int rows = 64;
       dim3 grid((N + rows - 1) / rows, L);
+      const int nvr = D % 128 == 0 ? D / 128 : 0;
+      const bool al = (uintptr_t)q.states % 16 == 0 && (uintptr_t)dn % 16 == 0 &&
+                      (uintptr_t)q.dstates % 16 == 0;
+#define WM_SNW(NV_)                                                                               \
+  do {                                                                                            \
+    const size_t smb = (size_t)D * 4 * (1 + 8);                                                   \
+    cudaFuncSetAttribute(bwd_src_norm_wr<S, NV_>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                         (int)smb);                                                               \
+    bwd_src_norm_wr<S, NV_><<<grid, 256, smb, st>>>((const S*)q.states, N, L, D, inv,             \
+                                                    (const S*)sig, dn, rows, be == 0, q.dstates, \
+                                                    q.g.dsrc_norm + (size_t)be * L * D);          \
+  } while (0)
       WM_DISPATCH_S(c.dtype, {
-        bwd_src_norm_w<S><<<grid, 256, (size_t)D * 4, st>>>((const S*)q.states, N, L, D, inv,
-                                                            (const S*)sig, dn, rows, be == 0,
-                                                            q.dstates,
-                                                            q.g.dsrc_norm + (size_t)be * L * D);
+        if (al && nvr == 14) WM_SNW(14);
+        else if (al && nvr == 8) WM_SNW(8);
+        else if (al && nvr == 4) WM_SNW(4);
+        else if (al && nvr == 2) WM_SNW(2);
+        else if (al && nvr == 1) WM_SNW(1);
+        else
+          bwd_src_norm_w<S><<<grid, 256, (size_t)D * 4, st>>>((const S*)q.states, N, L, D, inv,
+                                                              (const S*)sig, dn, rows, be == 0,
+                                                              q.dstates,
+                                                              q.g.dsrc_norm + (size_t)be * L * D);
       });
+#undef WM_SNW
     }
   }
   if (!ok) return cudaErrorUnknown;
