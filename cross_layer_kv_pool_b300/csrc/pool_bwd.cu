@@ -338,6 +338,70 @@ __global__ void __launch_bounds__(256) bwd_rms_w(const float* __restrict__ x, lo
   for (int t = threadIdx.x; t < D; t += blockDim.x) atomicAdd(&dw[(size_t)gi * D + t], acc[t]);
 }
 
+// bwd_rms_w with each row held in registers (NV float4 columns a lane, D =
+// 128 NV; 16-byte aligned rows), the gains in shared memory and each warp's
+// d w summed in a shared row of its own (as bwd_src_norm_wr). Dynamic shared
+// memory: (1 + warps) D floats.
+template <int NV>
+__global__ void __launch_bounds__(256, 1) bwd_rms_wr(const float* __restrict__ x, long long xstride_gain,
+                                                     long long xstride_row, const float* __restrict__ rr,
+                                                     long long rr_stride_gain, long long rr_stride_row,
+                                                     const float* __restrict__ w, int D, int rows_total,
+                                                     int rows, float* __restrict__ dxy,
+                                                     float* __restrict__ dw) {
+  extern __shared__ float sm[];
+  const int nw = (int)(blockDim.x >> 5);
+  float* wgs = sm;        // [D] the gains
+  float* wacc = sm + D;   // [warps][D] each warp's d w
+  const int gi = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int t = threadIdx.x; t < D; t += blockDim.x) wgs[t] = w[(size_t)gi * D + t];
+  for (int t = threadIdx.x; t < nw * D; t += blockDim.x) wacc[t] = 0.f;
+  __syncthreads();
+  float* acc = wacc + (size_t)warp * D + 4 * lane;
+  const int r0 = blockIdx.x * rows, r1 = min(r0 + rows, rows_total);
+  for (int q = r0 + warp; q < r1; q += nw) {
+    const float* xr = x + gi * xstride_gain + q * xstride_row + 4 * lane;
+    float* dr = dxy + gi * xstride_gain + q * xstride_row + 4 * lane;
+    const float rv = rr[gi * rr_stride_gain + q * rr_stride_row];
+    float4 dy[NV], xv[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      dy[k] = *reinterpret_cast<const float4*>(dr + 128 * k);
+      xv[k] = *reinterpret_cast<const float4*>(xr + 128 * k);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const float4 wv = *reinterpret_cast<const float4*>(wgs + 4 * lane + 128 * k);
+      s = fmaf(wv.x * dy[k].x, xv[k].x,
+               fmaf(wv.y * dy[k].y, xv[k].y, fmaf(wv.z * dy[k].z, xv[k].z, fmaf(wv.w * dy[k].w, xv[k].w, s))));
+    }
+    s = warp_sum(s);
+    const float c3 = s / ((float)D * rv * rv * rv), iv = 1.f / rv;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const float4 wv = *reinterpret_cast<const float4*>(wgs + 4 * lane + 128 * k);
+      float4* ak = reinterpret_cast<float4*>(acc + 128 * k);
+      float4 a4 = *ak;
+      a4.x += xv[k].x * iv * dy[k].x;
+      a4.y += xv[k].y * iv * dy[k].y;
+      a4.z += xv[k].z * iv * dy[k].z;
+      a4.w += xv[k].w * iv * dy[k].w;
+      *ak = a4;
+      *reinterpret_cast<float4*>(dr + 128 * k) =
+          make_float4(wv.x * dy[k].x * iv - xv[k].x * c3, wv.y * dy[k].y * iv - xv[k].y * c3,
+                      wv.z * dy[k].z * iv - xv[k].z * c3, wv.w * dy[k].w * iv - xv[k].w * c3);
+    }
+  }
+  __syncthreads();
+  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    float v = 0.f;
+    for (int i = 0; i < nw; ++i) v += wacc[(size_t)i * D + t];
+    atomicAdd(&dw[(size_t)gi * D + t], v);
+  }
+}
+
 // dn[r][R_i] += dx[r][i]
 // The same four columns at a time (D % 4 == 0, 16-byte aligned rows).
 __global__ void bwd_scatter_dx4(const float4* __restrict__ dx, int N, int L, int D4, int p,
@@ -1052,9 +1116,25 @@ cudaError_t run_pool_backward(const PoolBwdArgs& q, cudaStream_t st) {
     {  // channel norm backward, in place: dc -> dm
       const int rows = 64;
       dim3 grid((N + rows - 1) / rows, k);
-      bwd_rms_w<<<grid, 256, (size_t)D * 4, st>>>(m, (long long)N * D, D, rj, 1, k,
-                                                  tau32 + (size_t)be * k * D, D, N, rows, dc,
-                                                  q.g.dchan_norm + (size_t)be * k * D);
+      const int nvr = D % 128 == 0 ? D / 128 : 0;
+      const float* tau_b = tau32 + (size_t)be * k * D;
+      const bool al = (uintptr_t)m % 16 == 0 && (uintptr_t)dc % 16 == 0 && (uintptr_t)tau_b % 16 == 0;
+#define WM_RMW(NV_)                                                                            \
+  do {                                                                                         \
+    const size_t smb = (size_t)D * 4 * (1 + 8);                                                \
+    cudaFuncSetAttribute(bwd_rms_wr<NV_>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb); \
+    bwd_rms_wr<NV_><<<grid, 256, smb, st>>>(m, (long long)N * D, D, rj, 1, k, tau_b, D, N, rows, dc, \
+                                            q.g.dchan_norm + (size_t)be * k * D);                 \
+  } while (0)
+      if (al && nvr == 14) WM_RMW(14);
+      else if (al && nvr == 8) WM_RMW(8);
+      else if (al && nvr == 4) WM_RMW(4);
+      else if (al && nvr == 2) WM_RMW(2);
+      else if (al && nvr == 1) WM_RMW(1);
+      else
+        bwd_rms_w<<<grid, 256, (size_t)D * 4, st>>>(m, (long long)N * D, D, rj, 1, k, tau_b, D, N,
+                                                    rows, dc, q.g.dchan_norm + (size_t)be * k * D);
+#undef WM_RMW
     }
     // mix backward per row r: da_r [k x L] = dm_r [k x D] n_r^T; dn_r [L x D] = a_r^T dm_r
     if (k <= 16 && L <= 32 && D % 16 == 0 && (uintptr_t)dc % 8 == 0 && (uintptr_t)n % 8 == 0)
