@@ -251,8 +251,13 @@ __global__ void bwd_knorm(const S* __restrict__ dK, const float* __restrict__ kt
   float dk_acc = 0.f;
   const long long r0 = (long long)blockIdx.x * rows;
   for (long long r = r0; r < r0 + rows && r < N; ++r) {
-    double sn, cs;
-    sincos((double)pos[r] * theta, &sn, &cs);
+    // the angle and its reduction to [-pi, pi] in double, the sine and
+    // cosine of the reduced angle in fp32 (double-precision sincos per row
+    // and thread cost more than the rest of the kernel)
+    const double ang = (double)pos[r] * theta;
+    const double ared = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+    float sn, cs;
+    sincosf((float)ared, &sn, &cs);
     for (int hh = 0; hh < Hkv; ++hh) {
       const float g = to_f(dK[(((size_t)r * k + j) * Hkv + hh) * d + t]);
       buf[t] = g;
